@@ -1,0 +1,336 @@
+"""Pins of the CPU oracle against facts fixed outside it (no GPU).
+
+Each test checks the oracle against the format definitions the pages name, values
+the pages print, closed forms, special cases that reduce to a library routine, or
+brute force on tiny inputs.  A plausible mistake in the oracle (a dropped term, a
+wrong sign or index, a transposed operand, a wrong tie rule) fails one of them.
+"""
+import ctypes
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import csa2_inputs as gen
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _gold(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+def _fnptr(orc, name):
+    return ctypes.cast(getattr(orc.lib(), name), ctypes.c_void_p)
+
+
+# ------------------------------------------------------------------ E2M1 -----------
+
+def test_e2m1_value_set_and_round_trip(orc):
+    g = _gold("e2m1_values.json")
+    mags = {int(k): v for k, v in g["code_to_magnitude"].items()}
+    for c in range(16):
+        want = mags[c & 7] * (-1.0 if c & 8 else 1.0)
+        got = orc.lib().orc_e2m1_decode(c)
+        assert got == want and math.copysign(1.0, got) == math.copysign(1.0, want) or (want == 0 and got == 0)
+        # every representable value re-encodes to its own code (negative zero keeps its sign)
+        assert orc.lib().orc_e2m1_encode(ctypes.c_float(got)) == c
+    values = sorted({abs(orc.lib().orc_e2m1_decode(c)) for c in range(16)})
+    assert values == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_exhaustive_vs_brute_force(orc, pins_lib):
+    """Every float32 bit pattern: oracle decision table == nearest magnitude, ties to even."""
+    mag = (ctypes.c_double * 8)(*[0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    bad = ctypes.c_uint32()
+    n_bad = pins_lib.pin_e2m1_sweep(_fnptr(orc, "orc_e2m1_encode"), mag, os.cpu_count() or 4,
+                                    ctypes.byref(bad))
+    assert n_bad == 0, f"{n_bad} mismatches, first pattern 0x{bad.value:08x}"
+
+
+# ------------------------------------------------------------------ E4M3 -----------
+
+def _e4m3_table_from_torch():
+    codes = torch.arange(256, dtype=torch.uint8)
+    vals = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return vals
+
+
+def test_e4m3_decode_matches_torch_and_anchors(orc):
+    vals = _e4m3_table_from_torch()
+    for c in range(256):
+        got = orc.lib().orc_e4m3_decode(c)
+        if c in (0x7F, 0xFF):
+            assert math.isnan(got) and math.isnan(vals[c])
+        else:
+            assert got == vals[c], hex(c)
+    for a in _gold("e4m3_anchors.json")["anchors"]:
+        assert orc.lib().orc_e4m3_encode(ctypes.c_float(a["value"])) == int(a["code"], 16)
+        assert orc.lib().orc_e4m3_decode(int(a["code"], 16)) == a["value"]
+
+
+def test_e4m3_exhaustive_vs_nearest(orc, pins_lib):
+    """Every finite non-negative float32: oracle == nearest finite E4M3 value (ties to
+    even code, saturating at 448).  The value table is torch's float8_e4m3fn decode."""
+    vals = _e4m3_table_from_torch()[:127]
+    assert np.all(np.diff(vals) > 0)
+    tab = (ctypes.c_double * 127)(*vals.tolist())
+    bad = ctypes.c_uint32()
+    n_bad = pins_lib.pin_e4m3_sweep(_fnptr(orc, "orc_e4m3_encode"), tab, os.cpu_count() or 4,
+                                    ctypes.byref(bad))
+    assert n_bad == 0, f"{n_bad} mismatches, first pattern 0x{bad.value:08x}"
+
+
+def test_e4m3_full_brute_force_sample(orc, pins_lib):
+    """All 127 candidates compared, on random patterns of both signs."""
+    vals = _e4m3_table_from_torch()[:127]
+    tab = (ctypes.c_double * 127)(*vals.tolist())
+    rng = np.random.default_rng(7)
+    pats = np.concatenate([rng.integers(0, 2**32, 2_000_000, dtype=np.uint64).astype(np.uint32),
+                           np.array([0x80000000, 0x3F880000, 0xBF880000], np.uint32)])
+    bad = ctypes.c_uint32()
+    n_bad = pins_lib.pin_e4m3_brute(_fnptr(orc, "orc_e4m3_encode"), tab,
+                                    pats.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32)), pats.size,
+                                    ctypes.byref(bad))
+    assert n_bad == 0, f"first bad 0x{bad.value:08x}"
+
+
+def test_e4m3_encode_matches_torch_in_range(orc):
+    """torch's float32 -> float8_e4m3fn cast rounds to nearest even; inside the finite
+    range it must agree with the oracle bit for bit."""
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.uniform(0, 448, 500_000), np.exp(rng.uniform(-25, 6, 500_000))])
+    x = x[x <= 448].astype(np.float32)
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = orc.e4m3_encode(x)
+    assert np.array_equal(got, want)
+
+
+# ------------------------------------------------------------------ blocks ---------
+
+def test_quant_blocks_worked_by_hand(orc):
+    for blk in _gold("quant_blocks.json")["blocks"]:
+        x = np.array(blk["x"], dtype=np.float32).reshape(1, 16)
+        codes, scales = orc.quantize(x)
+        assert scales[0, 0] == int(blk["scale"], 16), blk["name"]
+        assert [int(c, 16) for c in blk["codes"]] == codes[0].tolist(), blk["name"]
+
+
+def test_quant_block_properties(orc):
+    """On latent-like data: each block's largest code magnitude is 5, 6 or 7 unless the
+    scale is zero; dequantised error stays within half an E2M1 step of y times s."""
+    gains = gen.latent_gains(0)
+    x = gen.latent_rows(0, 0, 0, np.arange(256), gains)
+    codes, scales = orc.quantize(x)
+    deq = orc.dequantize(codes, scales)
+    nib = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(256, 512)
+    mag = (nib & 7).reshape(256, 32, 16).max(axis=-1)
+    s = orc.e4m3_decode(scales.ravel()).reshape(256, 32)
+    assert np.all((mag >= 5) | (s == 0))
+    # E2M1 gaps: half-step at |y| <= 2 is 0.25, <= 4 is 0.5, <= 6 is 1
+    y = np.abs(x.astype(np.float64)) / np.repeat(s, 16, axis=1)
+    half = np.where(y <= 2, 0.25, np.where(y <= 4, 0.5, 1.0))
+    err = np.abs(x - deq) / np.repeat(s, 16, axis=1)
+    assert np.all(err <= half * (1 + 1e-6))
+
+
+def test_dequant_is_exact_product(orc):
+    """Every (code, scale) pair decodes to e2m1 x e4m3, which float32 holds exactly."""
+    e2 = np.array([orc.lib().orc_e2m1_decode(c) for c in range(16)])
+    e4 = np.array([orc.lib().orc_e4m3_decode(b) for b in range(127)])
+    prod = np.outer(e4, e2)
+    assert np.array_equal(prod.astype(np.float32).astype(np.float64), prod)
+    codes = np.arange(256, dtype=np.uint8).reshape(1, 256).repeat(127, 0)
+    codes = np.concatenate([codes, codes], axis=1)[:, :256]
+    scales = np.repeat(np.arange(127, dtype=np.uint8).reshape(127, 1), 32, axis=1)
+    deq = orc.dequantize(codes, scales)
+    for r in (0, 1, 56, 126):
+        for c in range(0, 512, 37):
+            byte = codes[r, c // 2]
+            code = (byte >> 4) if c % 2 else (byte & 0xF)
+            assert deq[r, c] == e2[code] * e4[r]
+
+
+# ------------------------------------------------------------------ projection -----
+
+def _bf16(x):
+    return gen.f32_to_bf16_bits(np.asarray(x, np.float32))
+
+
+def test_projection_identity_reproduces_codec(orc):
+    """W = [I_512; 0] makes C = H[:, :512] exactly, so the write path's codes must equal
+    the block quantiser applied to H's first 512 columns (page 5 CED equation)."""
+    rng = np.random.default_rng(11)
+    H = _bf16(rng.standard_normal((24, 640)) * 3)
+    Wt = np.zeros((512 + 128, 640), np.uint16)
+    Wt[np.arange(512), np.arange(512)] = 0x3F80                       # 1.0 in bf16
+    Wt[512 + np.arange(128), 512 + np.arange(128)] = 0x3F80
+    codes, scales, keys, C = orc.kv_write_rows(H, Wt, 1, 1)
+    Hf = gen.bf16_bits_to_f32(H)
+    c2, s2 = orc.quantize(Hf[:, :512].copy())
+    assert np.array_equal(codes[0], c2) and np.array_equal(scales[0], s2)
+    assert np.array_equal(keys[0], H[:, 512:640])                       # bf16 -> fp32 -> bf16 round trip
+
+
+def test_projection_one_hot_columns_and_library_gemm(orc):
+    rng = np.random.default_rng(12)
+    H = _bf16(rng.standard_normal((8, 256)))
+    Wt = _bf16(rng.standard_normal((64, 256)) / 16)
+    perm = rng.permutation(256)[:16]
+    Wt[:16] = 0
+    Wt[np.arange(16), perm] = 0x3F80
+    C = orc.project(H, Wt)
+    Hf = gen.bf16_bits_to_f32(H).astype(np.float64)
+    Wf = gen.bf16_bits_to_f32(Wt).astype(np.float64)
+    assert np.array_equal(C[:, :16], Hf[:, perm].astype(np.float32))  # selects H's columns, not rows
+    ref = Hf @ Wf.T                                                     # library GEMM in float64
+    np.testing.assert_allclose(C, ref.astype(np.float32), rtol=1e-6, atol=1e-7)
+
+
+# ------------------------------------------------------------------ indexer --------
+
+def test_index_score_special_cases(orc):
+    """One-hot keys read off one coordinate of each head: score = sum_h max(0, q[h, d])
+    (ReLU per head, then a sum over the 4 heads; no transposition of q)."""
+    rng = np.random.default_rng(5)
+    q = _bf16(rng.standard_normal((4, 128)))
+    keys = np.zeros((128, 128), np.uint16)
+    keys[np.arange(128), np.arange(128)] = 0x3F80
+    s = orc.index_scores(q, keys)
+    qf = gen.bf16_bits_to_f32(q).astype(np.float64)
+    assert np.array_equal(s, np.maximum(qf, 0).sum(axis=0))
+    # doubling a key doubles the score (exact in bf16 and double)
+    k = _bf16(rng.standard_normal((16, 128)))
+    k2 = _bf16(gen.bf16_bits_to_f32(k) * 2)
+    assert np.array_equal(orc.index_scores(q, k2), 2 * orc.index_scores(q, k))
+    # permuting heads leaves scores unchanged; negating q flips which heads contribute
+    assert np.array_equal(orc.index_scores(q[[2, 0, 3, 1]], k), orc.index_scores(q, k))
+    neg = q ^ np.uint16(0x8000)
+    both = orc.index_scores(q, k) + orc.index_scores(neg, k)
+    dots = np.abs(qf @ gen.bf16_bits_to_f32(k).astype(np.float64).T).sum(axis=0)
+    np.testing.assert_allclose(both, dots, rtol=1e-12)
+
+
+def _brute_topk(scores, tokens, k):
+    order = sorted(range(len(scores)), key=lambda i: (-scores[i], tokens[i]))
+    sel = sorted(tokens[i] for i in order[:k])
+    return np.array(sel + [-1] * (k - len(sel)), np.int32)
+
+
+@pytest.mark.parametrize("n,k", [(1, 4), (5, 5), (17, 4), (64, 16), (64, 64), (40, 100)])
+def test_select_topk_brute_force_with_ties(orc, n, k):
+    rng = np.random.default_rng(n * 131 + k)
+    scores = rng.integers(0, 4, n).astype(np.float64)      # many exact ties, zeros like ReLU
+    tokens = np.sort(rng.choice(1000, n, replace=False)).astype(np.int32)
+    assert np.array_equal(orc.select_topk(scores, tokens, k), _brute_topk(scores, tokens, k))
+
+
+def test_full_mode_pool_contains_topk_and_small_context(orc):
+    rng = np.random.default_rng(9)
+    keys = _bf16(rng.standard_normal((300, 128)))
+    q = _bf16(rng.standard_normal((4, 128)))
+    idx, pool, s = orc.index_full(q, keys, 32, 128)
+    assert set(idx[idx >= 0]) <= set(pool[pool >= 0])
+    assert np.all(np.diff(idx) > 0) and np.all(np.diff(pool) > 0)
+    assert s[idx].min() >= np.sort(s)[-32]
+    # N <= K selects every token
+    idx2, pool2, _ = orc.index_full(q, keys[:20], 32, 128)
+    assert np.array_equal(idx2[:20], np.arange(20)) and np.all(idx2[20:] == -1)
+
+
+def test_reindex_restricted_to_pool_and_equal_to_full(orc):
+    """Page 5 Hierarchical Sparse Indexer: Reindex searches only the pool.  With the
+    Full layer's own query, Reindex over its pool returns Full's top-K exactly."""
+    rng = np.random.default_rng(10)
+    keys = _bf16(rng.standard_normal((2000, 128)))
+    qf = _bf16(rng.standard_normal((4, 128)))
+    idx_full, pool, _ = orc.index_full(qf, keys, 64, 512)
+    idx_re, _ = orc.index_reindex(qf, keys, pool, 64)
+    assert np.array_equal(idx_re, idx_full)
+    q2 = _bf16(rng.standard_normal((4, 128)))
+    idx2, _ = orc.index_reindex(q2, keys, pool, 64)
+    assert set(idx2[idx2 >= 0]) <= set(pool)
+    small = pool.copy()
+    small[40:] = -1
+    idx3, _ = orc.index_reindex(q2, keys, small, 64)
+    assert np.array_equal(idx3[:40], small[:40]) and np.all(idx3[40:] == -1)
+
+
+def test_reuse_passes_indices_through(orc):
+    x = np.array([3, 9, 27, -1], np.int32)
+    assert np.array_equal(orc.index_reuse(x), x)
+
+
+# ------------------------------------------------------------------ attention ------
+
+def test_attention_dense_case_matches_library_sdpa(orc):
+    """K = N: sparse attention over every row equals dense scaled-dot-product attention
+    (torch's library routine, float64)."""
+    rng = np.random.default_rng(21)
+    q = _bf16(rng.standard_normal((16, 512)))
+    chat = rng.standard_normal((70, 512)).round(3)
+    scale = np.float32(1 / math.sqrt(512))
+    out, lse = orc.sparse_attention(q, chat, float(scale))
+    qt = torch.from_numpy(gen.bf16_bits_to_f32(q).astype(np.float64)).view(1, 16, 512)
+    kt = torch.from_numpy(chat).view(1, 1, 70, 512).expand(1, 16, 70, 512)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt.view(1, 16, 1, 512), kt, kt,
+                                                           scale=float(scale)).view(16, 512)
+    np.testing.assert_allclose(out, ref.numpy().astype(np.float32), rtol=2e-6, atol=1e-6)
+    ref_lse = torch.logsumexp(float(scale) * (qt.view(16, 512) @ torch.from_numpy(chat).T), dim=-1)
+    np.testing.assert_allclose(lse, ref_lse.numpy().astype(np.float32), rtol=1e-6)
+
+
+def test_attention_closed_forms(orc):
+    rng = np.random.default_rng(22)
+    q = _bf16(rng.standard_normal((16, 512)))
+    row = rng.standard_normal(512)
+    # all rows equal -> output is that row, lse = scale*q.row + ln n
+    out, lse = orc.sparse_attention(q, np.tile(row, (9, 1)), 0.05)
+    np.testing.assert_allclose(out, np.tile(row, (16, 1)).astype(np.float32), rtol=1e-6, atol=1e-7)
+    qf = gen.bf16_bits_to_f32(q).astype(np.float64)
+    np.testing.assert_allclose(lse, (0.05 * qf @ row + math.log(9)).astype(np.float32), rtol=1e-6)
+    # q = 0 -> mean of the rows
+    chat = rng.standard_normal((13, 512))
+    out0, lse0 = orc.sparse_attention(np.zeros((16, 512), np.uint16), chat, 0.05)
+    np.testing.assert_allclose(out0, np.tile(chat.mean(0), (16, 1)).astype(np.float32), rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(lse0, np.float32(math.log(13)), rtol=1e-7)
+    # a single row -> that row; no rows -> zeros and -inf
+    out1, _ = orc.sparse_attention(q, chat[4:5], 0.05)
+    assert np.array_equal(out1, np.tile(chat[4].astype(np.float32), (16, 1)))
+    outn, lsen = orc.sparse_attention(q, np.zeros((0, 512)), 0.05)
+    assert np.all(outn == 0) and np.all(np.isneginf(lsen))
+    # row order does not matter
+    perm = rng.permutation(13)
+    o_a, _ = orc.sparse_attention(q, chat, 0.05)
+    o_b, _ = orc.sparse_attention(q, chat[perm], 0.05)
+    np.testing.assert_allclose(o_a, o_b, rtol=1e-6, atol=1e-7)
+
+
+def test_attention_large_logit_stability(orc):
+    """exp never overflows: a huge logit gap gives one-hot weights."""
+    q = _bf16(np.full((16, 512), 4.0))
+    chat = np.zeros((3, 512))
+    chat[1] = 50.0
+    out, _ = orc.sparse_attention(q, chat, 1.0)
+    assert np.all(np.isfinite(out)) and np.allclose(out, 50.0)
+
+
+# ------------------------------------------------------------------ footprint ------
+
+def test_footprint_arithmetic_printed_on_pages(orc):
+    g = _gold("footprint.json")
+    b = g["bytes_per_token"]
+    assert b == orc.PAGES_FOOTPRINT
+    assert orc.session_bytes(b["v4.1-flash"], g["session_tokens"]) == g["session_MB_printed"] * 10**6
+    assert round(orc.session_bytes(b["v4.1-flash"]) / 1e9, 2) == g["session_GB_printed"]
+    assert round(orc.session_bytes(b["v4-flash"]) / 1e9, 1) == g["v4flash_session_GB_printed"]
+    assert round(b["v4-flash"] / b["v4.1-flash"], 1) == g["ratio_vs_v4flash_printed"]
+    assert round(b["v4-flash"] / b["v4.1-flash"]) == 4
+    assert round(b["v1"] / b["v4.1-flash"]) == g["ratio_vs_v1_printed"]
+    # this layout: 256 B codes + 32 B scales + 256 B bf16 keys per Full group
+    assert orc.layout_bytes_per_token(1) == 544
+    assert orc.layout_bytes_per_token(5) == 2720
