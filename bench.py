@@ -1,0 +1,451 @@
+#!/usr/bin/env python
+"""Benchmark of the CSA2 FP4 compressed global KV cache decode step on B300.
+
+Default workload: 64 sequences x 131072 context tokens, 4-layer mode schedule
+Full -> Reindex -> Reuse -> Reuse, candidate pool 8192, top-K 2048, one decode query
+per sequence.  Metric: decode queries/s per layer (query tokens x layers / time), with
+the achieved HBM bandwidth of the dominant kernel against the measured peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun, one rank per GPU; ranks are independent replicas of the
+workload (weak scaling, no collective on the data path).  `--impl reference` times the
+CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA2 FP4-KV decode queries/s per layer; achieved HBM GB/s vs B300 peak"
+UNIT = "queries/s per layer"
+FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS = 1800.0
+
+
+# ------------------------------------------------------------------ helpers ------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": float(np.median(busy)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("CSA2_BENCH_BACKEND", "nccl")
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def shard_sequences(num_seqs: int, world: int, rank: int, scaling: str = "weak"):
+    """Sequences this rank serves.  Weak scaling: every rank serves a full, independent
+    replica of the batch.  Strong scaling: the batch is split into contiguous shards."""
+    if scaling == "weak" or world == 1:
+        return np.arange(num_seqs)
+    per = (num_seqs + world - 1) // world
+    return np.arange(rank * per, min(num_seqs, (rank + 1) * per))
+
+
+# ------------------------------------------------------------------ algorithmic bytes --
+
+def full_index_bytes(wl) -> int:
+    """Bytes a Full-layer index step must move: every context key row (256 B) of every
+    query's sequence (read once per sequence), the indexer queries, top-K and pool."""
+    per_seq = wl.seq_lens.astype(np.int64) * 256
+    return int(per_seq.sum() + wl.num_q * (4 * 128 * 2 + 4 * wl.topk + 4 * wl.pool_size))
+
+
+def reindex_bytes(wl) -> int:
+    return int(wl.num_q * (wl.pool_size * (4 + 256) + 4 * 128 * 2 + 4 * wl.topk))
+
+
+def attn_bytes(wl) -> int:
+    """Selected FP4 rows (256 B codes + 32 B scales), q, indices, out and lse."""
+    return int(wl.num_q * (wl.topk * (288 + 4) + 16 * 512 * 2 + 16 * 512 * 4 + 16 * 4))
+
+
+# ------------------------------------------------------------------ ours ---------
+
+def run_ours(args, world, rank, local):
+    import torch
+    import csa2_inputs as gen
+    import fp4_compressed_sparse_03_b300 as csa2
+    from fp4_compressed_sparse_03_b300.decode import DecodeStep
+    from fp4_compressed_sparse_03_b300.workload import all_queries_host, fill_decode_cache
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = {"decode_batch": gen.config_decode_batch, "long_context": gen.config_long_context,
+          "ragged": gen.config_ragged, "tiny": gen.config_tiny}[args.workload]()
+    cache = fill_decode_cache(wl, device=dev)
+    q_idx_h, q_h = all_queries_host(wl)
+    q_idx = torch.from_numpy(q_idx_h.view(np.int16)).to(dev)
+    q = torch.from_numpy(q_h.view(np.int16)).to(dev)
+    mq = int(wl.q_per_seq.max())
+    step = DecodeStep(cache, wl.q_seq, wl.schedule, wl.pool_size, wl.topk, mq)
+    L = len(wl.schedule)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        step.run(q_idx, q)
+    torch.cuda.synchronize(dev)
+    status, bits = csa2.csa2_read_status(step.dev_status)
+    if status != csa2.CSA2_OK:
+        raise RuntimeError(f"device status {bits:#x} after warm-up")
+
+    # per-call events inside the timed region (on the launching stream)
+    K = args.steps
+    full_layers = [l for l, m in enumerate(wl.schedule) if m == csa2.CSA2_FULL]
+    re_layers = [l for l, m in enumerate(wl.schedule) if m == csa2.CSA2_REINDEX]
+    ev = {(k, l, w): torch.cuda.Event(enable_timing=True)
+          for k in range(K) for l in range(L) for w in ("i0", "i1", "a1")}
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(K):
+        for l in range(L):
+            ev[(k, l, "i0")].record(stream)
+            step.layer_index(l, q_idx[l])
+            ev[(k, l, "i1")].record(stream)
+            step.layer_attn(l, q[l])
+            ev[(k, l, "a1")].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    ms_step = reduce_max(ms_total / K, world, dev)
+    status, bits = csa2.csa2_read_status(step.dev_status)
+    if status != csa2.CSA2_OK:
+        raise RuntimeError(f"device status {bits:#x} after timed steps")
+
+    def avg(l, a, b):
+        return float(np.mean([ev[(k, l, a)].elapsed_time(ev[(k, l, b)]) for k in range(K)]))
+
+    full_ms = float(np.mean([avg(l, "i0", "i1") for l in full_layers]))
+    re_ms = float(np.mean([avg(l, "i0", "i1") for l in re_layers])) if re_layers else 0.0
+    attn_ms = float(np.mean([avg(l, "i1", "a1") for l in range(L)]))
+    units = wl.num_q * L * world
+    value = units / (ms_step / 1e3)
+
+    hbm_peak, tc_peak, peak_src = load_peaks()
+    fb = full_index_bytes(wl)
+    achieved = fb / (full_ms / 1e3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            tj = json.load(f)
+        t = tj.get(args.workload)
+        if t and t.get("kernel_hash") == kernel_hash():
+            traffic = t.get("bytes_per_launch")
+
+    # ---- end to end: pinned host queries in, host outputs back, every step ----
+    q_idx_pin = torch.from_numpy(q_idx_h.view(np.int16)).pin_memory()
+    q_pin = torch.from_numpy(q_h.view(np.int16)).pin_memory()
+    out_pin = torch.empty(step.out.shape, dtype=torch.float32).pin_memory()
+    lse_pin = torch.empty(step.lse.shape, dtype=torch.float32).pin_memory()
+    idx_layers = [l for l, m in enumerate(wl.schedule) if m != csa2.CSA2_REUSE]
+    h2d = sum(q_idx_pin[l].numel() * 2 for l in idx_layers) + q_pin.numel() * 2
+    d2h = out_pin.numel() * 4 + lse_pin.numel() * 4
+    K2 = max(1, min(K, args.e2e_steps))
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    w0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(K2):
+        for l in idx_layers:
+            q_idx[l].copy_(q_idx_pin[l], non_blocking=True)
+        q.copy_(q_pin, non_blocking=True)
+        step.run(q_idx, q)
+        out_pin.copy_(step.out, non_blocking=True)
+        lse_pin.copy_(step.lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall_e2e = (time.perf_counter() - w0) / K2 * 1e3
+    barrier(world)
+    ms_e2e = reduce_max(max(e0.elapsed_time(e1) / K2, wall_e2e), world, dev)
+    e2e_value = units / (ms_e2e / 1e3)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, args.cpu_sample)
+
+    launches_per_step = count_launches(wl, step)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp4-e2m1/e4m3 kv, bf16 keys+queries, f32 accumulate",
+        "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": wl.name, "num_seqs": int(len(wl.seq_lens)),
+                   "context_tokens": int(wl.seq_lens.max()), "query_tokens": wl.num_q,
+                   "layers": L, "schedule": "".join("FRU"[m] for m in wl.schedule),
+                   "pool": wl.pool_size, "topk": wl.topk,
+                   "l2": "no flush: every step streams %.2f GB of indexer keys (> 126 MB L2)"
+                         % (fb / 1e9),
+                   "parallelism": f"replicas x{world}"},
+        "per_mode_ms": {"full_index": round(full_ms, 4), "reindex": round(re_ms, 4),
+                        "attention": round(attn_ms, 4)},
+        "roofline": {"bound": "hbm", "kernel": "csa2_index(FULL): score_q1_kernel + select_kernel",
+                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": fb, "traffic": traffic},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "steps": K2},
+        "gpu_launches": int(launches_per_step * K),
+        "clocks": clk,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def count_launches(wl, step) -> int:
+    """Kernels libcsa2 launches per decode step: Full and Reindex index calls launch a
+    scoring and a selection kernel; Reuse none; attention one kernel plus the split
+    combine when the selected set is split."""
+    import fp4_compressed_sparse_03_b300 as csa2
+    n = 0
+    for m in wl.schedule:
+        if m != csa2.CSA2_REUSE:
+            n += 2
+    ws = csa2.csa2_attn_workspace_size(step.num_q, step.topk)
+    n += len(wl.schedule) * (2 if ws > 0 else 1)
+    return n
+
+
+def kernel_hash() -> str:
+    """Hash of the CUDA sources; traffic counters are only reported for this exact build."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp4_compressed_sparse_03_b300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------------------ CPU oracle ---
+
+def _oracle_query_step(wl, qi, keys, codes, scales, q_idx_h, q_h, scale):
+    """The whole layer schedule for one query on the CPU oracle."""
+    import csa2_inputs as gen
+    import oracle
+    idx, pool = {}, None
+    src = wl.index_source()
+    n = keys.shape[0]
+    for l, m in enumerate(wl.schedule):
+        if m == gen.FULL:
+            i, pool, _ = oracle.index_full(q_idx_h[l][qi], keys, wl.topk, wl.pool_size)
+            idx[l] = i
+        elif m == gen.REINDEX:
+            idx[l], _ = oracle.index_reindex(q_idx_h[l][qi], keys, pool, wl.topk)
+        else:
+            idx[l] = oracle.index_reuse(idx[src[l]])
+        oracle.attention_over_cache(q_h[l][qi], codes, scales, idx[src[l]], scale)
+    return n
+
+
+def cpu_baseline(wl, sample_queries: int):
+    """Time the oracle, as it stands, on a bounded sample of the workload: the full layer
+    schedule for `sample_queries` queries, one host thread per query."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import csa2_inputs as gen
+    import oracle
+    from csa2_inputs import native
+    from fp4_compressed_sparse_03_b300.workload import layer_queries_host
+
+    cores = os.cpu_count() or 1
+    qs = np.linspace(0, wl.num_q - 1, min(sample_queries, wl.num_q)).astype(int)
+    L = len(wl.schedule)
+    qh = [layer_queries_host(wl, l) for l in range(L)]
+    q_idx_h = np.stack([a for a, _ in qh])
+    q_h = np.stack([b for _, b in qh])
+    gains = gen.latent_gains(wl.seed, 0)
+
+    def prep(qi):  # resident inputs: keys and the quantised latent of the query's sequence
+        b = int(wl.q_seq[qi])
+        n = int(wl.seq_lens[b])
+        keys = native.key_rows_host(wl.seed, 0, b, 0, n)
+        codes, scales = oracle.quantize(native.latent_rows_host(wl.seed, 0, b, 0, n, gains))
+        return int(qi), keys, codes, scales
+
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        inputs = list(ex.map(prep, qs))
+    scale = float(np.float32(1.0 / math.sqrt(512.0)))
+    threads = min(cores, len(inputs))
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(lambda a: _oracle_query_step(wl, a[0], a[1], a[2], a[3], q_idx_h, q_h, scale),
+                    inputs))
+    dt = time.perf_counter() - t0
+    return {"value": round(len(inputs) * L / dt, 3), "unit": UNIT, "cores": threads,
+            "kind": "oracle",
+            "sample": f"{len(inputs)} of {wl.num_q} queries x {L} layers of {wl.name}, "
+                      f"{dt:.1f} s wall on {threads} threads"}
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm, on the same workload, metric and unit."""
+    import csa2_inputs as gen
+    if rank != 0:
+        return
+    wl = {"decode_batch": gen.config_decode_batch, "long_context": gen.config_long_context,
+          "ragged": gen.config_ragged, "tiny": gen.config_tiny}[args.workload]()
+    per_step = max(1, args.cpu_sample // max(1, args.steps))
+    for _ in range(max(0, min(args.warmup, 1))):
+        cpu_baseline(wl, 1)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(wl, per_step))
+    dt = time.perf_counter() - t0
+    v = float(np.mean([c["value"] for c in vals]))
+    cb = dict(vals[-1])
+    cb["value"] = round(v, 3)
+    cb["sample"] = f"{args.steps} steps x {per_step} queries x {len(wl.schedule)} layers of {wl.name}"
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (CPU oracle)",
+            "data": "synthetic (seeded counter-based generator)",
+            "config": {"workload": wl.name, "num_seqs": int(len(wl.seq_lens)),
+                       "context_tokens": int(wl.seq_lens.max()), "query_tokens": wl.num_q,
+                       "layers": len(wl.schedule), "pool": wl.pool_size, "topk": wl.topk},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(v, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_batch",
+                    choices=["decode_batch", "long_context", "ragged", "tiny"])
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--cpu-sample", type=int, default=32, help="queries timed on the oracle")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        args.warmup = max(3, args.warmup)
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -358,7 +358,6 @@ def config_write(seed: int = 2) -> WriteWorkload:
 
 
 def d_model_pow2_scale(d_model: int) -> int:
-    """Weights are N(0, 1/d_model); for d_model = 4**k the sd is the power of two 2**-k."""
-    k = math.log2(d_model) / 2
-    assert k == int(k)
-    return -int(k)
+    """Weights are N(0, 1/d_model) scaled by a power of two: the exponent of the power of
+    two nearest at or above 1/sqrt(d_model) (exactly 1/sqrt(d) = 2**-6 for d = 4096)."""
+    return -(int(math.log2(d_model)) // 2)

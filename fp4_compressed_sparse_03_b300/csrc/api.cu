@@ -1,0 +1,218 @@
+// libcsa2 C ABI: argument validation, workspace sizing and kernel launches.
+// The declarations and their contracts are in include/csa2.h.
+#include <algorithm>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace csa2 {
+cudaError_t launch_quantize(const float*, const int32_t*, uint8_t*, uint8_t*, int32_t, int32_t,
+                            int64_t, int32_t*, cudaStream_t, int);
+cudaError_t launch_dequantize(const uint8_t*, const uint8_t*, const int32_t*, float*, int32_t,
+                              int32_t, int64_t, int32_t*, cudaStream_t, int);
+cudaError_t launch_score_full(const uint16_t*, const uint16_t*, const int32_t*, int32_t, int32_t,
+                              const csa2_pages&, uint32_t*, int64_t, int32_t*, cudaStream_t, int);
+cudaError_t launch_score_reindex(const uint16_t*, const uint16_t*, const int32_t*, int32_t,
+                                 const csa2_pages&, const int32_t*, int32_t, uint32_t*, int32_t*,
+                                 cudaStream_t, int);
+cudaError_t launch_select(bool, const uint32_t*, int64_t, const int32_t*, const csa2_pages&,
+                          int32_t, const int32_t*, int32_t, int32_t, int32_t*, int32_t*, int32_t*,
+                          cudaStream_t);
+cudaError_t launch_attn(const uint16_t*, const uint8_t*, const uint8_t*, const int32_t*,
+                        const csa2_pages&, float*, float*, int32_t, const int32_t*, int32_t, float,
+                        void*, int32_t*, cudaStream_t, int);
+size_t attn_workspace_bytes(int32_t, int32_t, int);
+cudaError_t launch_kv_write(const uint16_t*, const uint16_t*, uint8_t*, uint8_t*, uint16_t*,
+                            int32_t, int32_t, int32_t, int32_t, const int32_t*, int64_t, int32_t*,
+                            cudaStream_t, int);
+}  // namespace csa2
+
+using namespace csa2;
+
+namespace {
+
+int device_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+csa2_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return CSA2_OK;
+  (void)cudaGetLastError();  // clear a sticky launch-configuration error
+  return CSA2_ERR_CUDA;
+}
+
+csa2_status check_pages(const csa2_pages* pg) {
+  if (pg == nullptr || pg->seq_lens == nullptr || pg->page_table == nullptr)
+    return CSA2_ERR_INVALID_ARGUMENT;
+  if (pg->page_size != kPage) return CSA2_ERR_UNSUPPORTED;
+  if (pg->num_seqs < 1 || pg->max_pages_per_seq < 1 || pg->num_pages < 1)
+    return CSA2_ERR_INVALID_ARGUMENT;
+  if ((int64_t)pg->max_pages_per_seq * kPage > (int64_t)INT32_MAX / 2) return CSA2_ERR_UNSUPPORTED;
+  return CSA2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t csa2_version(void) { return 10000; }
+
+const char* csa2_status_string(csa2_status s) {
+  switch (s) {
+    case CSA2_OK: return "ok";
+    case CSA2_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case CSA2_ERR_UNSUPPORTED: return "unsupported geometry";
+    case CSA2_ERR_CUDA: return "CUDA error";
+    case CSA2_ERR_DEVICE_FAULT: return "device-detected fault (bad index, page or slot)";
+    case CSA2_ERR_TIMEOUT: return "bounded device wait expired";
+  }
+  return "unknown status";
+}
+
+csa2_status csa2_quantize(const float* x, const int32_t* slot_of_token, uint8_t* codes,
+                          uint8_t* scales, int32_t T, int32_t D, int64_t num_slots,
+                          int32_t* dev_status, cudaStream_t stream) {
+  if (T < 0 || D <= 0 || num_slots < 0) return CSA2_ERR_INVALID_ARGUMENT;
+  if (D % kGroup != 0 || D > 4096) return CSA2_ERR_UNSUPPORTED;
+  if (T == 0) return CSA2_OK;
+  if (!x || !slot_of_token || !codes || !scales) return CSA2_ERR_INVALID_ARGUMENT;
+  if (!al16(x) || (reinterpret_cast<uintptr_t>(codes) & 7u)) return CSA2_ERR_INVALID_ARGUMENT;
+  return from_cuda(launch_quantize(x, slot_of_token, codes, scales, T, D, num_slots, dev_status,
+                                   stream, device_sms()));
+}
+
+csa2_status csa2_dequantize(const uint8_t* codes, const uint8_t* scales,
+                            const int32_t* slot_of_token, float* x, int32_t T, int32_t D,
+                            int64_t num_slots, int32_t* dev_status, cudaStream_t stream) {
+  if (T < 0 || D <= 0 || num_slots < 0) return CSA2_ERR_INVALID_ARGUMENT;
+  if (D % kGroup != 0 || D > 4096) return CSA2_ERR_UNSUPPORTED;
+  if (T == 0) return CSA2_OK;
+  if (!x || !slot_of_token || !codes || !scales) return CSA2_ERR_INVALID_ARGUMENT;
+  if (!al16(x) || (reinterpret_cast<uintptr_t>(codes) & 7u)) return CSA2_ERR_INVALID_ARGUMENT;
+  return from_cuda(launch_dequantize(codes, scales, slot_of_token, x, T, D, num_slots, dev_status,
+                                     stream, device_sms()));
+}
+
+size_t csa2_index_workspace_size(csa2_mode mode, int32_t num_q, int32_t max_pages_per_seq,
+                                 int32_t pool_size) {
+  if (num_q <= 0) return 0;
+  switch (mode) {
+    case CSA2_FULL:
+      return (size_t)num_q * (size_t)std::max(0, max_pages_per_seq) * kPage * sizeof(uint32_t);
+    case CSA2_REINDEX:
+      return (size_t)num_q * (size_t)std::max(0, pool_size) * sizeof(uint32_t);
+    default:
+      return 0;
+  }
+}
+
+csa2_status csa2_index(csa2_mode mode, const uint16_t* q_idx, const uint16_t* k_idx, int32_t* pool,
+                       int32_t topk, int32_t* out_idx, const csa2_pages* pages,
+                       const csa2_index_args* args, cudaStream_t stream) {
+  if (args == nullptr || out_idx == nullptr || topk < 1) return CSA2_ERR_INVALID_ARGUMENT;
+  if (args->num_q < 1 || args->q_seq == nullptr) return CSA2_ERR_INVALID_ARGUMENT;
+  if (mode == CSA2_REUSE) {
+    if (args->inherit_idx == nullptr) return CSA2_ERR_INVALID_ARGUMENT;
+    if (args->inherit_idx == out_idx) return CSA2_OK;
+    return from_cuda(cudaMemcpyAsync(out_idx, args->inherit_idx,
+                                     (size_t)args->num_q * topk * sizeof(int32_t),
+                                     cudaMemcpyDeviceToDevice, stream));
+  }
+  if (mode != CSA2_FULL && mode != CSA2_REINDEX) return CSA2_ERR_INVALID_ARGUMENT;
+  csa2_status ps = check_pages(pages);
+  if (ps != CSA2_OK) return ps;
+  if (!q_idx || !k_idx || !al16(q_idx) || !al16(k_idx)) return CSA2_ERR_INVALID_ARGUMENT;
+  if (args->max_q_per_seq < 1 || args->max_q_per_seq > 4) return CSA2_ERR_UNSUPPORTED;
+  const int32_t P = args->pool_size;
+  const size_t need = csa2_index_workspace_size(mode, args->num_q, pages->max_pages_per_seq, P);
+  if (args->workspace == nullptr || args->workspace_bytes < need || !al16(args->workspace))
+    return CSA2_ERR_INVALID_ARGUMENT;
+  if (args->num_q > 65535) return CSA2_ERR_UNSUPPORTED;  // grid.y of the selection
+  const int sms = device_sms();
+  uint32_t* ws = static_cast<uint32_t*>(args->workspace);
+  cudaError_t e;
+  if (mode == CSA2_FULL) {
+    if (pool != nullptr && P < 1) return CSA2_ERR_INVALID_ARGUMENT;
+    const int64_t stride = (int64_t)pages->max_pages_per_seq * kPage;
+    e = launch_score_full(q_idx, k_idx, args->q_seq, args->num_q, args->max_q_per_seq, *pages, ws,
+                          stride, args->dev_status, stream, sms);
+    if (e != cudaSuccess) return from_cuda(e);
+    e = launch_select(false, ws, stride, args->q_seq, *pages, args->num_q, nullptr,
+                      pool ? P : 0, topk, out_idx, pool, args->dev_status, stream);
+    return from_cuda(e);
+  }
+  // REINDEX
+  if (pool == nullptr || P < 1) return CSA2_ERR_INVALID_ARGUMENT;
+  e = launch_score_reindex(q_idx, k_idx, args->q_seq, args->num_q, *pages, pool, P, ws,
+                           args->dev_status, stream, sms);
+  if (e != cudaSuccess) return from_cuda(e);
+  e = launch_select(true, ws, P, args->q_seq, *pages, args->num_q, pool, P, topk, out_idx, nullptr,
+                    args->dev_status, stream);
+  return from_cuda(e);
+}
+
+size_t csa2_attn_workspace_size(int32_t num_q, int32_t topk) {
+  if (num_q <= 0 || topk <= 0) return 0;
+  return attn_workspace_bytes(num_q, topk, device_sms());
+}
+
+csa2_status csa2_sparse_attn(const uint16_t* q, const uint8_t* codes, const uint8_t* scales,
+                             const int32_t* idx, const csa2_pages* pages, float* out, float* lse,
+                             int32_t num_q, const int32_t* q_seq, int32_t topk, float softmax_scale,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                             cudaStream_t stream) {
+  if (num_q < 1 || topk < 1 || !q || !codes || !scales || !idx || !out || !q_seq)
+    return CSA2_ERR_INVALID_ARGUMENT;
+  csa2_status ps = check_pages(pages);
+  if (ps != CSA2_OK) return ps;
+  if (!al16(q) || !al16(codes) || !al16(scales) || (reinterpret_cast<uintptr_t>(out) & 7u))
+    return CSA2_ERR_INVALID_ARGUMENT;
+  if (!(softmax_scale == softmax_scale)) return CSA2_ERR_INVALID_ARGUMENT;
+  if (num_q > 65535) return CSA2_ERR_UNSUPPORTED;
+  const int sms = device_sms();
+  const size_t need = attn_workspace_bytes(num_q, topk, sms);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !al16(workspace)))
+    return CSA2_ERR_INVALID_ARGUMENT;
+  return from_cuda(launch_attn(q, codes, scales, idx, *pages, out, lse, num_q, q_seq, topk,
+                               softmax_scale, workspace, dev_status, stream, sms));
+}
+
+csa2_status csa2_kv_write(const uint16_t* H, const uint16_t* Wt, uint8_t* codes, uint8_t* scales,
+                          uint16_t* k_idx, int32_t T, int32_t d_model, int32_t n_kv_proj,
+                          int32_t n_idx_proj, const int32_t* slot_of_token, int64_t num_slots,
+                          int32_t* dev_status, cudaStream_t stream) {
+  if (T < 0 || d_model <= 0 || n_kv_proj < 0 || n_idx_proj < 0 || num_slots < 0)
+    return CSA2_ERR_INVALID_ARGUMENT;
+  if (n_kv_proj + n_idx_proj == 0 || T == 0) return CSA2_OK;
+  if (!H || !Wt || !slot_of_token) return CSA2_ERR_INVALID_ARGUMENT;
+  if (n_kv_proj > 0 && (!codes || !scales)) return CSA2_ERR_INVALID_ARGUMENT;
+  if (n_idx_proj > 0 && !k_idx) return CSA2_ERR_INVALID_ARGUMENT;
+  if (!al16(H) || !al16(Wt) || (codes && (reinterpret_cast<uintptr_t>(codes) & 7u)) ||
+      (k_idx && !al16(k_idx)))
+    return CSA2_ERR_INVALID_ARGUMENT;
+  if (T % 128 != 0 || d_model % 64 != 0) return CSA2_ERR_UNSUPPORTED;
+  return from_cuda(launch_kv_write(H, Wt, codes, scales, k_idx, T, d_model, n_kv_proj, n_idx_proj,
+                                   slot_of_token, num_slots, dev_status, stream, device_sms()));
+}
+
+csa2_status csa2_read_status(int32_t* dev_status, int32_t* host_bits, cudaStream_t stream) {
+  if (dev_status == nullptr) return CSA2_ERR_INVALID_ARGUMENT;
+  int32_t bits = 0;
+  cudaError_t e = cudaMemcpyAsync(&bits, dev_status, sizeof(int32_t), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dev_status, 0, sizeof(int32_t), stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (host_bits) *host_bits = bits;
+  if (bits & CSA2_DEV_TIMEOUT) return CSA2_ERR_TIMEOUT;
+  if (bits) return CSA2_ERR_DEVICE_FAULT;
+  return CSA2_OK;
+}
+
+}  // extern "C"

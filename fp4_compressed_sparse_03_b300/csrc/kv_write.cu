@@ -1,0 +1,416 @@
+// CED write path: C = H . W on the 5th-generation tensor cores, quantised on write.
+//
+// Tech-report digest (jiwasawa.github.io), section "Causal Encoder-Decoder (CED)
+// アーキテクチャ", equation C_l = H_{L/2} W_l^KV: every decoder layer's global KV is
+// a projection of the encoder's final hidden state.  ai2.x.ezic.info blog, section
+// "KVを捨てる、共有する、作り直す": the KV is held as FP4 E2M1 with one E4M3 scale per
+// 16 channels.
+//
+// Kernel design (sm_103a):
+//   - persistent CTAs, one per SM, 128 x 256 output tiles (bf16 operands, fp32
+//     accumulation), K consumed in 64-wide blocks through a 4-stage TMA ring
+//     (128-byte swizzle, both operands K-major);
+//   - warp 0 lane 0 issues TMA, warp 1 lane 0 issues tcgen05.mma (M=128, N=256, K=16)
+//     into one of two TMEM accumulators (2 x 256 columns), warps 2..5 run the epilogue
+//     of the previous tile while the next one accumulates;
+//   - epilogue: tcgen05.ld 32 columns of one row per thread, then per 16-channel block
+//     amax -> E4M3(amax/6) -> E2M1(x/s) packed codes + scale byte (latent
+//     projections), or bf16 RNE (indexer-key projections), stored at the token's slot;
+//   - tile order: groups of 16 M-tiles swept across all N-tiles, so the A tiles of a
+//     group stay in L2 while the B slices stream;
+//   - every mbarrier wait is bounded; on expiry the CTA raises CSA2_DEV_TIMEOUT, stops
+//     issuing, waits (bounded) for its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace csa2 {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;            // 16 KB
+constexpr int B_BYTES = BN * BK * 2;            // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
+constexpr int kThreads = 192;                   // 6 warps
+constexpr int kGroupM = 16;
+constexpr int kTmemCols = 512;
+
+struct Bars {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t fin;
+  uint32_t tmem_base;
+  volatile int abort;
+};
+
+__device__ __forceinline__ uint32_t saddr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(saddr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait.  Returns false (and flags the CTA) when the limit expires or another
+// role of the CTA already gave up.
+__device__ __forceinline__ bool mbar_wait(Bars* bars, uint64_t* b, uint32_t parity, int32_t* st,
+                                          uint32_t limit = kSpinLimit) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (mbar_try(b, parity)) return true;
+    if ((i & 1023u) == 1023u && bars->abort) return false;
+  }
+  bars->abort = 1;
+  report(st, CSA2_DEV_TIMEOUT);
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, uint64_t* bar, int x,
+                                            int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(saddr(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(saddr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(const void* p) {
+  const uint64_t addr = saddr(p);
+  uint64_t d = 0;
+  d |= (addr & 0x3FFFFull) >> 4;      // start address, bits 0-13
+  d |= (uint64_t)1 << 16;             // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset: next 8-row group
+  d |= (uint64_t)1 << 46;             // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;             // swizzle mode: 128 B
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major.
+__device__ __forceinline__ uint32_t idesc_bf16(int m, int n) {
+  uint32_t d = 0;
+  d |= 1u << 4;                      // D format: f32
+  d |= 1u << 7;                      // A format: bf16
+  d |= 1u << 10;                     // B format: bf16
+  d |= (uint32_t)(n >> 3) << 17;     // N / 8
+  d |= (uint32_t)(m >> 4) << 24;     // M / 16
+  return d;
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+struct WriteParams {
+  uint8_t* codes;
+  uint8_t* scales;
+  uint16_t* k_idx;
+  const int32_t* slot_of_token;
+  int64_t num_slots;
+  int32_t T, d_model, n_kv_proj, n_idx_proj, n_out;
+  int32_t* st;
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& m, int& n) {
+  const int per_group = kGroupM * num_n;
+  const int grp = tile / per_group;
+  const int first_m = grp * kGroupM;
+  const int gm = min(kGroupM, num_m - first_m);
+  const int r = tile - grp * per_group;
+  n = r / gm;
+  m = first_m + (r - n * gm);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    kv_write_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    WriteParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* base =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(base + STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&bars->tfull[a], 1);
+      mbar_init(&bars->tempty[a], 128);
+    }
+    mbar_init(&bars->fin, 1);
+    bars->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     saddr(&bars->tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  const int num_m = p.T / BM;
+  const int num_n = (p.n_out + BN - 1) / BN;
+  const int num_tiles = num_m * num_n;
+  const int kblocks = p.d_model / BK;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    uint32_t issued_mask = 0, last_par = 0;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      int m, n;
+      tile_coords(tile, num_m, num_n, m, n);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait(bars, &bars->empty[stage], phase ^ 1u, p.st)) {
+          ok = false;
+          break;
+        }
+        unsigned char* sa = base + stage * STAGE_BYTES;
+        mbar_expect_tx(&bars->full[stage], STAGE_BYTES);
+        tma_load_2d(sa, &tmA, &bars->full[stage], kb * BK, m * BM);
+        tma_load_2d(sa + A_BYTES, &tmB, &bars->full[stage], kb * BK, n * BN);
+        issued_mask |= 1u << stage;
+        last_par = (last_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // make sure no copy of ours is still landing in shared memory
+    for (int s = 0; s < STAGES; ++s)
+      if (issued_mask & (1u << s))
+        (void)mbar_wait(bars, &bars->full[s], (last_par >> s) & 1u, p.st, 1u << 20);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    const uint32_t idesc = idesc_bf16(BM, BN);
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      if (!mbar_wait(bars, &bars->tempty[acc], acc_phase ^ 1u, p.st)) break;
+      fence_after();
+      const uint32_t d = tmem + (uint32_t)(acc * BN);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait(bars, &bars->full[stage], phase, p.st)) {
+          ok = false;
+          break;
+        }
+        fence_after();
+        const unsigned char* sa = base + stage * STAGE_BYTES;
+        const uint64_t adesc = sw128_desc(sa), bdesc = sw128_desc(sa + A_BYTES);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)
+          umma_bf16(d, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc,
+                    (kb > 0 || k > 0) ? 1u : 0u);
+        umma_commit(&bars->empty[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      umma_commit(&bars->tfull[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    // wait until every MMA this thread issued has completed
+    umma_commit(&bars->fin);
+    (void)mbar_wait(bars, &bars->fin, 0, p.st, 1u << 20);
+  } else if (warp >= 2) {
+    // ---------------- epilogue: 128 threads, one output row each ----------------
+    const int quad = warp & 3;              // TMEM lanes 32*quad .. 32*quad+31
+    const int row = 32 * quad + lane;
+    const int kv_cols = p.n_kv_proj * kDkv;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      int m, n;
+      tile_coords(tile, num_m, num_n, m, n);
+      if (!mbar_wait(bars, &bars->tfull[acc], acc_phase, p.st)) break;
+      fence_after();
+      const int t = m * BM + row;
+      const int32_t slot = __ldg(p.slot_of_token + t);
+      const bool slot_ok = slot >= 0 && slot < p.num_slots;
+      if (!slot_ok) report(p.st, CSA2_DEV_BAD_SLOT);
+      const uint32_t tbase = tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(acc * BN);
+      uint32_t sc[4] = {0, 0, 0, 0};
+      const int col0 = n * BN;
+      const bool kv_tile = col0 < kv_cols;
+#pragma unroll 1
+      for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t r[32];
+        tmem_ld32(tbase + (uint32_t)(32 * ch), r);
+        const int col = col0 + 32 * ch;
+        if (!slot_ok || col >= p.n_out) continue;
+        if (kv_tile) {
+          const int proj = col / kDkv, c = col - proj * kDkv;
+          uint32_t w[4];
+          uint32_t s2 = 0;
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(r[16 * g + i]);
+            const uint32_t sb = quantize16(x, w[2 * g], w[2 * g + 1]);
+            s2 |= sb << (8 * g);
+          }
+          uint8_t* crow = p.codes + ((int64_t)proj * p.num_slots + slot) * kCodeRow + c / 2;
+          *reinterpret_cast<uint4*>(crow) = make_uint4(w[0], w[1], w[2], w[3]);
+          const int sidx = (c / kGroup) & 15;  // position of this pair within the 16-scale run
+          sc[sidx >> 2] |= s2 << (8 * (sidx & 3));
+        } else {
+          const int ic = col - kv_cols;
+          const int proj = ic / kDidx, c = ic - proj * kDidx;
+          uint32_t h[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            h[i] = f32_to_bf16_rn(__uint_as_float(r[2 * i])) |
+                   (f32_to_bf16_rn(__uint_as_float(r[2 * i + 1])) << 16);
+          uint4* krow = reinterpret_cast<uint4*>(
+              p.k_idx + ((int64_t)proj * p.num_slots + slot) * kDidx + c);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) krow[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+        }
+      }
+      if (kv_tile && slot_ok) {
+        const int proj = col0 / kDkv, c = col0 - proj * kDkv;
+        *reinterpret_cast<uint4*>(p.scales + ((int64_t)proj * p.num_slots + slot) * kScaleRow +
+                                  c / kGroup) = make_uint4(sc[0], sc[1], sc[2], sc[3]);
+      }
+      fence_before();
+      mbar_arrive(&bars->tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap* tm, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t kv_write_smem_bytes() { return (size_t)STAGES * STAGE_BYTES + sizeof(Bars) + 1024; }
+
+cudaError_t launch_kv_write(const uint16_t* H, const uint16_t* Wt, uint8_t* codes, uint8_t* scales,
+                            uint16_t* k_idx, int32_t T, int32_t d_model, int32_t n_kv_proj,
+                            int32_t n_idx_proj, const int32_t* slot_of_token, int64_t num_slots,
+                            int32_t* st, cudaStream_t s, int num_sms) {
+  const int32_t n_out = n_kv_proj * kDkv + n_idx_proj * kDidx;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, H, T, d_model, BM) || !make_map(&tb, Wt, n_out, d_model, BN))
+    return cudaErrorInvalidValue;
+  WriteParams p{codes, scales, k_idx, slot_of_token, num_slots, T, d_model, n_kv_proj, n_idx_proj,
+                n_out, st};
+  const size_t smem = kv_write_smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(kv_write_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  const int tiles = (T / BM) * ((n_out + BN - 1) / BN);
+  const int grid = std::max(1, std::min(tiles, num_sms));
+  kv_write_kernel<<<grid, kThreads, smem, s>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

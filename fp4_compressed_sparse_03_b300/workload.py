@@ -1,0 +1,85 @@
+"""Synthetic decode / write workloads placed in HBM.
+
+The random values come from the seeded counter-based generator of ``csa2_inputs``
+(device kernels, bit-identical to its host definition); the latent is quantised into
+the paged pools by libcsa2's own codec (csa2_quantize), exactly as a serving system
+would fill its cache.  Everything here runs before any timed region.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import csa2_inputs as gen
+from csa2_inputs import native
+
+from . import check, csa2_quantize
+from .decode import DecodeCache
+
+_CHUNK = 1 << 18  # latent rows staged per quantise call (512 MB of fp32)
+
+
+def fill_decode_cache(wl: gen.DecodeWorkload, n_groups: int | None = None, device="cuda",
+                      stream=None) -> DecodeCache:
+    """A DecodeCache holding every Full group's quantised latent and indexer keys."""
+    if n_groups is None:
+        n_groups = max(1, sum(1 for m in wl.schedule if m == gen.FULL))
+    lay = wl.layout
+    cache = DecodeCache(lay.seq_lens, lay.page_table, lay.num_pages, n_groups, device)
+    B = len(lay.seq_lens)
+    max_len = int(lay.seq_lens.max()) if B else 0
+    stage = torch.empty((min(_CHUNK, max(max_len, 1)), gen.D_KV), dtype=torch.float32,
+                        device=cache.device)
+    for g in range(n_groups):
+        skeys = torch.as_tensor(native.seq_keys(wl.seed, gen.TAG_KEY, g, B).view(np.int64),
+                                device=cache.device)
+        native.fill_keys_paged_dev(cache.keys[g], skeys, cache.seq_lens, cache.page_table, stream)
+        gains = torch.as_tensor(gen.latent_gains(wl.seed, g), device=cache.device)
+        for b in range(B):
+            n_b = int(lay.seq_lens[b])
+            key = gen.stream_key(wl.seed, gen.TAG_LATENT, (g << 24) | b)
+            for t0 in range(0, n_b, _CHUNK):
+                n = min(_CHUNK, n_b - t0)
+                native.fill_latent_dev(stage[:n], key, t0, gains, stream)
+                slots = torch.as_tensor(lay.slots(b, np.arange(t0, t0 + n)).astype(np.int32),
+                                        device=cache.device)
+                check(csa2_quantize(stage[:n], slots, cache.codes[g], cache.scales[g], n, gen.D_KV,
+                                    cache.num_slots, None, stream), "csa2_quantize")
+    torch.cuda.synchronize()
+    return cache
+
+
+def layer_queries_host(wl: gen.DecodeWorkload, layer: int):
+    """(q_idx bf16 bits [num_q, 4, 128], q bf16 bits [num_q, 16, 512]) of one layer."""
+    nq = wl.num_q
+    q_idx = np.empty((nq, gen.H_IDX, gen.D_IDX), np.uint16)
+    q = np.empty((nq, gen.H_Q, gen.D_KV), np.uint16)
+    for i in range(nq):
+        kq = gen.stream_key(wl.seed, gen.TAG_QIDX, (layer << 24) | i)
+        q_idx[i] = native.normal_bf16_host(kq, 0, gen.H_IDX * gen.D_IDX).reshape(gen.H_IDX, gen.D_IDX)
+        ka = gen.stream_key(wl.seed, gen.TAG_Q, (layer << 24) | i)
+        q[i] = native.normal_bf16_host(ka, 0, gen.H_Q * gen.D_KV).reshape(gen.H_Q, gen.D_KV)
+    return q_idx, q
+
+
+def all_queries_host(wl: gen.DecodeWorkload):
+    """Stacked per-layer queries: q_idx [L, num_q, 4, 128], q [L, num_q, 16, 512] (bf16 bits)."""
+    qs = [layer_queries_host(wl, l) for l in range(len(wl.schedule))]
+    return np.stack([a for a, _ in qs]), np.stack([b for _, b in qs])
+
+
+def fill_write_inputs(ww: gen.WriteWorkload, device="cuda", stream=None):
+    """(H [T, d] bf16 bits, Wt [n_out, d] bf16 bits, slot_of_token [T]) on the device."""
+    dev = torch.device(device)
+    H = torch.empty((ww.T, ww.d_model), dtype=torch.int16, device=dev)
+    native.fill_bf16_dev(H, gen.stream_key(ww.seed, gen.TAG_H), 0, 0, stream)
+    Wt = torch.empty((ww.n_out, ww.d_model), dtype=torch.int16, device=dev)
+    p2 = gen.d_model_pow2_scale(ww.d_model)
+    kv = ww.n_kv_proj * gen.D_KV
+    if kv:
+        native.fill_bf16_dev(Wt[:kv], gen.stream_key(ww.seed, gen.TAG_WKV), 0, p2, stream)
+    if ww.n_out > kv:
+        native.fill_bf16_dev(Wt[kv:], gen.stream_key(ww.seed, gen.TAG_WIDX), 0, p2, stream)
+    slots = torch.as_tensor(ww.slot_of_token(), device=dev)
+    torch.cuda.synchronize()
+    return H, Wt, slots

@@ -1,0 +1,216 @@
+/*
+ * libcsa2 — C ABI of the CSA2 FP4 compressed global KV cache on B300 (sm_103a).
+ *
+ * The library implements the three data-parallel steps of the compressed global KV
+ * cache of a CED/CSA2 decoder as described for DeepSeek-V4.1-Flash:
+ *   - the write path: the CED projection C_l = H_{L/2} W_l^KV (tech-report digest,
+ *     jiwasawa.github.io, section "Causal Encoder-Decoder (CED) アーキテクチャ",
+ *     the equation there), quantised on write to FP4 E2M1 with one E4M3 scale per
+ *     16 channels (ai2.x.ezic.info blog, section "KVを捨てる、共有する、作り直す");
+ *   - the CSA2 indexer in Full, Reindex and Reuse modes with the hierarchical
+ *     candidate pool (digest, section "Compressed Sparse Attention 2 (CSA2) による
+ *     極限のKV cache圧縮"; zaikei.co.jp article, section "CSA2とFP4でキャッシュを圧縮");
+ *   - the read path: gather + dequantise + sparse attention over the selected
+ *     entries (zaikei article, same section: the cache is dequantised before
+ *     attention; digest, "Reuse Mode").
+ *
+ * Conventions for every call:
+ *   - All data pointers are DEVICE pointers unless a parameter says "host".
+ *     bf16 values are passed as raw 16-bit patterns (uint16_t).
+ *   - The caller owns every buffer.  Except where a function says otherwise, the
+ *     library allocates no device memory; scratch is passed in as `workspace`,
+ *     sized by the *_workspace_size queries.
+ *   - Calls are asynchronous and ordered on `stream`.  The library keeps no state
+ *     between calls and may be called from several host threads.
+ *   - Host-detectable errors (null pointers, misalignment, unsupported sizes) return
+ *     at once, before any launch.  Problems found on the device (an index outside
+ *     its sequence, a page id outside the pool, a slot outside the pool, a wait
+ *     that exceeded its limit) never abort a kernel: the offending entry is skipped
+ *     and a CSA2_DEV_* bit is OR-ed into *dev_status (a device int32 the caller
+ *     zeroes once and reads with csa2_read_status).  dev_status may be NULL, in
+ *     which case such problems go unreported.
+ *   - No call traps, asserts on the device, or throws across the ABI.
+ *
+ * Fixed geometry (checked, CSA2_ERR_UNSUPPORTED otherwise): latent width 512,
+ * 16 channels per scale, indexer head dim 128 with 4 heads, 16 attention query
+ * heads over the shared latent (MQA, head dim 512), 64 tokens per page.
+ *
+ * Layouts in HBM (one pool per Full-layer group; slot = page_id * 64 + token % 64):
+ *   codes   uint8  [num_pages * 64][256]   E2M1 pairs, channel 2j in the low nibble
+ *                                          of byte j, 2j+1 in the high nibble
+ *   scales  uint8  [num_pages * 64][32]    E4M3 (OCP E4M3FN) bytes, one per 16 channels
+ *   k_idx   bf16   [num_pages * 64][128]   indexer keys
+ */
+#ifndef CSA2_H
+#define CSA2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* cudaStream_t; /* same opaque type as the CUDA runtime's */
+
+#if defined(__GNUC__)
+#define CSA2_API __attribute__((visibility("default")))
+#else
+#define CSA2_API
+#endif
+
+typedef enum {
+  CSA2_OK = 0,
+  CSA2_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad size, misaligned buffer      */
+  CSA2_ERR_UNSUPPORTED = 2,      /* a geometry this build does not implement        */
+  CSA2_ERR_CUDA = 3,             /* a CUDA runtime call or launch failed            */
+  CSA2_ERR_DEVICE_FAULT = 4,     /* csa2_read_status: a CSA2_DEV_* fault bit was set */
+  CSA2_ERR_TIMEOUT = 5           /* csa2_read_status: a bounded device wait expired */
+} csa2_status;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define CSA2_DEV_BAD_INDEX 0x1 /* selected index outside [-1, seq_len) or pool entry out of range */
+#define CSA2_DEV_BAD_PAGE 0x2  /* page-table entry outside [0, num_pages)                        */
+#define CSA2_DEV_BAD_SLOT 0x4  /* write slot outside [0, num_slots)                              */
+#define CSA2_DEV_TIMEOUT 0x8   /* a bounded wait (mbarrier) exceeded its iteration limit          */
+#define CSA2_DEV_BAD_QSEQ 0x10 /* q_seq entry outside [0, num_seqs) or not non-decreasing         */
+
+/* CSA2 layer modes (digest, section "CSA2": each layer is statically assigned one). */
+typedef enum {
+  CSA2_FULL = 0,    /* score every context token with this layer's indexer query; new top-K
+                       and (optionally) the hierarchical candidate pool                    */
+  CSA2_REINDEX = 1, /* re-score only the pool of the most recent Full layer, with that
+                       layer's keys and this layer's query; new top-K                        */
+  CSA2_REUSE = 2    /* inherit the indices of the most recent Full/Reindex layer            */
+} csa2_mode;
+
+/* Paged cache geometry.  All pointers are device pointers. */
+typedef struct {
+  int32_t num_seqs;          /* B                                                       */
+  const int32_t* seq_lens;   /* [B] context tokens per sequence (>= 0)                   */
+  const int32_t* page_table; /* [B][max_pages_per_seq] physical page id of logical page  */
+  int32_t max_pages_per_seq; /* row length of page_table                                 */
+  int32_t num_pages;         /* physical pages in each pool                              */
+  int32_t page_size;         /* tokens per page; must be 64                              */
+} csa2_pages;
+
+/* Per-call indexer arguments. */
+typedef struct {
+  int32_t num_q;             /* query tokens in the batch                                */
+  const int32_t* q_seq;      /* [num_q] sequence of each query, non-decreasing (device)  */
+  int32_t max_q_per_seq;     /* host bound on queries per sequence, 1..4; > 1 selects the
+                                tensor-core batched scoring of speculative draft tokens   */
+  int32_t pool_size;         /* P: FULL writes top-min(P, N) into `pool` when pool != NULL;
+                                REINDEX reads P entries per query from `pool`             */
+  const int32_t* inherit_idx;/* REUSE: [num_q][topk] indices to inherit                   */
+  void* workspace;           /* scratch, >= csa2_index_workspace_size() bytes, 256-B aligned */
+  size_t workspace_bytes;
+  int32_t* dev_status;       /* device int32 status word, may be NULL                    */
+} csa2_index_args;
+
+/* ------------------------------------------------------------------ write path ----
+ * CED projection + quantise on write (digest, "Causal Encoder-Decoder (CED)": the
+ * decoder's global KV is projected from the encoder's final hidden state,
+ * C_l = H_{L/2} W_l^KV; blog: stored as FP4 E2M1 with an E4M3 scale per 16 channels).
+ *
+ *   H      bf16 [T][d_model]                 encoder final hidden state, row-major
+ *   Wt     bf16 [n_out][d_model]              all projections stacked output-major
+ *          (Wt[n][k] = W[k][n]); n_out = n_kv_proj*512 + n_idx_proj*128, first the
+ *          n_kv_proj latent projections (512 columns each), then the n_idx_proj
+ *          indexer-key projections (128 columns each)
+ *   codes  uint8 [n_kv_proj][num_slots][256] output pools, one per latent projection
+ *   scales uint8 [n_kv_proj][num_slots][32]
+ *   k_idx  bf16  [n_idx_proj][num_slots][128] (may be NULL iff n_idx_proj == 0)
+ *   slot_of_token int32 [T] physical row of each token, in [0, num_slots)
+ *
+ * Arithmetic: C = H.W with fp32 accumulation on the tensor cores; per token and
+ * 16-channel block s = E4M3_RNE_satfinite(amax/6), codes = E2M1_RNE_sat(C/s) (IEEE
+ * division, sign kept, s == 0 gives zero codes); indexer keys = bf16_RNE(C).
+ * Requires T % 128 == 0, d_model % 64 == 0, 16-B aligned H and Wt.  Tokens whose slot
+ * is out of range are skipped (CSA2_DEV_BAD_SLOT).
+ */
+CSA2_API csa2_status csa2_kv_write(const uint16_t* H, const uint16_t* Wt, uint8_t* codes, uint8_t* scales,
+                          uint16_t* k_idx, int32_t T, int32_t d_model, int32_t n_kv_proj,
+                          int32_t n_idx_proj, const int32_t* slot_of_token, int64_t num_slots,
+                          int32_t* dev_status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------ indexer -------
+ * One CSA2 layer's index step (digest, section "CSA2" modes and "Hierarchical Sparse
+ * Indexer").  Score of context token s for a query with indexer heads q_h (bf16
+ * [4][128]): score_s = sum_{h<4} max(0, q_h . k_s), fp32 accumulation.  Positive
+ * per-head weights are folded into q_h by the caller.  Ranking is (score descending,
+ * token ascending).
+ *
+ *   FULL:    scores all N = seq_len tokens of the query's sequence; writes
+ *            out_idx[q][0..K) = top-min(K, N) tokens, ascending, -1 padded, and, when
+ *            pool != NULL and pool_size > 0, pool[q][0..P) = top-min(P, N) likewise.
+ *   REINDEX: reads pool[q][0..P) (ascending, -1 padded, as a FULL call wrote it);
+ *            scores only its valid entries with this layer's q_idx and the k_idx pool
+ *            of the Full layer; out_idx = top-min(K, #valid) of the pool.
+ *   REUSE:   out_idx = inherit_idx (one device copy; nothing if the pointers match).
+ *
+ *   q_idx   bf16 [num_q][4][128]     (unused by REUSE)
+ *   k_idx   bf16 key pool [num_pages*64][128] of the Full layer (unused by REUSE)
+ *   pool    int32 [num_q][pool_size]  FULL: output (nullable); REINDEX: input
+ *   out_idx int32 [num_q][topk]
+ * Workspace: csa2_index_workspace_size(mode, ...) bytes.
+ */
+CSA2_API csa2_status csa2_index(csa2_mode mode, const uint16_t* q_idx, const uint16_t* k_idx, int32_t* pool,
+                       int32_t topk, int32_t* out_idx, const csa2_pages* pages,
+                       const csa2_index_args* args, cudaStream_t stream);
+
+CSA2_API size_t csa2_index_workspace_size(csa2_mode mode, int32_t num_q, int32_t max_pages_per_seq,
+                                 int32_t pool_size);
+
+/* ------------------------------------------------------------------ read path -----
+ * Gather-dequantise sparse attention (zaikei article: the FP4 cache is dequantised
+ * before attention; digest "Reuse Mode": sparse attention over the top-K entries).
+ * MQA over the shared latent: K = V = c_hat_s = e2m1(code) * e4m3(scale) (exact).
+ *   out[q][h] = sum_s softmax_s(softmax_scale * q_h . c_hat_s) c_hat_s
+ *   lse[q][h] = natural-log sum-exp of the scaled logits
+ * over the valid entries s of idx[q] (-1 entries are skipped).  A query with no valid
+ * entry gets out = 0 and lse = -inf.
+ *
+ *   q      bf16 [num_q][16][512]
+ *   codes, scales  the Full layer's pools (layout above)
+ *   idx    int32 [num_q][topk], entries in [-1, seq_len)
+ *   out    fp32 [num_q][16][512];  lse fp32 [num_q][16] (nullable)
+ *   q_seq  int32 [num_q]
+ * Workspace: csa2_attn_workspace_size(num_q, topk) bytes (may be 0).
+ * fp32 online softmax, split over the selected set, merged by log-sum-exp.
+ */
+CSA2_API csa2_status csa2_sparse_attn(const uint16_t* q, const uint8_t* codes, const uint8_t* scales,
+                             const int32_t* idx, const csa2_pages* pages, float* out, float* lse,
+                             int32_t num_q, const int32_t* q_seq, int32_t topk, float softmax_scale,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                             cudaStream_t stream);
+
+CSA2_API size_t csa2_attn_workspace_size(int32_t num_q, int32_t topk);
+
+/* ------------------------------------------------------------------ codec ---------
+ * Standalone quantise / dequantise of latent rows (blog: E2M1 values, one E4M3 scale
+ * per 16 channels).  Same arithmetic as the write path's epilogue.
+ *   x      fp32 [T][D], D % 16 == 0, D <= 4096, 16-B aligned
+ *   slot_of_token int32 [T] destination / source row in [0, num_slots)
+ *   codes  uint8 [num_slots][D/2];  scales uint8 [num_slots][D/16]
+ */
+CSA2_API csa2_status csa2_quantize(const float* x, const int32_t* slot_of_token, uint8_t* codes,
+                          uint8_t* scales, int32_t T, int32_t D, int64_t num_slots,
+                          int32_t* dev_status, cudaStream_t stream);
+CSA2_API csa2_status csa2_dequantize(const uint8_t* codes, const uint8_t* scales,
+                            const int32_t* slot_of_token, float* x, int32_t T, int32_t D,
+                            int64_t num_slots, int32_t* dev_status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------ status --------
+ * Synchronises `stream`, copies *dev_status to *host_bits (host, nullable), resets
+ * the device word to 0 and returns CSA2_ERR_TIMEOUT if CSA2_DEV_TIMEOUT was set,
+ * CSA2_ERR_DEVICE_FAULT if any other bit was set, CSA2_OK otherwise. */
+CSA2_API csa2_status csa2_read_status(int32_t* dev_status, int32_t* host_bits, cudaStream_t stream);
+
+CSA2_API const char* csa2_status_string(csa2_status s);
+CSA2_API int32_t csa2_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA2_H */

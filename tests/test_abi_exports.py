@@ -1,0 +1,59 @@
+"""The C-ABI library loads and exports every symbol the public header declares; the
+host-side argument checks answer before any device work (no GPU needed)."""
+import ctypes
+import os
+import re
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "csa2.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    return re.findall(r"CSA2_API\s+[\w\s\*]+?\b(csa2_\w+)\s*\(", src)
+
+
+def test_header_declares_the_three_calls():
+    names = set(declared_functions())
+    assert {"csa2_kv_write", "csa2_index", "csa2_sparse_attn"} <= names
+    assert len(names) >= 10
+
+
+def test_library_exports_every_declared_symbol():
+    from fp4_compressed_sparse_03_b300 import build
+    lib = ctypes.CDLL(build.build())
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_host_side_checks_without_device():
+    import fp4_compressed_sparse_03_b300 as csa2
+    assert csa2.version() >= 10000
+    assert csa2.status_string(csa2.CSA2_ERR_TIMEOUT).startswith("bounded")
+    L = csa2._lib
+    # null argument blocks are rejected before any CUDA call
+    assert L.csa2_index(0, None, None, None, 16, None, None, None, None) == csa2.CSA2_ERR_INVALID_ARGUMENT
+    assert L.csa2_quantize(None, None, None, None, -1, 512, 0, None, None) == csa2.CSA2_ERR_INVALID_ARGUMENT
+    assert L.csa2_quantize(None, None, None, None, 4, 24, 4, None, None) == csa2.CSA2_ERR_UNSUPPORTED
+    assert L.csa2_kv_write(None, None, None, None, None, 4, 64, 1, 0, None, 4, None, None) == \
+        csa2.CSA2_ERR_INVALID_ARGUMENT
+    assert L.csa2_read_status(None, None, None) == csa2.CSA2_ERR_INVALID_ARGUMENT
+    # workspace sizing is host arithmetic
+    assert csa2.csa2_index_workspace_size(csa2.CSA2_FULL, 64, 2048, 8192) == 64 * 2048 * 64 * 4
+    assert csa2.csa2_index_workspace_size(csa2.CSA2_REINDEX, 64, 2048, 8192) == 64 * 8192 * 4
+    assert csa2.csa2_index_workspace_size(csa2.CSA2_REUSE, 64, 2048, 8192) == 0
+
+
+def test_generator_library_host_path():
+    import numpy as np
+    import csa2_inputs as gen
+    from csa2_inputs import native
+    assert np.array_equal(native.key_rows_host(3, 1, 2, 10, 50), gen.key_rows(3, 1, 2, np.arange(10, 60)))
+    g = gen.latent_gains(3, 1)
+    assert np.array_equal(native.latent_rows_host(3, 1, 2, 5, 20, g),
+                          gen.latent_rows(3, 1, 2, np.arange(5, 25), g))
+
+
+def test_graft_build_entry():
+    import __graft_entry__
+    __graft_entry__.build()

@@ -1,0 +1,340 @@
+"""Decode path parity: CSA2 indexer (Full / Reindex / Reuse, hierarchical pool) and
+FP4 gather-dequantise sparse attention, CUDA path through the C ABI vs the oracle.
+
+Modes: tech-report digest (jiwasawa.github.io), "Compressed Sparse Attention 2 (CSA2)";
+format and dequantisation before attention: zaikei.co.jp article, "CSA2とFP4でキャッシュを
+圧縮".  Index sets must match except for ties within 1e-5 relative; attention outputs
+within 2e-3 x RMS per query."""
+import numpy as np
+import pytest
+import torch
+
+import csa2_inputs as gen
+import fp4_compressed_sparse_03_b300 as csa2
+import oracle
+from csa2_inputs import native
+from fp4_compressed_sparse_03_b300.decode import DecodeCache, DecodeStep
+from fp4_compressed_sparse_03_b300.workload import all_queries_host, fill_decode_cache
+from gpu_common import (SOFTMAX_SCALE, TIE_REL_TOL, assert_attn_close, assert_topk_close, dev,
+                        host)
+
+pytestmark = pytest.mark.gpu
+
+
+# ------------------------------------------------------------------ oracle side ----
+
+class OracleQuery:
+    """The oracle's view of one query token: its sequence's keys per group (regenerated
+    on the host), the per-layer indices and the per-layer attention outputs."""
+
+    def __init__(self, wl: gen.DecodeWorkload, qi: int, q_idx, q):
+        self.wl, self.qi = wl, qi
+        self.b = int(wl.q_seq[qi])
+        self.n = int(wl.seq_lens[self.b])
+        self.groups = wl.groups()
+        self.keys = {}
+        self.idx, self.pool, self.scores, self.full_scores = {}, {}, {}, {}
+        self.q_idx, self.q = q_idx, q
+
+    def keys_of(self, g):
+        if g not in self.keys:
+            self.keys[g] = native.key_rows_host(self.wl.seed, g, self.b, 0, self.n)
+        return self.keys[g]
+
+    def run_index(self):
+        wl = self.wl
+        src = wl.index_source()
+        for l, m in enumerate(wl.schedule):
+            g = self.groups[l]
+            if m == gen.FULL:
+                s = oracle.index_scores(self.q_idx[l][self.qi], self.keys_of(g))
+                tok = np.arange(self.n, dtype=np.int32)
+                self.idx[l] = oracle.select_topk(s, tok, wl.topk)
+                self.pool[g] = oracle.select_topk(s, tok, wl.pool_size) if wl.pool_size else None
+                self.scores[l] = s
+            elif m == gen.REINDEX:
+                self.idx[l], _ = oracle.index_reindex(self.q_idx[l][self.qi], self.keys_of(g),
+                                                      self.pool[g], wl.topk)
+                self.scores[l] = oracle.index_scores(self.q_idx[l][self.qi], self.keys_of(g))
+            else:
+                self.idx[l] = oracle.index_reuse(self.idx[src[l]])
+
+    def attention(self, l):
+        g = self.groups[l]
+        sel = self.idx[self.wl.index_source()[l]]
+        sel = sel[sel >= 0]
+        gains = gen.latent_gains(self.wl.seed, g)
+        x = gen.latent_rows(self.wl.seed, g, self.b, sel, gains)
+        codes, scales = oracle.quantize(x)
+        chat = oracle.dequantize(codes, scales)
+        return oracle.sparse_attention(self.q[l][self.qi], chat, SOFTMAX_SCALE)
+
+
+def _near(v, ref):
+    return abs(v - ref) <= TIE_REL_TOL * max(1.0, abs(ref))
+
+
+def check_query(wl, step: DecodeStep, oq: OracleQuery, attn_budget=None):
+    """Compare one query's indices (every layer) and attention outputs."""
+    qi = oq.qi
+    src = wl.index_source()
+    same_src = {}
+    for l, m in enumerate(wl.schedule):
+        g = oq.groups[l]
+        got = host(step.indices(l)[qi])
+        if m == gen.FULL:
+            s = oq.scores[l]
+            assert_topk_close(got, oq.idx[l], lambda t: s[t], f"q{qi} L{l} full idx")
+            if step.use_pool:
+                gp = host(step.pool[g][qi])
+                assert_topk_close(gp, oq.pool[g], lambda t: s[t], f"q{qi} L{l} pool")
+                oq.gpu_pool = gp
+            same_src[l] = set(got[got >= 0]) == set(oq.idx[l][oq.idx[l] >= 0])
+        elif m == gen.REINDEX:
+            s1 = oq.scores[l]
+            s0 = oq.scores[max(k for k in range(l) if wl.schedule[k] == gen.FULL)]
+            gp = oq.gpu_pool
+            gpool, opool = set(gp[gp >= 0]), set(oq.pool[g][oq.pool[g] >= 0])
+            gset, oset = set(got[got >= 0]), set(oq.idx[l][oq.idx[l] >= 0])
+            assert gset <= gpool, f"q{qi} L{l}: reindex output outside the pool"
+            if gpool == opool:
+                assert_topk_close(got, oq.idx[l], lambda t: s1[t], f"q{qi} L{l} reindex")
+            else:
+                kth = min(s1[t] for t in oset) if oset else 0.0
+                p_kth = min(s0[t] for t in opool) if opool else 0.0
+                for t in gset ^ oset:
+                    assert _near(s1[t], kth) or (
+                        (t not in opool or t not in gpool) and _near(s0[t], p_kth)), \
+                        f"q{qi} L{l}: reindex token {t}"
+            same_src[l] = gset == oset
+        else:
+            assert np.array_equal(got, host(step.indices(src[l])[qi]))
+    compared = 0
+    for l in range(len(wl.schedule)):
+        if attn_budget is not None and compared >= attn_budget:
+            break
+        if not same_src[src[l]]:
+            continue
+        out_o, lse_o = oq.attention(l)
+        assert_attn_close(host(step.out[l][qi]), out_o, host(step.lse[l][qi]), lse_o,
+                          f"q{qi} L{l} attention")
+        compared += 1
+    return compared
+
+
+def run_workload(wl, max_q_per_seq=None, n_groups=None):
+    cache = fill_decode_cache(wl, n_groups)
+    q_idx, q = all_queries_host(wl)
+    mq = int(wl.q_per_seq.max()) if max_q_per_seq is None else max_q_per_seq
+    step = DecodeStep(cache, wl.q_seq, wl.schedule, wl.pool_size, wl.topk, mq)
+    step.run(dev(q_idx), dev(q))
+    torch.cuda.synchronize()
+    status, bits = csa2.csa2_read_status(step.dev_status)
+    assert status == csa2.CSA2_OK, bits
+    return cache, step, q_idx, q
+
+
+def check_sampled(wl, queries, step, q_idx, q, attn_budget=None, min_attn=1):
+    total = 0
+    for qi in queries:
+        oq = OracleQuery(wl, int(qi), q_idx, q)
+        oq.run_index()
+        total += check_query(wl, step, oq, attn_budget)
+    assert total >= min_attn
+
+
+# ------------------------------------------------------------------ generator ------
+
+def test_device_generator_matches_host_definition():
+    key = gen.stream_key(5, gen.TAG_KEY, 3)
+    a = torch.empty(10000, dtype=torch.int16, device="cuda")
+    native.fill_bf16_dev(a, key, 777, -6)
+    torch.cuda.synchronize()
+    want = gen.normal_bf16(key, np.arange(777, 10777), pow2=-6)
+    assert np.array_equal(host(a).view(np.uint16), want)
+    gains = gen.latent_gains(5)
+    x = torch.empty((300, 512), dtype=torch.float32, device="cuda")
+    native.fill_latent_dev(x, gen.stream_key(5, gen.TAG_LATENT, 9), 40, dev(gains))
+    torch.cuda.synchronize()
+    assert np.array_equal(host(x), gen.latent_rows(5, 0, 9, np.arange(40, 340), gains))
+    wl = gen.DecodeWorkload("t", 5, np.array([200, 64, 1], np.int32), np.ones(3, np.int32),
+                            [gen.FULL], 0, 16)
+    cache = fill_decode_cache(wl)
+    keys = host(cache.keys[0]).view(np.uint16)
+    for b in range(3):
+        n = int(wl.seq_lens[b])
+        slots = wl.layout.slots(b, np.arange(n))
+        assert np.array_equal(keys[slots], gen.key_rows(5, 0, b, np.arange(n)))
+
+
+# ------------------------------------------------------------------ small cases ----
+
+def test_tiny_full_layer():
+    """1 sequence x 4096 tokens, identity pages, one Full layer, top-K 256."""
+    wl = gen.config_tiny(0)
+    _, step, q_idx, q = run_workload(wl)
+    check_sampled(wl, [0], step, q_idx, q)
+
+
+@pytest.mark.parametrize("drafts", [False, True])
+def test_small_ragged_all_modes(drafts):
+    """Ragged lengths (N < K, N = 1, partial pages), shuffled pages, F->Ri->Ru->Ru with
+    a pool; with drafts, several queries per sequence go through the batched scorer."""
+    lens = np.array([5000, 64, 1, 300, 2113, 130], np.int32)
+    qps = np.array([3, 1, 2, 4, 1, 2], np.int32) if drafts else np.ones(6, np.int32)
+    wl = gen.DecodeWorkload("small", 11 + drafts, lens, qps,
+                            [gen.FULL, gen.REINDEX, gen.REUSE, gen.REUSE], pool_size=512, topk=128)
+    _, step, q_idx, q = run_workload(wl)
+    check_sampled(wl, range(wl.num_q), step, q_idx, q, min_attn=wl.num_q)
+
+
+def test_two_groups_pool_larger_than_context():
+    lens = np.array([700, 3000], np.int32)
+    wl = gen.DecodeWorkload("groups", 17, lens, np.ones(2, np.int32),
+                            [gen.FULL, gen.REINDEX, gen.FULL, gen.REINDEX, gen.REUSE],
+                            pool_size=1024, topk=256)
+    _, step, q_idx, q = run_workload(wl)
+    check_sampled(wl, range(2), step, q_idx, q)
+
+
+def test_attention_random_index_sets():
+    """Attention alone on seeded random selections (with -1 padding and an empty set),
+    single- and multi-split launches."""
+    lens = np.array([3000, 100, 5000], np.int32)
+    wl = gen.DecodeWorkload("attn", 23, lens, np.ones(3, np.int32), [gen.FULL], 0, 16)
+    cache = fill_decode_cache(wl)
+    for topk, nq in [(256, 3), (2048, 3), (64, 3)]:
+        q_seq = np.array([0, 1, 2][:nq], np.int32)
+        idx = np.stack([gen.random_index_set(23, 100 * topk + i, int(lens[b]), topk,
+                                             n_invalid=(7 if i == 0 else 0))
+                        for i, b in enumerate(q_seq)])
+        if topk == 64:
+            idx[1] = -1
+        q = np.stack([gen.q_rows(23, topk, np.array([i]))[0] for i in range(nq)])
+        out = torch.zeros((nq, 16, 512), dtype=torch.float32, device="cuda")
+        lse = torch.zeros((nq, 16), dtype=torch.float32, device="cuda")
+        ws = torch.empty(max(csa2.csa2_attn_workspace_size(nq, topk), 16), dtype=torch.uint8,
+                         device="cuda")
+        csa2.check(csa2.csa2_sparse_attn(dev(q), cache.codes[0], cache.scales[0], dev(idx),
+                                         cache.pages, out, lse, nq, dev(q_seq), topk,
+                                         SOFTMAX_SCALE, ws), "attn")
+        for i, b in enumerate(q_seq):
+            sel = idx[i][idx[i] >= 0]
+            x = gen.latent_rows(23, 0, int(b), sel, gen.latent_gains(23))
+            c, s = oracle.quantize(x)
+            o, l = oracle.sparse_attention(q[i], oracle.dequantize(c, s), SOFTMAX_SCALE)
+            if sel.size == 0:
+                assert np.all(host(out[i]) == 0) and np.all(np.isneginf(host(lse[i])))
+            else:
+                assert_attn_close(host(out[i]), o, host(lse[i]), l, f"topk {topk} q{i}")
+
+
+def test_attention_dense_equals_all_tokens():
+    """K = N: the sparse path over every token equals the oracle's dense attention."""
+    wl = gen.DecodeWorkload("dense", 29, np.array([512], np.int32), np.ones(1, np.int32),
+                            [gen.FULL], 0, 512)
+    cache = fill_decode_cache(wl)
+    idx = np.arange(512, dtype=np.int32).reshape(1, 512)
+    q = gen.q_rows(29, 0, np.array([0]))
+    out = torch.zeros((1, 16, 512), dtype=torch.float32, device="cuda")
+    lse = torch.zeros((1, 16), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(csa2.csa2_attn_workspace_size(1, 512), 16), dtype=torch.uint8, device="cuda")
+    csa2.check(csa2.csa2_sparse_attn(dev(q), cache.codes[0], cache.scales[0], dev(idx), cache.pages,
+                                     out, lse, 1, dev(np.zeros(1, np.int32)), 512, SOFTMAX_SCALE, ws),
+               "attn")
+    x = gen.latent_rows(29, 0, 0, np.arange(512), gen.latent_gains(29))
+    c, s = oracle.quantize(x)
+    o, l = oracle.sparse_attention(q[0], oracle.dequantize(c, s), SOFTMAX_SCALE)
+    assert_attn_close(host(out[0]), o, host(lse[0]), l, "dense")
+
+
+def test_page_shuffle_invariance():
+    """The same logical cache under two physical page permutations gives bitwise equal
+    indices and outputs."""
+    lens = np.array([4000, 2500], np.int32)
+    res = []
+    for shuffle_seed in (101, 202):
+        wl = gen.DecodeWorkload("perm", 31, lens, np.ones(2, np.int32),
+                                [gen.FULL, gen.REINDEX, gen.REUSE], 512, 128)
+        wl.layout = gen.make_layout(shuffle_seed, lens, True)
+        _, step, _, _ = run_workload(wl)
+        res.append((host(step.idx), host(step.out), host(step.lse)))
+    assert np.array_equal(res[0][0], res[1][0])
+    assert np.array_equal(res[0][1], res[1][1]) and np.array_equal(res[0][2], res[1][2])
+
+
+def test_bad_indices_are_reported_and_skipped():
+    lens = np.array([1000], np.int32)
+    wl = gen.DecodeWorkload("bad", 37, lens, np.ones(1, np.int32), [gen.FULL], 0, 16)
+    cache = fill_decode_cache(wl)
+    idx = np.array([[3, 17, 999, 1000, 5000, -5, -1, 40]], np.int32)
+    q = gen.q_rows(37, 0, np.array([0]))
+    out = torch.zeros((1, 16, 512), dtype=torch.float32, device="cuda")
+    lse = torch.zeros((1, 16), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(csa2.csa2_attn_workspace_size(1, 8), 16), dtype=torch.uint8, device="cuda")
+    csa2.check(csa2.csa2_sparse_attn(dev(q), cache.codes[0], cache.scales[0], dev(idx), cache.pages,
+                                     out, lse, 1, dev(np.zeros(1, np.int32)), 8, SOFTMAX_SCALE, ws,
+                                     None, st), "attn")
+    status, bits = csa2.csa2_read_status(st)
+    assert status == csa2.CSA2_ERR_DEVICE_FAULT and bits & csa2.CSA2_DEV_BAD_INDEX
+    sel = np.array([3, 17, 999, 40])
+    x = gen.latent_rows(37, 0, 0, sel, gen.latent_gains(37))
+    c, s = oracle.quantize(x)
+    o, l = oracle.sparse_attention(q[0], oracle.dequantize(c, s), SOFTMAX_SCALE)
+    assert_attn_close(host(out[0]), o, host(lse[0]), l, "bad idx skipped")
+
+
+def test_index_host_argument_errors():
+    lens = np.array([100], np.int32)
+    wl = gen.DecodeWorkload("err", 41, lens, np.ones(1, np.int32), [gen.FULL], 0, 16)
+    cache = fill_decode_cache(wl)
+    qs = dev(np.zeros(1, np.int32))
+    out = torch.zeros((1, 16), dtype=torch.int32, device="cuda")
+    q_idx = dev(gen.q_idx_rows(41, 0, np.array([0])))
+    ws = torch.empty(csa2.csa2_index_workspace_size(csa2.CSA2_FULL, 1, cache.max_pages, 0),
+                     dtype=torch.uint8, device="cuda")
+    small = csa2.make_index_args(1, qs, 1, 0, None, ws, 16)
+    assert csa2.csa2_index(csa2.CSA2_FULL, q_idx, cache.keys[0], None, 16, out, cache.pages,
+                           small) == csa2.CSA2_ERR_INVALID_ARGUMENT
+    args = csa2.make_index_args(1, qs, 5, 0, None, ws)
+    assert csa2.csa2_index(csa2.CSA2_FULL, q_idx, cache.keys[0], None, 16, out, cache.pages,
+                           args) == csa2.CSA2_ERR_UNSUPPORTED
+    bad_pages = csa2.make_pages(cache.seq_lens, cache.page_table, cache.num_pages, 32)
+    args = csa2.make_index_args(1, qs, 1, 0, None, ws)
+    assert csa2.csa2_index(csa2.CSA2_FULL, q_idx, cache.keys[0], None, 16, out, bad_pages,
+                           args) == csa2.CSA2_ERR_UNSUPPORTED
+    assert csa2.csa2_index(csa2.CSA2_REINDEX, q_idx, cache.keys[0], None, 16, out, cache.pages,
+                           args) == csa2.CSA2_ERR_INVALID_ARGUMENT
+    # REUSE copies the inherited indices
+    inherit = dev(np.arange(16, dtype=np.int32).reshape(1, 16))
+    args = csa2.make_index_args(1, qs, 1, 0, inherit, None)
+    assert csa2.csa2_index(csa2.CSA2_REUSE, None, None, None, 16, out, cache.pages, args) == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(host(out), np.arange(16).reshape(1, 16))
+
+
+# ------------------------------------------------------------------ full-size ------
+
+def test_decode_batch_64x131072_sampled():
+    """64 sequences x 131072 tokens, F->Ri->Ru->Ru, pool 8192, K 2048 (the benchmark's
+    launch configuration); 8 sampled queries compared in full."""
+    wl = gen.config_decode_batch()
+    _, step, q_idx, q = run_workload(wl)
+    check_sampled(wl, [0, 9, 18, 27, 36, 45, 54, 63], step, q_idx, q, min_attn=16)
+
+
+def test_long_context_4x1m():
+    wl = gen.config_long_context()
+    _, step, q_idx, q = run_workload(wl)
+    check_sampled(wl, range(4), step, q_idx, q, min_attn=6)
+
+
+def test_ragged_serving_sampled():
+    """256 sequences (lognormal lengths 1K..256K), 1-4 draft queries each (batched
+    tensor-core scoring), 20 layers in 5 Full groups; 12 sampled queries."""
+    wl = gen.config_ragged()
+    _, step, q_idx, q = run_workload(wl)
+    rng = np.random.default_rng(4)
+    picks = np.sort(rng.choice(wl.num_q, 12, replace=False))
+    check_sampled(wl, picks, step, q_idx, q, attn_budget=6, min_attn=30)
