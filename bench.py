@@ -171,8 +171,7 @@ def run_ours(args, world, rank, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl = {"decode_batch": gen.config_decode_batch, "long_context": gen.config_long_context,
-          "ragged": gen.config_ragged, "tiny": gen.config_tiny}[args.workload]()
+    wl = workload_of(args.workload)
     cache = fill_decode_cache(wl, device=dev)
     q_idx_h, q_h = all_queries_host(wl)
     q_idx = torch.from_numpy(q_idx_h.view(np.int16)).to(dev)
@@ -305,6 +304,16 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def workload_of(name: str):
+    import csa2_inputs as gen
+    if name == "decode_batch16":   # the decode batch with 16 of its 64 sequences (profiling size)
+        wl = gen.config_decode_batch()
+        return gen.DecodeWorkload("decode_batch_16x131072", wl.seed, wl.seq_lens[:16],
+                                  wl.q_per_seq[:16], wl.schedule, wl.pool_size, wl.topk)
+    return {"decode_batch": gen.config_decode_batch, "long_context": gen.config_long_context,
+            "ragged": gen.config_ragged, "tiny": gen.config_tiny}[name]()
+
+
 def count_launches(wl, step) -> int:
     """Kernels libcsa2 launches per decode step: Full and Reindex index calls launch a
     scoring and a selection kernel; Reuse none; attention one kernel plus the split
@@ -396,8 +405,7 @@ def run_reference(args, world, rank):
     import csa2_inputs as gen
     if rank != 0:
         return
-    wl = {"decode_batch": gen.config_decode_batch, "long_context": gen.config_long_context,
-          "ragged": gen.config_ragged, "tiny": gen.config_tiny}[args.workload]()
+    wl = workload_of(args.workload)
     per_step = max(1, args.cpu_sample // max(1, args.steps))
     for _ in range(max(0, min(args.warmup, 1))):
         cpu_baseline(wl, 1)
@@ -431,7 +439,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_batch",
-                    choices=["decode_batch", "long_context", "ragged", "tiny"])
+                    choices=["decode_batch", "decode_batch16", "long_context", "ragged", "tiny"])
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-sample", type=int, default=32, help="queries timed on the oracle")
     ap.add_argument("--no-cpu-baseline", action="store_true")

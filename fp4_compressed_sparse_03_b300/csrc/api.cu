@@ -11,10 +11,12 @@ cudaError_t launch_quantize(const float*, const int32_t*, uint8_t*, uint8_t*, in
 cudaError_t launch_dequantize(const uint8_t*, const uint8_t*, const int32_t*, float*, int32_t,
                               int32_t, int64_t, int32_t*, cudaStream_t, int);
 cudaError_t launch_score_full(const uint16_t*, const uint16_t*, const int32_t*, int32_t, int32_t,
-                              const csa2_pages&, uint32_t*, int64_t, int32_t*, cudaStream_t, int);
+                              const csa2_pages&, uint32_t*, int64_t, void*, int32_t*, cudaStream_t,
+                              int);
 cudaError_t launch_score_reindex(const uint16_t*, const uint16_t*, const int32_t*, int32_t,
-                                 const csa2_pages&, const int32_t*, int32_t, uint32_t*, int32_t*,
-                                 cudaStream_t, int);
+                                 const csa2_pages&, const int32_t*, int32_t, uint32_t*, void*,
+                                 int32_t*, cudaStream_t, int);
+size_t runlist_bytes(int32_t num_q);
 cudaError_t launch_select(bool, const uint32_t*, int64_t, const int32_t*, const csa2_pages&,
                           int32_t, const int32_t*, int32_t, int32_t, int32_t*, int32_t*, int32_t*,
                           cudaStream_t);
@@ -99,17 +101,19 @@ csa2_status csa2_dequantize(const uint8_t* codes, const uint8_t* scales,
                                      stream, device_sms()));
 }
 
+// Scores (one 32-bit key per candidate) followed, at a 256-byte boundary, by the
+// scorer's run list.
+static size_t scores_bytes(csa2_mode mode, int32_t num_q, int32_t max_pages_per_seq,
+                           int32_t pool_size) {
+  const size_t n = mode == CSA2_FULL ? (size_t)std::max(0, max_pages_per_seq) * kPage
+                                     : (size_t)std::max(0, pool_size);
+  return ((size_t)num_q * n * sizeof(uint32_t) + 255) / 256 * 256;
+}
+
 size_t csa2_index_workspace_size(csa2_mode mode, int32_t num_q, int32_t max_pages_per_seq,
                                  int32_t pool_size) {
-  if (num_q <= 0) return 0;
-  switch (mode) {
-    case CSA2_FULL:
-      return (size_t)num_q * (size_t)std::max(0, max_pages_per_seq) * kPage * sizeof(uint32_t);
-    case CSA2_REINDEX:
-      return (size_t)num_q * (size_t)std::max(0, pool_size) * sizeof(uint32_t);
-    default:
-      return 0;
-  }
+  if (num_q <= 0 || (mode != CSA2_FULL && mode != CSA2_REINDEX)) return 0;
+  return scores_bytes(mode, num_q, max_pages_per_seq, pool_size) + runlist_bytes(num_q);
 }
 
 csa2_status csa2_index(csa2_mode mode, const uint16_t* q_idx, const uint16_t* k_idx, int32_t* pool,
@@ -140,8 +144,10 @@ csa2_status csa2_index(csa2_mode mode, const uint16_t* q_idx, const uint16_t* k_
   if (mode == CSA2_FULL) {
     if (pool != nullptr && P < 1) return CSA2_ERR_INVALID_ARGUMENT;
     const int64_t stride = (int64_t)pages->max_pages_per_seq * kPage;
+    void* rl = static_cast<char*>(args->workspace) +
+               scores_bytes(mode, args->num_q, pages->max_pages_per_seq, P);
     e = launch_score_full(q_idx, k_idx, args->q_seq, args->num_q, args->max_q_per_seq, *pages, ws,
-                          stride, args->dev_status, stream, sms);
+                          stride, rl, args->dev_status, stream, sms);
     if (e != cudaSuccess) return from_cuda(e);
     e = launch_select(false, ws, stride, args->q_seq, *pages, args->num_q, nullptr,
                       pool ? P : 0, topk, out_idx, pool, args->dev_status, stream);
@@ -149,7 +155,9 @@ csa2_status csa2_index(csa2_mode mode, const uint16_t* q_idx, const uint16_t* k_
   }
   // REINDEX
   if (pool == nullptr || P < 1) return CSA2_ERR_INVALID_ARGUMENT;
-  e = launch_score_reindex(q_idx, k_idx, args->q_seq, args->num_q, *pages, pool, P, ws,
+  void* rl = static_cast<char*>(args->workspace) +
+             scores_bytes(mode, args->num_q, pages->max_pages_per_seq, P);
+  e = launch_score_reindex(q_idx, k_idx, args->q_seq, args->num_q, *pages, pool, P, ws, rl,
                            args->dev_status, stream, sms);
   if (e != cudaSuccess) return from_cuda(e);
   e = launch_select(true, ws, P, args->q_seq, *pages, args->num_q, pool, P, topk, out_idx, nullptr,

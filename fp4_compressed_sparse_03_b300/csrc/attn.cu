@@ -5,14 +5,15 @@
 // "Reuse Mode": sparse attention runs directly over the inherited top-K entries.
 // MQA over the shared latent: K = V = c_hat (512 channels), 16 query heads.
 //
-// One CTA (8 warps) handles one (query, split) pair: up to `split_len` selected
+// One CTA (4 warps) handles one (query, split) pair: up to `split_len` selected
 // entries in tiles of 64 tokens.  Per tile:
-//   1. cp.async gathers 64 x (256 B codes + 32 B scales) into a 3-stage staging ring;
-//   2. the tile is dequantised once into f16 in shared memory (E2M1 x E4M3 is exact
-//      in f16: at most 6 significant bits, magnitudes 2^-10 .. 2688);
-//   3. S = Q . C^T on tensor cores (m16n8k16, 16 heads = M), fp32 accumulation;
-//   4. fp32 online softmax in the exp2 domain;
-//   5. O += P . C on tensor cores, each warp owning 64 output channels.
+//   1. cp.async gathers 32 x (256 B codes + 32 B scales) into a 4-stage staging ring;
+//   2. S = Q . C^T on tensor cores (m16n8k16, 16 heads = M), fp32 accumulation, with
+//      the dequantisation fused in: each lane turns its token's 4-byte code word into
+//      its B fragments (E2M1 x E4M3 is exact in f16: at most 6 significant bits,
+//      magnitudes 2^-10 .. 2688) and also stores them into the f16 tile C;
+//   3. fp32 online softmax in the exp2 domain;
+//   4. O += P . C on tensor cores, each warp owning 128 output channels.
 // Q is converted to f16 after a per-query power-of-two prescale (exact for every
 // value within 2^28 of the largest |q|); the scale is undone in the logit factor.
 // Several splits per query are merged by a log-sum-exp combine kernel.
@@ -20,13 +21,16 @@
 
 namespace csa2 {
 
-constexpr int kAttnThreads = 256;
-constexpr int kTile = 64;
-constexpr int kStages = 3;
-constexpr int kRowH = kDkv + 8;        // f16 elements per padded Q / C row (1040 B)
-constexpr int kPRow = kTile + 8;       // f16 per padded P row
-constexpr int kSRow = kTile + 4;       // fp32 per padded S row
-constexpr int kStageBytes = kTile * (kCodeRow + kScaleRow);  // 18432
+constexpr int kAttnThreads = 128;   // 4 warps
+constexpr int kAttnWarps = kAttnThreads / 32;
+constexpr int kTile = 32;            // tokens per tile
+constexpr int kStages = 4;           // cp.async staging ring
+constexpr int kMaxSplit = 1024;      // selected entries per CTA at most
+constexpr int kRowH = kDkv + 8;      // f16 elements per padded Q / C row (1040 B)
+constexpr int kPRow = kTile + 8;     // f16 per padded P row
+constexpr int kSRow = kTile + 4;     // fp32 per padded S row
+constexpr int kCodeStride = kCodeRow + 16;  // padded staging row: conflict-free code reads
+constexpr int kStageBytes = kTile * (kCodeStride + kScaleRow);  // 9728
 
 struct AttnSmem {
   __half qs[kHq][kRowH];
@@ -34,9 +38,9 @@ struct AttnSmem {
   unsigned char stage[kStages][kStageBytes];
   float ss[kHq][kSRow];
   __half ps[kHq][kPRow];
-  int valid[kStages][kTile];
+  int32_t slot[kMaxSplit];           // physical row of each selected entry, -1 if skipped
   float m_run[kHq], l_run[kHq], alpha[kHq];
-  uint32_t red[kAttnThreads / 32];
+  uint32_t red[kAttnWarps];
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -79,43 +83,26 @@ struct AttnGeom {
   int32_t num_seqs;
 };
 
-// Issue the gathers of tile `tile` (entries j0 + 64*tile ...) into staging buffer `sb`.
-__device__ __forceinline__ void issue_tile(AttnSmem& sm, int sb, const int32_t* __restrict__ idx_q,
-                                           int jbeg, int jend, const uint8_t* __restrict__ codes,
-                                           const uint8_t* __restrict__ scales, const AttnGeom& g,
-                                           int b, int n_ctx, int32_t* st) {
+// Issue the gathers of the tile starting at local entry `e0` into staging buffer `sb`.
+__device__ __forceinline__ void issue_tile(AttnSmem& sm, int sb, int e0, int ecount,
+                                           const uint8_t* __restrict__ codes,
+                                           const uint8_t* __restrict__ scales) {
   unsigned char* stage = sm.stage[sb];
   for (int ch = threadIdx.x; ch < kTile * 18; ch += kAttnThreads) {
     const int tok = ch / 18, part = ch - tok * 18;
-    const int j = jbeg + tok;
-    int valid = 0;
-    int64_t slot = 0;
-    if (j < jend) {
-      const int s = __ldg(idx_q + j);
-      if (s >= 0 && s < n_ctx) {
-        const int32_t pg = __ldg(g.page_table + (int64_t)b * g.max_pages + (s >> 6));
-        if (pg >= 0 && pg < g.num_pages) {
-          valid = 1;
-          slot = (int64_t)pg * kPage + (s & (kPage - 1));
-        } else if (part == 0) {
-          report(st, CSA2_DEV_BAD_PAGE);
-        }
-      } else if (s != -1 && part == 0) {
-        report(st, CSA2_DEV_BAD_INDEX);
-      }
-    }
-    if (part == 0) sm.valid[sb][tok] = valid;
-    if (valid) {
+    const int e = e0 + tok;
+    const int32_t slot = e < ecount ? sm.slot[e] : -1;
+    if (slot >= 0) {
       if (part < 16)
-        cp_async16(stage + tok * kCodeRow + part * 16, codes + slot * kCodeRow + part * 16);
+        cp_async16(stage + tok * kCodeStride + part * 16, codes + (int64_t)slot * kCodeRow + part * 16);
       else
-        cp_async16(stage + kTile * kCodeRow + tok * kScaleRow + (part - 16) * 16,
-                   scales + slot * kScaleRow + (part - 16) * 16);
+        cp_async16(stage + kTile * kCodeStride + tok * kScaleRow + (part - 16) * 16,
+                   scales + (int64_t)slot * kScaleRow + (part - 16) * 16);
     }
   }
 }
 
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __launch_bounds__(kAttnThreads, 2)
     sparse_attn_kernel(const uint16_t* __restrict__ q, const uint8_t* __restrict__ codes,
                        const uint8_t* __restrict__ scales, const int32_t* __restrict__ idx,
                        AttnGeom g, const int32_t* __restrict__ q_seq, int32_t topk, int32_t split_len,
@@ -125,23 +112,42 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   AttnSmem& sm = *reinterpret_cast<AttnSmem*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int qi = blockIdx.y, split = blockIdx.x, nsplit = gridDim.x;
-  const int jbeg0 = split * split_len;
-  const int jend = min(topk, jbeg0 + split_len);
-  const int ntiles = jend > jbeg0 ? (jend - jbeg0 + kTile - 1) / kTile : 0;
+  const int jbeg = split * split_len;
+  const int ecount = max(0, min(topk, jbeg + split_len) - jbeg);
+  const int ntiles = (ecount + kTile - 1) / kTile;
   int b = __ldg(q_seq + qi);
   int n_ctx = 0;
   if (b < 0 || b >= g.num_seqs) {
     if (tid == 0) report(st, CSA2_DEV_BAD_QSEQ);
     b = 0;
   } else {
-    n_ctx = __ldg(g.seq_lens + b);
+    n_ctx = min(max(0, __ldg(g.seq_lens + b)), g.max_pages * kPage);
   }
-  const int32_t* idx_q = idx + (int64_t)qi * topk;
+  const int32_t* idx_q = idx + (int64_t)qi * topk + jbeg;
+
+  // ---- resolve every selected entry of this split to its physical row ----
+  for (int e = tid; e < ecount; e += kAttnThreads) {
+    const int s = __ldg(idx_q + e);
+    int32_t slot = -1;
+    if (s >= 0 && s < n_ctx) {
+      const int32_t pg = __ldg(g.page_table + (int64_t)b * g.max_pages + (s >> 6));
+      if (pg >= 0 && pg < g.num_pages) slot = pg * kPage + (s & (kPage - 1));
+      else report(st, CSA2_DEV_BAD_PAGE);
+    } else if (s != -1) {
+      report(st, CSA2_DEV_BAD_INDEX);
+    }
+    sm.slot[e] = slot;
+  }
+  if (tid < kHq) {
+    sm.m_run[tid] = -INFINITY;
+    sm.l_run[tid] = 0.0f;
+  }
+  __syncthreads();
 
   // start the first gathers before touching Q
 #pragma unroll
   for (int s = 0; s < kStages - 1; ++s) {
-    if (s < ntiles) issue_tile(sm, s, idx_q, jbeg0 + s * kTile, jend, codes, scales, g, b, n_ctx, st);
+    if (s < ntiles) issue_tile(sm, s, s * kTile, ecount, codes, scales);
     cp_async_commit();
   }
 
@@ -156,13 +162,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   mx = __reduce_max_sync(0xffffffffu, mx);
   if (lane == 0) sm.red[warp] = mx;
-  if (tid < kHq) {
-    sm.m_run[tid] = -INFINITY;
-    sm.l_run[tid] = 0.0f;
-  }
   __syncthreads();
   uint32_t mxa = 0;
-  for (int w = 0; w < kAttnThreads / 32; ++w) mxa = max(mxa, sm.red[w]);
+  for (int w = 0; w < kAttnWarps; ++w) mxa = max(mxa, sm.red[w]);
   int sh = 0;
   if (mxa != 0) {
     const int e = (int)((mxa >> 7) & 0xFF) - 127;  // bf16 exponent of max |q|
@@ -171,98 +173,98 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const float pre = __uint_as_float((uint32_t)(127 + sh) << 23);   // 2^sh
   const float post = __uint_as_float((uint32_t)(127 - sh) << 23);  // 2^-sh
   const float kq = softmax_scale * 1.4426950408889634f * post;  // logits in the exp2 domain
-  for (int i = tid; i < kHq * kDkv / 2; i += kAttnThreads) {
-    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(qq) + i);
-    const __half2 h = __floats2half2_rn(bf16lo(w) * pre, bf16hi(w) * pre);
-    const int hd = (2 * i) / kDkv, c = (2 * i) % kDkv;
-    *reinterpret_cast<__half2*>(&sm.qs[hd][c]) = h;
+  for (int i = tid; i < kHq * kDkv / 8; i += kAttnThreads) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(qq) + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t hv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __half2 h = __floats2half2_rn(bf16lo(w[e]) * pre, bf16hi(w[e]) * pre);
+      hv[e] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    const int hd = (8 * i) / kDkv, c = (8 * i) % kDkv;
+    *reinterpret_cast<uint4*>(&sm.qs[hd][c]) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
   }
 
-  float acc[8][4];
+  float acc[16][4];
 #pragma unroll
-  for (int n = 0; n < 8; ++n)
+  for (int n = 0; n < 16; ++n)
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[n][e] = 0.0f;
 
   const int gq = lane >> 2, cq = lane & 3;
+  const int lm = lane >> 3, lr = lane & 7;  // ldmatrix: matrix and row served by this lane
   for (int t = 0; t < ntiles; ++t) {
     const int sb = t % kStages;
     cp_async_wait<kStages - 2>();
     __syncthreads();  // tile t staged; previous tile's readers of cs / ps are done
     {
       const int nt = t + kStages - 1;
-      if (nt < ntiles)
-        issue_tile(sm, nt % kStages, idx_q, jbeg0 + nt * kTile, jend, codes, scales, g, b, n_ctx, st);
+      if (nt < ntiles) issue_tile(sm, nt % kStages, nt * kTile, ecount, codes, scales);
       cp_async_commit();
     }
-    // ---- dequantise: (token, 16-channel group) units ----
+    // ---- S = Q . C^T with fused dequantisation: warp w -> tokens 8w .. 8w+7 ----
+    // Lane (gq, cq) serves token gq of the warp.  For channel block p (32 channels,
+    // k-steps 2p and 2p + 1) its k-slots {2cq, 2cq+1, 2cq+8, 2cq+9} map to channels
+    // 32p + 8cq + {0..3} (k-step 2p) and 32p + 8cq + {4..7} (k-step 2p + 1), so one
+    // 4-byte code word gives its B fragments and the A fragments of Q come from 16-byte
+    // reads of head rows gq and gq + 8 at the same channels.
     const unsigned char* stage = sm.stage[sb];
-    for (int uidx = tid; uidx < kTile * 32; uidx += kAttnThreads) {
-      const int tok = uidx >> 5, grp = uidx & 31;
-      uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-      if (sm.valid[sb][tok]) {
-        const uint2 cw = *reinterpret_cast<const uint2*>(stage + tok * kCodeRow + grp * 8);
-        const float s = e4m3_decode(stage[kTile * kCodeRow + tok * kScaleRow + grp]);
-        const __half2 s2 = __float2half2_rn(s);
-        uint32_t r[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t byte = ((k < 4 ? cw.x : cw.y) >> (8 * (k & 3))) & 0xFFu;
-          const uint32_t h2 = e2m1x2_to_f16x2(byte);
-          const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h2), s2);
-          r[k] = *reinterpret_cast<const uint32_t*>(&v);
-        }
-        o0 = make_uint4(r[0], r[1], r[2], r[3]);
-        o1 = make_uint4(r[4], r[5], r[6], r[7]);
-      }
-      uint4* dst = reinterpret_cast<uint4*>(&sm.cs[tok][grp * 16]);
-      dst[0] = o0;
-      dst[1] = o1;
-    }
-    __syncthreads();
-
-    // ---- S = Q . C^T: warp w -> tokens 8w .. 8w+7, all 512 channels ----
+    const int e0 = t * kTile;
     {
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      const int tok0 = 8 * warp;
+      const int tok = 8 * warp + gq;
+      const bool tv = (e0 + tok < ecount) && sm.slot[e0 + tok] >= 0;
+      const unsigned char* crow = stage + tok * kCodeStride;
+      const unsigned char* srow = stage + kTile * kCodeStride + tok * kScaleRow;
+      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
-      for (int kk = 0; kk < kDkv / 16; kk += 2) {
-        uint32_t a0[4], a1[4], bb[4];
-        {
-          const int m = lane >> 3, r = lane & 7;
-          ldsm_x4(a0, &sm.qs[(m & 1) * 8 + r][16 * kk + (m >> 1) * 8]);
-          ldsm_x4(a1, &sm.qs[(m & 1) * 8 + r][16 * (kk + 1) + (m >> 1) * 8]);
-          ldsm_x4(bb, &sm.cs[tok0 + r][16 * kk + m * 8]);
+      for (int p = 0; p < kDkv / 32; ++p) {
+        const int ch = 32 * p + 8 * cq;
+        const uint4 qa = *reinterpret_cast<const uint4*>(&sm.qs[gq][ch]);
+        const uint4 qb = *reinterpret_cast<const uint4*>(&sm.qs[gq + 8][ch]);
+        uint32_t h[4] = {0u, 0u, 0u, 0u};
+        if (tv) {
+          const uint32_t cw = *reinterpret_cast<const uint32_t*>(crow + ch / 2);
+          const __half2 s2 = __float2half2_rn(e4m3_decode(srow[ch >> 4]));
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t h2 = e2m1x2_to_f16x2((cw >> (8 * k)) & 0xFFu);
+            const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h2), s2);
+            h[k] = *reinterpret_cast<const uint32_t*>(&v);
+          }
         }
-        mma_f16(d, a0, bb[0], bb[1]);
-        mma_f16(d, a1, bb[2], bb[3]);
+        *reinterpret_cast<uint4*>(&sm.cs[tok][ch]) = make_uint4(h[0], h[1], h[2], h[3]);
+        const uint32_t a0[4] = {qa.x, qb.x, qa.y, qb.y}, a1[4] = {qa.z, qb.z, qa.w, qb.w};
+        mma_f16(d0, a0, h[0], h[1]);
+        mma_f16(d1, a1, h[2], h[3]);
       }
-      // d0,d1: head gq, tokens 2cq, 2cq+1; d2,d3: head gq+8
-      const int tk = tok0 + 2 * cq;
-      const bool v0 = sm.valid[sb][tk], v1 = sm.valid[sb][tk + 1];
-      sm.ss[gq][tk] = v0 ? d[0] * kq : -INFINITY;
-      sm.ss[gq][tk + 1] = v1 ? d[1] * kq : -INFINITY;
-      sm.ss[gq + 8][tk] = v0 ? d[2] * kq : -INFINITY;
-      sm.ss[gq + 8][tk + 1] = v1 ? d[3] * kq : -INFINITY;
+      // d: heads gq (0..1) and gq + 8 (2..3), tokens 8w + 2cq, 8w + 2cq + 1
+      const int tk = 8 * warp + 2 * cq;
+      const bool v0 = (e0 + tk < ecount) && sm.slot[e0 + tk] >= 0;
+      const bool v1 = (e0 + tk + 1 < ecount) && sm.slot[e0 + tk + 1] >= 0;
+      sm.ss[gq][tk] = v0 ? (d0[0] + d1[0]) * kq : -INFINITY;
+      sm.ss[gq][tk + 1] = v1 ? (d0[1] + d1[1]) * kq : -INFINITY;
+      sm.ss[gq + 8][tk] = v0 ? (d0[2] + d1[2]) * kq : -INFINITY;
+      sm.ss[gq + 8][tk + 1] = v1 ? (d0[3] + d1[3]) * kq : -INFINITY;
     }
     __syncthreads();
 
-    // ---- online softmax: warp w -> heads 2w, 2w+1 ----
+    // ---- online softmax: warp w -> heads 4w .. 4w+3, lane -> token ----
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int h = 2 * warp + hh;
-      const float s0 = sm.ss[h][lane], s1 = sm.ss[h][lane + 32];
-      float tmax = fmaxf(s0, s1);
+    for (int hh = 0; hh < 4; ++hh) {
+      const int h = 4 * warp + hh;
+      const float s0 = sm.ss[h][lane];
+      float tmax = s0;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
       const float m_old = sm.m_run[h];
       const float m_new = fmaxf(m_old, tmax);
       const float al = (m_new == -INFINITY) ? 1.0f : exp2f(m_old - m_new);
-      const float p0 = (s0 == -INFINITY) ? 0.0f : exp2f(s0 - m_new);
-      const float p1 = (s1 == -INFINITY) ? 0.0f : exp2f(s1 - m_new);
-      sm.ps[h][lane] = __float2half_rn(p0);
-      sm.ps[h][lane + 32] = __float2half_rn(p1);
-      float ps = p0 + p1;
+      const __half p0 = __float2half_rn((s0 == -INFINITY) ? 0.0f : exp2f(s0 - m_new));
+      sm.ps[h][lane] = p0;
+      // the normaliser sums the same f16-rounded weights the P.C product uses, so the
+      // output stays an exact weighted average of the rows
+      float ps = __half2float(p0);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
       __syncwarp();
@@ -274,26 +276,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     __syncthreads();
 
-    // ---- O += P . C: warp w -> channels 64w .. 64w+63 ----
+    // ---- O += P . C: warp w -> channels 128w .. 128w+127 ----
     {
       const float al0 = sm.alpha[gq], al1 = sm.alpha[gq + 8];
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
+      for (int n = 0; n < 16; ++n) {
         acc[n][0] *= al0;
         acc[n][1] *= al0;
         acc[n][2] *= al1;
         acc[n][3] *= al1;
       }
-      const int m = lane >> 3, r = lane & 7;
 #pragma unroll
       for (int ks = 0; ks < kTile / 16; ++ks) {
         uint32_t a[4];
-        ldsm_x4(a, &sm.ps[(m & 1) * 8 + r][16 * ks + (m >> 1) * 8]);
+        ldsm_x4(a, &sm.ps[(lm & 1) * 8 + lr][16 * ks + (lm >> 1) * 8]);
 #pragma unroll
-        for (int np = 0; np < 4; ++np) {
+        for (int np = 0; np < 8; ++np) {
           uint32_t bb[4];
           // matrices: (tok 0-7, ch n0), (tok 8-15, ch n0), (tok 0-7, ch n0+8), (tok 8-15, ch n0+8)
-          ldsm_x4_t(bb, &sm.cs[16 * ks + (m & 1) * 8 + r][64 * warp + 16 * np + (m >> 1) * 8]);
+          ldsm_x4_t(bb, &sm.cs[16 * ks + (lm & 1) * 8 + lr][128 * warp + 16 * np + (lm >> 1) * 8]);
           mma_f16(acc[2 * np], a, bb[0], bb[1]);
           mma_f16(acc[2 * np + 1], a, bb[2], bb[3]);
         }
@@ -309,8 +310,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const float i0 = l0 > 0.f ? 1.0f / l0 : 0.f, i1 = l1 > 0.f ? 1.0f / l1 : 0.f;
     float* o = out + (int64_t)qi * kHq * kDkv;
 #pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      const int ch = 64 * warp + 8 * n + 2 * cq;
+    for (int n = 0; n < 16; ++n) {
+      const int ch = 128 * warp + 8 * n + 2 * cq;
       *reinterpret_cast<float2*>(o + gq * kDkv + ch) = make_float2(acc[n][0] * i0, acc[n][1] * i0);
       *reinterpret_cast<float2*>(o + (gq + 8) * kDkv + ch) = make_float2(acc[n][2] * i1, acc[n][3] * i1);
     }
@@ -322,8 +323,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   } else {
     float* o = part_o + ((int64_t)qi * nsplit + split) * kHq * kDkv;
 #pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      const int ch = 64 * warp + 8 * n + 2 * cq;
+    for (int n = 0; n < 16; ++n) {
+      const int ch = 128 * warp + 8 * n + 2 * cq;
       *reinterpret_cast<float2*>(o + gq * kDkv + ch) = make_float2(acc[n][0], acc[n][1]);
       *reinterpret_cast<float2*>(o + (gq + 8) * kDkv + ch) = make_float2(acc[n][2], acc[n][3]);
     }
@@ -335,58 +336,91 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
 }
 
-// Merge the splits of each query: out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
-__global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ part_o,
+// Merge the splits of each (query, head): out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+__global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restrict__ part_o,
                                                            const float* __restrict__ part_ml,
                                                            int nsplit, float* __restrict__ out,
                                                            float* __restrict__ lse) {
-  const int qi = blockIdx.x;
-  __shared__ float wgt[64][kHq];
-  __shared__ float inv[kHq];
+  const int qi = blockIdx.x, h = blockIdx.y;
+  __shared__ float wgt[64];
+  __shared__ float inv;
   const float* ml = part_ml + (int64_t)qi * nsplit * 2 * kHq;
-  if (threadIdx.x < kHq) {
-    const int h = threadIdx.x;
+  if (threadIdx.x < 32) {
     float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ml[s * 2 * kHq + h]);
+    for (int s = threadIdx.x; s < nsplit; s += 32) M = fmaxf(M, ml[s * 2 * kHq + h]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float L = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
+    for (int s = threadIdx.x; s < nsplit; s += 32) {
       const float m = ml[s * 2 * kHq + h], l = ml[s * 2 * kHq + kHq + h];
       const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
-      wgt[s][h] = w;
+      wgt[s] = w;
       L += w * l;
     }
-    inv[h] = L > 0.f ? 1.0f / L : 0.f;
-    if (lse) lse[(int64_t)qi * kHq + h] = L > 0.f ? M * 0.6931471805599453f + logf(L) : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (threadIdx.x == 0) {
+      inv = L > 0.f ? 1.0f / L : 0.f;
+      if (lse) lse[(int64_t)qi * kHq + h] = L > 0.f ? M * 0.6931471805599453f + logf(L) : -INFINITY;
+    }
   }
   __syncthreads();
-  const float4* po = reinterpret_cast<const float4*>(part_o + (int64_t)qi * nsplit * kHq * kDkv);
-  float4* o = reinterpret_cast<float4*>(out + (int64_t)qi * kHq * kDkv);
-  for (int i = threadIdx.x; i < kHq * kDkv / 4; i += blockDim.x) {
-    const int h = (4 * i) / kDkv;
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < nsplit; ++s) {
-      const float w = wgt[s][h];
-      if (w == 0.f) continue;
-      const float4 v = po[(int64_t)s * kHq * kDkv / 4 + i];
-      a.x += w * v.x;
-      a.y += w * v.y;
-      a.z += w * v.z;
-      a.w += w * v.w;
+  // 128 threads x 4 channels
+  const float4* po = reinterpret_cast<const float4*>(part_o + ((int64_t)qi * nsplit * kHq + h) * kDkv);
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  int s = 0;
+  for (; s + 4 <= nsplit; s += 4) {  // four independent loads in flight
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __ldcs(po + (int64_t)(s + u) * kHq * kDkv / 4 + threadIdx.x);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float w = wgt[s + u];
+      a.x += w * v[u].x;
+      a.y += w * v[u].y;
+      a.z += w * v[u].z;
+      a.w += w * v[u].w;
     }
-    const float iv = inv[h];
-    o[i] = make_float4(a.x * iv, a.y * iv, a.z * iv, a.w * iv);
   }
+  for (; s < nsplit; ++s) {
+    const float w = wgt[s];
+    const float4 v = __ldcs(po + (int64_t)s * kHq * kDkv / 4 + threadIdx.x);
+    a.x += w * v.x;
+    a.y += w * v.y;
+    a.z += w * v.z;
+    a.w += w * v.w;
+  }
+  const float iv = inv;
+  reinterpret_cast<float4*>(out + ((int64_t)qi * kHq + h) * kDkv)[threadIdx.x] =
+      make_float4(a.x * iv, a.y * iv, a.z * iv, a.w * iv);
 }
 
+// Splits per query: the count that minimises (waves of two CTAs per SM) x (tiles per
+// CTA + a fixed start-up cost of ~4 tiles), with at most kMaxSplit entries per CTA.
 int attn_splits(int32_t num_q, int32_t topk, int num_sms) {
-  const int max_splits = std::max(1, std::min(64, (topk + kTile - 1) / kTile));
-  int want = (2 * num_sms + num_q - 1) / std::max(1, num_q);
-  return std::max(1, std::min(max_splits, want));
+  const int tiles = std::max(1, (topk + kTile - 1) / kTile);
+  const int min_splits = (tiles * kTile + kMaxSplit - 1) / kMaxSplit;
+  const int max_splits = std::max(min_splits, std::min(64, tiles));
+  int best = std::max(1, min_splits);
+  double best_cost = 1e300;
+  for (int sp = std::max(1, min_splits); sp <= max_splits; ++sp) {
+    const int per = (tiles + sp - 1) / sp;     // tiles per split
+    const int real = (tiles + per - 1) / per;  // splits actually used
+    const int64_t ctas = (int64_t)num_q * real;
+    const int64_t waves = (ctas + 2 * num_sms - 1) / (2 * num_sms);
+    const double cost = (double)waves * (per + 4);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = real;
+    }
+  }
+  return best;
 }
 
 int attn_split_len(int32_t topk, int splits) {
-  int len = (topk + splits - 1) / splits;
-  return (len + kTile - 1) / kTile * kTile;
+  const int tiles = std::max(1, (topk + kTile - 1) / kTile);
+  const int per = (tiles + splits - 1) / splits;
+  return per * kTile;
 }
 
 size_t attn_smem_bytes() { return sizeof(AttnSmem); }
@@ -413,7 +447,7 @@ cudaError_t launch_attn(const uint16_t* q, const uint8_t* codes, const uint8_t* 
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (splits > 1) {
-    attn_combine_kernel<<<num_q, 256, 0, s>>>(part_o, part_ml, splits, out, lse);
+    attn_combine_kernel<<<dim3(num_q, kHq), 128, 0, s>>>(part_o, part_ml, splits, out, lse);
     e = cudaGetLastError();
   }
   return e;

@@ -6,21 +6,23 @@
 // writes one 32-bit ranking key per candidate into the workspace:
 //     key = (bits(score) & 0x7fffffff) + 1   for a valid candidate (score >= 0),
 //     key = 0                                for an invalid one (pool padding, bad page).
-// Keys order like the scores, and every valid key is above every invalid one.
-// Selection (cluster radix select) then takes the top-min(K, #valid) keys with the
-// lower candidate position winning ties, and writes their tokens in ascending order.
+// Keys order like the scores, every valid key is above every invalid one, and bit 31
+// of a valid key is always clear.  Selection (cluster radix select) then takes the
+// top-min(K, #valid) keys, the lower candidate position winning ties, and writes
+// their tokens in ascending order.
 //
 // Kernels:
-//   score_q1_kernel      one query per sequence (Full) or per pool (Reindex): a
-//                        bandwidth-bound warp dot product on CUDA cores (packed FFMA2)
-//   score_batched_kernel up to 4 draft queries per sequence (Full): 16 query-head rows
-//                        x 8 keys x 16 dims per tensor-core MMA, keys read once
-//   select_kernel        8-CTA cluster per query: 3 histogram passes (11/11/10 bits)
-//                        merged through distributed shared memory, then an ordered
-//                        compaction
+//   group_prefix_kernel  compact work list (runs of queries, units of rows)
+//   score_pages_kernel   FULL: 64-token pages streamed by TMA into a shared ring, scored
+//                        by tensor-core MMAs (1-4 draft queries of a sequence at once)
+//   score_gather_kernel  REINDEX: pool rows gathered by per-lane cp.async rings, scored
+//                        by the same MMAs
+//   select_kernel        8-CTA cluster per query: four 8-bit radix passes with per-warp
+//                        histograms merged through distributed shared memory, then an
+//                        ordered compaction with warp scans
 #include <cooperative_groups.h>
 
-#include "common.cuh"
+#include "async.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -28,10 +30,8 @@ namespace csa2 {
 
 // ------------------------------------------------------------------ scoring -------
 
-constexpr int kScoreThreads = 256;   // 8 warps
-constexpr int kUnitPages = 16;       // pages per Full work unit (1024 keys)
-constexpr int kUnitPool = 1024;      // pool positions per Reindex work unit
-constexpr int kDepth = 4;            // key groups in flight per warp
+constexpr int kScoreThreads = 256;     // 8 warps
+constexpr int kScoreWarps = kScoreThreads / 32;
 
 struct ScoreGeom {
   const int32_t* seq_lens;
@@ -45,636 +45,1093 @@ __device__ __forceinline__ uint32_t rank_key(float score) {
   return (__float_as_uint(score) & 0x7FFFFFFFu) + 1u;
 }
 
-// Lane layout of a warp over 8 keys: quad = lane/4 picks the key, c = lane%4 the
-// 64-byte quarter of its 256-byte row: bytes [64j + 16c, 64j + 16c + 16), j = 0..3,
-// i.e. dims 32j + 8c .. 32j + 8c + 7.  Each lane therefore holds the same 32 dims of
-// every key and keeps the matching 4 x 32 query values in registers.
-struct QRegs {
-  unsigned long long p[kHidx][4][4];  // [head][j][pair] = (q[32j+8c+2e], q[32j+8c+2e+1])
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+
+// The warp's contiguous share [g0, g1) of `total` groups.
+__device__ __forceinline__ void warp_share(int64_t total, int64_t& g0, int64_t& g1) {
+  const int64_t nw = (int64_t)gridDim.x * kScoreWarps;
+  const int64_t w = (int64_t)blockIdx.x * kScoreWarps + (threadIdx.x >> 5);
+  const int64_t per = (total + nw - 1) / nw;
+  g0 = min(total, w * per);
+  g1 = min(total, g0 + per);
+}
+
+// Compact work list of a scoring launch.  A run is one query (single-query scorer) or
+// the queries of one sequence (batched scorer); run r covers used(r) = ceil(rows / u)
+// work units of u rows (u = 8: a group of 8 key rows; u = 64: a whole page).  group_prefix_kernel (one CTA) writes
+//   meta[0] = R (runs), meta[1] = total groups,
+//   run_q0[r] = first query of run r (r <= R, run_q0[R] = num_q),
+//   prefix[r] = groups before run r (r <= R).
+struct RunList {
+  const int64_t* meta;
+  const int64_t* prefix;
+  const int32_t* run_q0;
 };
 
-__device__ __forceinline__ void load_q1(QRegs& qr, const uint16_t* __restrict__ q, int c) {
-#pragma unroll
-  for (int h = 0; h < kHidx; ++h)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(q + h * kDidx + 32 * j + 8 * c));
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) qr.p[h][j][e] = pack2(bf16lo(w[e]), bf16hi(w[e]));
-    }
+__device__ __forceinline__ int run_rows(bool reindex, const int32_t* __restrict__ q_seq, int q,
+                                        const ScoreGeom& g, int32_t pool_size) {
+  if (reindex) return pool_size;
+  const int b = __ldg(q_seq + q);
+  if (b < 0 || b >= g.num_seqs) return 0;
+  return min(max(0, __ldg(g.seq_lens + b)), g.max_pages * kPage);
 }
 
-// Full score of the quad's key, returned on all 4 lanes of the quad.
-__device__ __forceinline__ float score_q1(const QRegs& qr, const uint4 (&kv)[4], int c) {
-  unsigned long long acc[kHidx] = {0ull, 0ull, 0ull, 0ull};
+__global__ void __launch_bounds__(1024) group_prefix_kernel(bool batched, bool reindex,
+                                                            const int32_t* __restrict__ q_seq,
+                                                            int32_t num_q, ScoreGeom g,
+                                                            int32_t pool_size, int32_t unit_rows,
+                                                            int64_t* meta, int64_t* prefix,
+                                                            int32_t* run_q0) {
+  __shared__ int64_t wsum[32];
+  __shared__ int64_t carry_s;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  auto block_incl_scan = [&](int64_t v) -> int64_t {  // inclusive scan, returns the value
+    int64_t x = v;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t w[4] = {kv[j].x, kv[j].y, kv[j].z, kv[j].w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const unsigned long long k2 = pack2(bf16lo(w[e]), bf16hi(w[e]));
-#pragma unroll
-      for (int h = 0; h < kHidx; ++h) ffma2(acc[h], k2, qr.p[h][j][e]);
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
     }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    int64_t add = 0;
+    for (int w = 0; w < warp; ++w) add += wsum[w];
+    __syncthreads();
+    return x + add;
+  };
+  // pass 1: run starts
+  if (tid == 0) carry_s = 0;
+  __syncthreads();
+  for (int base = 0; base < num_q; base += 1024) {
+    const int i = base + tid;
+    int start = 0;
+    if (i < num_q) {
+      const int b = __ldg(q_seq + i);
+      start = (!batched || i == 0 || b != __ldg(q_seq + i - 1)) ? 1 : 0;
+    }
+    const int64_t incl = block_incl_scan(start);
+    const int64_t carry = carry_s;
+    if (start) run_q0[carry + incl - 1] = i;
+    __syncthreads();
+    if (tid == 1023) carry_s = carry + incl;
+    __syncthreads();
   }
-  float d[kHidx];
-#pragma unroll
-  for (int h = 0; h < kHidx; ++h) d[h] = lo2(acc[h]) + hi2(acc[h]);
-  // reduce-scatter over the quad: lane c ends with head c's full dot product
-  const bool up = (c & 2) != 0;
-  float a0 = up ? d[2] : d[0], a1 = up ? d[3] : d[1];
-  const float b0 = up ? d[0] : d[2], b1 = up ? d[1] : d[3];
-  a0 += __shfl_xor_sync(0xffffffffu, b0, 2);
-  a1 += __shfl_xor_sync(0xffffffffu, b1, 2);
-  const bool odd = (c & 1) != 0;
-  float mine = odd ? a1 : a0;
-  const float other = odd ? a0 : a1;
-  mine += __shfl_xor_sync(0xffffffffu, other, 1);
-  float r = mine > 0.0f ? mine : 0.0f;  // ReLU per head
-  r += __shfl_xor_sync(0xffffffffu, r, 1);
-  r += __shfl_xor_sync(0xffffffffu, r, 2);
-  return r;
+  const int R = (int)carry_s;
+  if (tid == 0) run_q0[R] = num_q;
+  __threadfence_block();
+  __syncthreads();
+  // pass 2: groups per run, exclusive prefix
+  if (tid == 0) carry_s = 0;
+  __syncthreads();
+  for (int base = 0; base < R; base += 1024) {
+    const int r = base + tid;
+    int64_t used = 0;
+    if (r < R) used = (run_rows(reindex, q_seq, run_q0[r], g, pool_size) + unit_rows - 1) / unit_rows;
+    const int64_t incl = block_incl_scan(used);
+    const int64_t carry = carry_s;
+    if (r < R) prefix[r + 1] = carry + incl;
+    __syncthreads();
+    if (tid == 1023) carry_s = carry + incl;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    prefix[0] = 0;
+    meta[0] = R;
+    meta[1] = carry_s;
+  }
 }
 
-__device__ __forceinline__ void load_row(uint4 (&kv)[4], const uint16_t* row, int c) {
-  const char* p = reinterpret_cast<const char*>(row) + 16 * c;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) kv[j] = ldg_stream(p + 64 * j);
+// Cursor over the compact list: run index and its [start, end) group range.
+struct RunCursor {
+  int r;
+  int64_t start, end;
+};
+__device__ __forceinline__ void cursor_seek(RunCursor& cu, const RunList& rl, int R, int64_t gg) {
+  int lo = 0, hi = R - 1;  // last run with prefix[r] <= gg
+  while (lo < hi) {
+    const int m = (lo + hi + 1) >> 1;
+    if (__ldg(rl.prefix + m) <= gg) lo = m; else hi = m - 1;
+  }
+  cu.r = lo;
+  cu.start = __ldg(rl.prefix + lo);
+  cu.end = __ldg(rl.prefix + lo + 1);
+}
+__device__ __forceinline__ void cursor_advance(RunCursor& cu, const RunList& rl, int64_t gg) {
+  while (gg >= cu.end) {
+    ++cu.r;
+    cu.start = cu.end;
+    cu.end = __ldg(rl.prefix + cu.r + 1);
+  }
 }
 
-// One query per unit.  FULL: unit = (query, 16 consecutive pages of its sequence).
-// REINDEX: unit = (query, 1024 consecutive pool positions).
-template <bool kReindex>
+// REINDEX: each query's P pool positions are a run of 16-row groups; the rows are
+// gathered (pool entry -> page table -> slot) through the per-lane cp.async ring and
+// scored on the tensor cores exactly like the page scorer (M = 16 gathered keys,
+// N = 8 columns holding the query's 4 heads, K = 128 dims in the shared permuted order).
+constexpr int kGatherRing = 4;                       // 16-row groups staged per warp
+constexpr int kGatherGroup = 16 * kKeyRow;           // 4 KB
+constexpr int kGatherSmem = kScoreWarps * kGatherRing * kGatherGroup;  // 128 KB
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 __global__ void __launch_bounds__(kScoreThreads, 1)
-    score_q1_kernel(const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ keys,
-                    const int32_t* __restrict__ q_seq, int32_t num_q, ScoreGeom g,
-                    const int32_t* __restrict__ pool, int32_t pool_size,
-                    uint32_t* __restrict__ ws, int64_t ws_stride, int32_t units_per_q, int32_t* st) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int quad = lane >> 2, c = lane & 3;
-  const int64_t total_units = (int64_t)num_q * units_per_q;
-  QRegs qr;
-  int cur_q = -1;
-  for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
-    const int q = (int)(u / units_per_q);
-    const int chunk = (int)(u - (int64_t)q * units_per_q);
-    const int b = __ldg(q_seq + q);
-    if (b < 0 || b >= g.num_seqs) {
-      if (threadIdx.x == 0 && chunk == 0) report(st, CSA2_DEV_BAD_QSEQ);
-      continue;
-    }
-    const int n_ctx = __ldg(g.seq_lens + b);
-    int begin, count;  // candidate positions [begin, begin + count)
-    if (kReindex) {
-      begin = chunk * kUnitPool;
-      count = min(kUnitPool, pool_size - begin);
-    } else {
-      begin = chunk * kUnitPages * kPage;
-      count = min(kUnitPages * kPage, n_ctx - begin);
-    }
-    if (count <= 0) continue;
-    if (q != cur_q) {
-      load_q1(qr, q_idx + (int64_t)q * kHidx * kDidx, c);
-      cur_q = q;
-    }
-    uint32_t* out = ws + (int64_t)q * ws_stride;
-    const int groups = (count + 7) >> 3;
-    const int mine = groups > warp ? (groups - warp + 7) >> 3 : 0;
-
-    // Resolve the row of the quad's key in group k of this warp; false if invalid.
-    auto locate = [&](int k, const uint16_t*& row) -> bool {
-      const int pos = begin + 8 * (warp + 8 * k) + quad;
-      row = keys;
-      if (pos >= begin + count) return false;
-      int t;
-      if (kReindex) {
-        t = __ldg(pool + (int64_t)q * pool_size + pos);
-        if (t < 0) {
-          if (t != -1 && c == 0) report(st, CSA2_DEV_BAD_INDEX);
-          return false;
-        }
-        if (t >= n_ctx) {
-          if (c == 0) report(st, CSA2_DEV_BAD_INDEX);
-          return false;
-        }
-      } else {
-        t = pos;
-      }
-      const int32_t pg = __ldg(g.page_table + (int64_t)b * g.max_pages + (t >> 6));
-      if (pg < 0 || pg >= g.num_pages) {
-        if (c == 0) report(st, CSA2_DEV_BAD_PAGE);
-        return false;
-      }
-      row = keys + ((int64_t)pg * kPage + (t & (kPage - 1))) * kDidx;
-      return true;
-    };
-
-    uint4 buf[kDepth][4];
-    bool ok[kDepth];
-#pragma unroll
-    for (int i = 0; i < kDepth; ++i) {
-      ok[i] = false;
-      if (i < mine) {
-        const uint16_t* row;
-        ok[i] = locate(i, row);
-        load_row(buf[i], row, c);
-      }
-    }
-    for (int k0 = 0; k0 < mine; k0 += kDepth) {
-#pragma unroll
-      for (int i = 0; i < kDepth; ++i) {
-        const int k = k0 + i;
-        if (k < mine) {
-          const float s = score_q1(qr, buf[i], c);
-          const int pos = begin + 8 * (warp + 8 * k) + quad;
-          if (c == 0 && pos < begin + count) out[pos] = ok[i] ? rank_key(s) : 0u;
-          if (k + kDepth < mine) {
-            const uint16_t* row;
-            ok[i] = locate(k + kDepth, row);
-            load_row(buf[i], row, c);
-          }
-        }
-      }
-    }
-  }
-}
-
-// Batched draft queries (Full): for one sequence with T <= 4 queries, the 4T
-// query-head rows form the A operand (16 rows, zero padded) of m16n8k16 bf16 MMAs and
-// 8 keys form B, so every key row is read once for all of the sequence's queries.
-// The 128 dims are visited in a permuted order shared by A and B: lane c's 16-byte
-// load of dims 32j+8c..+7 supplies its B fragments for k-steps 2j and 2j+1.
-__global__ void __launch_bounds__(kScoreThreads, 2)
-    score_batched_kernel(const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ keys,
-                         const int32_t* __restrict__ q_seq, int32_t num_q, ScoreGeom g,
-                         uint32_t* __restrict__ ws, int64_t ws_stride, int32_t units_per_seq,
-                         int32_t* st) {
+    score_gather_kernel(const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ keys,
+                        const int32_t* __restrict__ q_seq, int32_t num_q, ScoreGeom g,
+                        const int32_t* __restrict__ pool, int32_t pool_size,
+                        uint32_t* __restrict__ ws, RunList rl, int32_t* st) {
+  extern __shared__ __align__(128) unsigned char gather_smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gq = lane >> 2, c = lane & 3;
-  const int64_t total_units = (int64_t)g.num_seqs * units_per_seq;
-  uint32_t a[8][4];
-  int cur_b = -1, q0 = 0, T = 0;
-  for (int64_t u = blockIdx.x; u < total_units; u += gridDim.x) {
-    const int b = (int)(u / units_per_seq);
-    const int chunk = (int)(u - (int64_t)b * units_per_seq);
-    const int n_ctx = __ldg(g.seq_lens + b);
-    const int begin = chunk * kUnitPages * kPage;
-    const int count = min(kUnitPages * kPage, n_ctx - begin);
-    if (count <= 0) continue;
-    if (b != cur_b) {
-      // queries of sequence b: [lower_bound(b), upper_bound(b)) in the sorted q_seq
-      int lo = 0, hi = num_q;
-      while (lo < hi) {
-        const int m = (lo + hi) >> 1;
-        if (__ldg(q_seq + m) < b) lo = m + 1; else hi = m;
+  const uint32_t ring = smem_addr(gather_smem) + warp * kGatherRing * kGatherGroup;
+  const int R = (int)__ldg(rl.meta);
+  int64_t g0, g1;
+  warp_share(__ldg(rl.meta + 1), g0, g1);
+  if (g0 >= g1) return;
+
+  // token -> key row of query q (nullptr: skip), with fault reporting
+  auto row_of = [&](int q, int b, int n_ctx, int pos) -> const uint16_t* {
+    if (pos >= pool_size) return nullptr;
+    const int t = __ldg(pool + (int64_t)q * pool_size + pos);
+    if (t < 0 || t >= n_ctx) {
+      if (t != -1 && c == 0) report(st, CSA2_DEV_BAD_INDEX);
+      return nullptr;
+    }
+    const int32_t pg = __ldg(g.page_table + (int64_t)b * g.max_pages + (t >> 6));
+    if (pg < 0 || pg >= g.num_pages) {
+      if (c == 0) report(st, CSA2_DEV_BAD_PAGE);
+      return nullptr;
+    }
+    return keys + ((int64_t)pg * kPage + (t & (kPage - 1))) * kDidx;
+  };
+  struct QInfo {
+    int q = -1, b = -1, n_ctx = 0;
+  };
+  auto info = [&](int q) {
+    QInfo f;
+    f.q = q;
+    const int b = __ldg(q_seq + q);
+    if (b >= 0 && b < g.num_seqs) {
+      f.b = b;
+      f.n_ctx = min(max(0, __ldg(g.seq_lens + b)), g.max_pages * kPage);
+    }
+    return f;
+  };
+  RunCursor lc, cc;
+  cursor_seek(lc, rl, R, g0);
+  cc = lc;
+  QInfo li = info(lc.r), ci;
+  uint32_t okmask = 0;  // 2 bits per ring slot: rows gq and gq + 8 of the group loaded
+  auto issue = [&](int64_t gg, int sl) {
+    okmask &= ~(3u << (2 * sl));
+    if (gg < g1) {
+      cursor_advance(lc, rl, gg);
+      if (lc.r != li.q) li = info(lc.r);
+      if (li.b >= 0) {
+        const int pos = (int)(gg - lc.start) * 16 + gq;
+        const uint32_t slot = ring + sl * kGatherGroup;
+        const uint16_t* ra = row_of(li.q, li.b, li.n_ctx, pos);
+        const uint16_t* rb = row_of(li.q, li.b, li.n_ctx, pos + 8);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int k = 4 * j + c;
+          if (ra) cp_async16(slot + gq * kKeyRow + ((k ^ gq) << 4), reinterpret_cast<const char*>(ra) + 16 * k);
+          if (rb) cp_async16(slot + (gq + 8) * kKeyRow + ((k ^ gq) << 4), reinterpret_cast<const char*>(rb) + 16 * k);
+        }
+        okmask |= ((ra ? 1u : 0u) | (rb ? 2u : 0u)) << (2 * sl);
       }
-      int lo2 = lo, hi2 = num_q;
-      while (lo2 < hi2) {
-        const int m = (lo2 + hi2) >> 1;
-        if (__ldg(q_seq + m) <= b) lo2 = m + 1; else hi2 = m;
+    }
+    cp_async_commit();
+  };
+  uint32_t bq[4][4];
+  int slot = 0;
+#pragma unroll
+  for (int i = 0; i < kGatherRing - 1; ++i) issue(g0 + i, i);
+  for (int64_t gg = g0; gg < g1; ++gg) {
+    issue(gg + kGatherRing - 1, (slot + kGatherRing - 1) & (kGatherRing - 1));
+    cp_async_wait<kGatherRing - 1>();
+    cursor_advance(cc, rl, gg);
+    if (cc.r != ci.q) {
+      ci = info(cc.r);
+      if (ci.b < 0 && lane == 0) report(st, CSA2_DEV_BAD_QSEQ);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {  // B fragments: column gq < 4 holds head gq
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (gq < kHidx)
+          v = __ldg(reinterpret_cast<const uint4*>(q_idx + ((int64_t)ci.q * kHidx + gq) * kDidx +
+                                                   32 * j + 8 * c));
+        bq[j][0] = v.x; bq[j][1] = v.y; bq[j][2] = v.z; bq[j][3] = v.w;
       }
-      q0 = lo;
-      T = lo2 - lo;
+    }
+    const uint32_t sbase = ring + slot * kGatherGroup;
+    uint4 k0[4], k1[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int k = 4 * j + c;
+      k0[j] = lds128(sbase + gq * kKeyRow + ((k ^ gq) << 4));
+      k1[j] = lds128(sbase + (gq + 8) * kKeyRow + ((k ^ gq) << 4));
+    }
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      mma_bf16_16816(d, k0[j].x, k1[j].x, k0[j].y, k1[j].y, bq[j][0], bq[j][1]);
+      mma_bf16_16816(d, k0[j].z, k1[j].z, k0[j].w, k1[j].w, bq[j][2], bq[j][3]);
+    }
+    float s0 = fmaxf(d[0], 0.f) + fmaxf(d[1], 0.f);
+    float s1 = fmaxf(d[2], 0.f) + fmaxf(d[3], 0.f);
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+    if (c == 0 && ci.b >= 0) {
+      const uint32_t ok = okmask >> (2 * slot);
+      const int pos = (int)(gg - cc.start) * 16 + gq;
+      uint32_t* out = ws + (int64_t)ci.q * pool_size;
+      if (pos < pool_size) out[pos] = (ok & 1u) ? rank_key(s0) : 0u;
+      if (pos + 8 < pool_size) out[pos + 8] = (ok & 2u) ? rank_key(s1) : 0u;
+    }
+    slot = (slot + 1) & (kGatherRing - 1);
+  }
+}
+
+// ------------------------------------------------------------------ TMA page scorer --
+// Full mode, contiguous context: the unit of work is a whole 64-token page (16 KB of
+// keys).  One producer thread streams pages through a 2D tensor map (two 64 x 64 bf16
+// boxes per page, 128-byte swizzle) into a 12-slot shared-memory ring.  The 8 consumer
+// warps take the pages in pairs: warp w scores rows 8w .. 8w+7 of both pages of a pair
+// as the 16 rows of one tensor-core tile:
+//   D[16 keys][8 cols] = K[16 keys][16 dims] x Q^T[16 dims][8 cols]   (m16n8k16, bf16)
+// where the 8 columns of an n-tile are (query, head) pairs 4t + h of two queries, so
+// one n-tile serves 1-2 queries and two serve 3-4 draft queries of a sequence.  Dims
+// are visited in the same permuted order on both sides: lane c's 16-byte chunk of dims
+// 32j + 8c .. +7 supplies its A and B fragments for k-steps 2j and 2j + 1.
+// Measured on B300, the CUDA-core form of this dot product (packed FFMA2, one key
+// per 4 lanes) ran at 124 us of pure arithmetic for 2.1M keys against 85 us to stream
+// them, so the contraction runs on the tensor cores even for a single query.
+
+constexpr int kPageStages = 12;
+constexpr int kPageBytes = kPage * kKeyRow;            // 16 KB
+constexpr int kConsumerWarps = 8;
+constexpr int kTmaThreads = (kConsumerWarps + 1) * 32;  // + 1 producer warp
+
+struct PageRing {
+  uint64_t full[kPageStages];
+  uint64_t empty[kPageStages];
+  int32_t run[kPageStages];   // run of the staged page
+  int32_t page[kPageStages];  // page index within the run
+  int32_t valid[kPageStages]; // 1 if its keys were loaded
+  volatile int abort;
+};
+constexpr size_t kTmaSmem = (size_t)kPageStages * kPageBytes + sizeof(PageRing) + 1024;
+
+// Row `row` (0..63), 16-byte chunk `k` (0..15) of a staged page: two 8 KB halves
+// (dims 0-63, 64-127), each 64 rows of 128 bytes with the chunk index XOR-ed by row % 8.
+__device__ __forceinline__ uint32_t page_chunk(uint32_t base, int row, int k) {
+  return base + (uint32_t)((k >> 3) * 8192 + row * 128 + (((k & 7) ^ (row & 7)) << 4));
+}
+__device__ __forceinline__ void read_page_row(uint4 (&kv)[4], uint32_t base, int row, int c) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) kv[j] = lds128(page_chunk(base, row, 4 * j + c));
+}
+
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    score_pages_kernel(const __grid_constant__ CUtensorMap keymap, const uint16_t* __restrict__ q_idx,
+                       const int32_t* __restrict__ q_seq, int32_t num_q, ScoreGeom g,
+                       uint32_t* __restrict__ ws, int64_t ws_stride, RunList rl, int32_t* st) {
+  extern __shared__ __align__(1024) unsigned char page_smem_raw[];
+  unsigned char* data = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(page_smem_raw) + 1023) & ~uintptr_t(1023));
+  PageRing* ring = reinterpret_cast<PageRing*>(data + kPageStages * kPageBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, c = lane & 3;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPageStages; ++s) {
+      mbar_init(&ring->full[s], 1);
+      mbar_init(&ring->empty[s], kConsumerWarps);
+    }
+    ring->abort = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  const int R = (int)__ldg(rl.meta);
+  const int64_t total = __ldg(rl.meta + 1);
+  const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+  const int64_t p0 = min(total, (int64_t)blockIdx.x * per), p1 = min(total, p0 + per);
+  const uint32_t data_s = saddr(data);
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer ----------------
+    if (lane == 0 && p0 < p1) {
+      RunCursor cu;
+      cursor_seek(cu, rl, R, p0);
+      uint32_t issued = 0, last_par = 0;
+      for (int64_t i = p0; i < p1; ++i) {
+        const int s = (int)((i - p0) % kPageStages);
+        const uint32_t ph = (uint32_t)(((i - p0) / kPageStages) & 1);
+        if (!mbar_wait(&ring->abort, &ring->empty[s], ph ^ 1u, st)) break;
+        cursor_advance(cu, rl, i);
+        const int page = (int)(i - cu.start);
+        const int b = __ldg(q_seq + __ldg(rl.run_q0 + cu.r));
+        int32_t pg = -1;
+        if (b >= 0 && b < g.num_seqs) pg = __ldg(g.page_table + (int64_t)b * g.max_pages + page);
+        ring->run[s] = cu.r;
+        ring->page[s] = page;
+        if (pg >= 0 && pg < g.num_pages) {
+          ring->valid[s] = 1;
+          unsigned char* dst = data + s * kPageBytes;
+          mbar_expect_tx(&ring->full[s], kPageBytes);
+          tma_load_2d(dst, &keymap, &ring->full[s], 0, pg * kPage);
+          tma_load_2d(dst + 8192, &keymap, &ring->full[s], 64, pg * kPage);
+          issued |= 1u << s;
+          last_par = (last_par & ~(1u << s)) | (ph << s);
+        } else {
+          ring->valid[s] = 0;
+          report(st, CSA2_DEV_BAD_PAGE);
+          mbar_arrive(&ring->full[s]);
+        }
+      }
+      if (ring->abort)  // our copies must land before the CTA's shared memory is released
+        for (int s = 0; s < kPageStages; ++s)
+          if (issued & (1u << s)) (void)mbar_wait(&ring->abort, &ring->full[s], (last_par >> s) & 1u, st, 1u << 20);
+    }
+  } else {
+    // ---------------- consumers: every warp takes every page, two pages per step ----
+    const int rr = 8 * warp + gq;  // this lane's row in each page of the pair
+    int cur_run = -1, rows = 0, q0 = 0, T = 0, NT = 0;
+    uint32_t bq[2][4][4];  // [n-tile][j][word]: B fragments of Q^T
+    auto enter = [&](int r) {
+      if (r == cur_run) return;
+      cur_run = r;
+      q0 = __ldg(rl.run_q0 + r);
+      T = __ldg(rl.run_q0 + r + 1) - q0;
       if (T > 4) {
-        if (threadIdx.x == 0 && chunk == 0) report(st, CSA2_DEV_BAD_QSEQ);
+        if (lane == 0) report(st, CSA2_DEV_BAD_QSEQ);
         T = 4;
       }
-      cur_b = b;
-      // A fragments: rows r = 4t + h; lane holds rows gq and gq + 8.
+      NT = (T + 1) >> 1;
+      const int b = __ldg(q_seq + q0);
+      rows = (b >= 0 && b < g.num_seqs) ? min(max(0, __ldg(g.seq_lens + b)), g.max_pages * kPage) : 0;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int t = 2 * nt + (gq >> 2), h = gq & 3;  // column gq of n-tile nt
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (t < T)
+            v = __ldg(reinterpret_cast<const uint4*>(
+                q_idx + ((int64_t)(q0 + t) * kHidx + h) * kDidx + 32 * j + 8 * c));
+          bq[nt][j][0] = v.x; bq[nt][j][1] = v.y; bq[nt][j][2] = v.z; bq[nt][j][3] = v.w;
+        }
+      }
+    };
+    // MMA over (row a of one page, row b of another page) with the current run's Q;
+    // scores of a (b) go to page pa (pb); use_a / use_b select which halves to store.
+    auto tile = [&](const uint4 (&ka)[4], const uint4 (&kb)[4], int pa, int pb, bool va, bool vb,
+                    bool use_a, bool use_b) {
+      float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        uint32_t u0[4] = {0, 0, 0, 0}, u1[4] = {0, 0, 0, 0};
-        const int t0 = gq >> 2, t1 = t0 + 2, h = gq & 3;
-        if (t0 < T) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-              q_idx + ((int64_t)(q0 + t0) * kHidx + h) * kDidx + 32 * j + 8 * c));
-          u0[0] = v.x; u0[1] = v.y; u0[2] = v.z; u0[3] = v.w;
+        // k-step 2j: words x, y; k-step 2j + 1: words z, w
+        mma_bf16_16816(d[0], ka[j].x, kb[j].x, ka[j].y, kb[j].y, bq[0][j][0], bq[0][j][1]);
+        mma_bf16_16816(d[0], ka[j].z, kb[j].z, ka[j].w, kb[j].w, bq[0][j][2], bq[0][j][3]);
+        if (NT > 1) {
+          mma_bf16_16816(d[1], ka[j].x, kb[j].x, ka[j].y, kb[j].y, bq[1][j][0], bq[1][j][1]);
+          mma_bf16_16816(d[1], ka[j].z, kb[j].z, ka[j].w, kb[j].w, bq[1][j][2], bq[1][j][3]);
         }
-        if (t1 < T) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-              q_idx + ((int64_t)(q0 + t1) * kHidx + h) * kDidx + 32 * j + 8 * c));
-          u1[0] = v.x; u1[1] = v.y; u1[2] = v.z; u1[3] = v.w;
+      }
+      // d[nt][0..1]: row a, columns 2c, 2c+1; d[nt][2..3]: row b.  Columns 4t'+h of
+      // query t' = 2nt + c/2: ReLU, then sum the query's 4 heads over lanes c, c^1.
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        if (nt >= NT) break;
+        float s0 = fmaxf(d[nt][0], 0.f) + fmaxf(d[nt][1], 0.f);
+        float s1 = fmaxf(d[nt][2], 0.f) + fmaxf(d[nt][3], 0.f);
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+        const int t = 2 * nt + (c >> 1);
+        if ((c & 1) == 0 && t < T) {
+          uint32_t* out = ws + (int64_t)(q0 + t) * ws_stride;
+          const int ta = pa * kPage + rr, tb = pb * kPage + rr;
+          if (use_a && ta < rows) out[ta] = va ? rank_key(s0) : 0u;
+          if (use_b && tb < rows) out[tb] = vb ? rank_key(s1) : 0u;
         }
-        a[2 * j][0] = u0[0]; a[2 * j][1] = u1[0]; a[2 * j][2] = u0[1]; a[2 * j][3] = u1[1];
-        a[2 * j + 1][0] = u0[2]; a[2 * j + 1][1] = u1[2]; a[2 * j + 1][2] = u0[3]; a[2 * j + 1][3] = u1[3];
       }
-    }
-    if (T == 0) continue;
-    const int groups = (count + 7) >> 3;
-    const int mine = groups > warp ? (groups - warp + 7) >> 3 : 0;
-    auto locate = [&](int k, const uint16_t*& row) -> bool {
-      const int t = begin + 8 * (warp + 8 * k) + gq;
-      row = keys;
-      if (t >= begin + count) return false;
-      const int32_t pg = __ldg(g.page_table + (int64_t)b * g.max_pages + (t >> 6));
-      if (pg < 0 || pg >= g.num_pages) {
-        if (c == 0) report(st, CSA2_DEV_BAD_PAGE);
-        return false;
-      }
-      row = keys + ((int64_t)pg * kPage + (t & (kPage - 1))) * kDidx;
-      return true;
     };
-    uint4 buf[kDepth][4];
-    bool ok[kDepth];
-#pragma unroll
-    for (int i = 0; i < kDepth; ++i) {
-      ok[i] = false;
-      if (i < mine) {
-        const uint16_t* row;
-        ok[i] = locate(i, row);
-        load_row(buf[i], row, c);
+    const uint4 zero4[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                            make_uint4(0, 0, 0, 0)};
+    for (int64_t i = p0; i < p1; i += 2) {
+      const int s0 = (int)((i - p0) % kPageStages);
+      const uint32_t ph0 = (uint32_t)(((i - p0) / kPageStages) & 1);
+      if (!mbar_wait(&ring->abort, &ring->full[s0], ph0, st)) break;
+      const bool has1 = i + 1 < p1;
+      const int s1 = (int)((i + 1 - p0) % kPageStages);
+      if (has1) {
+        const uint32_t ph1 = (uint32_t)(((i + 1 - p0) / kPageStages) & 1);
+        if (!mbar_wait(&ring->abort, &ring->full[s1], ph1, st)) break;
       }
-    }
-    for (int k0 = 0; k0 < mine; k0 += kDepth) {
-#pragma unroll
-      for (int i = 0; i < kDepth; ++i) {
-        const int k = k0 + i;
-        if (k < mine) {
-          float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t bw[4] = {buf[i][j].x, buf[i][j].y, buf[i][j].z, buf[i][j].w};
-#pragma unroll
-            for (int hs = 0; hs < 2; ++hs) {
-              const uint32_t* aa = a[2 * j + hs];
-              asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
-                  "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                  : "r"(aa[0]), "r"(aa[1]), "r"(aa[2]), "r"(aa[3]), "r"(bw[2 * hs]),
-                    "r"(bw[2 * hs + 1]));
-            }
-          }
-          // d0,d1: row gq (t = gq/4, head gq%4), keys 2c, 2c+1; d2,d3: row gq + 8 (t + 2)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float r = d[e] > 0.0f ? d[e] : 0.0f;
-            r += __shfl_xor_sync(0xffffffffu, r, 4);
-            r += __shfl_xor_sync(0xffffffffu, r, 8);
-            d[e] = r;
-          }
-          // validity of keys 2c and 2c+1 of this group: held by quads 2c and 2c+1
-          const int okb = ok[i] ? 1 : 0;
-          const int ok0 = __shfl_sync(0xffffffffu, okb, (2 * c) * 4);
-          const int ok1 = __shfl_sync(0xffffffffu, okb, (2 * c + 1) * 4);
-          if ((gq & 3) == 0) {
-            const int t0 = gq >> 2;
-            const int base = begin + 8 * (warp + 8 * k);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int t = t0 + ((e >> 1) << 1);
-              const int pos = base + 2 * c + (e & 1);
-              const int okk = (e & 1) ? ok1 : ok0;
-              if (t < T && pos < begin + count)
-                ws[(int64_t)(q0 + t) * ws_stride + pos] = okk ? rank_key(d[e]) : 0u;
-            }
-          }
-          if (k + kDepth < mine) {
-            const uint16_t* row;
-            ok[i] = locate(k + kDepth, row);
-            load_row(buf[i], row, c);
-          }
+      const int run0 = ring->run[s0], page0 = ring->page[s0];
+      const bool v0 = ring->valid[s0] != 0;
+      const int run1 = has1 ? ring->run[s1] : run0, page1 = has1 ? ring->page[s1] : page0;
+      const bool v1 = has1 && ring->valid[s1] != 0;
+      uint4 k0[4], k1[4];
+      read_page_row(k0, data_s + s0 * kPageBytes, rr, c);
+      if (has1) read_page_row(k1, data_s + s1 * kPageBytes, rr, c);
+      __syncwarp();
+      if (lane == 0) {  // the keys are in registers now
+        mbar_arrive(&ring->empty[s0]);
+        if (has1) mbar_arrive(&ring->empty[s1]);
+      }
+      enter(run0);
+      if (has1 && run1 == run0) {
+        tile(k0, k1, page0, page1, v0, v1, true, true);
+      } else {
+        tile(k0, zero4, page0, page0, v0, false, true, false);
+        if (has1) {
+          enter(run1);
+          tile(k1, zero4, page1, page1, v1, false, true, false);
         }
       }
     }
   }
+  __syncthreads();
 }
 
 // ------------------------------------------------------------------ selection -----
 
 constexpr int kSelCluster = 8;
 constexpr int kSelThreads = 512;
+constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelCacheKeys = 16384;  // per-CTA keys kept in shared memory (64 KB)
-constexpr int kBins = 2048;
+constexpr int kDigit = 256;
+constexpr int kSamplesPerCta = 256;
+constexpr int kSamples = kSelCluster * kSamplesPerCta;  // 2048 samples per query
+constexpr int kCandCap = 256;                           // kept positions per warp per target
 
 struct SelShared {
-  uint32_t hist[2][2][kBins];        // [buffer][target][bin]
-  uint32_t counts[4];                // gtK, eqK, gtP, eqP of this CTA
-  uint32_t nvalid;                   // valid keys of this CTA
-  uint32_t warp_tmp[kSelThreads / 32][2];
+  union {
+    uint32_t whist[kSelWarps][2][kDigit];  // per-warp histograms (full-sweep path)
+    struct {
+      uint32_t samp[kSamples];              // the cluster's samples
+      uint32_t mysamp[kSamplesPerCta];      // this CTA's samples (read by the cluster)
+      uint32_t samp2[2048];                 // histogram of the samples' top 11 bits
+      uint16_t cand[2][kSelWarps][kCandCap];  // kept positions per target, per warp
+    } f;
+  } u;
+  uint32_t lhist[2][kDigit];                // CTA histograms (samples, kept keys)
+  uint32_t chist[2][2][kDigit];             // [buffer][target][bin]: read by the cluster
+  uint32_t wcnt[kSelWarps][4];              // per-warp (gt, eq) counts of both targets
+  uint32_t ccnt[4];                         // this CTA's (gt, eq) counts
+  uint32_t wvalid[kSelWarps];
+  uint32_t cvalid;
+  uint32_t wcand[kSelWarps][2];             // kept keys per warp and target
+  uint32_t ccand[2];
+  uint32_t cover;                           // a warp of this CTA overflowed its buffer
+  uint32_t nzs;                             // non-zero samples of the cluster
+  uint32_t scan[2][kDigit / 32];
   uint32_t res_prefix[2], res_above[2];
-  uint32_t scan_carry[2][2];
 };
 
-// Exclusive suffix sums of (v0, v1) over the threads of the block:
-// out = sum over threads with a larger index.  Also returns block totals.
-__device__ __forceinline__ void block_suffix2(SelShared& sh, uint32_t v0, uint32_t v1,
-                                              uint32_t& s0, uint32_t& s1, uint32_t& t0,
-                                              uint32_t& t1) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t x0 = v0, x1 = v1;  // inclusive suffix within the warp
+// The key cache follows SelShared at a 128-byte boundary (it is read as uint4).
+constexpr size_t kSelCacheOff = (sizeof(SelShared) + 127) / 128 * 128;
+static_assert(kSelCacheOff % 16 == 0, "key cache must be 16-byte aligned");
+
+// Warp-wide exclusive prefix sum of v and the warp total.
+__device__ __forceinline__ uint32_t warp_excl(uint32_t v, uint32_t& total) {
+  const int lane = threadIdx.x & 31;
+  uint32_t x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y0 = __shfl_down_sync(0xffffffffu, x0, o);
-    const uint32_t y1 = __shfl_down_sync(0xffffffffu, x1, o);
-    if (lane + o < 32) {
-      x0 += y0;
-      x1 += y1;
-    }
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
-  __syncthreads();
-  if (lane == 0) {
-    sh.warp_tmp[warp][0] = x0;
-    sh.warp_tmp[warp][1] = x1;
-  }
-  __syncthreads();
-  uint32_t w0 = 0, w1 = 0, a0 = 0, a1 = 0;
-  for (int w = 0; w < kSelThreads / 32; ++w) {
-    if (w > warp) {
-      w0 += sh.warp_tmp[w][0];
-      w1 += sh.warp_tmp[w][1];
-    }
-    a0 += sh.warp_tmp[w][0];
-    a1 += sh.warp_tmp[w][1];
-  }
-  s0 = w0 + x0 - v0;
-  s1 = w1 + x1 - v1;
-  t0 = a0;
-  t1 = a1;
+  total = __shfl_sync(0xffffffffu, x, 31);
+  return x - v;
 }
 
-// Exclusive prefix sums (lower thread index) of (v0, v1), plus block totals.
-__device__ __forceinline__ void block_prefix2(SelShared& sh, uint32_t v0, uint32_t v1,
-                                              uint32_t& p0, uint32_t& p1, uint32_t& t0,
-                                              uint32_t& t1) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t x0 = v0, x1 = v1;
+// One radix step for up to two targets.  Thread tid holds v = keys in bin tid % 256 of
+// target tid / 256 (keys whose higher digits equal pre_t).  For each target with
+// want_t > 0, find the bin in which the count of keys in strictly higher bins plus
+// abv_t first reaches want_t, and extend pre_t by it (abv_t += keys above that bin).
+__device__ __forceinline__ void find_bins(SelShared& sh, uint32_t v, int width, uint32_t want0,
+                                          uint32_t want1, uint32_t& pre0, uint32_t& pre1,
+                                          uint32_t& abv0, uint32_t& abv1) {
+  const int tid = threadIdx.x, lane = tid & 31, t = tid / kDigit, bin = tid % kDigit;
+  const int tw = bin >> 5;
+  uint32_t x = v;  // inclusive suffix sum within the warp
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y0 = __shfl_up_sync(0xffffffffu, x0, o);
-    const uint32_t y1 = __shfl_up_sync(0xffffffffu, x1, o);
-    if (lane >= o) {
-      x0 += y0;
-      x1 += y1;
+    const uint32_t y = __shfl_down_sync(0xffffffffu, x, o);
+    if (lane + o < 32) x += y;
+  }
+  if (lane == 0) sh.scan[t][tw] = x;
+  __syncthreads();
+  const uint32_t want_t = t == 0 ? want0 : want1;
+  if (want_t > 0) {
+    uint32_t later = 0;
+    for (int w = tw + 1; w < kDigit / 32; ++w) later += sh.scan[t][w];
+    const uint32_t above_bin = (t == 0 ? abv0 : abv1) + later + x - v;
+    if (above_bin < want_t && above_bin + v >= want_t) {
+      sh.res_prefix[t] = ((t == 0 ? pre0 : pre1) << width) | (uint32_t)bin;
+      sh.res_above[t] = above_bin;
     }
   }
   __syncthreads();
-  if (lane == 31) {
-    sh.warp_tmp[warp][0] = x0;
-    sh.warp_tmp[warp][1] = x1;
+  if (want0 > 0) {
+    pre0 = sh.res_prefix[0];
+    abv0 = sh.res_above[0];
+  }
+  if (want1 > 0) {
+    pre1 = sh.res_prefix[1];
+    abv1 = sh.res_above[1];
   }
   __syncthreads();
-  uint32_t w0 = 0, w1 = 0, a0 = 0, a1 = 0;
-  for (int w = 0; w < kSelThreads / 32; ++w) {
-    if (w < warp) {
-      w0 += sh.warp_tmp[w][0];
-      w1 += sh.warp_tmp[w][1];
-    }
-    a0 += sh.warp_tmp[w][0];
-    a1 += sh.warp_tmp[w][1];
-  }
-  p0 = w0 + x0 - v0;
-  p1 = w1 + x1 - v1;
-  t0 = a0;
-  t1 = a1;
 }
 
-// Top-k selection for one query per cluster (gridDim.y = num_q).  Targets: t = 0 is
+__device__ __forceinline__ int digit_shift(int pass) {
+  return pass == 0 ? 23 : pass == 1 ? 15 : pass == 2 ? 7 : 0;
+}
+__device__ __forceinline__ int digit_width(int pass) { return pass == 3 ? 7 : 8; }
+
+// Top-k selection for one query per 8-CTA cluster (gridDim.y = num_q).  Target t = 0 is
 // the top-K output, t = 1 the candidate pool (FULL with a pool output only).
+//
+// Fast path: every CTA takes 256 evenly spaced samples of its range; from the
+// cluster's 2048 samples each target gets a threshold tau_t: the lower edge of the
+// 1/8-octave bin holding the r-th largest sample, r = 1.25 e + 4 sqrt(e) + 8, where
+// e = want * 2048 / n samples are expected above the answer.  One ordered sweep keeps the positions of keys >= tau_t; if the kept
+// keys number at least want_t (and no warp overflowed its buffer) they contain every
+// key of the answer, ties included, so the exact radix select and the ordered output
+// run over the kept keys only.  Otherwise the cluster falls back to radix passes over
+// the whole range.  Either way the result is exact.
 template <bool kReindex>
-__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads, 1)
+__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads, 2)
     select_kernel(const uint32_t* __restrict__ ws, int64_t ws_stride,
                   const int32_t* __restrict__ q_seq, const int32_t* __restrict__ seq_lens,
                   int32_t num_seqs, const int32_t* __restrict__ pool_in, int32_t pool_size,
                   int32_t topk, int32_t* __restrict__ out_idx, int32_t* __restrict__ pool_out,
-                  int32_t* st) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+                  int32_t max_ctx, int32_t* st) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
   SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
-  uint32_t* cache = reinterpret_cast<uint32_t*>(smem_raw + sizeof(SelShared));
+  uint32_t* cache = reinterpret_cast<uint32_t*>(smem_raw + kSelCacheOff);  // 16-B vector reads
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int q = blockIdx.y;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   int n;
   if (kReindex) {
     n = pool_size;
   } else {
     const int b = __ldg(q_seq + q);
-    n = (b >= 0 && b < num_seqs) ? __ldg(seq_lens + b) : 0;
+    n = (b >= 0 && b < num_seqs) ? min(max(0, __ldg(seq_lens + b)), max_ctx) : 0;
   }
-  const int ntargets = (!kReindex && pool_out != nullptr && pool_size > 0) ? 2 : 1;
-  const uint32_t want_max[2] = {(uint32_t)topk, (uint32_t)(kReindex ? 0 : pool_size)};
+  const bool two = (!kReindex && pool_out != nullptr && pool_size > 0);
+  const uint32_t want_max0 = (uint32_t)topk, want_max1 = two ? (uint32_t)pool_size : 0u;
 
-  // this CTA's range of candidate positions
+  // This CTA's range of candidate positions, cut into 16 contiguous warp segments
+  // (multiples of 128) so that outputs keep index order with warp scans.
   int L = (n + kSelCluster - 1) / kSelCluster;
-  L = (L + 3) & ~3;
+  L = (L + 127) & ~127;
   const int lo = min(n, rank * L), hi = min(n, lo + L);
   const int len = hi - lo;
+  int S = (len + kSelWarps - 1) / kSelWarps;
+  S = (S + 127) & ~127;
+  const int seg_lo = min(len, warp * S), seg_hi = min(len, seg_lo + S);
   const uint32_t* src = ws + (int64_t)q * ws_stride + lo;
   const bool cached = len <= kSelCacheKeys;
   if (cached) {
     for (int i = tid; i < len; i += kSelThreads) cache[i] = __ldcg(src + i);
+    __syncthreads();
   }
   auto key_at = [&](int i) -> uint32_t { return cached ? cache[i] : __ldcg(src + i); };
-
-  // ---- pass 0: histogram of bits 31..21 of the valid keys; count valid keys ----
-  for (int i = tid; i < kBins; i += kSelThreads) sh.hist[0][0][i] = 0;
-  __syncthreads();
-  uint32_t my_valid = 0;
-  for (int i = tid; i < len; i += kSelThreads) {
-    const uint32_t k = key_at(i);
-    if (k != 0) {
-      atomicAdd(&sh.hist[0][0][k >> 21], 1u);
-      ++my_valid;
+  // keys i .. i+3 of this CTA's range (i a multiple of 4); positions past seg_hi read 0
+  auto load4 = [&](int i, uint32_t (&k)[4]) {
+    if (cached && i + 4 <= seg_hi) {
+      const uint4 v = *reinterpret_cast<const uint4*>(cache + i);
+      k[0] = v.x; k[1] = v.y; k[2] = v.z; k[3] = v.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) k[e] = (i + e < seg_hi) ? key_at(i + e) : 0u;
     }
-  }
-  my_valid = __reduce_add_sync(0xffffffffu, my_valid);
-  if (tid == 0) sh.nvalid = 0;
-  __syncthreads();
-  if ((tid & 31) == 0) atomicAdd(&sh.nvalid, my_valid);
-  cluster.sync();
+  };
 
-  uint32_t nvalid = 0;
-  for (int r = 0; r < kSelCluster; ++r) nvalid += *cluster.map_shared_rank(&sh.nvalid, r);
-  uint32_t want[2], prefix[2] = {0, 0}, above[2] = {0, 0};
-  for (int t = 0; t < 2; ++t) want[t] = min(want_max[t], nvalid);
+  uint32_t want0 = 0, want1 = 0, pre0 = 0, pre1 = 0, abv0 = 0, abv1 = 0;
+  int32_t* out0 = out_idx + (int64_t)q * topk;
+  int32_t* out1 = two ? pool_out + (int64_t)q * pool_size : nullptr;
+  const int32_t* pin = kReindex ? pool_in + (int64_t)q * pool_size + lo : nullptr;
 
-  // ---- radix passes: (shift of the examined digit, digit width, prefix shift) ----
-  const int shifts[3] = {21, 10, 0};
-  const int widths[3] = {11, 11, 10};
-  for (int pass = 0; pass < 3; ++pass) {
-    const int buf = pass & 1;
-    const int shift = shifts[pass], width = widths[pass];
-    const uint32_t dmask = (1u << width) - 1u;
-    if (pass > 0) {
-      for (int t = 0; t < ntargets; ++t)
-        for (int i = tid; i < kBins; i += kSelThreads) sh.hist[buf][t][i] = 0;
+  // ======== fast path, part 1: samples -> thresholds -> one filtering sweep ========
+  const bool fast_ok = L <= 65535;  // kept positions are stored as 16 bits
+  bool fast = false;
+  if (fast_ok) {
+    for (int i = tid; i < kSamplesPerCta; i += kSelThreads) {
+      uint32_t v = 0;
+      if (len >= kSamplesPerCta) v = key_at((int)(((int64_t)i * len) / kSamplesPerCta));
+      else if (i < len) v = key_at(i);
+      sh.u.f.mysamp[i] = v;
+    }
+    cluster.sync();
+    uint32_t nz = 0;
+    for (int i = tid; i < kSamples; i += kSelThreads) {
+      const uint32_t v = *cluster.map_shared_rank(&sh.u.f.mysamp[i % kSamplesPerCta], i / kSamplesPerCta);
+      sh.u.f.samp[i] = v;
+      nz += v != 0;
+    }
+    nz = __reduce_add_sync(0xffffffffu, nz);
+    if (tid == 0) sh.nzs = 0;
+    __syncthreads();
+    if (lane == 0) atomicAdd(&sh.nzs, nz);
+    __syncthreads();
+    const uint32_t n_s = sh.nzs;
+    // rank of the threshold among the non-zero samples, per target
+    uint32_t r0 = 0, r1 = 0;
+    {
+      const double e0 = (double)want_max0 * kSamples / (double)max(n, 1);
+      const double e1 = (double)want_max1 * kSamples / (double)max(n, 1);
+      r0 = (uint32_t)ceil(1.25 * e0 + 4.0 * sqrt(e0) + 8.0);
+      r1 = two ? (uint32_t)ceil(1.25 * e1 + 4.0 * sqrt(e1) + 8.0) : 0u;
+      r0 = min(r0, n_s);
+      r1 = min(r1, n_s);
+    }
+    // tau_t = lower edge of the bin (top 11 key bits: exponent + 3 mantissa bits) in
+    // which the count of samples from the top reaches r_t; at least r_t samples are >= it
+    for (int i = tid; i < 2048; i += kSelThreads) sh.u.f.samp2[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < kSamples; i += kSelThreads) {
+      const uint32_t k = sh.u.f.samp[i];
+      if (k != 0) atomicAdd(&sh.u.f.samp2[k >> 20], 1u);
+    }
+    __syncthreads();
+    uint32_t tau0 = 1u, tau1 = 1u;
+    {
+      // thread tid owns bins 4 tid .. 4 tid + 3; suffix counts over the block
+      uint32_t v4[4], mine = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v4[e] = sh.u.f.samp2[4 * tid + e];
+        mine += v4[e];
+      }
+      uint32_t x = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_down_sync(0xffffffffu, x, o);
+        if (lane + o < 32) x += y;
+      }
+      if (lane == 0) sh.wvalid[warp] = x;  // warp totals (reused scratch)
       __syncthreads();
-      for (int i = tid; i < len; i += kSelThreads) {
-        const uint32_t k = key_at(i);
-        if (k == 0) continue;
-        const uint32_t hiBits = k >> (shift + width);
-        for (int t = 0; t < ntargets; ++t)
-          if (want[t] > 0 && hiBits == prefix[t]) atomicAdd(&sh.hist[buf][t][(k >> shift) & dmask], 1u);
+      uint32_t later = 0;
+      for (int w = warp + 1; w < kSelWarps; ++w) later += sh.wvalid[w];
+      uint32_t acc = later + x - mine;  // samples in bins above this thread's bins
+      if (tid == 0) {
+        sh.res_prefix[0] = 1u;
+        sh.res_prefix[1] = 1u;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const uint32_t r_t = t == 0 ? r0 : r1;
+        if (r_t == 0) continue;
+        uint32_t a = acc;
+        for (int e = 3; e >= 0; --e) {
+          if (a < r_t && a + v4[e] >= r_t) sh.res_prefix[t] = (uint32_t)(4 * tid + e) << 20;
+          a += v4[e];
+        }
+      }
+      __syncthreads();
+      tau0 = max(1u, sh.res_prefix[0]);
+      tau1 = max(1u, sh.res_prefix[1]);
+      __syncthreads();
+    }
+    // ordered filtering sweep, 4 consecutive keys per lane per step
+    uint32_t cnt0 = 0, cnt1 = 0, nval = 0;
+    for (int i0 = seg_lo; i0 < seg_hi; i0 += 128) {
+      const int i = i0 + 4 * lane;
+      uint32_t k[4];
+      load4(i, k);
+      uint32_t m0 = 0, m1 = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        nval += k[e] != 0;
+        if (k[e] != 0 && k[e] >= tau0) m0 |= 1u << e;
+        if (two && k[e] != 0 && k[e] >= tau1) m1 |= 1u << e;
+      }
+      uint32_t tot;
+      uint32_t p = cnt0 + warp_excl(__popc(m0), tot);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (m0 & (1u << e)) {
+          if (p < kCandCap) sh.u.f.cand[0][warp][p] = (uint16_t)(i + e);
+          ++p;
+        }
+      cnt0 += tot;
+      if (two) {
+        p = cnt1 + warp_excl(__popc(m1), tot);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (m1 & (1u << e)) {
+            if (p < kCandCap) sh.u.f.cand[1][warp][p] = (uint16_t)(i + e);
+            ++p;
+          }
+        cnt1 += tot;
+      }
+    }
+    nval = __reduce_add_sync(0xffffffffu, nval);
+    if (lane == 0) {
+      sh.wcand[warp][0] = cnt0;
+      sh.wcand[warp][1] = cnt1;
+      sh.wvalid[warp] = nval;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t a = 0, b = 0, v = 0, ov = 0;
+      for (int w = 0; w < kSelWarps; ++w) {
+        a += sh.wcand[w][0];
+        b += sh.wcand[w][1];
+        v += sh.wvalid[w];
+        ov |= (sh.wcand[w][0] > kCandCap || sh.wcand[w][1] > kCandCap) ? 1u : 0u;
+      }
+      sh.ccand[0] = a;
+      sh.ccand[1] = b;
+      sh.cvalid = v;
+      sh.cover = ov;
+    }
+    cluster.sync();
+    uint32_t nvalid = 0, ct0 = 0, ct1 = 0, ovf = 0;
+#pragma unroll
+    for (int r = 0; r < kSelCluster; ++r) {
+      nvalid += *cluster.map_shared_rank(&sh.cvalid, r);
+      ct0 += *cluster.map_shared_rank(&sh.ccand[0], r);
+      ct1 += *cluster.map_shared_rank(&sh.ccand[1], r);
+      ovf |= *cluster.map_shared_rank(&sh.cover, r);
+    }
+    want0 = min(want_max0, nvalid);
+    want1 = min(want_max1, nvalid);
+    fast = ovf == 0 && ct0 >= want0 && (!two || ct1 >= want1);
+  }
+
+  if (fast) {
+    // ======== fast path, part 2: exact radix select over the kept keys ========
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+      const int buf = pass & 1, shift = digit_shift(pass), width = digit_width(pass);
+      const uint32_t dmask = (1u << width) - 1u;
+      sh.lhist[tid / kDigit][tid % kDigit] = 0;
+      __syncthreads();
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const uint32_t want_t = t == 0 ? want0 : want1, pre_t = t == 0 ? pre0 : pre1;
+        if (want_t == 0) continue;
+        const uint32_t cnt = sh.wcand[warp][t];
+        for (uint32_t j = lane; j < cnt; j += 32) {
+          const uint32_t k = key_at(sh.u.f.cand[t][warp][j]);
+          if (pass == 0 || (k >> (shift + width)) == pre_t)
+            atomicAdd(&sh.lhist[t][(k >> shift) & dmask], 1u);
+        }
+      }
+      __syncthreads();
+      sh.chist[buf][tid / kDigit][tid % kDigit] = sh.lhist[tid / kDigit][tid % kDigit];
+      cluster.sync();
+      uint32_t v = 0;
+      {
+        uint32_t part[kSelCluster];
+#pragma unroll
+        for (int r = 0; r < kSelCluster; ++r)
+          part[r] = *cluster.map_shared_rank(&sh.chist[buf][tid / kDigit][tid % kDigit], r);
+#pragma unroll
+        for (int r = 0; r < kSelCluster; ++r) v += part[r];
+      }
+      find_bins(sh, v, width, want0, want1, pre0, pre1, abv0, abv1);
+    }
+    // counts per warp over its kept keys
+    uint32_t gt[2] = {0, 0}, eq[2] = {0, 0};
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const uint32_t want_t = t == 0 ? want0 : want1, T = t == 0 ? pre0 : pre1;
+      if (want_t == 0) continue;
+      const uint32_t cnt = sh.wcand[warp][t];
+      for (uint32_t j = lane; j < cnt; j += 32) {
+        const uint32_t k = key_at(sh.u.f.cand[t][warp][j]);
+        gt[t] += k > T;
+        eq[t] += k == T;
+      }
+      gt[t] = __reduce_add_sync(0xffffffffu, gt[t]);
+      eq[t] = __reduce_add_sync(0xffffffffu, eq[t]);
+    }
+    if (lane == 0) {
+      sh.wcnt[warp][0] = gt[0];
+      sh.wcnt[warp][1] = eq[0];
+      sh.wcnt[warp][2] = gt[1];
+      sh.wcnt[warp][3] = eq[1];
+    }
+  } else {
+    // ======== full-sweep path: four radix passes over the whole range ========
+    want0 = want1 = pre0 = pre1 = abv0 = abv1 = 0;
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+      const int buf = pass & 1, shift = digit_shift(pass), width = digit_width(pass);
+      const uint32_t dmask = (1u << width) - 1u;
+      const bool h1 = pass > 0 && two && want1 > 0;  // second histogram needed
+      for (int i = lane; i < kDigit; i += 32) {
+        sh.u.whist[warp][0][i] = 0;
+        sh.u.whist[warp][1][i] = 0;
+      }
+      __syncwarp();
+      uint32_t nval = 0;
+      for (int i = seg_lo + 4 * lane; i < seg_hi; i += 128) {
+        uint32_t k[4];
+        load4(i, k);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t kk = k[e];
+          if (kk == 0) continue;
+          ++nval;
+          const uint32_t top = kk >> (shift + width), d = (kk >> shift) & dmask;
+          if (pass == 0 || (want0 > 0 && top == pre0)) atomicAdd(&sh.u.whist[warp][0][d], 1u);
+          if (h1 && top == pre1) atomicAdd(&sh.u.whist[warp][1][d], 1u);
+        }
+      }
+      if (pass == 0) {
+        nval = __reduce_add_sync(0xffffffffu, nval);
+        if (lane == 0) sh.wvalid[warp] = nval;
+      }
+      __syncthreads();
+      {
+        const int t = tid / kDigit, bin = tid % kDigit;
+        uint32_t sum = 0;
+#pragma unroll 4
+        for (int w = 0; w < kSelWarps; ++w) sum += sh.u.whist[w][t][bin];
+        sh.chist[buf][t][bin] = sum;
+        if (pass == 0 && tid == 0) {
+          uint32_t v = 0;
+          for (int w = 0; w < kSelWarps; ++w) v += sh.wvalid[w];
+          sh.cvalid = v;
+        }
       }
       cluster.sync();
-    }
-    // sum the cluster's histograms: thread handles bins 4*tid .. 4*tid+3
-    for (int t = 0; t < ntargets; ++t) {
+      if (pass == 0) {
+        uint32_t nvalid = 0;
+#pragma unroll
+        for (int r = 0; r < kSelCluster; ++r) nvalid += *cluster.map_shared_rank(&sh.cvalid, r);
+        want0 = min(want_max0, nvalid);
+        want1 = min(want_max1, nvalid);
+      }
+      const int t = tid / kDigit, bin = tid % kDigit;
       const int tsrc = pass == 0 ? 0 : t;
-      uint32_t v[4] = {0, 0, 0, 0};
-      if (4 * tid < (1 << width)) {
-        for (int r = 0; r < kSelCluster; ++r) {
-          const uint4 x = *reinterpret_cast<const uint4*>(
-              cluster.map_shared_rank(&sh.hist[buf][tsrc][4 * tid], r));
-          v[0] += x.x; v[1] += x.y; v[2] += x.z; v[3] += x.w;
-        }
+      uint32_t v = 0;
+      if (bin <= (int)dmask) {
+        uint32_t part[kSelCluster];
+#pragma unroll
+        for (int r = 0; r < kSelCluster; ++r) part[r] = *cluster.map_shared_rank(&sh.chist[buf][tsrc][bin], r);
+#pragma unroll
+        for (int r = 0; r < kSelCluster; ++r) v += part[r];
       }
-      const uint32_t mysum = v[0] + v[1] + v[2] + v[3];
-      uint32_t suf, dummy, tot, dummy2;
-      block_suffix2(sh, mysum, 0u, suf, dummy, tot, dummy2);
-      if (want[t] > 0) {
-        // bins above this thread's 4 bins hold `above + suf` keys
-        uint32_t acc = above[t] + suf;
-        if (acc < want[t] && acc + mysum >= want[t]) {
-          for (int e = 3; e >= 0; --e) {
-            if (acc + v[e] >= want[t]) {
-              sh.res_prefix[t] = (prefix[t] << width) | (uint32_t)(4 * tid + e);
-              sh.res_above[t] = acc;
-              break;
-            }
-            acc += v[e];
-          }
-        }
+      find_bins(sh, v, width, want0, want1, pre0, pre1, abv0, abv1);
+    }
+    uint32_t gt0 = 0, eq0 = 0, gt1 = 0, eq1 = 0;
+    for (int i = seg_lo + 4 * lane; i < seg_hi; i += 128) {
+      uint32_t k[4];
+      load4(i, k);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        gt0 += want0 > 0 && k[e] > pre0;
+        eq0 += want0 > 0 && k[e] == pre0;
+        gt1 += want1 > 0 && k[e] > pre1;
+        eq1 += want1 > 0 && k[e] == pre1;
       }
-      __syncthreads();
-      if (want[t] > 0) {
-        prefix[t] = sh.res_prefix[t];
-        above[t] = sh.res_above[t];
-      }
-      __syncthreads();
+    }
+    gt0 = __reduce_add_sync(0xffffffffu, gt0);
+    eq0 = __reduce_add_sync(0xffffffffu, eq0);
+    gt1 = __reduce_add_sync(0xffffffffu, gt1);
+    eq1 = __reduce_add_sync(0xffffffffu, eq1);
+    if (lane == 0) {
+      sh.wcnt[warp][0] = gt0;
+      sh.wcnt[warp][1] = eq0;
+      sh.wcnt[warp][2] = gt1;
+      sh.wcnt[warp][3] = eq1;
     }
   }
-  // prefix[t] is now the exact key T_t of the want[t]-th largest; above[t] counts keys > T_t.
-
-  // ---- ordered compaction ----
-  uint32_t gt[2] = {0, 0}, eq[2] = {0, 0};
-  for (int i = tid; i < len; i += kSelThreads) {
-    const uint32_t k = key_at(i);
-    for (int t = 0; t < ntargets; ++t) {
-      if (want[t] == 0) continue;
-      gt[t] += k > prefix[t];
-      eq[t] += k == prefix[t];
-    }
-  }
-  for (int t = 0; t < 2; ++t) {
-    gt[t] = __reduce_add_sync(0xffffffffu, gt[t]);
-    eq[t] = __reduce_add_sync(0xffffffffu, eq[t]);
-  }
-  if (tid < 4) sh.counts[tid] = 0;
+  // preT is the exact key of the want-th largest valid key, abvT the number of keys
+  // strictly greater; wcnt holds every warp's (gt, eq) counts over what it will emit.
   __syncthreads();
-  if ((tid & 31) == 0) {
-    atomicAdd(&sh.counts[0], gt[0]);
-    atomicAdd(&sh.counts[1], eq[0]);
-    atomicAdd(&sh.counts[2], gt[1]);
-    atomicAdd(&sh.counts[3], eq[1]);
+  if (tid < 4) {
+    uint32_t s2 = 0;
+    for (int w = 0; w < kSelWarps; ++w) s2 += sh.wcnt[w][tid];
+    sh.ccnt[tid] = s2;
   }
   cluster.sync();
-  uint32_t base[2] = {0, 0}, take[2] = {0, 0};
-  for (int t = 0; t < ntargets; ++t) {
-    if (want[t] == 0) continue;
-    const uint32_t quota = want[t] - above[t];
-    uint32_t ties_before = 0;
-    for (int r = 0; r < kSelCluster; ++r) {
-      const uint32_t g_r = *cluster.map_shared_rank(&sh.counts[2 * t], r);
-      const uint32_t e_r = *cluster.map_shared_rank(&sh.counts[2 * t + 1], r);
-      const uint32_t tk = quota > ties_before ? min(quota - ties_before, e_r) : 0u;
-      if (r < rank) base[t] += g_r + tk;
-      if (r == rank) take[t] = tk;
+  // output base and tie quota of this warp for target t
+  auto place = [&](int t, uint32_t want_t, uint32_t abv_t, uint32_t& wbase, uint32_t& wtake) {
+    const uint32_t quota = want_t - abv_t;  // ties of the boundary key, lowest positions first
+    uint32_t ties_before = 0, base = 0;
+    for (int r = 0; r < rank; ++r) {
+      const uint32_t g_r = *cluster.map_shared_rank(&sh.ccnt[2 * t], r);
+      const uint32_t e_r = *cluster.map_shared_rank(&sh.ccnt[2 * t + 1], r);
+      base += g_r + (quota > ties_before ? min(quota - ties_before, e_r) : 0u);
       ties_before += e_r;
     }
-  }
-  // walk the range in tiles of 4 consecutive keys per thread
-  int32_t* outp[2] = {out_idx + (int64_t)q * topk,
-                      pool_out ? pool_out + (int64_t)q * pool_size : nullptr};
-  uint32_t tie_run[2] = {0, 0}, sel_run[2] = {0, 0};
-  const int32_t* pin = kReindex ? pool_in + (int64_t)q * pool_size + lo : nullptr;
-  for (int t0 = 0; t0 < len; t0 += 4 * kSelThreads) {
-    const int i0 = t0 + 4 * tid;
-    uint32_t k4[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) k4[e] = (i0 + e < len) ? key_at(i0 + e) : 0u;
-    for (int t = 0; t < ntargets; ++t) {
-      if (want[t] == 0) continue;
-      uint32_t nt = 0;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) nt += (k4[e] == prefix[t]);
-      uint32_t tie_pre, d0, tie_tot, d1;
-      block_prefix2(sh, nt, 0u, tie_pre, d0, tie_tot, d1);
-      uint32_t tr = tie_run[t] + tie_pre;
-      uint32_t selmask = 0, ns = 0;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const bool is_tie = k4[e] == prefix[t];
-        const bool s = (k4[e] > prefix[t]) || (is_tie && tr < take[t]);
-        tr += is_tie;
-        if (s) {
-          selmask |= 1u << e;
-          ++ns;
-        }
+    for (int w = 0; w < warp; ++w) {
+      const uint32_t g_w = sh.wcnt[w][2 * t], e_w = sh.wcnt[w][2 * t + 1];
+      base += g_w + (quota > ties_before ? min(quota - ties_before, e_w) : 0u);
+      ties_before += e_w;
+    }
+    wbase = base;
+    wtake = quota > ties_before ? min(quota - ties_before, sh.wcnt[warp][2 * t + 1]) : 0u;
+  };
+  uint32_t wbase0 = 0, wtake0 = 0, wbase1 = 0, wtake1 = 0;
+  if (want0 > 0) place(0, want0, abv0, wbase0, wtake0);
+  if (want1 > 0) place(1, want1, abv1, wbase1, wtake1);
+  // emit the selected keys of a batch of (up to) 32 x NK keys held by the lanes, in
+  // index order lane-major: lane l holds batch items [NK l, NK l + NK)
+  auto emit = [&](const uint32_t* k, const int* pos, int nk, uint32_t T, uint32_t take,
+                  uint32_t wbase, uint32_t want_t, uint32_t& tie_run, uint32_t& sel_run,
+                  int32_t* outp) {
+    uint32_t nt = 0;
+    for (int e = 0; e < nk; ++e) nt += k[e] == T;
+    uint32_t ttot;
+    uint32_t tr = tie_run + warp_excl(nt, ttot);
+    uint32_t selm = 0, ns = 0;
+    for (int e = 0; e < nk; ++e) {
+      const bool tie = k[e] == T;
+      const bool sel = k[e] > T || (tie && tr < take);
+      tr += tie;
+      if (sel) {
+        selm |= 1u << e;
+        ++ns;
       }
-      uint32_t sel_pre, d2, sel_tot, d3;
-      block_prefix2(sh, ns, 0u, sel_pre, d2, sel_tot, d3);
-      uint32_t pos = base[t] + sel_run[t] + sel_pre;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (selmask & (1u << e)) {
-          const int token = kReindex ? __ldg(pin + i0 + e) : lo + i0 + e;
-          if (pos < want[t]) outp[t][pos] = token;
-          ++pos;
-        }
+    }
+    uint32_t stot;
+    uint32_t p = wbase + sel_run + warp_excl(ns, stot);
+    for (int e = 0; e < nk; ++e)
+      if (selm & (1u << e)) {
+        const int i = pos[e];
+        const int token = kReindex ? __ldg(pin + i) : lo + i;
+        if (p < want_t) outp[p] = token;
+        ++p;
       }
-      tie_run[t] += tie_tot;
-      sel_run[t] += sel_tot;
+    tie_run += ttot;
+    sel_run += stot;
+  };
+  if (fast) {
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const uint32_t want_t = t == 0 ? want0 : want1;
+      if (want_t == 0) continue;
+      const uint32_t T = t == 0 ? pre0 : pre1;
+      const uint32_t take = t == 0 ? wtake0 : wtake1, wbase = t == 0 ? wbase0 : wbase1;
+      int32_t* outp = t == 0 ? out0 : out1;
+      const uint32_t cnt = sh.wcand[warp][t];
+      uint32_t tie_run = 0, sel_run = 0;
+      for (uint32_t j0 = 0; j0 < cnt; j0 += 32) {
+        const uint32_t j = j0 + lane;
+        uint32_t k[1] = {0u};
+        int pos[1] = {0};
+        if (j < cnt) {
+          pos[0] = sh.u.f.cand[t][warp][j];
+          k[0] = key_at(pos[0]);
+        }
+        emit(k, pos, 1, T, take, wbase, want_t, tie_run, sel_run, outp);
+      }
+    }
+  } else {
+    uint32_t tie_run0 = 0, sel_run0 = 0, tie_run1 = 0, sel_run1 = 0;
+    for (int i0 = seg_lo; i0 < seg_hi; i0 += 128) {
+      const int i = i0 + 4 * lane;
+      uint32_t k[4];
+      load4(i, k);
+      const int pos[4] = {i, i + 1, i + 2, i + 3};
+      if (want0 > 0) emit(k, pos, 4, pre0, wtake0, wbase0, want0, tie_run0, sel_run0, out0);
+      if (want1 > 0) emit(k, pos, 4, pre1, wtake1, wbase1, want1, tie_run1, sel_run1, out1);
     }
   }
   // -1 padding after the selected entries
   if (rank == 0) {
-    for (int i = (int)want[0] + tid; i < topk; i += kSelThreads) outp[0][i] = -1;
-    if (ntargets == 2)
-      for (int i = (int)want[1] + tid; i < pool_size; i += kSelThreads) outp[1][i] = -1;
+    for (int i = (int)want0 + tid; i < topk; i += kSelThreads) out0[i] = -1;
+    if (two)
+      for (int i = (int)want1 + tid; i < pool_size; i += kSelThreads) out1[i] = -1;
   }
   cluster.sync();  // no CTA leaves while others may still read its shared memory
 }
 
 // ------------------------------------------------------------------ launchers -----
 
-size_t select_smem_bytes() { return sizeof(SelShared) + (size_t)kSelCacheKeys * 4; }
+size_t select_smem_bytes() { return kSelCacheOff + (size_t)kSelCacheKeys * 4; }
+
+// Bytes of the run list that follows the scores in the workspace.
+size_t runlist_bytes(int32_t num_q) {
+  return (size_t)2 * 8 + (size_t)(num_q + 1) * 8 + (size_t)(num_q + 1) * 4;
+}
+
+static RunList make_runlist(void* base, int32_t num_q) {
+  int64_t* meta = reinterpret_cast<int64_t*>(base);
+  int64_t* prefix = meta + 2;
+  int32_t* run_q0 = reinterpret_cast<int32_t*>(prefix + num_q + 1);
+  return RunList{meta, prefix, run_q0};
+}
 
 cudaError_t launch_score_full(const uint16_t* q_idx, const uint16_t* keys, const int32_t* q_seq,
                               int32_t num_q, int32_t max_q_per_seq, const csa2_pages& pg,
-                              uint32_t* ws, int64_t ws_stride, int32_t* st, cudaStream_t s,
-                              int num_sms) {
+                              uint32_t* ws, int64_t ws_stride, void* runlist, int32_t* st,
+                              cudaStream_t s, int num_sms) {
   ScoreGeom g{pg.seq_lens, pg.page_table, pg.max_pages_per_seq, pg.num_pages, pg.num_seqs};
-  const int units = (pg.max_pages_per_seq + kUnitPages - 1) / kUnitPages;
-  if (max_q_per_seq <= 1) {
-    int64_t total = (int64_t)num_q * units;
-    int grid = (int)std::min<int64_t>(total, (int64_t)num_sms);
-    if (grid < 1) grid = 1;
-    score_q1_kernel<false><<<grid, kScoreThreads, 0, s>>>(q_idx, keys, q_seq, num_q, g, nullptr, 0,
-                                                          ws, ws_stride, units, st);
-  } else {
-    int64_t total = (int64_t)pg.num_seqs * units;
-    int grid = (int)std::min<int64_t>(total, (int64_t)num_sms * 2);
-    if (grid < 1) grid = 1;
-    score_batched_kernel<<<grid, kScoreThreads, 0, s>>>(q_idx, keys, q_seq, num_q, g, ws,
-                                                        ws_stride, units, st);
-  }
+  RunList rl = make_runlist(runlist, num_q);
+  const bool batched = max_q_per_seq > 1;
+  group_prefix_kernel<<<1, 1024, 0, s>>>(batched, false, q_seq, num_q, g, 0, kPage,
+                                         const_cast<int64_t*>(rl.meta),
+                                         const_cast<int64_t*>(rl.prefix),
+                                         const_cast<int32_t*>(rl.run_q0));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap keymap;
+  if (!make_bf16_map(&keymap, keys, (int64_t)pg.num_pages * kPage, kDidx, 64, kPage))
+    return cudaErrorInvalidValue;
+  const int grid = std::max(1, num_sms);
+  e = cudaFuncSetAttribute(score_pages_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kTmaSmem);
+  if (e != cudaSuccess) return e;
+  score_pages_kernel<<<grid, kTmaThreads, kTmaSmem, s>>>(keymap, q_idx, q_seq, num_q, g, ws,
+                                                         ws_stride, rl, st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_score_reindex(const uint16_t* q_idx, const uint16_t* keys, const int32_t* q_seq,
                                  int32_t num_q, const csa2_pages& pg, const int32_t* pool,
-                                 int32_t pool_size, uint32_t* ws, int32_t* st, cudaStream_t s,
-                                 int num_sms) {
+                                 int32_t pool_size, uint32_t* ws, void* runlist, int32_t* st,
+                                 cudaStream_t s, int num_sms) {
   ScoreGeom g{pg.seq_lens, pg.page_table, pg.max_pages_per_seq, pg.num_pages, pg.num_seqs};
-  const int units = (pool_size + kUnitPool - 1) / kUnitPool;
-  int64_t total = (int64_t)num_q * units;
-  int grid = (int)std::min<int64_t>(total, (int64_t)num_sms);
-  if (grid < 1) grid = 1;
-  score_q1_kernel<true><<<grid, kScoreThreads, 0, s>>>(q_idx, keys, q_seq, num_q, g, pool,
-                                                       pool_size, ws, pool_size, units, st);
+  RunList rl = make_runlist(runlist, num_q);
+  group_prefix_kernel<<<1, 1024, 0, s>>>(false, true, q_seq, num_q, g, pool_size, 16,
+                                         const_cast<int64_t*>(rl.meta),
+                                         const_cast<int64_t*>(rl.prefix),
+                                         const_cast<int32_t*>(rl.run_q0));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(score_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kGatherSmem);
+  if (e != cudaSuccess) return e;
+  const int grid = std::max(1, num_sms);
+  score_gather_kernel<<<grid, kScoreThreads, kGatherSmem, s>>>(q_idx, keys, q_seq, num_q, g, pool,
+                                                              pool_size, ws, rl, st);
   return cudaGetLastError();
 }
 
@@ -683,6 +1140,7 @@ cudaError_t launch_select(bool reindex, const uint32_t* ws, int64_t ws_stride, c
                           int32_t pool_size, int32_t topk, int32_t* out_idx, int32_t* pool_out,
                           int32_t* st, cudaStream_t s) {
   const size_t smem = select_smem_bytes();
+  const int32_t max_ctx = pg.max_pages_per_seq * kPage;
   dim3 grid(kSelCluster, num_q);
   if (reindex) {
     cudaError_t e = cudaFuncSetAttribute(select_kernel<true>,
@@ -690,14 +1148,14 @@ cudaError_t launch_select(bool reindex, const uint32_t* ws, int64_t ws_stride, c
     if (e != cudaSuccess) return e;
     select_kernel<true><<<grid, kSelThreads, smem, s>>>(ws, ws_stride, q_seq, pg.seq_lens,
                                                         pg.num_seqs, pool_in, pool_size, topk,
-                                                        out_idx, nullptr, st);
+                                                        out_idx, nullptr, max_ctx, st);
   } else {
     cudaError_t e = cudaFuncSetAttribute(select_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     select_kernel<false><<<grid, kSelThreads, smem, s>>>(ws, ws_stride, q_seq, pg.seq_lens,
                                                          pg.num_seqs, nullptr, pool_size, topk,
-                                                         out_idx, pool_out, st);
+                                                         out_idx, pool_out, max_ctx, st);
   }
   return cudaGetLastError();
 }

@@ -20,9 +20,7 @@
 //     group stay in L2 while the B slices stream;
 //   - every mbarrier wait is bounded; on expiry the CTA raises CSA2_DEV_TIMEOUT, stops
 //     issuing, waits (bounded) for its own copies and MMAs, frees TMEM and returns.
-#include <cuda.h>
-
-#include "common.cuh"
+#include "async.cuh"
 
 namespace csa2 {
 
@@ -45,52 +43,6 @@ struct Bars {
   uint32_t tmem_base;
   volatile int abort;
 };
-
-__device__ __forceinline__ uint32_t saddr(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(saddr(b)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait.  Returns false (and flags the CTA) when the limit expires or another
-// role of the CTA already gave up.
-__device__ __forceinline__ bool mbar_wait(Bars* bars, uint64_t* b, uint32_t parity, int32_t* st,
-                                          uint32_t limit = kSpinLimit) {
-  for (uint32_t i = 0; i < limit; ++i) {
-    if (mbar_try(b, parity)) return true;
-    if ((i & 1023u) == 1023u && bars->abort) return false;
-  }
-  bars->abort = 1;
-  report(st, CSA2_DEV_TIMEOUT);
-  return false;
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, uint64_t* bar, int x,
-                                            int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-      "%3}], [%4];" ::"r"(saddr(dst)),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(saddr(bar))
-      : "memory");
-}
 
 __device__ __forceinline__ void fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -192,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars->fin, 1);
     bars->abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_fence_init();
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -221,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int m, n;
       tile_coords(tile, num_m, num_n, m, n);
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (!mbar_wait(bars, &bars->empty[stage], phase ^ 1u, p.st)) {
+        if (!mbar_wait(&bars->abort, &bars->empty[stage], phase ^ 1u, p.st)) {
           ok = false;
           break;
         }
@@ -240,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // make sure no copy of ours is still landing in shared memory
     for (int s = 0; s < STAGES; ++s)
       if (issued_mask & (1u << s))
-        (void)mbar_wait(bars, &bars->full[s], (last_par >> s) & 1u, p.st, 1u << 20);
+        (void)mbar_wait(&bars->abort, &bars->full[s], (last_par >> s) & 1u, p.st, 1u << 20);
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
     const uint32_t idesc = idesc_bf16(BM, BN);
@@ -248,11 +200,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-      if (!mbar_wait(bars, &bars->tempty[acc], acc_phase ^ 1u, p.st)) break;
+      if (!mbar_wait(&bars->abort, &bars->tempty[acc], acc_phase ^ 1u, p.st)) break;
       fence_after();
       const uint32_t d = tmem + (uint32_t)(acc * BN);
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (!mbar_wait(bars, &bars->full[stage], phase, p.st)) {
+        if (!mbar_wait(&bars->abort, &bars->full[stage], phase, p.st)) {
           ok = false;
           break;
         }
@@ -278,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // wait until every MMA this thread issued has completed
     umma_commit(&bars->fin);
-    (void)mbar_wait(bars, &bars->fin, 0, p.st, 1u << 20);
+    (void)mbar_wait(&bars->abort, &bars->fin, 0, p.st, 1u << 20);
   } else if (warp >= 2) {
     // ---------------- epilogue: 128 threads, one output row each ----------------
     const int quad = warp & 3;              // TMEM lanes 32*quad .. 32*quad+31
@@ -289,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       int m, n;
       tile_coords(tile, num_m, num_n, m, n);
-      if (!mbar_wait(bars, &bars->tfull[acc], acc_phase, p.st)) break;
+      if (!mbar_wait(&bars->abort, &bars->tfull[acc], acc_phase, p.st)) break;
       fence_after();
       const int t = m * BM + row;
       const int32_t slot = __ldg(p.slot_of_token + t);
@@ -351,45 +303,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_before();
   __syncthreads();
   if (warp == 1) {
+    __syncwarp();
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                  : "memory");
   }
 }
-
-namespace {
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  }
-  return fn;
-}
-
-bool make_map(CUtensorMap* tm, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-}  // namespace
 
 size_t kv_write_smem_bytes() { return (size_t)STAGES * STAGE_BYTES + sizeof(Bars) + 1024; }
 
@@ -399,7 +318,7 @@ cudaError_t launch_kv_write(const uint16_t* H, const uint16_t* Wt, uint8_t* code
                             int32_t* st, cudaStream_t s, int num_sms) {
   const int32_t n_out = n_kv_proj * kDkv + n_idx_proj * kDidx;
   CUtensorMap ta, tb;
-  if (!make_map(&ta, H, T, d_model, BM) || !make_map(&tb, Wt, n_out, d_model, BN))
+  if (!make_bf16_map(&ta, H, T, d_model, BK, BM) || !make_bf16_map(&tb, Wt, n_out, d_model, BK, BN))
     return cudaErrorInvalidValue;
   WriteParams p{codes, scales, k_idx, slot_of_token, num_slots, T, d_model, n_kv_proj, n_idx_proj,
                 n_out, st};

@@ -3,7 +3,10 @@
 write (ai2.x.ezic.info blog, "KVを捨てる、共有する、作り直す").  FP4 codes must equal the
 oracle's except where the pre-quantisation value lies within 1e-3 of a rounding
 boundary; E4M3 scales except where amax/6 lies within 1e-3 of an E4M3 midpoint;
-bf16 keys within one unit in the last place."""
+bf16 keys within bf16 rounding of the oracle's value plus the fp32 accumulation error
+(|k - C| <= 2^-8 |C| + 1e-4: d = 4096 products of magnitude ~1/64, summed in a
+different order in fp32, differ by ~1e-5 typically; near-zero keys can therefore be
+several bf16 units apart)."""
 import numpy as np
 import pytest
 import torch
@@ -54,8 +57,13 @@ def compare(codes_g, scales_g, keys_g, codes_o, scales_o, keys_o, C, what=""):
         assert np.all(near_b[cdiff]), f"{what}: code mismatch away from a rounding boundary"
         bad_blocks += int(sdiff.sum()) + int(cdiff.any(axis=2).sum())
     if keys_o.size:
-        kd = np.abs(keys_g.astype(np.int32) - keys_o.astype(np.int32))
-        assert kd.max(initial=0) <= 1, f"{what}: bf16 key off by more than one ulp"
+        kg_val = gen.bf16_bits_to_f32(keys_g).astype(np.float64)
+        base = nkv * 512
+        Ck = np.stack([C[:, base + p * 128: base + (p + 1) * 128] for p in range(keys_o.shape[0])])
+        assert np.all(np.abs(kg_val - Ck) <= 2.0**-8 * np.abs(Ck) + 1e-4), \
+            f"{what}: bf16 key beyond rounding + accumulation error"
+        exact = np.mean(keys_g == keys_o)
+        assert exact > 0.99, f"{what}: only {exact:.4%} of keys bit-equal"
     return bad_blocks
 
 
