@@ -289,7 +289,7 @@ def run_ours(args, world, rank, local):
                    "parallelism": f"replicas x{world}"},
         "per_mode_ms": {"full_index": round(full_ms, 4), "reindex": round(re_ms, 4),
                         "attention": round(attn_ms, 4)},
-        "roofline": {"bound": "hbm", "kernel": "csa2_index(FULL): score_q1_kernel + select_kernel",
+        "roofline": {"bound": "hbm", "kernel": "csa2_index(FULL) call: group_prefix_kernel + score_pages_kernel + select_kernel<0>",
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": fb, "traffic": traffic},
@@ -302,6 +302,137 @@ def run_ours(args, world, rank, local):
         line["cpu_baseline"] = cpu
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def run_write(args, world, rank, local):
+    """The CED write path alone: one csa2_kv_write over the whole write workload per step
+    (H [32768, 4096] bf16 times 20 latent + 20 indexer-key projections, quantised on
+    write).  The roofline is the tensor pipe: 2 T d n_out flops per call."""
+    import torch
+    import csa2_inputs as gen
+    import fp4_compressed_sparse_03_b300 as csa2
+    from fp4_compressed_sparse_03_b300.workload import fill_write_inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ww = gen.config_write()
+    H, Wt, slots = fill_write_inputs(ww, device=dev)
+    num_slots = ww.num_pages * 64
+    codes = torch.empty((ww.n_kv_proj, num_slots, 256), dtype=torch.uint8, device=dev)
+    scales = torch.empty((ww.n_kv_proj, num_slots, 32), dtype=torch.uint8, device=dev)
+    keys = torch.empty((ww.n_idx_proj, num_slots, 128), dtype=torch.int16, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call(h=H, sl=slots):
+        csa2.check(csa2.csa2_kv_write(h, Wt, codes, scales, keys, ww.T, ww.d_model, ww.n_kv_proj,
+                                      ww.n_idx_proj, sl, num_slots, st, stream))
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(K):
+        evs[k][0].record(stream)
+        call()
+        evs[k][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    status, bits = csa2.csa2_read_status(st)
+    if status != csa2.CSA2_OK:
+        raise RuntimeError(f"device status {bits:#x} after timed steps")
+    ms_step = reduce_max(t0.elapsed_time(t1) / K, world, dev)
+    kern_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    units = ww.T * world
+    value = units / (ms_step / 1e3)
+    flops = 2.0 * ww.T * ww.d_model * ww.n_out
+    _, tc_peak, peak_src = load_peaks()
+    achieved = flops / (kern_ms / 1e3) / 1e12
+
+    # end to end: H from pinned host memory in, every code, scale and key back out
+    H_pin = torch.empty(H.shape, dtype=H.dtype).pin_memory()
+    H_pin.copy_(H)
+    c_pin = torch.empty(codes.shape, dtype=codes.dtype).pin_memory()
+    s_pin = torch.empty(scales.shape, dtype=scales.dtype).pin_memory()
+    k_pin = torch.empty(keys.shape, dtype=keys.dtype).pin_memory()
+    H_dev = torch.empty_like(H)
+    K2 = max(1, min(K, args.e2e_steps, 10))
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    w0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(K2):
+        H_dev.copy_(H_pin, non_blocking=True)
+        call(H_dev)
+        c_pin.copy_(codes, non_blocking=True)
+        s_pin.copy_(scales, non_blocking=True)
+        k_pin.copy_(keys, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall = (time.perf_counter() - w0) / K2 * 1e3
+    ms_e2e = reduce_max(max(e0.elapsed_time(e1) / K2, wall), world, dev)
+    h2d = H.numel() * 2
+    d2h = codes.numel() + scales.numel() + keys.numel() * 2
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_write(ww, args.cpu_sample)
+    line = {
+        "metric": "CED write path: tokens/s projected and quantised on write", "value": round(value, 1),
+        "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 operands, f32 accumulate, fp4-e2m1/e4m3 + bf16 out",
+        "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": ww.name, "tokens": ww.T, "d_model": ww.d_model,
+                   "latent_projections": ww.n_kv_proj, "key_projections": ww.n_idx_proj,
+                   "l2": "no flush: H is %.0f MB (> 126 MB L2)" % (H.numel() * 2 / 1e6),
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "kernel": "csa2_kv_write: kv_write_kernel",
+                     "achieved": round(achieved, 1), "peak": tc_peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / tc_peak, 4), "peak_source": peak_src + " bf16 burst",
+                     "algorithmic_flops_per_launch": flops, "traffic": None},
+        "e2e": {"value": round(units / (ms_e2e / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": K2},
+        "gpu_launches": K,
+        "clocks": clk,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def cpu_baseline_write(ww, sample_rows: int):
+    """The oracle's write path (double-accumulated projection, then quantise / round) on
+    `sample_rows` token rows, one host thread per row."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    cores = os.cpu_count() or 1
+    rows = np.linspace(0, ww.T - 1, max(1, sample_rows)).astype(np.int64)
+    Wt = ww.w_rows(np.arange(ww.n_out))
+    Hs = [ww.h_rows(np.array([r])) for r in rows]
+    threads = min(cores, len(Hs))
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(lambda h: oracle.kv_write_rows(h, Wt, ww.n_kv_proj, ww.n_idx_proj), Hs))
+    dt = time.perf_counter() - t0
+    return {"value": round(len(Hs) / dt, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(Hs)} of {ww.T} token rows x {ww.n_out} output columns of {ww.name}, "
+                      f"{dt:.1f} s wall on {threads} threads"}
 
 
 def workload_of(name: str):
@@ -405,6 +536,8 @@ def run_reference(args, world, rank):
     import csa2_inputs as gen
     if rank != 0:
         return
+    if args.workload == "ced_write":
+        return run_reference_write(args, world)
     wl = workload_of(args.workload)
     per_step = max(1, args.cpu_sample // max(1, args.steps))
     for _ in range(max(0, min(args.warmup, 1))):
@@ -432,6 +565,32 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_reference_write(args, world):
+    import csa2_inputs as gen
+    ww = gen.config_write()
+    per_step = max(1, args.cpu_sample // max(1, args.steps))
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline_write(ww, per_step))
+    dt = time.perf_counter() - t0
+    v = float(np.mean([c["value"] for c in vals]))
+    cb = dict(vals[-1])
+    cb["value"] = round(v, 3)
+    cb["sample"] = f"{args.steps} steps x {per_step} token rows of {ww.name}"
+    line = {"impl": "reference", "metric": "CED write path: tokens/s projected and quantised on write",
+            "value": round(v, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64 (CPU oracle)", "data": "synthetic (seeded counter-based generator)",
+            "config": {"workload": ww.name, "tokens": ww.T, "d_model": ww.d_model,
+                       "latent_projections": ww.n_kv_proj, "key_projections": ww.n_idx_proj},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -439,7 +598,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_batch",
-                    choices=["decode_batch", "decode_batch16", "long_context", "ragged", "tiny"])
+                    choices=["decode_batch", "decode_batch16", "long_context", "ragged", "tiny",
+                             "ced_write"])
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-sample", type=int, default=32, help="queries timed on the oracle")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -447,6 +607,9 @@ def main():
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.workload == "ced_write":
+        args.warmup = max(3, args.warmup)
+        run_write(args, world, rank, local)
     else:
         args.warmup = max(3, args.warmup)
         run_ours(args, world, rank, local)

@@ -5,7 +5,7 @@ CPU-baseline leg of ``bench.py`` may import this package.  The product path
 (``fp4_compressed_sparse_03_b300`` / ``libcsa2``) never imports it, and the two
 share no code: the arithmetic lives in plain C (``csa2_oracle.c``); this module
 only marshals numpy arrays and composes the per-mode steps in the order the pages
-give them (page 5, "Compressed Sparse Attention 2 (CSA2)": Full, Reindex and Reuse
+give them (tech-report digest, "Compressed Sparse Attention 2 (CSA2)": Full, Reindex and Reuse
 modes and the Hierarchical Sparse Indexer).
 
 Every function is plain and slow; floating-point sums are in double.
@@ -122,7 +122,7 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
 
 
 def kv_write_rows(H: np.ndarray, Wt: np.ndarray, n_kv_proj: int, n_idx_proj: int):
-    """Write path for some token rows (page 5 CED equation, page 1 FP4 format).
+    """Write path for some token rows (tech-report digest CED equation, ezic blog FP4 format).
 
     Returns (codes [n_kv_proj, R, 256], scales [n_kv_proj, R, 32], keys [n_idx_proj, R, 128]).
     The pre-quantisation value is the float32 of the double-accumulated product.
@@ -161,7 +161,7 @@ def select_topk(scores: np.ndarray, tokens: np.ndarray, k: int) -> np.ndarray:
 
 
 def index_full(q_idx: np.ndarray, keys: np.ndarray, topk: int, pool_size: int):
-    """Full mode (page 5 "Full Mode"; pool: "Hierarchical Sparse Indexer").
+    """Full mode (tech-report digest "Full Mode"; pool: "Hierarchical Sparse Indexer").
 
     Scores every context token; the pool is the top-min(P, N) and the selection the
     top-min(K, N) by (score desc, token asc), both ascending and -1 padded.
@@ -175,7 +175,7 @@ def index_full(q_idx: np.ndarray, keys: np.ndarray, topk: int, pool_size: int):
 
 
 def index_reindex(q_idx: np.ndarray, keys: np.ndarray, pool: np.ndarray, topk: int):
-    """Reindex mode (page 5 "Reindex Mode" + "Hierarchical Sparse Indexer"): re-score
+    """Reindex mode (tech-report digest "Reindex Mode" + "Hierarchical Sparse Indexer"): re-score
     only the valid entries of the pool with this layer's query and the keys of the
     Full layer; keep the top-min(K, |pool|).  Returns (idx [K], scores of the pool)."""
     valid = pool[pool >= 0].astype(np.int32)
@@ -184,7 +184,7 @@ def index_reindex(q_idx: np.ndarray, keys: np.ndarray, pool: np.ndarray, topk: i
 
 
 def index_reuse(inherit_idx: np.ndarray) -> np.ndarray:
-    """Reuse mode (page 5 "Reuse Mode"): the indices of the earlier layer, unchanged."""
+    """Reuse mode (tech-report digest "Reuse Mode"): the indices of the earlier layer, unchanged."""
     return np.array(inherit_idx, dtype=np.int32, copy=True)
 
 
@@ -215,7 +215,7 @@ def attention_over_cache(q: np.ndarray, codes_rows: np.ndarray, scales_rows: np.
 # ------------------------------------------------------------------- footprint ---
 
 PAGES_FOOTPRINT = {
-    # page 2 "CSA2とFP4でキャッシュを圧縮": HBM-resident global KV bytes per token
+    # zaikei article "CSA2とFP4でキャッシュを圧縮": HBM-resident global KV bytes per token
     "v4.1-flash": 890,
     "v4-flash": 3514,
     "v3.2": 48068,
@@ -231,5 +231,5 @@ def layout_bytes_per_token(n_full_groups: int = 1, d_kv: int = 512, group: int =
 
 
 def session_bytes(bytes_per_token: int, tokens: int = 1_000_000) -> int:
-    """Cache bytes of one session (page 1: 890 B x 1M tokens ~ 890 MB)."""
+    """Cache bytes of one session (ezic blog: 890 B x 1M tokens ~ 890 MB)."""
     return bytes_per_token * tokens

@@ -28,7 +28,7 @@ static double bf16_value(uint16_t b) { return (double)u32_as_f32((uint32_t)b << 
  * the subnormal 0.m * 2^0 = {0, 0.5}; fields 1..3 encode 1.m * 2^(e-1).  The
  * representable magnitudes are therefore 0, 0.5, 1, 1.5, 2, 3, 4, 6 (codes 0..7).
  *
- * Encoding reading (page 1 gives the format, not the rounding): round to nearest,
+ * Encoding reading (ezic blog gives the format, not the rounding): round to nearest,
  * ties to the even code (mantissa bit 0), saturate to 6, keep the sign bit even
  * when the magnitude rounds to zero.  Written as the decision table that this rule
  * produces between consecutive magnitudes:

@@ -6,9 +6,9 @@
  * no code, header, table or helper with it.
  *
  * Plain, slow, single-threaded C.  Floating-point sums are carried in double.
- * Each function cites the passage of the pages ("DeepSeek-V4.1-Flash" web pages:
- * ai2.x.ezic.info blog = page 1, zaikei.co.jp article = page 2, jiwasawa.github.io
- * tech-report digest = page 5) it follows.
+ * Each function cites the passage of the pages of the "DeepSeek-V4.1-Flash" web pages it
+ * follows: the ai2.x.ezic.info blog ("ezic blog"), the zaikei.co.jp article ("zaikei
+ * article") and the jiwasawa.github.io tech-report digest ("tech-report digest").
  */
 #ifndef CSA2_ORACLE_H
 #define CSA2_ORACLE_H
@@ -18,12 +18,12 @@
 extern "C" {
 #endif
 
-/* FP4 E2M1 element codec (page 1 "KVを捨てる、共有する、作り直す": main KV held as
- * 4-bit E2M1 floats; page 5 "FP4 メイン KV Cache": OCP E2M1).  code = s<<3|e<<1|m. */
+/* FP4 E2M1 element codec (ezic blog "KVを捨てる、共有する、作り直す": main KV held as
+ * 4-bit E2M1 floats; tech-report digest "FP4 メイン KV Cache": OCP E2M1).  code = s<<3|e<<1|m. */
 uint8_t orc_e2m1_encode(float y);
 double orc_e2m1_decode(uint8_t code);
 
-/* FP8 E4M3 (OCP E4M3FN) scale codec (page 1: one E4M3 scale per 16 channels). */
+/* FP8 E4M3 (OCP E4M3FN) scale codec (ezic blog: one E4M3 scale per 16 channels). */
 uint8_t orc_e4m3_encode(float v);
 double orc_e4m3_decode(uint8_t b);
 
@@ -34,13 +34,13 @@ void orc_quantize_rows(const float* x, int64_t T, int32_t D, uint8_t* codes, uin
 void orc_dequantize_rows(const uint8_t* codes, const uint8_t* scales, int64_t T, int32_t D,
                          double* out);
 
-/* CED projection (page 5 "Causal Encoder-Decoder (CED)" equation C_l = H_{L/2} W_l^KV):
+/* CED projection (tech-report digest "Causal Encoder-Decoder (CED)" equation C_l = H_{L/2} W_l^KV):
  * C[r][n] = fl32(sum_k H[r][k] * Wt[n][k]) with the sum in double.  H is bf16
  * [nrows][d_model]; the projection is stored output-major, Wt[n][k] = W[k][n]. */
 void orc_project_rows(const uint16_t* H, const uint16_t* Wt, int64_t nrows, int32_t d_model,
                       int32_t n_out, float* C);
 
-/* Indexer score (page 5 "CSA2" Full/Reindex modes; scoring formula is a reading):
+/* Indexer score (tech-report digest "CSA2" Full/Reindex modes; scoring formula is a reading):
  * score[s] = sum_{h<4} max(0, sum_{d<128} q[h][d] * key[s][d]) in double. */
 void orc_index_scores(const uint16_t* q, const uint16_t* keys, int64_t n, double* score);
 
@@ -49,8 +49,8 @@ void orc_index_scores(const uint16_t* q, const uint16_t* keys, int64_t n, double
 void orc_select_topk(const double* score, const int32_t* token, int64_t n, int32_t k,
                      int32_t* out);
 
-/* Sparse attention over selected latent rows (page 5 "Reuse Mode": sparse attention
- * over the top-K entries; page 2: the FP4 cache is dequantised before attention).
+/* Sparse attention over selected latent rows (tech-report digest "Reuse Mode": sparse attention
+ * over the top-K entries; zaikei article: the FP4 cache is dequantised before attention).
  * q bf16 [16][512]; chat double [n][512] (dequantised rows); K = V = latent.
  * out[h] = softmax_s(scale * q_h.chat_s) . chat, lse[h] = natural-log sum-exp.
  * n == 0 gives out = 0 and lse = -inf. */

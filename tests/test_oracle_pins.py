@@ -163,7 +163,7 @@ def _bf16(x):
 
 def test_projection_identity_reproduces_codec(orc):
     """W = [I_512; 0] makes C = H[:, :512] exactly, so the write path's codes must equal
-    the block quantiser applied to H's first 512 columns (page 5 CED equation)."""
+    the block quantiser applied to H's first 512 columns (tech-report digest CED equation)."""
     rng = np.random.default_rng(11)
     H = _bf16(rng.standard_normal((24, 640)) * 3)
     Wt = np.zeros((512 + 128, 640), np.uint16)
