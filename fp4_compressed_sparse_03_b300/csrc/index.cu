@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 // per 4 lanes) ran at 124 us of pure arithmetic for 2.1M keys against 85 us to stream
 // them, so the contraction runs on the tensor cores even for a single query.
 
-constexpr int kPageStages = 12;
+constexpr int kPageStages = 8;
 constexpr int kPageBytes = kPage * kKeyRow;            // 16 KB
 constexpr int kConsumerWarps = 8;
 constexpr int kTmaThreads = (kConsumerWarps + 1) * 32;  // + 1 producer warp
