@@ -67,6 +67,10 @@ _attn = _sig("csa2_sparse_attn", ctypes.c_int,
              [_vp, _vp, _vp, _vp, ctypes.POINTER(Csa2Pages), _vp, _vp, _i32, _vp, _i32,
               ctypes.c_float, _vp, _sz, _vp, _vp])
 _attn_ws = _sig("csa2_attn_workspace_size", _sz, [_i32, _i32])
+_attn_static = _sig("csa2_sparse_attn_static", ctypes.c_int,
+                    [_vp, _vp, _vp, _vp, ctypes.POINTER(Csa2Pages), _vp, _vp, _i32, _vp, _i32,
+                     ctypes.c_float, _vp, _vp])
+ATTN_STATIC_SCRATCH_BYTES = 16 << 20  # CSA2_ATTN_STATIC_SCRATCH_BYTES
 _quantize = _sig("csa2_quantize", ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp])
 _dequantize = _sig("csa2_dequantize", ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp])
 _read_status = _sig("csa2_read_status", ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp])
@@ -157,6 +161,13 @@ def csa2_sparse_attn(q, codes, scales, idx, pages: Csa2Pages, out, lse, num_q, q
 
 def csa2_attn_workspace_size(num_q, topk) -> int:
     return int(_attn_ws(num_q, topk))
+
+
+def csa2_sparse_attn_static(q, codes, scales, idx, pages: Csa2Pages, out, lse, num_q, q_seq, topk,
+                            softmax_scale, dev_status=None, stream=None) -> int:
+    return _attn_static(_ptr(q), _ptr(codes), _ptr(scales), _ptr(idx), ctypes.byref(pages),
+                        _ptr(out), _ptr(lse), num_q, _ptr(q_seq), topk,
+                        ctypes.c_float(softmax_scale), _ptr(dev_status), _stream(stream))
 
 
 def csa2_quantize(x, slot_of_token, codes, scales, T, D, num_slots, dev_status=None,

@@ -1,0 +1,65 @@
+// csa2_sparse_attn_static: the read path with its split-softmax partials held in a
+// fixed device array of this library instead of caller-provided workspace.
+//
+// For callers that cannot allocate device memory around the call: plain C clients of
+// the ABI that hold no device allocator of their own, and decode loops that must not
+// call cudaMalloc / cudaFree while kernels are in flight, because those calls can
+// synchronise the device and stall the whole step.
+//
+// The partials of every split (16 x 512 fp32 output rows plus the running max and sum
+// of each head) are written in full by the attention kernel before the combine kernel
+// reads them, so nothing in the array has to start at zero and no clearing pass runs.
+// The array is shared by every call on a device: calls that overlap in time (on two
+// streams, or from two host threads) race on it.
+#include <mutex>
+
+#include "csa2.h"
+
+static __device__ __align__(256) unsigned char g_attn_scratch[CSA2_ATTN_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_attn_scratch on the current device, resolved on the first call
+// made with that device current.
+csa2_status scratch_of_current_device(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return CSA2_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return CSA2_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();
+      return CSA2_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return CSA2_OK;
+}
+
+}  // namespace
+
+extern "C" csa2_status csa2_sparse_attn_static(const uint16_t* q, const uint8_t* codes,
+                                                const uint8_t* scales, const int32_t* idx,
+                                                const csa2_pages* pages, float* out, float* lse,
+                                                int32_t num_q, const int32_t* q_seq, int32_t topk,
+                                                float softmax_scale, int32_t* dev_status,
+                                                cudaStream_t stream) {
+  if (num_q < 1 || topk < 1) return CSA2_ERR_INVALID_ARGUMENT;
+  if (csa2_attn_workspace_size(num_q, topk) > (size_t)CSA2_ATTN_STATIC_SCRATCH_BYTES)
+    return CSA2_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  const csa2_status s = scratch_of_current_device(&scratch);
+  if (s != CSA2_OK) return s;
+  return csa2_sparse_attn(q, codes, scales, idx, pages, out, lse, num_q, q_seq, topk,
+                          softmax_scale, scratch, (size_t)CSA2_ATTN_STATIC_SCRATCH_BYTES,
+                          dev_status, stream);
+}

@@ -187,6 +187,27 @@ CSA2_API csa2_status csa2_sparse_attn(const uint16_t* q, const uint8_t* codes, c
 
 CSA2_API size_t csa2_attn_workspace_size(int32_t num_q, int32_t topk);
 
+/* csa2_sparse_attn without caller workspace.  The pages have no counterpart to this
+ * entry point: it exists for callers that cannot allocate device memory around the
+ * call (plain C clients that hold no device allocator, or decode loops that must not
+ * call cudaMalloc / cudaFree, which can synchronise the device, while work is in flight).
+ *
+ * Same arguments, arithmetic and results as csa2_sparse_attn.  The split partials go
+ * to a fixed device array of CSA2_ATTN_STATIC_SCRATCH_BYTES inside this library; the
+ * call allocates nothing.  The first call on a device, made with that device current,
+ * resolves the array's device address (cudaGetSymbolAddress); make that first call
+ * before any stream capture.  Returns CSA2_ERR_UNSUPPORTED when
+ * csa2_attn_workspace_size(num_q, topk) exceeds CSA2_ATTN_STATIC_SCRATCH_BYTES, and
+ * CSA2_ERR_CUDA if the address cannot be resolved.  The array is shared by all calls
+ * on a device: calls that overlap in time (several streams or host threads) race. */
+#define CSA2_ATTN_STATIC_SCRATCH_BYTES (16u << 20)
+CSA2_API csa2_status csa2_sparse_attn_static(const uint16_t* q, const uint8_t* codes,
+                                             const uint8_t* scales, const int32_t* idx,
+                                             const csa2_pages* pages, float* out, float* lse,
+                                             int32_t num_q, const int32_t* q_seq, int32_t topk,
+                                             float softmax_scale, int32_t* dev_status,
+                                             cudaStream_t stream);
+
 /* ------------------------------------------------------------------ codec ---------
  * Standalone quantise / dequantise of latent rows (blog: E2M1 values, one E4M3 scale
  * per 16 channels).  Same arithmetic as the write path's epilogue.
