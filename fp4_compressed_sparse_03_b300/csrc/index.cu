@@ -206,6 +206,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   extern __shared__ __align__(128) unsigned char gather_smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gq = lane >> 2, c = lane & 3;
+  // chunk XOR of this lane's rows: the two rows read in one quarter-warp phase
+  // (gq = 2p, 2p + 1) get masks p and p + 4, so their 16-byte chunks fill all 32 banks
+  const int sw = (gq >> 1) | ((gq & 1) << 2);
   const uint32_t ring = smem_addr(gather_smem) + warp * kGatherRing * kGatherGroup;
   const int R = (int)__ldg(rl.meta);
   int64_t g0, g1;
@@ -258,8 +261,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int k = 4 * j + c;
-          if (ra) cp_async16(slot + gq * kKeyRow + ((k ^ gq) << 4), reinterpret_cast<const char*>(ra) + 16 * k);
-          if (rb) cp_async16(slot + (gq + 8) * kKeyRow + ((k ^ gq) << 4), reinterpret_cast<const char*>(rb) + 16 * k);
+          if (ra) cp_async16(slot + gq * kKeyRow + ((k ^ sw) << 4), reinterpret_cast<const char*>(ra) + 16 * k);
+          if (rb) cp_async16(slot + (gq + 8) * kKeyRow + ((k ^ sw) << 4), reinterpret_cast<const char*>(rb) + 16 * k);
         }
         okmask |= ((ra ? 1u : 0u) | (rb ? 2u : 0u)) << (2 * sl);
       }
@@ -291,8 +294,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int k = 4 * j + c;
-      k0[j] = lds128(sbase + gq * kKeyRow + ((k ^ gq) << 4));
-      k1[j] = lds128(sbase + (gq + 8) * kKeyRow + ((k ^ gq) << 4));
+      k0[j] = lds128(sbase + gq * kKeyRow + ((k ^ sw) << 4));
+      k1[j] = lds128(sbase + (gq + 8) * kKeyRow + ((k ^ sw) << 4));
     }
     float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -318,7 +321,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 // ------------------------------------------------------------------ TMA page scorer --
 // Full mode, contiguous context: the unit of work is a whole 64-token page (16 KB of
 // keys).  One producer thread streams pages through a 2D tensor map (two 64 x 64 bf16
-// boxes per page, 128-byte swizzle) into a 12-slot shared-memory ring.  The 8 consumer
+// boxes per page, 128-byte swizzle) into an 8-slot shared-memory ring.  The 8 consumer
 // warps take the pages in pairs: warp w scores rows 8w .. 8w+7 of both pages of a pair
 // as the 16 rows of one tensor-core tile:
 //   D[16 keys][8 cols] = K[16 keys][16 dims] x Q^T[16 dims][8 cols]   (m16n8k16, bf16)
@@ -417,7 +420,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     }
   } else {
     // ---------------- consumers: every warp takes every page, two pages per step ----
-    const int rr = 8 * warp + gq;  // this lane's row in each page of the pair
+    // this lane's row in each page of the pair: the two lanes groups gq = 2p, 2p + 1 of a
+    // quarter-warp phase read rows whose 128-byte swizzle masks (row % 8) are p and p + 4,
+    // so their 16-byte chunks land in disjoint bank halves (no bank conflict)
+    const int rr = 8 * warp + ((gq >> 1) | ((gq & 1) << 2));
     int cur_run = -1, rows = 0, q0 = 0, T = 0, NT = 0;
     uint32_t bq[2][4][4];  // [n-tile][j][word]: B fragments of Q^T
     auto enter = [&](int r) {
