@@ -5,48 +5,60 @@
 // "Reuse Mode": sparse attention runs directly over the inherited top-K entries.
 // MQA over the shared latent: K = V = c_hat (512 channels), 16 query heads.
 //
-// One CTA (4 warps) handles one (query, split) pair: up to `split_len` selected
-// entries in tiles of 64 tokens.  Per tile:
-//   1. cp.async gathers 32 x (256 B codes + 32 B scales) into a 4-stage staging ring;
-//   2. S = Q . C^T on tensor cores (m16n8k16, 16 heads = M), fp32 accumulation, with
-//      the dequantisation fused in: each lane turns its token's 4-byte code word into
-//      its B fragments (E2M1 x E4M3 is exact in f16: at most 6 significant bits,
-//      magnitudes 2^-10 .. 2688) and also stores them into the f16 tile C;
-//   3. fp32 online softmax in the exp2 domain;
-//   4. O += P . C on tensor cores, each warp owning 128 output channels.
+// One CTA (8 warps, one per SM) handles one (query, split) pair: up to `split_len`
+// selected entries in tiles of 128 tokens, on the 5th-generation tensor cores:
+//   1. cp.async gathers the tile's 128 x (256 B codes + 32 B scales) into a 2-stage
+//      staging ring two tiles ahead (1D bulk copies were measured slower: the copy
+//      engine took ~50 cycles per 256-byte row);
+//   2. the warps dequantise the tile into an f16 tile C [128 tokens][512 channels]
+//      laid out as eight 128-byte-swizzled [128][64] chunks (E2M1 x E4M3 is exact in
+//      f16: at most 6 significant bits, magnitudes 2^-10 .. 2688);
+//   3. S^T = C . Q^T: tcgen05.mma M=128 (tokens) x N=16 (heads) x K=512, C K-major,
+//      fp32 accumulator in TMEM;
+//   4. fp32 softmax in the exp2 domain with a lazily moved reference max per head: the
+//      reference only moves (and the TMEM accumulator is rescaled) when a tile's max
+//      exceeds it by more than 2^8, so every weight is at most 2^8;
+//   5. O^T += C^T . P^T: M=128 (channels) x N=16 (heads) x K=128 (tokens) per 128-channel
+//      block, reading the same C tile as an MN-major operand; P^T is f16, and the
+//      normaliser sums the same f16-rounded weights.
 // Q is converted to f16 after a per-query power-of-two prescale (exact for every
 // value within 2^28 of the largest |q|); the scale is undone in the logit factor.
 // Several splits per query are merged by a log-sum-exp combine kernel.
-#include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace csa2 {
 
-constexpr int kAttnThreads = 128;   // 4 warps
+constexpr int kAttnThreads = 256;   // 8 warps
 constexpr int kAttnWarps = kAttnThreads / 32;
-constexpr int kTile = 32;            // tokens per tile
-constexpr int kStages = 4;           // cp.async staging ring
+constexpr int kTile = 128;           // tokens per tile = UMMA M
+constexpr int kRawStages = 2;        // cp.async staging ring
 constexpr int kMaxSplit = 1024;      // selected entries per CTA at most
-constexpr int kRowH = kDkv + 8;      // f16 elements per padded Q / C row (1040 B)
-constexpr int kPRow = kTile + 8;     // f16 per padded P row
-constexpr int kSRow = kTile + 4;     // fp32 per padded S row
-constexpr int kCodeStride = kCodeRow + 16;  // padded staging row: conflict-free code reads
-constexpr int kStageBytes = kTile * (kCodeStride + kScaleRow);  // 9728
+constexpr int kChunkBytes = kTile * 128;        // one 64-channel chunk of C: 16 KB
+constexpr int kCBytes = (kDkv / 64) * kChunkBytes;  // 128 KB
+constexpr int kQChunk = kHq * 128;              // one 64-channel chunk of Q: 2 KB
+constexpr int kQBytes = (kDkv / 64) * kQChunk;  // 16 KB
+constexpr int kPBytes = (kTile / 64) * kQChunk; // P^T [16 heads][128 tokens]: 4 KB
+constexpr int kRawCodeBytes = kTile * kCodeRow;             // 32 KB
+constexpr int kRawBytes = kRawCodeBytes + kTile * kScaleRow;  // 36 KB
+constexpr uint32_t kTmemCols = 128;  // S^T at columns 0..15, O^T blocks at 32 + 16 j
+constexpr uint32_t kOCol = 32;
+constexpr float kRescaleGap = 8.0f;  // log2 units
 
-struct AttnSmem {
-  __half qs[kHq][kRowH];
-  __half cs[kTile][kRowH];
-  unsigned char stage[kStages][kStageBytes];
-  float ss[kHq][kSRow];
-  __half ps[kHq][kPRow];
-  int32_t slot[kMaxSplit];           // physical row of each selected entry, -1 if skipped
-  float m_run[kHq], l_run[kHq], alpha[kHq];
-  uint32_t red[kAttnWarps];
+struct AttnCtl {
+  uint64_t bar_s, bar_pv, bar_fin;
+  uint32_t tmem;
+  volatile int abort;
+  float red_max[kHq][4];
+  float red_sum[kHq][4];
+  uint32_t qmax[kAttnWarps];
+  int32_t slot[kMaxSplit];  // physical row of each selected entry, -1 if skipped
 };
+constexpr size_t kAttnSmem = 1024 + kCBytes + kQBytes + kPBytes + kRawStages * kRawBytes + sizeof(AttnCtl);
+static_assert(kAttnSmem <= 232448, "sparse attention needs more than 227 KB of shared memory");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
-
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src));
 }
@@ -56,23 +68,11 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N));
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(p)));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(p)));
-}
-__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                        uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+// Bounded wait on an mbarrier phase that ignores the CTA's abort flag (used to drain).
+__device__ __forceinline__ bool mbar_drain(uint64_t* b, uint32_t parity, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i)
+    if (mbar_try(b, parity)) return true;
+  return false;
 }
 
 struct AttnGeom {
@@ -83,34 +83,132 @@ struct AttnGeom {
   int32_t num_seqs;
 };
 
-// Issue the gathers of the tile starting at local entry `e0` into staging buffer `sb`.
-__device__ __forceinline__ void issue_tile(AttnSmem& sm, int sb, int e0, int ecount,
-                                           const uint8_t* __restrict__ codes,
+// Gather the codes and scales of the tile starting at local entry `e0` into `stage`:
+// thread -> row tid / 2; the two threads of a row take the 16-byte parts of even and odd
+// index (16 code parts, then 2 scale parts), so each pair of lanes moves 32 contiguous bytes.
+__device__ __forceinline__ void issue_tile(unsigned char* stage, int e0, int ecount,
+                                           const int32_t* slot, const uint8_t* __restrict__ codes,
                                            const uint8_t* __restrict__ scales) {
-  unsigned char* stage = sm.stage[sb];
-  for (int ch = threadIdx.x; ch < kTile * 18; ch += kAttnThreads) {
-    const int tok = ch / 18, part = ch - tok * 18;
-    const int e = e0 + tok;
-    const int32_t slot = e < ecount ? sm.slot[e] : -1;
-    if (slot >= 0) {
-      if (part < 16)
-        cp_async16(stage + tok * kCodeStride + part * 16, codes + (int64_t)slot * kCodeRow + part * 16);
-      else
-        cp_async16(stage + kTile * kCodeStride + tok * kScaleRow + (part - 16) * 16,
-                   scales + (int64_t)slot * kScaleRow + (part - 16) * 16);
+  const int r = threadIdx.x >> 1, h = threadIdx.x & 1;
+  const int e = e0 + r;
+  const int32_t sl = e < ecount ? slot[e] : -1;
+  if (sl < 0) return;
+  const uint8_t* src = codes + (int64_t)sl * kCodeRow;
+  unsigned char* dst = stage + r * kCodeRow;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) cp_async16(dst + 16 * (2 * j + h), src + 16 * (2 * j + h));
+  cp_async16(stage + kRawCodeBytes + r * kScaleRow + 16 * h, scales + (int64_t)sl * kScaleRow + 16 * h);
+}
+static_assert(kAttnThreads == 2 * kTile, "issue_tile maps two threads to each row of a tile");
+
+// Staged tile -> f16 C in eight swizzled [128][64] chunks.  Warp w takes rows w, w + 8,
+// ...; lane L takes scale group L of the row (channels 16 L .. 16 L + 15 = code bytes
+// 8 L .. 8 L + 7), i.e. 16-byte units 2 (L % 4) and 2 (L % 4) + 1 of chunk L / 4, stored at
+// unit u ^ (row % 8).  Lanes of odd chunks store their two units in the opposite order,
+// so each quarter-warp store phase covers all eight units of a 128-byte row segment.
+// Loads of four rows are issued before any store.  Invalid rows become zeros.
+__device__ __forceinline__ void dequant_tile(const unsigned char* stage, unsigned char* Cs, int e0,
+                                             int ecount, const int32_t* slot, int warp, int lane) {
+  constexpr int kBatch = 4;
+  const unsigned char* rc = stage;
+  const unsigned char* rs = stage + kRawCodeBytes;
+  const int kc = lane >> 2, u0 = 2 * (lane & 3);
+  const int swap = kc & 1;
+  unsigned char* cbase = Cs + kc * kChunkBytes;
+#pragma unroll 1
+  for (int r0 = warp; r0 < kTile; r0 += kAttnWarps * kBatch) {
+    uint2 cw[kBatch];
+    uint32_t sb[kBatch];
+    bool ok[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int r = r0 + kAttnWarps * b;
+      const int e = e0 + r;
+      ok[b] = e < ecount && slot[e] >= 0;
+      cw[b] = *reinterpret_cast<const uint2*>(rc + r * kCodeRow + 8 * lane);
+      sb[b] = rs[r * kScaleRow + lane];
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int r = r0 + kAttnWarps * b;
+      uint32_t hv[8];
+      if (ok[b]) {
+        uint32_t s2;
+        const uint16_t sp = (uint16_t)(sb[b] | (sb[b] << 8));
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"(sp));
+        const uint32_t w[2] = {cw[b].x, cw[b].y};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t c2 = e2m1x2_to_f16x2((w[k >> 2] >> (8 * (k & 3))) & 0xFFu);
+          const __half2 x = __hmul2(*reinterpret_cast<const __half2*>(&c2),
+                                    *reinterpret_cast<const __half2*>(&s2));
+          hv[k] = *reinterpret_cast<const uint32_t*>(&x);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) hv[k] = 0u;
+      }
+      unsigned char* row = cbase + r * 128;
+      const int x7 = r & 7;
+      const uint4 a = make_uint4(hv[0], hv[1], hv[2], hv[3]), c = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+      if (swap) {
+        *reinterpret_cast<uint4*>(row + (((u0 + 1) ^ x7) << 4)) = c;
+        *reinterpret_cast<uint4*>(row + ((u0 ^ x7) << 4)) = a;
+      } else {
+        *reinterpret_cast<uint4*>(row + ((u0 ^ x7) << 4)) = a;
+        *reinterpret_cast<uint4*>(row + (((u0 + 1) ^ x7) << 4)) = c;
+      }
     }
   }
 }
 
-__global__ void __launch_bounds__(kAttnThreads, 2)
+// Butterfly over the warp: lane l ends with the reduction, over all 32 lanes, of value
+// (l >> 2) & 7 of the 8 each lane holds.
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce8(float (&v)[8], int lane) {
+  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const bool hi = lane & 16;
+    const float send = hi ? v[i] : v[i + 4];
+    const float keep = hi ? v[i + 4] : v[i];
+    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const bool hi = lane & 8;
+    const float send = hi ? v[i] : v[i + 2];
+    const float keep = hi ? v[i + 2] : v[i];
+    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+  }
+  {
+    const bool hi = lane & 4;
+    const float send = hi ? v[0] : v[1];
+    const float keep = hi ? v[1] : v[0];
+    v[0] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+  }
+  float x = v[0];
+  x = op(x, __shfl_xor_sync(0xffffffffu, x, 2));
+  x = op(x, __shfl_xor_sync(0xffffffffu, x, 1));
+  return x;
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 1)
     sparse_attn_kernel(const uint16_t* __restrict__ q, const uint8_t* __restrict__ codes,
                        const uint8_t* __restrict__ scales, const int32_t* __restrict__ idx,
                        AttnGeom g, const int32_t* __restrict__ q_seq, int32_t topk, int32_t split_len,
                        float softmax_scale, float* __restrict__ out, float* __restrict__ lse,
                        float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* st) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  AttnSmem& sm = *reinterpret_cast<AttnSmem*>(smem_raw);
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* Cs = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* Qs = Cs + kCBytes;
+  unsigned char* Ps = Qs + kQBytes;
+  unsigned char* raw = Ps + kPBytes;
+  AttnCtl& ctl = *reinterpret_cast<AttnCtl*>(raw + kRawStages * kRawBytes);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int sp = warp & 3;   // TMEM sub-partition: lanes 32 sp .. 32 sp + 31
+  const int hg = warp >> 2;  // heads 8 hg .. 8 hg + 7 in the softmax; O blocks 2 hg, 2 hg + 1
   const int qi = blockIdx.y, split = blockIdx.x, nsplit = gridDim.x;
   const int jbeg = split * split_len;
   const int ecount = max(0, min(topk, jbeg + split_len) - jbeg);
@@ -136,35 +234,45 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     } else if (s != -1) {
       report(st, CSA2_DEV_BAD_INDEX);
     }
-    sm.slot[e] = slot;
+    ctl.slot[e] = slot;
   }
-  if (tid < kHq) {
-    sm.m_run[tid] = -INFINITY;
-    sm.l_run[tid] = 0.0f;
+  if (tid == 0) {
+    mbar_init(&ctl.bar_s, 1);
+    mbar_init(&ctl.bar_pv, 1);
+    mbar_init(&ctl.bar_fin, 1);
+    ctl.abort = 0;
+    mbar_fence_init();
   }
+  if (warp == 0) tmem_alloc(&ctl.tmem, kTmemCols);
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem;
 
   // start the first gathers before touching Q
 #pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) {
-    if (s < ntiles) issue_tile(sm, s, s * kTile, ecount, codes, scales);
+  for (int i = 0; i < kRawStages; ++i) {
+    if (i < ntiles) issue_tile(raw + i * kRawBytes, i * kTile, ecount, ctl.slot, codes, scales);
     cp_async_commit();
   }
 
-  // ---- Q: max |q| -> power-of-two prescale -> f16 ----
-  const uint16_t* qq = q + (int64_t)qi * kHq * kDkv;
+  // ---- Q: one pass into registers, max |q| -> power-of-two prescale -> f16 chunks ----
+  const uint4* qv = reinterpret_cast<const uint4*>(q + (int64_t)qi * kHq * kDkv);
+  uint4 qr[4];
   uint32_t mx = 0;
-  for (int i = tid; i < kHq * kDkv / 8; i += kAttnThreads) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(qq) + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    qr[k] = __ldg(qv + tid + kAttnThreads * k);
+    const uint32_t w[4] = {qr[k].x, qr[k].y, qr[k].z, qr[k].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) mx = max(mx, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
   }
   mx = __reduce_max_sync(0xffffffffu, mx);
-  if (lane == 0) sm.red[warp] = mx;
+  if (lane == 0) ctl.qmax[warp] = mx;
   __syncthreads();
   uint32_t mxa = 0;
-  for (int w = 0; w < kAttnWarps; ++w) mxa = max(mxa, sm.red[w]);
+#pragma unroll
+  for (int w = 0; w < kAttnWarps; ++w) mxa = max(mxa, ctl.qmax[w]);
   int sh = 0;
   if (mxa != 0) {
     const int e = (int)((mxa >> 7) & 0xFF) - 127;  // bf16 exponent of max |q|
@@ -173,166 +281,190 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   const float pre = __uint_as_float((uint32_t)(127 + sh) << 23);   // 2^sh
   const float post = __uint_as_float((uint32_t)(127 - sh) << 23);  // 2^-sh
   const float kq = softmax_scale * 1.4426950408889634f * post;  // logits in the exp2 domain
-  for (int i = tid; i < kHq * kDkv / 8; i += kAttnThreads) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(qq) + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = tid + kAttnThreads * k;  // 8 channels 8i .. 8i + 7
+    const int hd = (8 * i) / kDkv, c = (8 * i) % kDkv;
+    const uint32_t w[4] = {qr[k].x, qr[k].y, qr[k].z, qr[k].w};
     uint32_t hv[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const __half2 h = __floats2half2_rn(bf16lo(w[e]) * pre, bf16hi(w[e]) * pre);
       hv[e] = *reinterpret_cast<const uint32_t*>(&h);
     }
-    const int hd = (8 * i) / kDkv, c = (8 * i) % kDkv;
-    *reinterpret_cast<uint4*>(&sm.qs[hd][c]) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    const int u = (c & 63) >> 3;
+    *reinterpret_cast<uint4*>(Qs + (c >> 6) * kQChunk + hd * 128 + ((u ^ (hd & 7)) << 4)) =
+        make_uint4(hv[0], hv[1], hv[2], hv[3]);
   }
+  fence_proxy_async_smem();
 
-  float acc[16][4];
+  // per-head reference max (log2 units) and normaliser, identical in every thread
+  float m_used[kHq], l_run[kHq];
 #pragma unroll
-  for (int n = 0; n < 16; ++n)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[n][e] = 0.0f;
+  for (int h = 0; h < kHq; ++h) {
+    m_used[h] = -INFINITY;
+    l_run[h] = 0.0f;
+  }
+  const uint32_t idesc_s = umma_idesc_f16(kTile, kHq, false, false, false);
+  const uint32_t idesc_o = umma_idesc_f16(128, kHq, false, true, false);
+  const uint32_t cs_addr = smem_u32(Cs), qs_addr = smem_u32(Qs), ps_addr = smem_u32(Ps);
+  const int tt = 32 * sp + lane;  // this thread's token row of the S tile
 
-  const int gq = lane >> 2, cq = lane & 3;
-  const int lm = lane >> 3, lr = lane & 7;  // ldmatrix: matrix and row served by this lane
   for (int t = 0; t < ntiles; ++t) {
-    const int sb = t % kStages;
-    cp_async_wait<kStages - 2>();
-    __syncthreads();  // tile t staged; previous tile's readers of cs / ps are done
-    {
-      const int nt = t + kStages - 1;
-      if (nt < ntiles) issue_tile(sm, nt % kStages, nt * kTile, ecount, codes, scales);
-      cp_async_commit();
-    }
-    // ---- S = Q . C^T with fused dequantisation: warp w -> tokens 8w .. 8w+7 ----
-    // Lane (gq, cq) serves token gq of the warp.  For channel block p (32 channels,
-    // k-steps 2p and 2p + 1) its k-slots {2cq, 2cq+1, 2cq+8, 2cq+9} map to channels
-    // 32p + 8cq + {0..3} (k-step 2p) and 32p + 8cq + {4..7} (k-step 2p + 1), so one
-    // 4-byte code word gives its B fragments and the A fragments of Q come from 16-byte
-    // reads of head rows gq and gq + 8 at the same channels.
-    const unsigned char* stage = sm.stage[sb];
-    const int e0 = t * kTile;
-    {
-      const int tok = 8 * warp + gq;
-      const bool tv = (e0 + tok < ecount) && sm.slot[e0 + tok] >= 0;
-      const unsigned char* crow = stage + tok * kCodeStride;
-      const unsigned char* srow = stage + kTile * kCodeStride + tok * kScaleRow;
-      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-      for (int p = 0; p < kDkv / 32; ++p) {
-        const int ch = 32 * p + 8 * cq;
-        const uint4 qa = *reinterpret_cast<const uint4*>(&sm.qs[gq][ch]);
-        const uint4 qb = *reinterpret_cast<const uint4*>(&sm.qs[gq + 8][ch]);
-        uint32_t h[4] = {0u, 0u, 0u, 0u};
-        if (tv) {
-          const uint32_t cw = *reinterpret_cast<const uint32_t*>(crow + ch / 2);
-          const __half2 s2 = __float2half2_rn(e4m3_decode(srow[ch >> 4]));
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t h2 = e2m1x2_to_f16x2((cw >> (8 * k)) & 0xFFu);
-            const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h2), s2);
-            h[k] = *reinterpret_cast<const uint32_t*>(&v);
-          }
-        }
-        *reinterpret_cast<uint4*>(&sm.cs[tok][ch]) = make_uint4(h[0], h[1], h[2], h[3]);
-        const uint32_t a0[4] = {qa.x, qb.x, qa.y, qb.y}, a1[4] = {qa.z, qb.z, qa.w, qb.w};
-        mma_f16(d0, a0, h[0], h[1]);
-        mma_f16(d1, a1, h[2], h[3]);
-      }
-      // d: heads gq (0..1) and gq + 8 (2..3), tokens 8w + 2cq, 8w + 2cq + 1
-      const int tk = 8 * warp + 2 * cq;
-      const bool v0 = (e0 + tk < ecount) && sm.slot[e0 + tk] >= 0;
-      const bool v1 = (e0 + tk + 1 < ecount) && sm.slot[e0 + tk + 1] >= 0;
-      sm.ss[gq][tk] = v0 ? (d0[0] + d1[0]) * kq : -INFINITY;
-      sm.ss[gq][tk + 1] = v1 ? (d0[1] + d1[1]) * kq : -INFINITY;
-      sm.ss[gq + 8][tk] = v0 ? (d0[2] + d1[2]) * kq : -INFINITY;
-      sm.ss[gq + 8][tk + 1] = v1 ? (d0[3] + d1[3]) * kq : -INFINITY;
-    }
+    unsigned char* stage = raw + (t % kRawStages) * kRawBytes;
+    // the previous tile's P.C product must be done with C and P before they are rewritten
+    if (tid == 0 && t > 0) (void)mbar_wait(&ctl.abort, &ctl.bar_pv, (uint32_t)((t - 1) & 1), st);
+    cp_async_wait<kRawStages - 1>();
     __syncthreads();
+    if (ctl.abort) break;
+    dequant_tile(stage, Cs, t * kTile, ecount, ctl.slot, warp, lane);
+    fence_proxy_async_smem();
+    __syncthreads();  // C complete; the staging buffer is free again
 
-    // ---- online softmax: warp w -> heads 4w .. 4w+3, lane -> token ----
+    // ---- S^T = C . Q^T, issued before the next gathers so the two overlap ----
+    if (tid == 0) {
+      tc_fence_after();
 #pragma unroll
-    for (int hh = 0; hh < 4; ++hh) {
-      const int h = 4 * warp + hh;
-      const float s0 = sm.ss[h][lane];
-      float tmax = s0;
+      for (int kc = 0; kc < kDkv / 64; ++kc)
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-      const float m_old = sm.m_run[h];
-      const float m_new = fmaxf(m_old, tmax);
-      const float al = (m_new == -INFINITY) ? 1.0f : exp2f(m_old - m_new);
-      const __half p0 = __float2half_rn((s0 == -INFINITY) ? 0.0f : exp2f(s0 - m_new));
-      sm.ps[h][lane] = p0;
-      // the normaliser sums the same f16-rounded weights the P.C product uses, so the
-      // output stays an exact weighted average of the rows
-      float ps = __half2float(p0);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-      __syncwarp();
-      if (lane == 0) {
-        sm.m_run[h] = m_new;
-        sm.l_run[h] = sm.l_run[h] * al + ps;
-        sm.alpha[h] = al;
-      }
+        for (int kk = 0; kk < 4; ++kk)
+          umma_f16(tmem, umma_desc_sw128(cs_addr + kc * kChunkBytes, 16, 1024) + 2 * kk,
+                   umma_desc_sw128(qs_addr + kc * kQChunk, 16, 1024) + 2 * kk, idesc_s,
+                   (kc | kk) != 0 ? 1u : 0u);
+      umma_commit(&ctl.bar_s);
     }
+    if (t + kRawStages < ntiles)
+      issue_tile(stage, (t + kRawStages) * kTile, ecount, ctl.slot, codes, scales);
+    cp_async_commit();
+    if (tid == 0) (void)mbar_wait(&ctl.abort, &ctl.bar_s, (uint32_t)(t & 1), st);
     __syncthreads();
+    if (ctl.abort) break;
+    tc_fence_after();
 
-    // ---- O += P . C: warp w -> channels 128w .. 128w+127 ----
-    {
-      const float al0 = sm.alpha[gq], al1 = sm.alpha[gq + 8];
+    // ---- softmax: thread -> token tt, heads 8 hg .. 8 hg + 7 ----
+    uint32_t sr[8];
+    tmem_ld8(tmem + ((uint32_t)(32 * sp) << 16) + (uint32_t)(8 * hg), sr);
+    const int e = t * kTile + tt;
+    const bool valid = e < ecount && ctl.slot[e] >= 0;
+    float s[8], v[8];
 #pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        acc[n][0] *= al0;
-        acc[n][1] *= al0;
-        acc[n][2] *= al1;
-        acc[n][3] *= al1;
-      }
+    for (int i = 0; i < 8; ++i) {
+      s[i] = valid ? __uint_as_float(sr[i]) * kq : -INFINITY;
+      v[i] = s[i];
+    }
+    const int hl = (lane >> 2) & 7;
+    const float wmax = warp_reduce8<true>(v, lane);
+    if ((lane & 3) == 0) ctl.red_max[8 * hg + hl][sp] = wmax;
+    __syncthreads();
+    float alpha[kHq];
+    bool moved = false;
 #pragma unroll
-      for (int ks = 0; ks < kTile / 16; ++ks) {
-        uint32_t a[4];
-        ldsm_x4(a, &sm.ps[(lm & 1) * 8 + lr][16 * ks + (lm >> 1) * 8]);
+    for (int h = 0; h < kHq; ++h) {
+      const float4 r = *reinterpret_cast<const float4*>(ctl.red_max[h]);
+      const float mt = fmaxf(fmaxf(r.x, r.y), fmaxf(r.z, r.w));
+      const float mu = m_used[h];
+      float mn = mu;
+      if (mu == -INFINITY || mt > mu + kRescaleGap) mn = fmaxf(mu, mt);
+      alpha[h] = (mn == mu) ? 1.0f : exp2f(mu - mn);
+      moved |= (mn != mu);
+      m_used[h] = mn;
+    }
+    const int tk = tt & 63, pu = tk >> 3;
+    unsigned char* prow = Ps + (tt >> 6) * kQChunk;
 #pragma unroll
-        for (int np = 0; np < 8; ++np) {
-          uint32_t bb[4];
-          // matrices: (tok 0-7, ch n0), (tok 8-15, ch n0), (tok 0-7, ch n0+8), (tok 8-15, ch n0+8)
-          ldsm_x4_t(bb, &sm.cs[16 * ks + (lm & 1) * 8 + lr][128 * warp + 16 * np + (lm >> 1) * 8]);
-          mma_f16(acc[2 * np], a, bb[0], bb[1]);
-          mma_f16(acc[2 * np + 1], a, bb[2], bb[3]);
-        }
-      }
+    for (int i = 0; i < 8; ++i) {
+      const float mh = hg ? m_used[8 + i] : m_used[i];
+      const __half ph = __float2half_rn(s[i] == -INFINITY ? 0.0f : exp2f(s[i] - mh));
+      *reinterpret_cast<__half*>(prow + (8 * hg + i) * 128 + ((pu ^ i) << 4) + (tk & 7) * 2) = ph;
+      v[i] = __half2float(ph);
+    }
+    const float wsum = warp_reduce8<false>(v, lane);
+    if ((lane & 3) == 0) ctl.red_sum[8 * hg + hl][sp] = wsum;
+    if (moved && t > 0) {  // move the accumulated O^T to the new reference
+      uint32_t o[32];
+      const uint32_t ta = tmem + ((uint32_t)(32 * sp) << 16) + kOCol + (uint32_t)(32 * hg);
+      tmem_ld32(ta, o);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha[i & 15]);
+      tmem_st32(ta, o);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < kHq; ++h) {
+      const float4 r = *reinterpret_cast<const float4*>(ctl.red_sum[h]);
+      l_run[h] = l_run[h] * alpha[h] + ((r.x + r.y) + (r.z + r.w));
+    }
+
+    // ---- O^T += C^T . P^T, one 128-channel block at a time ----
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int j = 0; j < kDkv / 128; ++j)
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_f16(tmem + kOCol + 16 * j,
+                   umma_desc_sw128(cs_addr + 2 * j * kChunkBytes + kk * 2048, kChunkBytes, 1024),
+                   umma_desc_sw128(ps_addr + (kk >> 2) * kQChunk, 16, 1024) + 2 * (kk & 3),
+                   idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(&ctl.bar_pv);
     }
   }
   cp_async_wait<0>();
+  if (tid == 0) {
+    if (ntiles > 0 && !ctl.abort) (void)mbar_wait(&ctl.abort, &ctl.bar_pv, (uint32_t)((ntiles - 1) & 1), st);
+    // every MMA this thread issued has completed before TMEM is read or released
+    umma_commit(&ctl.bar_fin);
+    (void)mbar_drain(&ctl.bar_fin, 0, 1u << 20);
+  }
   __syncthreads();
+  tc_fence_after();
+  const bool have = ntiles > 0 && !ctl.abort;
 
-  // ---- epilogue ----
-  const float l0 = sm.l_run[gq], l1 = sm.l_run[gq + 8];
-  if (nsplit == 1) {
-    const float i0 = l0 > 0.f ? 1.0f / l0 : 0.f, i1 = l1 > 0.f ? 1.0f / l1 : 0.f;
-    float* o = out + (int64_t)qi * kHq * kDkv;
+  // ---- epilogue: thread -> channel 128 j + 32 sp + lane of blocks j = 2 hg, 2 hg + 1 ----
+  uint32_t o[32];
+  if (have) {
+    tmem_ld32(tmem + ((uint32_t)(32 * sp) << 16) + kOCol + (uint32_t)(32 * hg), o);
+  } else {
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      const int ch = 128 * warp + 8 * n + 2 * cq;
-      *reinterpret_cast<float2*>(o + gq * kDkv + ch) = make_float2(acc[n][0] * i0, acc[n][1] * i0);
-      *reinterpret_cast<float2*>(o + (gq + 8) * kDkv + ch) = make_float2(acc[n][2] * i1, acc[n][3] * i1);
+    for (int i = 0; i < 32; ++i) o[i] = 0u;
+  }
+  if (nsplit == 1) {
+    float* ob = out + (int64_t)qi * kHq * kDkv;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int h = i & 15, ch = 128 * (2 * hg + (i >> 4)) + 32 * sp + lane;
+      const float l = l_run[h];
+      ob[h * kDkv + ch] = l > 0.f ? __uint_as_float(o[i]) / l : 0.f;
     }
-    if (lse != nullptr && tid < kHq) {
-      const float l = sm.l_run[tid];
-      lse[(int64_t)qi * kHq + tid] =
-          l > 0.f ? sm.m_run[tid] * 0.6931471805599453f + logf(l) : -INFINITY;
+    if (lse != nullptr) {
+#pragma unroll
+      for (int h = 0; h < kHq; ++h)
+        if (tid == h)
+          lse[(int64_t)qi * kHq + h] =
+              l_run[h] > 0.f ? m_used[h] * 0.6931471805599453f + logf(l_run[h]) : -INFINITY;
     }
   } else {
-    float* o = part_o + ((int64_t)qi * nsplit + split) * kHq * kDkv;
+    float* ob = part_o + ((int64_t)qi * nsplit + split) * kHq * kDkv;
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      const int ch = 128 * warp + 8 * n + 2 * cq;
-      *reinterpret_cast<float2*>(o + gq * kDkv + ch) = make_float2(acc[n][0], acc[n][1]);
-      *reinterpret_cast<float2*>(o + (gq + 8) * kDkv + ch) = make_float2(acc[n][2], acc[n][3]);
+    for (int i = 0; i < 32; ++i) {
+      const int h = i & 15, ch = 128 * (2 * hg + (i >> 4)) + 32 * sp + lane;
+      ob[h * kDkv + ch] = __uint_as_float(o[i]);
     }
-    if (tid < kHq) {
-      float* ml = part_ml + ((int64_t)qi * nsplit + split) * 2 * kHq;
-      ml[tid] = sm.m_run[tid];
-      ml[kHq + tid] = sm.l_run[tid];
-    }
+    float* ml = part_ml + ((int64_t)qi * nsplit + split) * 2 * kHq;
+#pragma unroll
+    for (int h = 0; h < kHq; ++h)
+      if (tid == h) {
+        ml[h] = m_used[h];
+        ml[kHq + h] = l_run[h];
+      }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -395,8 +527,8 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restri
       make_float4(a.x * iv, a.y * iv, a.z * iv, a.w * iv);
 }
 
-// Splits per query: the count that minimises (waves of two CTAs per SM) x (tiles per
-// CTA + a fixed start-up cost of ~4 tiles), with at most kMaxSplit entries per CTA.
+// Splits per query: the count that minimises (waves of one CTA per SM) x (tiles per
+// CTA + a fixed start-up cost of ~2 tiles), with at most kMaxSplit entries per CTA.
 int attn_splits(int32_t num_q, int32_t topk, int num_sms) {
   const int tiles = std::max(1, (topk + kTile - 1) / kTile);
   const int min_splits = (tiles * kTile + kMaxSplit - 1) / kMaxSplit;
@@ -407,8 +539,8 @@ int attn_splits(int32_t num_q, int32_t topk, int num_sms) {
     const int per = (tiles + sp - 1) / sp;     // tiles per split
     const int real = (tiles + per - 1) / per;  // splits actually used
     const int64_t ctas = (int64_t)num_q * real;
-    const int64_t waves = (ctas + 2 * num_sms - 1) / (2 * num_sms);
-    const double cost = (double)waves * (per + 4);
+    const int64_t waves = (ctas + num_sms - 1) / num_sms;
+    const double cost = (double)waves * (per + 2);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = real;
@@ -423,7 +555,7 @@ int attn_split_len(int32_t topk, int splits) {
   return per * kTile;
 }
 
-size_t attn_smem_bytes() { return sizeof(AttnSmem); }
+size_t attn_smem_bytes() { return kAttnSmem; }
 
 cudaError_t launch_attn(const uint16_t* q, const uint8_t* codes, const uint8_t* scales,
                         const int32_t* idx, const csa2_pages& pg, float* out, float* lse,
