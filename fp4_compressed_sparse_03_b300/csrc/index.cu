@@ -321,22 +321,26 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 // ------------------------------------------------------------------ TMA page scorer --
 // Full mode, contiguous context: the unit of work is a whole 64-token page (16 KB of
 // keys).  One producer thread streams pages through a 2D tensor map (two 64 x 64 bf16
-// boxes per page, 128-byte swizzle) into an 8-slot shared-memory ring.  The 8 consumer
-// warps take the pages in pairs: warp w scores rows 8w .. 8w+7 of both pages of a pair
+// boxes per page, 128-byte swizzle) into a 4-slot shared-memory ring; two such CTAs run
+// on each SM.  The 4 consumer warps take every page: warp w scores rows 16w .. 16w+15
 // as the 16 rows of one tensor-core tile:
 //   D[16 keys][8 cols] = K[16 keys][16 dims] x Q^T[16 dims][8 cols]   (m16n8k16, bf16)
 // where the 8 columns of an n-tile are (query, head) pairs 4t + h of two queries, so
 // one n-tile serves 1-2 queries and two serve 3-4 draft queries of a sequence.  Dims
 // are visited in the same permuted order on both sides: lane c's 16-byte chunk of dims
-// 32j + 8c .. +7 supplies its A and B fragments for k-steps 2j and 2j + 1.
-// Measured on B300, the CUDA-core form of this dot product (packed FFMA2, one key
-// per 4 lanes) ran at 124 us of pure arithmetic for 2.1M keys against 85 us to stream
-// them, so the contraction runs on the tensor cores even for a single query.
+// 32j + 8c .. +7 supplies its A and B fragments for k-steps 2j and 2j + 1.  A consumer
+// releases a page as soon as it holds its rows in registers.
+// Measured on B300: the CUDA-core form of this dot product (packed FFMA2, one key per 4
+// lanes) ran at 124 us of pure arithmetic for 2.1M keys against 85 us to stream them,
+// so the contraction runs on the tensor cores even for a single query; and one 9-warp
+// CTA per SM with an 8-page ring streamed 2.1M keys in 115 us where two 5-warp CTAs
+// per SM with 4-page rings take 96 us (ring depth alone made no difference).
 
-constexpr int kPageStages = 8;
+constexpr int kPageStages = 4;  // ring depth per CTA
 constexpr int kPageBytes = kPage * kKeyRow;            // 16 KB
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 4;
 constexpr int kTmaThreads = (kConsumerWarps + 1) * 32;  // + 1 producer warp
+constexpr int kScoreCtasPerSm = 2;
 
 struct PageRing {
   uint64_t full[kPageStages];
@@ -358,18 +362,19 @@ __device__ __forceinline__ void read_page_row(uint4 (&kv)[4], uint32_t base, int
   for (int j = 0; j < 4; ++j) kv[j] = lds128(page_chunk(base, row, 4 * j + c));
 }
 
-__global__ void __launch_bounds__(kTmaThreads, 1)
+__global__ void __launch_bounds__(kTmaThreads, kScoreCtasPerSm)
     score_pages_kernel(const __grid_constant__ CUtensorMap keymap, const uint16_t* __restrict__ q_idx,
                        const int32_t* __restrict__ q_seq, int32_t num_q, ScoreGeom g,
                        uint32_t* __restrict__ ws, int64_t ws_stride, RunList rl, int32_t* st) {
   extern __shared__ __align__(1024) unsigned char page_smem_raw[];
   unsigned char* data = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(page_smem_raw) + 1023) & ~uintptr_t(1023));
-  PageRing* ring = reinterpret_cast<PageRing*>(data + kPageStages * kPageBytes);
+  constexpr int S = kPageStages;
+  PageRing* ring = reinterpret_cast<PageRing*>(data + S * kPageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, c = lane & 3;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kPageStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&ring->full[s], 1);
       mbar_init(&ring->empty[s], kConsumerWarps);
     }
@@ -389,9 +394,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       RunCursor cu;
       cursor_seek(cu, rl, R, p0);
       uint32_t issued = 0, last_par = 0;
+      int s = 0;
+      uint32_t ph = 0;
       for (int64_t i = p0; i < p1; ++i) {
-        const int s = (int)((i - p0) % kPageStages);
-        const uint32_t ph = (uint32_t)(((i - p0) / kPageStages) & 1);
         if (!mbar_wait(&ring->abort, &ring->empty[s], ph ^ 1u, st)) break;
         cursor_advance(cu, rl, i);
         const int page = (int)(i - cu.start);
@@ -413,17 +418,21 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
           report(st, CSA2_DEV_BAD_PAGE);
           mbar_arrive(&ring->full[s]);
         }
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       if (ring->abort)  // our copies must land before the CTA's shared memory is released
-        for (int s = 0; s < kPageStages; ++s)
+        for (int s = 0; s < S; ++s)
           if (issued & (1u << s)) (void)mbar_wait(&ring->abort, &ring->full[s], (last_par >> s) & 1u, st, 1u << 20);
     }
   } else {
-    // ---------------- consumers: every warp takes every page, two pages per step ----
-    // this lane's row in each page of the pair: the two lanes groups gq = 2p, 2p + 1 of a
+    // ---------------- consumers: every warp takes every page ----
+    // this lane's rows rr and rr + 8 of each page: the lane groups gq = 2p, 2p + 1 of a
     // quarter-warp phase read rows whose 128-byte swizzle masks (row % 8) are p and p + 4,
     // so their 16-byte chunks land in disjoint bank halves (no bank conflict)
-    const int rr = 8 * warp + ((gq >> 1) | ((gq & 1) << 2));
+    const int rr = 16 * warp + ((gq >> 1) | ((gq & 1) << 2));
     int cur_run = -1, rows = 0, q0 = 0, T = 0, NT = 0;
     uint32_t bq[2][4][4];  // [n-tile][j][word]: B fragments of Q^T
     auto enter = [&](int r) {
@@ -451,10 +460,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         }
       }
     };
-    // MMA over (row a of one page, row b of another page) with the current run's Q;
-    // scores of a (b) go to page pa (pb); use_a / use_b select which halves to store.
-    auto tile = [&](const uint4 (&ka)[4], const uint4 (&kb)[4], int pa, int pb, bool va, bool vb,
-                    bool use_a, bool use_b) {
+    // MMA over rows ra and rb of one page with the current run's Q
+    auto tile = [&](const uint4 (&ka)[4], const uint4 (&kb)[4], int page, int ra, int rb,
+                    bool valid) {
       float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -478,46 +486,29 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         const int t = 2 * nt + (c >> 1);
         if ((c & 1) == 0 && t < T) {
           uint32_t* out = ws + (int64_t)(q0 + t) * ws_stride;
-          const int ta = pa * kPage + rr, tb = pb * kPage + rr;
-          if (use_a && ta < rows) out[ta] = va ? rank_key(s0) : 0u;
-          if (use_b && tb < rows) out[tb] = vb ? rank_key(s1) : 0u;
+          const int ta = page * kPage + ra, tb = page * kPage + rb;
+          if (ta < rows) out[ta] = valid ? rank_key(s0) : 0u;
+          if (tb < rows) out[tb] = valid ? rank_key(s1) : 0u;
         }
       }
     };
-    const uint4 zero4[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
-                            make_uint4(0, 0, 0, 0)};
-    for (int64_t i = p0; i < p1; i += 2) {
-      const int s0 = (int)((i - p0) % kPageStages);
-      const uint32_t ph0 = (uint32_t)(((i - p0) / kPageStages) & 1);
-      if (!mbar_wait(&ring->abort, &ring->full[s0], ph0, st)) break;
-      const bool has1 = i + 1 < p1;
-      const int s1 = (int)((i + 1 - p0) % kPageStages);
-      if (has1) {
-        const uint32_t ph1 = (uint32_t)(((i + 1 - p0) / kPageStages) & 1);
-        if (!mbar_wait(&ring->abort, &ring->full[s1], ph1, st)) break;
-      }
-      const int run0 = ring->run[s0], page0 = ring->page[s0];
-      const bool v0 = ring->valid[s0] != 0;
-      const int run1 = has1 ? ring->run[s1] : run0, page1 = has1 ? ring->page[s1] : page0;
-      const bool v1 = has1 && ring->valid[s1] != 0;
+    int s = 0;
+    uint32_t ph = 0;
+    for (int64_t i = p0; i < p1; ++i) {
+      if (!mbar_wait(&ring->abort, &ring->full[s], ph, st)) break;
+      const int run = ring->run[s], page = ring->page[s];
+      const bool valid = ring->valid[s] != 0;
       uint4 k0[4], k1[4];
-      read_page_row(k0, data_s + s0 * kPageBytes, rr, c);
-      if (has1) read_page_row(k1, data_s + s1 * kPageBytes, rr, c);
+      read_page_row(k0, data_s + s * kPageBytes, rr, c);
+      read_page_row(k1, data_s + s * kPageBytes, rr + 8, c);
       __syncwarp();
-      if (lane == 0) {  // the keys are in registers now
-        mbar_arrive(&ring->empty[s0]);
-        if (has1) mbar_arrive(&ring->empty[s1]);
+      if (lane == 0) mbar_arrive(&ring->empty[s]);  // the keys are in registers now
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
       }
-      enter(run0);
-      if (has1 && run1 == run0) {
-        tile(k0, k1, page0, page1, v0, v1, true, true);
-      } else {
-        tile(k0, zero4, page0, page0, v0, false, true, false);
-        if (has1) {
-          enter(run1);
-          tile(k1, zero4, page1, page1, v1, false, true, false);
-        }
-      }
+      enter(run);
+      tile(k0, k1, page, rr, rr + 8, valid);
     }
   }
   __syncthreads();
@@ -1111,7 +1102,7 @@ cudaError_t launch_score_full(const uint16_t* q_idx, const uint16_t* keys, const
   CUtensorMap keymap;
   if (!make_bf16_map(&keymap, keys, (int64_t)pg.num_pages * kPage, kDidx, 64, kPage))
     return cudaErrorInvalidValue;
-  const int grid = std::max(1, num_sms);
+  const int grid = std::max(1, kScoreCtasPerSm * num_sms);
   e = cudaFuncSetAttribute(score_pages_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kTmaSmem);
   if (e != cudaSuccess) return e;
