@@ -8,8 +8,8 @@
 // One CTA (8 warps, one per SM) handles one (query, split) pair: up to `split_len`
 // selected entries in tiles of 128 tokens, on the 5th-generation tensor cores:
 //   1. cp.async gathers the tile's 128 x (256 B codes + 32 B scales) into a 2-stage
-//      staging ring two tiles ahead (1D bulk copies were measured slower: the copy
-//      engine took ~50 cycles per 256-byte row);
+//      staging ring (1D bulk copies were measured slower: the copy engine took ~50
+//      cycles per 256-byte row);
 //   2. the warps dequantise the tile into an f16 tile C [128 tokens][512 channels]
 //      laid out as eight 128-byte-swizzled [128][64] chunks (E2M1 x E4M3 is exact in
 //      f16: at most 6 significant bits, magnitudes 2^-10 .. 2688);
@@ -21,9 +21,14 @@
 //   5. O^T += C^T . P^T: M=128 (channels) x N=16 (heads) x K=128 (tokens) per 128-channel
 //      block, reading the same C tile as an MN-major operand; P^T is f16, and the
 //      normaliser sums the same f16-rounded weights.
+// Steps 5 (tile t) and 2-3 (tile t+1) are pipelined by 128-channel chunk pairs: block
+// j of the P.C product commits its own mbarrier, the next tile's chunk pair j is
+// dequantised as soon as block j is done, and its logit MMAs are issued right after.
 // Q is converted to f16 after a per-query power-of-two prescale (exact for every
 // value within 2^28 of the largest |q|); the scale is undone in the logit factor.
 // Several splits per query are merged by a log-sum-exp combine kernel.
+#include <cstddef>
+
 #include "tcgen05.cuh"
 
 namespace csa2 {
@@ -44,15 +49,22 @@ constexpr uint32_t kTmemCols = 128;  // S^T at columns 0..15, O^T blocks at 32 +
 constexpr uint32_t kOCol = 32;
 constexpr float kRescaleGap = 8.0f;  // log2 units
 
+constexpr int kPairs = kDkv / 128;  // 128-channel chunk pairs = O^T blocks
+
 struct AttnCtl {
-  uint64_t bar_s, bar_pv, bar_fin;
+  alignas(16) float red_max[kHq][4];  // read back as float4 per head
+  alignas(16) float red_sum[kHq][4];
+  uint64_t bar_s, bar_fin;
+  uint64_t bar_pv[kPairs];  // block j of the current tile's P.C product (and all before it)
   uint32_t tmem;
   volatile int abort;
-  float red_max[kHq][4];
-  float red_sum[kHq][4];
   uint32_t qmax[kAttnWarps];
   int32_t slot[kMaxSplit];  // physical row of each selected entry, -1 if skipped
 };
+static_assert(offsetof(AttnCtl, red_max) % 16 == 0 && offsetof(AttnCtl, red_sum) % 16 == 0,
+              "per-head reductions are read as float4");
+static_assert(offsetof(AttnCtl, bar_s) % 8 == 0 && offsetof(AttnCtl, bar_pv) % 8 == 0,
+              "mbarriers need 8-byte alignment");
 constexpr size_t kAttnSmem = 1024 + kCBytes + kQBytes + kPBytes + kRawStages * kRawBytes + sizeof(AttnCtl);
 static_assert(kAttnSmem <= 232448, "sparse attention needs more than 227 KB of shared memory");
 
@@ -66,6 +78,13 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N));
+}
+
+// 2^x by the MUFU ex2 instruction (flushes subnormal results to zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Bounded wait on an mbarrier phase that ignores the CTA's abort flag (used to drain).
@@ -86,6 +105,9 @@ struct AttnGeom {
 // Gather the codes and scales of the tile starting at local entry `e0` into `stage`:
 // thread -> row tid / 2; the two threads of a row take the 16-byte parts of even and odd
 // index (16 code parts, then 2 scale parts), so each pair of lanes moves 32 contiguous bytes.
+// Codes are staged chunk-pair-major, [pair j][row][64 B] (code bytes 64 j .. 64 j + 63 of
+// each row), so that the dequantiser's four rows per load instruction are contiguous;
+// scales are staged [row][32 B].
 __device__ __forceinline__ void issue_tile(unsigned char* stage, int e0, int ecount,
                                            const int32_t* slot, const uint8_t* __restrict__ codes,
                                            const uint8_t* __restrict__ scales) {
@@ -94,70 +116,73 @@ __device__ __forceinline__ void issue_tile(unsigned char* stage, int e0, int eco
   const int32_t sl = e < ecount ? slot[e] : -1;
   if (sl < 0) return;
   const uint8_t* src = codes + (int64_t)sl * kCodeRow;
-  unsigned char* dst = stage + r * kCodeRow;
+  unsigned char* dst = stage + r * 64;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) cp_async16(dst + 16 * (2 * j + h), src + 16 * (2 * j + h));
+  for (int j = 0; j < 8; ++j) {
+    const int part = 2 * j + h;  // bytes 16 part .. +15 = pair part / 4, offset 16 (part % 4)
+    cp_async16(dst + (part >> 2) * (kTile * 64) + 16 * (part & 3), src + 16 * part);
+  }
   cp_async16(stage + kRawCodeBytes + r * kScaleRow + 16 * h, scales + (int64_t)sl * kScaleRow + 16 * h);
 }
 static_assert(kAttnThreads == 2 * kTile, "issue_tile maps two threads to each row of a tile");
 
-// Staged tile -> f16 C in eight swizzled [128][64] chunks.  Warp w takes rows w, w + 8,
-// ...; lane L takes scale group L of the row (channels 16 L .. 16 L + 15 = code bytes
-// 8 L .. 8 L + 7), i.e. 16-byte units 2 (L % 4) and 2 (L % 4) + 1 of chunk L / 4, stored at
-// unit u ^ (row % 8).  Lanes of odd chunks store their two units in the opposite order,
-// so each quarter-warp store phase covers all eight units of a 128-byte row segment.
-// Loads of four rows are issued before any store.  Invalid rows become zeros.
-__device__ __forceinline__ void dequant_tile(const unsigned char* stage, unsigned char* Cs, int e0,
-                                             int ecount, const int32_t* slot, int warp, int lane) {
-  constexpr int kBatch = 4;
+// Staged tile -> chunks 2j, 2j + 1 (channels 128 j .. 128 j + 127) of the f16 tile C.
+// Lane -> (row sub-index lane / 8, scale group 8 j + lane % 8 = 16 channels = code bytes
+// 64 j + 8 (lane % 8) .. +7); warp w takes rows 4 (w + 8 i) + lane / 8, i = 0..3, so each
+// 8-byte load instruction reads 256 contiguous staged bytes.  The
+// group's 16 channels are units 2 (lane % 4), +1 of chunk 2 j + (lane % 8) / 4, stored at
+// unit u ^ (row % 8); lanes of the odd chunk store their two units in the opposite
+// order, so each quarter-warp store phase covers all eight units of a 128-byte row
+// segment.  All loads are issued before any store.  Invalid rows become zeros.
+__device__ __forceinline__ void dequant_pair(const unsigned char* stage, unsigned char* Cs, int j,
+                                             int e0, int ecount, const int32_t* slot, int warp,
+                                             int lane) {
+  constexpr int kIter = kTile / (4 * kAttnWarps);  // 4
   const unsigned char* rc = stage;
   const unsigned char* rs = stage + kRawCodeBytes;
-  const int kc = lane >> 2, u0 = 2 * (lane & 3);
-  const int swap = kc & 1;
-  unsigned char* cbase = Cs + kc * kChunkBytes;
-#pragma unroll 1
-  for (int r0 = warp; r0 < kTile; r0 += kAttnWarps * kBatch) {
-    uint2 cw[kBatch];
-    uint32_t sb[kBatch];
-    bool ok[kBatch];
+  const int l8 = lane & 7, rsub = lane >> 3;
+  const int ch = 2 * j + (l8 >> 2), u0 = 2 * (l8 & 3), swap = l8 >> 2;
+  unsigned char* cbase = Cs + ch * kChunkBytes;
+  uint2 cw[kIter];
+  uint32_t sb[kIter];
+  bool ok[kIter];
 #pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      const int r = r0 + kAttnWarps * b;
-      const int e = e0 + r;
-      ok[b] = e < ecount && slot[e] >= 0;
-      cw[b] = *reinterpret_cast<const uint2*>(rc + r * kCodeRow + 8 * lane);
-      sb[b] = rs[r * kScaleRow + lane];
+  for (int i = 0; i < kIter; ++i) {
+    const int r = 4 * (warp + kAttnWarps * i) + rsub;
+    const int e = e0 + r;
+    ok[i] = e < ecount && slot[e] >= 0;
+    cw[i] = *reinterpret_cast<const uint2*>(rc + j * (kTile * 64) + r * 64 + 8 * l8);
+    sb[i] = rs[r * kScaleRow + 8 * j + l8];
+  }
+#pragma unroll
+  for (int i = 0; i < kIter; ++i) {
+    const int r = 4 * (warp + kAttnWarps * i) + rsub;
+    uint32_t hv[8];
+    if (ok[i]) {
+      uint32_t s2;
+      const uint16_t sp = (uint16_t)(sb[i] | (sb[i] << 8));
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"(sp));
+      const uint32_t w[2] = {cw[i].x, cw[i].y};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t c2 = e2m1x2_to_f16x2((w[k >> 2] >> (8 * (k & 3))) & 0xFFu);
+        const __half2 x = __hmul2(*reinterpret_cast<const __half2*>(&c2),
+                                  *reinterpret_cast<const __half2*>(&s2));
+        hv[k] = *reinterpret_cast<const uint32_t*>(&x);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) hv[k] = 0u;
     }
-#pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      const int r = r0 + kAttnWarps * b;
-      uint32_t hv[8];
-      if (ok[b]) {
-        uint32_t s2;
-        const uint16_t sp = (uint16_t)(sb[b] | (sb[b] << 8));
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"(sp));
-        const uint32_t w[2] = {cw[b].x, cw[b].y};
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t c2 = e2m1x2_to_f16x2((w[k >> 2] >> (8 * (k & 3))) & 0xFFu);
-          const __half2 x = __hmul2(*reinterpret_cast<const __half2*>(&c2),
-                                    *reinterpret_cast<const __half2*>(&s2));
-          hv[k] = *reinterpret_cast<const uint32_t*>(&x);
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) hv[k] = 0u;
-      }
-      unsigned char* row = cbase + r * 128;
-      const int x7 = r & 7;
-      const uint4 a = make_uint4(hv[0], hv[1], hv[2], hv[3]), c = make_uint4(hv[4], hv[5], hv[6], hv[7]);
-      if (swap) {
-        *reinterpret_cast<uint4*>(row + (((u0 + 1) ^ x7) << 4)) = c;
-        *reinterpret_cast<uint4*>(row + ((u0 ^ x7) << 4)) = a;
-      } else {
-        *reinterpret_cast<uint4*>(row + ((u0 ^ x7) << 4)) = a;
-        *reinterpret_cast<uint4*>(row + (((u0 + 1) ^ x7) << 4)) = c;
-      }
+    unsigned char* row = cbase + r * 128;
+    const int x7 = r & 7;
+    const uint4 a = make_uint4(hv[0], hv[1], hv[2], hv[3]), c = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+    if (swap) {
+      *reinterpret_cast<uint4*>(row + (((u0 + 1) ^ x7) << 4)) = c;
+      *reinterpret_cast<uint4*>(row + ((u0 ^ x7) << 4)) = a;
+    } else {
+      *reinterpret_cast<uint4*>(row + ((u0 ^ x7) << 4)) = a;
+      *reinterpret_cast<uint4*>(row + (((u0 + 1) ^ x7) << 4)) = c;
     }
   }
 }
@@ -238,7 +263,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   if (tid == 0) {
     mbar_init(&ctl.bar_s, 1);
-    mbar_init(&ctl.bar_pv, 1);
+    for (int j = 0; j < kPairs; ++j) mbar_init(&ctl.bar_pv[j], 1);
     mbar_init(&ctl.bar_fin, 1);
     ctl.abort = 0;
     mbar_fence_init();
@@ -310,32 +335,49 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t cs_addr = smem_u32(Cs), qs_addr = smem_u32(Qs), ps_addr = smem_u32(Ps);
   const int tt = 32 * sp + lane;  // this thread's token row of the S tile
 
-  for (int t = 0; t < ntiles; ++t) {
-    unsigned char* stage = raw + (t % kRawStages) * kRawBytes;
-    // the previous tile's P.C product must be done with C and P before they are rewritten
-    if (tid == 0 && t > 0) (void)mbar_wait(&ctl.abort, &ctl.bar_pv, (uint32_t)((t - 1) & 1), st);
-    cp_async_wait<kRawStages - 1>();
-    __syncthreads();
-    if (ctl.abort) break;
-    dequant_tile(stage, Cs, t * kTile, ecount, ctl.slot, warp, lane);
-    fence_proxy_async_smem();
-    __syncthreads();  // C complete; the staging buffer is free again
-
-    // ---- S^T = C . Q^T, issued before the next gathers so the two overlap ----
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kc = 0; kc < kDkv / 64; ++kc)
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_f16(tmem, umma_desc_sw128(cs_addr + kc * kChunkBytes, 16, 1024) + 2 * kk,
-                   umma_desc_sw128(qs_addr + kc * kQChunk, 16, 1024) + 2 * kk, idesc_s,
-                   (kc | kk) != 0 ? 1u : 0u);
-      umma_commit(&ctl.bar_s);
+  // Build C for tile u from its staged rows, chunk pair by chunk pair, issuing the logit
+  // MMAs of each pair as soon as it is written.  For u > 0, pair j is overwritten only
+  // after block j of tile u - 1's P.C product has completed.  Returns false on abort.
+  auto build_tile = [&](int u) -> bool {
+    unsigned char* stage = raw + (u % kRawStages) * kRawBytes;
+    if (u > 0) {  // tile u + 1 goes into the stage tile u - 1 has released
+      if (u + 1 < ntiles)
+        issue_tile(raw + ((u + 1) % kRawStages) * kRawBytes, (u + 1) * kTile, ecount, ctl.slot,
+                   codes, scales);
+      cp_async_commit();
     }
-    if (t + kRawStages < ntiles)
-      issue_tile(stage, (t + kRawStages) * kTile, ecount, ctl.slot, codes, scales);
-    cp_async_commit();
+    cp_async_wait<1>();  // every group but the newest has landed: tile u is staged
+    const uint32_t par = (uint32_t)((u - 1) & 1);
+    if (tid == 0 && u > 0) (void)mbar_wait(&ctl.abort, &ctl.bar_pv[0], par, st);
+    __syncthreads();
+    if (ctl.abort) return false;
+    for (int j = 0; j < kPairs; ++j) {
+      dequant_pair(stage, Cs, j, u * kTile, ecount, ctl.slot, warp, lane);
+      fence_proxy_async_smem();
+      if (tid == 0 && u > 0 && j + 1 < kPairs)
+        (void)mbar_wait(&ctl.abort, &ctl.bar_pv[j + 1], par, st);
+      __syncthreads();
+      if (ctl.abort) return false;
+      if (tid == 0) {
+        tc_fence_after();
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int kc = 2 * j + c2;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_f16(tmem, umma_desc_sw128(cs_addr + kc * kChunkBytes, 16, 1024) + 2 * kk,
+                     umma_desc_sw128(qs_addr + kc * kQChunk, 16, 1024) + 2 * kk, idesc_s,
+                     (kc | kk) != 0 ? 1u : 0u);
+        }
+      }
+    }
+    if (tid == 0) umma_commit(&ctl.bar_s);
+    return true;
+  };
+
+  bool ok = ntiles == 0 || build_tile(0);
+  for (int t = 0; ok && t < ntiles; ++t) {
+    // ---- wait for S^T of tile t ----
     if (tid == 0) (void)mbar_wait(&ctl.abort, &ctl.bar_s, (uint32_t)(t & 1), st);
     __syncthreads();
     if (ctl.abort) break;
@@ -365,16 +407,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const float mu = m_used[h];
       float mn = mu;
       if (mu == -INFINITY || mt > mu + kRescaleGap) mn = fmaxf(mu, mt);
-      alpha[h] = (mn == mu) ? 1.0f : exp2f(mu - mn);
-      moved |= (mn != mu);
+      alpha[h] = 1.0f;
+      if (mn != mu) {  // uniform: every thread holds the same reference maxima
+        alpha[h] = ex2(mu - mn);
+        moved = true;
+      }
       m_used[h] = mn;
     }
     const int tk = tt & 63, pu = tk >> 3;
     unsigned char* prow = Ps + (tt >> 6) * kQChunk;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float mh = hg ? m_used[8 + i] : m_used[i];
-      const __half ph = __float2half_rn(s[i] == -INFINITY ? 0.0f : exp2f(s[i] - mh));
+      float mh = hg ? m_used[8 + i] : m_used[i];
+      if (mh == -INFINITY) mh = 0.0f;  // no valid entry yet: every s is -inf as well
+      const __half ph = __float2half_rn(ex2(s[i] - mh));  // 2^-inf = 0 for skipped entries
       *reinterpret_cast<__half*>(prow + (8 * hg + i) * 128 + ((pu ^ i) << 4) + (tk & 7) * 2) = ph;
       v[i] = __half2float(ph);
     }
@@ -397,23 +443,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       l_run[h] = l_run[h] * alpha[h] + ((r.x + r.y) + (r.z + r.w));
     }
 
-    // ---- O^T += C^T . P^T, one 128-channel block at a time ----
+    // ---- O^T += C^T . P^T, one 128-channel block at a time, one barrier per block ----
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
-      for (int j = 0; j < kDkv / 128; ++j)
+      for (int j = 0; j < kPairs; ++j) {
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           umma_f16(tmem + kOCol + 16 * j,
                    umma_desc_sw128(cs_addr + 2 * j * kChunkBytes + kk * 2048, kChunkBytes, 1024),
                    umma_desc_sw128(ps_addr + (kk >> 2) * kQChunk, 16, 1024) + 2 * (kk & 3),
                    idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
-      umma_commit(&ctl.bar_pv);
+        umma_commit(&ctl.bar_pv[j]);
+      }
     }
+    if (t + 1 < ntiles) ok = build_tile(t + 1);
   }
   cp_async_wait<0>();
   if (tid == 0) {
-    if (ntiles > 0 && !ctl.abort) (void)mbar_wait(&ctl.abort, &ctl.bar_pv, (uint32_t)((ntiles - 1) & 1), st);
+    if (ntiles > 0 && !ctl.abort)
+      (void)mbar_wait(&ctl.abort, &ctl.bar_pv[kPairs - 1], (uint32_t)((ntiles - 1) & 1), st);
     // every MMA this thread issued has completed before TMEM is read or released
     umma_commit(&ctl.bar_fin);
     (void)mbar_drain(&ctl.bar_fin, 0, 1u << 20);
