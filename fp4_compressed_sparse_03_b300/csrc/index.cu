@@ -17,7 +17,7 @@
 //                        by tensor-core MMAs (1-4 draft queries of a sequence at once)
 //   score_gather_kernel  REINDEX: pool rows gathered by per-lane cp.async rings, scored
 //                        by the same MMAs
-//   select_kernel        8-CTA cluster per query: four 8-bit radix passes with per-warp
+//   select_kernel        1-8-CTA cluster per query: four 8-bit radix passes with per-warp
 //                        histograms merged through distributed shared memory, then an
 //                        ordered compaction with warp scans
 #include <cooperative_groups.h>
@@ -516,20 +516,20 @@ __global__ void __launch_bounds__(kTmaThreads, kScoreCtasPerSm)
 
 // ------------------------------------------------------------------ selection -----
 
-constexpr int kSelCluster = 8;
+constexpr int kSelMaxCluster = 8;  // CTAs per query: 1, 2, 4 or 8, chosen per launch
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelCacheKeys = 16384;  // per-CTA keys kept in shared memory (64 KB)
 constexpr int kDigit = 256;
 constexpr int kSamplesPerCta = 256;
-constexpr int kSamples = kSelCluster * kSamplesPerCta;  // 2048 samples per query
+constexpr int kMaxSamples = kSelMaxCluster * kSamplesPerCta;  // up to 2048 samples per query
 constexpr int kCandCap = 256;                           // kept positions per warp per target
 
 struct SelShared {
   union {
     uint32_t whist[kSelWarps][2][kDigit];  // per-warp histograms (full-sweep path)
     struct {
-      uint32_t samp[kSamples];              // the cluster's samples
+      uint32_t samp[kMaxSamples];           // the cluster's samples
       uint32_t mysamp[kSamplesPerCta];      // this CTA's samples (read by the cluster)
       uint32_t samp2[2048];                 // histogram of the samples' top 11 bits
       uint16_t cand[2][kSelWarps][kCandCap];  // kept positions per target, per warp
@@ -610,24 +610,25 @@ __device__ __forceinline__ int digit_shift(int pass) {
 }
 __device__ __forceinline__ int digit_width(int pass) { return pass == 3 ? 7 : 8; }
 
-// Top-k selection for one query per 8-CTA cluster (gridDim.y = num_q).  Target t = 0 is
+// Top-k selection for one query per C-CTA cluster (gridDim.y = num_q).  Target t = 0 is
 // the top-K output, t = 1 the candidate pool (FULL with a pool output only).
 //
 // Fast path: every CTA takes 256 evenly spaced samples of its range; from the
-// cluster's 2048 samples each target gets a threshold tau_t: the lower edge of the
+// cluster's 256 C samples each target gets a threshold tau_t: the lower edge of the
 // 1/8-octave bin holding the r-th largest sample, r = 1.25 e + 4 sqrt(e) + 8, where
-// e = want * 2048 / n samples are expected above the answer.  One ordered sweep keeps the positions of keys >= tau_t; if the kept
+// e = want * 256 C / n samples are expected above the answer.  One ordered sweep keeps the positions of keys >= tau_t; if the kept
 // keys number at least want_t (and no warp overflowed its buffer) they contain every
 // key of the answer, ties included, so the exact radix select and the ordered output
 // run over the kept keys only.  Otherwise the cluster falls back to radix passes over
 // the whole range.  Either way the result is exact.
-template <bool kReindex>
-__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads, 2)
+template <bool kReindex, int C>
+__global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kSelThreads, 2)
     select_kernel(const uint32_t* __restrict__ ws, int64_t ws_stride,
                   const int32_t* __restrict__ q_seq, const int32_t* __restrict__ seq_lens,
                   int32_t num_seqs, const int32_t* __restrict__ pool_in, int32_t pool_size,
                   int32_t topk, int32_t* __restrict__ out_idx, int32_t* __restrict__ pool_out,
                   int32_t max_ctx, int32_t* st) {
+  constexpr int kS = C * kSamplesPerCta;  // samples per query
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
   uint32_t* cache = reinterpret_cast<uint32_t*>(smem_raw + kSelCacheOff);  // 16-B vector reads
@@ -648,7 +649,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
 
   // This CTA's range of candidate positions, cut into 16 contiguous warp segments
   // (multiples of 128) so that outputs keep index order with warp scans.
-  int L = (n + kSelCluster - 1) / kSelCluster;
+  int L = (n + C - 1) / C;
   L = (L + 127) & ~127;
   const int lo = min(n, rank * L), hi = min(n, lo + L);
   const int len = hi - lo;
@@ -690,7 +691,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
     }
     cluster.sync();
     uint32_t nz = 0;
-    for (int i = tid; i < kSamples; i += kSelThreads) {
+    for (int i = tid; i < kS; i += kSelThreads) {
       const uint32_t v = *cluster.map_shared_rank(&sh.u.f.mysamp[i % kSamplesPerCta], i / kSamplesPerCta);
       sh.u.f.samp[i] = v;
       nz += v != 0;
@@ -704,8 +705,8 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
     // rank of the threshold among the non-zero samples, per target
     uint32_t r0 = 0, r1 = 0;
     {
-      const double e0 = (double)want_max0 * kSamples / (double)max(n, 1);
-      const double e1 = (double)want_max1 * kSamples / (double)max(n, 1);
+      const double e0 = (double)want_max0 * kS / (double)max(n, 1);
+      const double e1 = (double)want_max1 * kS / (double)max(n, 1);
       r0 = (uint32_t)ceil(1.25 * e0 + 4.0 * sqrt(e0) + 8.0);
       r1 = two ? (uint32_t)ceil(1.25 * e1 + 4.0 * sqrt(e1) + 8.0) : 0u;
       r0 = min(r0, n_s);
@@ -715,7 +716,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
     // which the count of samples from the top reaches r_t; at least r_t samples are >= it
     for (int i = tid; i < 2048; i += kSelThreads) sh.u.f.samp2[i] = 0;
     __syncthreads();
-    for (int i = tid; i < kSamples; i += kSelThreads) {
+    for (int i = tid; i < kS; i += kSelThreads) {
       const uint32_t k = sh.u.f.samp[i];
       if (k != 0) atomicAdd(&sh.u.f.samp2[k >> 20], 1u);
     }
@@ -816,7 +817,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
     cluster.sync();
     uint32_t nvalid = 0, ct0 = 0, ct1 = 0, ovf = 0;
 #pragma unroll
-    for (int r = 0; r < kSelCluster; ++r) {
+    for (int r = 0; r < C; ++r) {
       nvalid += *cluster.map_shared_rank(&sh.cvalid, r);
       ct0 += *cluster.map_shared_rank(&sh.ccand[0], r);
       ct1 += *cluster.map_shared_rank(&sh.ccand[1], r);
@@ -851,12 +852,12 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
       cluster.sync();
       uint32_t v = 0;
       {
-        uint32_t part[kSelCluster];
+        uint32_t part[C];
 #pragma unroll
-        for (int r = 0; r < kSelCluster; ++r)
+        for (int r = 0; r < C; ++r)
           part[r] = *cluster.map_shared_rank(&sh.chist[buf][tid / kDigit][tid % kDigit], r);
 #pragma unroll
-        for (int r = 0; r < kSelCluster; ++r) v += part[r];
+        for (int r = 0; r < C; ++r) v += part[r];
       }
       find_bins(sh, v, width, want0, want1, pre0, pre1, abv0, abv1);
     }
@@ -929,7 +930,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
       if (pass == 0) {
         uint32_t nvalid = 0;
 #pragma unroll
-        for (int r = 0; r < kSelCluster; ++r) nvalid += *cluster.map_shared_rank(&sh.cvalid, r);
+        for (int r = 0; r < C; ++r) nvalid += *cluster.map_shared_rank(&sh.cvalid, r);
         want0 = min(want_max0, nvalid);
         want1 = min(want_max1, nvalid);
       }
@@ -937,11 +938,11 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
       const int tsrc = pass == 0 ? 0 : t;
       uint32_t v = 0;
       if (bin <= (int)dmask) {
-        uint32_t part[kSelCluster];
+        uint32_t part[C];
 #pragma unroll
-        for (int r = 0; r < kSelCluster; ++r) part[r] = *cluster.map_shared_rank(&sh.chist[buf][tsrc][bin], r);
+        for (int r = 0; r < C; ++r) part[r] = *cluster.map_shared_rank(&sh.chist[buf][tsrc][bin], r);
 #pragma unroll
-        for (int r = 0; r < kSelCluster; ++r) v += part[r];
+        for (int r = 0; r < C; ++r) v += part[r];
       }
       find_bins(sh, v, width, want0, want1, pre0, pre1, abv0, abv1);
     }
@@ -1132,29 +1133,59 @@ cudaError_t launch_score_reindex(const uint16_t* q_idx, const uint16_t* keys, co
   return cudaGetLastError();
 }
 
+// CTAs per query: enough kept-key capacity (4096 per CTA and target) for twice the
+// larger output, and enough CTAs that each one's keys fit its shared-memory cache.
+// Measured on the 64 x 131072 decode batch: 8 cached CTAs per query in two waves beat 4
+// uncached ones in one wave (Full), and one CTA per query is fastest for the 8192-entry
+// Reindex pools.
+int select_cluster(int32_t n, int32_t want_max) {
+  int c = 1;  // kept positions are 16-bit: at most 65535 keys per CTA on the fast path
+  while (c < kSelMaxCluster && ((int64_t)c * kSelWarps * kCandCap < 2LL * want_max ||
+                                (int64_t)c * kSelCacheKeys < n))
+    c *= 2;
+  return c;
+}
+
+template <bool R, int C>
+cudaError_t launch_select_c(const uint32_t* ws, int64_t ws_stride, const int32_t* q_seq,
+                            const csa2_pages& pg, int32_t num_q, const int32_t* pool_in,
+                            int32_t pool_size, int32_t topk, int32_t* out_idx, int32_t* pool_out,
+                            int32_t* st, cudaStream_t s) {
+  const size_t smem = select_smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(select_kernel<R, C>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  select_kernel<R, C><<<dim3(C, num_q), kSelThreads, smem, s>>>(
+      ws, ws_stride, q_seq, pg.seq_lens, pg.num_seqs, pool_in, pool_size, topk, out_idx, pool_out,
+      pg.max_pages_per_seq * kPage, st);
+  return cudaGetLastError();
+}
+
+template <bool R>
+cudaError_t launch_select_r(int c, const uint32_t* ws, int64_t ws_stride, const int32_t* q_seq,
+                            const csa2_pages& pg, int32_t num_q, const int32_t* pool_in,
+                            int32_t pool_size, int32_t topk, int32_t* out_idx, int32_t* pool_out,
+                            int32_t* st, cudaStream_t s) {
+  switch (c) {
+    case 1: return launch_select_c<R, 1>(ws, ws_stride, q_seq, pg, num_q, pool_in, pool_size, topk, out_idx, pool_out, st, s);
+    case 2: return launch_select_c<R, 2>(ws, ws_stride, q_seq, pg, num_q, pool_in, pool_size, topk, out_idx, pool_out, st, s);
+    case 4: return launch_select_c<R, 4>(ws, ws_stride, q_seq, pg, num_q, pool_in, pool_size, topk, out_idx, pool_out, st, s);
+    default: return launch_select_c<R, 8>(ws, ws_stride, q_seq, pg, num_q, pool_in, pool_size, topk, out_idx, pool_out, st, s);
+  }
+}
+
 cudaError_t launch_select(bool reindex, const uint32_t* ws, int64_t ws_stride, const int32_t* q_seq,
                           const csa2_pages& pg, int32_t num_q, const int32_t* pool_in,
                           int32_t pool_size, int32_t topk, int32_t* out_idx, int32_t* pool_out,
                           int32_t* st, cudaStream_t s) {
-  const size_t smem = select_smem_bytes();
-  const int32_t max_ctx = pg.max_pages_per_seq * kPage;
-  dim3 grid(kSelCluster, num_q);
-  if (reindex) {
-    cudaError_t e = cudaFuncSetAttribute(select_kernel<true>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    select_kernel<true><<<grid, kSelThreads, smem, s>>>(ws, ws_stride, q_seq, pg.seq_lens,
-                                                        pg.num_seqs, pool_in, pool_size, topk,
-                                                        out_idx, nullptr, max_ctx, st);
-  } else {
-    cudaError_t e = cudaFuncSetAttribute(select_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    select_kernel<false><<<grid, kSelThreads, smem, s>>>(ws, ws_stride, q_seq, pg.seq_lens,
-                                                         pg.num_seqs, nullptr, pool_size, topk,
-                                                         out_idx, pool_out, max_ctx, st);
-  }
-  return cudaGetLastError();
+  const int32_t n = reindex ? pool_size : pg.max_pages_per_seq * kPage;
+  const int32_t want_max = std::max(topk, (!reindex && pool_out) ? pool_size : 0);
+  const int c = select_cluster(n, want_max);
+  if (reindex)
+    return launch_select_r<true>(c, ws, ws_stride, q_seq, pg, num_q, pool_in, pool_size, topk,
+                                 out_idx, nullptr, st, s);
+  return launch_select_r<false>(c, ws, ws_stride, q_seq, pg, num_q, nullptr, pool_size, topk,
+                                out_idx, pool_out, st, s);
 }
 
 }  // namespace csa2
