@@ -30,8 +30,9 @@ namespace csa2 {
 
 // ------------------------------------------------------------------ scoring -------
 
-constexpr int kScoreThreads = 256;     // 8 warps
+constexpr int kScoreThreads = 128;     // Reindex scorer: 4 warps per CTA
 constexpr int kScoreWarps = kScoreThreads / 32;
+constexpr int kGatherCtasPerSm = 3;    // three such CTAs per SM
 
 struct ScoreGeom {
   const int32_t* seq_lens;
@@ -188,7 +189,7 @@ __device__ __forceinline__ void cursor_advance(RunCursor& cu, const RunList& rl,
 // N = 8 columns holding the query's 4 heads, K = 128 dims in the shared permuted order).
 constexpr int kGatherRing = 4;                       // 16-row groups staged per warp
 constexpr int kGatherGroup = 16 * kKeyRow;           // 4 KB
-constexpr int kGatherSmem = kScoreWarps * kGatherRing * kGatherGroup;  // 128 KB
+constexpr int kGatherSmem = kScoreWarps * kGatherRing * kGatherGroup;  // 64 KB
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -198,7 +199,7 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__global__ void __launch_bounds__(kScoreThreads, 1)
+__global__ void __launch_bounds__(kScoreThreads, kGatherCtasPerSm)
     score_gather_kernel(const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ keys,
                         const int32_t* __restrict__ q_seq, int32_t num_q, ScoreGeom g,
                         const int32_t* __restrict__ pool, int32_t pool_size,
@@ -1127,7 +1128,7 @@ cudaError_t launch_score_reindex(const uint16_t* q_idx, const uint16_t* keys, co
   e = cudaFuncSetAttribute(score_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kGatherSmem);
   if (e != cudaSuccess) return e;
-  const int grid = std::max(1, num_sms);
+  const int grid = std::max(1, kGatherCtasPerSm * num_sms);
   score_gather_kernel<<<grid, kScoreThreads, kGatherSmem, s>>>(q_idx, keys, q_seq, num_q, g, pool,
                                                               pool_size, ws, rl, st);
   return cudaGetLastError();
