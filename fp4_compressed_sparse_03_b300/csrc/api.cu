@@ -19,7 +19,7 @@ cudaError_t launch_score_reindex(const uint16_t*, const uint16_t*, const int32_t
 size_t runlist_bytes(int32_t num_q);
 cudaError_t launch_select(bool, const uint32_t*, int64_t, const int32_t*, const csa2_pages&,
                           int32_t, const int32_t*, int32_t, int32_t, int32_t*, int32_t*, int32_t*,
-                          cudaStream_t);
+                          cudaStream_t, int);
 cudaError_t launch_attn(const uint16_t*, const uint8_t*, const uint8_t*, const int32_t*,
                         const csa2_pages&, float*, float*, int32_t, const int32_t*, int32_t, float,
                         void*, int32_t*, cudaStream_t, int);
@@ -150,7 +150,7 @@ csa2_status csa2_index(csa2_mode mode, const uint16_t* q_idx, const uint16_t* k_
                           stride, rl, args->dev_status, stream, sms);
     if (e != cudaSuccess) return from_cuda(e);
     e = launch_select(false, ws, stride, args->q_seq, *pages, args->num_q, nullptr,
-                      pool ? P : 0, topk, out_idx, pool, args->dev_status, stream);
+                      pool ? P : 0, topk, out_idx, pool, args->dev_status, stream, sms);
     return from_cuda(e);
   }
   // REINDEX
@@ -161,7 +161,7 @@ csa2_status csa2_index(csa2_mode mode, const uint16_t* q_idx, const uint16_t* k_
                            args->dev_status, stream, sms);
   if (e != cudaSuccess) return from_cuda(e);
   e = launch_select(true, ws, P, args->q_seq, *pages, args->num_q, pool, P, topk, out_idx, nullptr,
-                    args->dev_status, stream);
+                    args->dev_status, stream, sms);
   return from_cuda(e);
 }
 

@@ -1072,6 +1072,357 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kSelThreads, 2)
   cluster.sync();  // no CTA leaves while others may still read its shared memory
 }
 
+// ------------------------------------------------------------ single-CTA selection --
+// FULL selection with one 1024-thread CTA per query (no cluster synchronisation):
+//   1. exact histogram of the top 11 key bits (8 exponent + 3 mantissa bits) over the
+//      query's keys, straight from L2;
+//   2. per target t (top-K, pool), the boundary bin B_t in which the count from the
+//      top first reaches want_t; every key of the answer has bin >= B_t;
+//   3. one ordered sweep keeps (position, key) of the keys with bin >= min B_t in
+//      per-warp lists (the warps own consecutive position segments);
+//   4. three radix passes over the kept keys of bin B_t fix the exact boundary key T_t;
+//   5. ordered emit: keys > T_t, then ties of T_t by lowest position up to the quota.
+// If a warp's list overflows (many keys in the boundary bins), the CTA falls back to
+// radix passes over the whole range; the result is the same.  The two sweeps over L2
+// keep eight 16-byte loads per lane in flight.
+constexpr int kBigThreads = 1024;
+constexpr int kBigWarps = kBigThreads / 32;
+constexpr int kBigCap = 512;    // kept keys per warp
+constexpr int kHistBins = 2048;
+constexpr int kBigBatch = 8;    // 16-byte loads in flight per lane in the sweeps
+
+struct BigShared {
+  uint32_t hist[kHistBins];
+  uint32_t wsel[2][kBigWarps];  // per-warp keys > T_t
+  uint32_t wtie[2][kBigWarps];  // per-warp keys == T_t
+  uint32_t wcnt[kBigWarps];     // per-warp kept keys
+  uint32_t rh[2][256];
+  uint32_t scan[2][kBigThreads / 32];
+  uint32_t res[2][2];           // per target: (bin, keys above it)
+  uint32_t nvalid;
+  uint32_t overflow;
+  union {
+    struct {
+      uint32_t pos[kBigWarps][kBigCap];
+      uint32_t key[kBigWarps][kBigCap];
+    } c;
+    uint32_t whist[kBigWarps][256];
+  } u;
+};
+
+// Block-wide: thread tid holds v = count of bin (tid % nb) for target tid / nb (two
+// targets, nb bins each, 2 nb <= 1024 threads).  For each target with want_t > 0, find
+// the bin where (abv_t + keys in strictly higher bins) < want_t <= ... + v, and return
+// it in res[t][0] (res[t][1] = keys above it, abv_t included).
+__device__ __forceinline__ void big_find(BigShared& sh, uint32_t v, int nb, uint32_t want0,
+                                         uint32_t want1, uint32_t abv0, uint32_t abv1) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int t = tid / nb, bin = tid % nb, tw = bin >> 5;
+  uint32_t x = (t < 2) ? v : 0u;  // inclusive suffix sum within the warp (bins descending)
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_down_sync(0xffffffffu, x, o);
+    if (lane + o < 32) x += y;
+  }
+  if (t < 2 && lane == 0) sh.scan[t][tw] = x;
+  __syncthreads();
+  if (t < 2) {
+    const uint32_t want_t = t == 0 ? want0 : want1;
+    if (want_t > 0) {
+      uint32_t later = 0;
+      for (int w = tw + 1; w < nb / 32; ++w) later += sh.scan[t][w];
+      const uint32_t above_bin = (t == 0 ? abv0 : abv1) + later + x - v;
+      if (above_bin < want_t && above_bin + v >= want_t) {
+        sh.res[t][0] = (uint32_t)bin;
+        sh.res[t][1] = above_bin;
+      }
+    }
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kBigThreads, 1)
+    select_cta_kernel(const uint32_t* __restrict__ ws, int64_t ws_stride,
+                      const int32_t* __restrict__ q_seq, const int32_t* __restrict__ seq_lens,
+                      int32_t num_seqs, int32_t pool_size, int32_t topk,
+                      int32_t* __restrict__ out_idx, int32_t* __restrict__ pool_out,
+                      int32_t max_ctx) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  BigShared& sh = *reinterpret_cast<BigShared*>(smem_raw);
+  const int q = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = __ldg(q_seq + q);
+  const int n = (b >= 0 && b < num_seqs) ? min(max(0, __ldg(seq_lens + b)), max_ctx) : 0;
+  const bool two = pool_out != nullptr && pool_size > 0;
+  const uint32_t* src = ws + (int64_t)q * ws_stride;
+  int32_t* out0 = out_idx + (int64_t)q * topk;
+  int32_t* out1 = two ? pool_out + (int64_t)q * pool_size : nullptr;
+
+  // position segment of this warp: multiples of 128, in position order across warps
+  int S = (n + kBigWarps - 1) / kBigWarps;
+  S = (S + 127) & ~127;
+  const int seg_lo = min(n, warp * S), seg_hi = min(n, seg_lo + S);
+  auto load4 = [&](int i, uint32_t (&k)[4]) {
+    if (i + 4 <= seg_hi) {
+      const uint4 v = __ldcg(reinterpret_cast<const uint4*>(src + i));
+      k[0] = v.x; k[1] = v.y; k[2] = v.z; k[3] = v.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) k[e] = (i + e < seg_hi) ? __ldcg(src + i + e) : 0u;
+    }
+  };
+
+  // ---- 1. histogram of the top 11 bits, valid-key count ----
+  for (int i = tid; i < kHistBins; i += kBigThreads) sh.hist[i] = 0;
+  if (tid == 0) {
+    sh.nvalid = 0;
+    sh.overflow = 0;
+  }
+  __syncthreads();
+  uint32_t nv = 0;
+  for (int i0 = seg_lo; i0 < seg_hi; i0 += 128 * kBigBatch) {
+    uint32_t k[kBigBatch][4];
+#pragma unroll
+    for (int bb = 0; bb < kBigBatch; ++bb) load4(i0 + 128 * bb + 4 * lane, k[bb]);
+#pragma unroll
+    for (int bb = 0; bb < kBigBatch; ++bb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (k[bb][e] != 0) {
+          ++nv;
+          atomicAdd(&sh.hist[min(k[bb][e] >> 20, (uint32_t)kHistBins - 1)], 1u);  // finite: < 2041
+        }
+  }
+  nv = __reduce_add_sync(0xffffffffu, nv);
+  if (lane == 0) atomicAdd(&sh.nvalid, nv);
+  __syncthreads();
+  const uint32_t nvalid = sh.nvalid;
+  const uint32_t want0 = min((uint32_t)topk, nvalid);
+  const uint32_t want1 = two ? min((uint32_t)pool_size, nvalid) : 0u;
+
+  // ---- 2. boundary bins (two bins per thread: 2 tid + 1 is the higher one) ----
+  uint32_t B0 = 0, B1 = 0, A0 = 0, A1 = 0;  // boundary bins and keys in higher bins
+  {
+    const uint32_t hi = sh.hist[2 * tid + 1], lo = sh.hist[2 * tid];
+    uint32_t x = hi + lo;  // inclusive suffix sum of pair counts within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_down_sync(0xffffffffu, x, o);
+      if (lane + o < 32) x += y;
+    }
+    if (lane == 0) sh.scan[0][warp] = x;
+    if (tid < 4) sh.res[tid >> 1][tid & 1] = 0;
+    __syncthreads();
+    uint32_t later = 0;
+    for (int w = warp + 1; w < kBigWarps; ++w) later += sh.scan[0][w];
+    const uint32_t above_hi = later + x - (hi + lo), above_lo = above_hi + hi;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const uint32_t want_t = t == 0 ? want0 : want1;
+      if (want_t == 0) continue;
+      if (above_hi < want_t && above_hi + hi >= want_t) {
+        sh.res[t][0] = 2 * tid + 1;
+        sh.res[t][1] = above_hi;
+      } else if (above_lo < want_t && above_lo + lo >= want_t) {
+        sh.res[t][0] = 2 * tid;
+        sh.res[t][1] = above_lo;
+      }
+    }
+    __syncthreads();
+    B0 = sh.res[0][0];
+    A0 = sh.res[0][1];
+    B1 = sh.res[1][0];
+    A1 = sh.res[1][1];
+    __syncthreads();
+  }
+  uint32_t bmin = want0 > 0 ? B0 : 0xFFFFFFFFu;
+  if (want1 > 0) bmin = min(bmin, B1);
+
+  // ---- 3. ordered sweep: keep keys with bin >= bmin ----
+  uint32_t cnt = 0;
+  if (want0 > 0) {
+    for (int i0 = seg_lo; i0 < seg_hi; i0 += 128 * kBigBatch) {
+      uint32_t k[kBigBatch][4];
+#pragma unroll
+      for (int bb = 0; bb < kBigBatch; ++bb) load4(i0 + 128 * bb + 4 * lane, k[bb]);
+#pragma unroll
+      for (int bb = 0; bb < kBigBatch; ++bb) {
+        const int i = i0 + 128 * bb + 4 * lane;
+        uint32_t m = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (k[bb][e] != 0 && (k[bb][e] >> 20) >= bmin) m |= 1u << e;
+        uint32_t tot;
+        uint32_t p = cnt + warp_excl(__popc(m), tot);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (m & (1u << e)) {
+            if (p < kBigCap) {
+              sh.u.c.pos[warp][p] = (uint32_t)(i + e);
+              sh.u.c.key[warp][p] = k[bb][e];
+            }
+            ++p;
+          }
+        cnt += tot;
+      }
+    }
+    if (lane == 0) {
+      sh.wcnt[warp] = cnt;
+      if (cnt > (uint32_t)kBigCap) atomicOr(&sh.overflow, 1u);
+    }
+  }
+  __syncthreads();
+  const bool kept = sh.overflow == 0;
+
+  // ---- 4. exact boundary keys T_t ----
+  uint32_t T0 = 0, T1 = 0, Q0 = 0, Q1 = 0;  // boundary key and ties to take
+  if (want0 > 0) {
+    uint32_t pre[2] = {B0, B1}, abv[2] = {A0, A1};
+    const uint32_t want[2] = {want0, want1};
+    // kept: digits of bits 19..12, 11..4, 3..0 within the boundary bin;
+    // full range: digits of bits 30..23, 22..15, 14..7, 6..0
+    const int passes = kept ? 3 : 4;
+    for (int pass = 0; pass < passes; ++pass) {
+      const int shift = kept ? (pass == 0 ? 12 : pass == 1 ? 4 : 0) : (pass == 0 ? 23 : pass == 1 ? 15 : pass == 2 ? 7 : 0);
+      const int width = kept ? (pass == 2 ? 4 : 8) : (pass == 3 ? 7 : 8);
+      const uint32_t dmask = (1u << width) - 1u;
+      if (!kept && pass == 0) {
+        pre[0] = pre[1] = 0;
+        abv[0] = abv[1] = 0;
+      }
+      for (int i = tid; i < 2 * 256; i += kBigThreads) sh.rh[i >> 8][i & 255] = 0;
+      __syncthreads();
+      if (kept) {
+        for (uint32_t j = lane; j < cnt; j += 32) {
+          const uint32_t k = sh.u.c.key[warp][j];
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            if (want[t] > 0 && (k >> (shift + width)) == pre[t])
+              atomicAdd(&sh.rh[t][(k >> shift) & dmask], 1u);
+        }
+      } else {
+        for (int i = seg_lo + 4 * lane; i < seg_hi; i += 128) {
+          uint32_t k[4];
+          load4(i, k);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (k[e] == 0) continue;
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+              if (want[t] > 0 && (pass == 0 || (k[e] >> (shift + width)) == pre[t]))
+                atomicAdd(&sh.rh[t][(k[e] >> shift) & dmask], 1u);
+          }
+        }
+      }
+      __syncthreads();
+      const uint32_t v = tid < 512 ? sh.rh[tid >> 8][tid & 255] : 0u;
+      big_find(sh, v, 256, want[0], want[1], abv[0], abv[1]);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if (want[t] > 0) {
+          pre[t] = (pre[t] << width) | sh.res[t][0];
+          abv[t] = sh.res[t][1];
+        }
+      __syncthreads();
+    }
+    T0 = pre[0];
+    Q0 = want0 - abv[0];
+    T1 = pre[1];
+    Q1 = want1 - abv[1];
+  }
+
+  // ---- 5. ordered emit ----
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const uint32_t want_t = t == 0 ? want0 : want1;
+    if (want_t == 0) continue;
+    const uint32_t T = t == 0 ? T0 : T1, quota = t == 0 ? Q0 : Q1;
+    int32_t* outp = t == 0 ? out0 : out1;
+    // per-warp counts of keys > T and == T
+    uint32_t gt = 0, eq = 0;
+    if (kept) {
+      for (uint32_t j = lane; j < cnt; j += 32) {
+        const uint32_t k = sh.u.c.key[warp][j];
+        gt += k > T;
+        eq += k == T;
+      }
+    } else {
+      for (int i = seg_lo + 4 * lane; i < seg_hi; i += 128) {
+        uint32_t k[4];
+        load4(i, k);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          gt += k[e] > T;
+          eq += k[e] == T;
+        }
+      }
+    }
+    gt = __reduce_add_sync(0xffffffffu, gt);
+    eq = __reduce_add_sync(0xffffffffu, eq);
+    if (lane == 0) {
+      sh.wsel[t][warp] = gt;
+      sh.wtie[t][warp] = eq;
+    }
+    __syncthreads();
+    uint32_t base = 0, ties_before = 0;
+    for (int w = 0; w < warp; ++w) {
+      const uint32_t e_w = sh.wtie[t][w];
+      base += sh.wsel[t][w] + (quota > ties_before ? min(quota - ties_before, e_w) : 0u);
+      ties_before += e_w;
+    }
+    const uint32_t take = quota > ties_before ? min(quota - ties_before, sh.wtie[t][warp]) : 0u;
+    uint32_t tie_run = 0, sel_run = 0;
+    auto emit = [&](const uint32_t* k, const uint32_t* pos, int nk) {
+      uint32_t nt = 0;
+      for (int e = 0; e < nk; ++e) nt += k[e] == T;
+      uint32_t ttot;
+      uint32_t tr = tie_run + warp_excl(nt, ttot);
+      uint32_t selm = 0, ns = 0;
+      for (int e = 0; e < nk; ++e) {
+        const bool tie = k[e] == T;
+        if (k[e] > T || (tie && tr < take)) {
+          selm |= 1u << e;
+          ++ns;
+        }
+        tr += tie;
+      }
+      uint32_t stot;
+      uint32_t p = base + sel_run + warp_excl(ns, stot);
+      for (int e = 0; e < nk; ++e)
+        if (selm & (1u << e)) {
+          if (p < want_t) outp[p] = (int32_t)pos[e];
+          ++p;
+        }
+      tie_run += ttot;
+      sel_run += stot;
+    };
+    if (kept) {
+      for (uint32_t j0 = 0; j0 < cnt; j0 += 32) {
+        const uint32_t j = j0 + lane;
+        uint32_t k[1] = {0u}, pos[1] = {0u};
+        if (j < cnt) {
+          k[0] = sh.u.c.key[warp][j];
+          pos[0] = sh.u.c.pos[warp][j];
+        }
+        emit(k, pos, 1);
+      }
+    } else {
+      for (int i0 = seg_lo; i0 < seg_hi; i0 += 128) {
+        const int i = i0 + 4 * lane;
+        uint32_t k[4];
+        load4(i, k);
+        const uint32_t pos[4] = {(uint32_t)i, (uint32_t)i + 1, (uint32_t)i + 2, (uint32_t)i + 3};
+        emit(k, pos, 4);
+      }
+    }
+    __syncthreads();
+  }
+  // -1 padding after the selected entries
+  for (int i = (int)want0 + tid; i < topk; i += kBigThreads) out0[i] = -1;
+  if (two)
+    for (int i = (int)want1 + tid; i < pool_size; i += kBigThreads) out1[i] = -1;
+}
+
 // ------------------------------------------------------------------ launchers -----
 
 size_t select_smem_bytes() { return kSelCacheOff + (size_t)kSelCacheKeys * 4; }
@@ -1178,9 +1529,23 @@ cudaError_t launch_select_r(int c, const uint32_t* ws, int64_t ws_stride, const 
 cudaError_t launch_select(bool reindex, const uint32_t* ws, int64_t ws_stride, const int32_t* q_seq,
                           const csa2_pages& pg, int32_t num_q, const int32_t* pool_in,
                           int32_t pool_size, int32_t topk, int32_t* out_idx, int32_t* pool_out,
-                          int32_t* st, cudaStream_t s) {
+                          int32_t* st, cudaStream_t s, int num_sms) {
   const int32_t n = reindex ? pool_size : pg.max_pages_per_seq * kPage;
   const int32_t want_max = std::max(topk, (!reindex && pool_out) ? pool_size : 0);
+  // FULL over contexts up to 2^18 tokens: one CTA per query, no cluster synchronisation
+  // (measured on B300: 64 queries x 131072 keys took ~90 us in two waves of 8-CTA clusters)
+  (void)num_sms;
+  if (!reindex && n <= (1 << 18) && want_max <= 8192) {
+    const size_t smem = sizeof(BigShared);
+    cudaError_t e = cudaFuncSetAttribute(select_cta_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    select_cta_kernel<<<num_q, kBigThreads, smem, s>>>(ws, ws_stride, q_seq, pg.seq_lens,
+                                                       pg.num_seqs, pool_out ? pool_size : 0,
+                                                       topk, out_idx, pool_out,
+                                                       pg.max_pages_per_seq * kPage);
+    return cudaGetLastError();
+  }
   const int c = select_cluster(n, want_max);
   if (reindex)
     return launch_select_r<true>(c, ws, ws_stride, q_seq, pg, num_q, pool_in, pool_size, topk,
