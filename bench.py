@@ -188,12 +188,17 @@ def run_ours(args, world, rank, local):
     if status != csa2.CSA2_OK:
         raise RuntimeError(f"device status {bits:#x} after warm-up")
 
-    # per-call events inside the timed region (on the launching stream)
+    # The step is replayed as a CUDA graph of the same libcsa2 launches, so the device
+    # time is not paced by per-call host work (about 12 calls per step).
+    g_step = step.capture(q_idx, q)
+    g_call = step.capture_calls(q_idx, q)
+    for _ in range(args.warmup):
+        g_step.replay()
+    torch.cuda.synchronize(dev)
+
     K = args.steps
     full_layers = [l for l, m in enumerate(wl.schedule) if m == csa2.CSA2_FULL]
     re_layers = [l for l, m in enumerate(wl.schedule) if m == csa2.CSA2_REINDEX]
-    ev = {(k, l, w): torch.cuda.Event(enable_timing=True)
-          for k in range(K) for l in range(L) for w in ("i0", "i1", "a1")}
     clocks = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize(dev)
@@ -202,14 +207,22 @@ def run_ours(args, world, rank, local):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for k in range(K):
+    for _ in range(K):
+        g_step.replay()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    # per-call times: the per-call graphs with events between them, on the same stream
+    K1 = max(1, min(K, 50))
+    ev = {(k, l, w): torch.cuda.Event(enable_timing=True)
+          for k in range(K1) for l in range(L) for w in ("i0", "i1", "a1")}
+    for k in range(K1):
         for l in range(L):
             ev[(k, l, "i0")].record(stream)
-            step.layer_index(l, q_idx[l])
+            if (l, "index") in g_call:
+                g_call[(l, "index")].replay()
             ev[(k, l, "i1")].record(stream)
-            step.layer_attn(l, q[l])
+            g_call[(l, "attn")].replay()
             ev[(k, l, "a1")].record(stream)
-    t1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     clk = clocks.stop()
@@ -220,7 +233,7 @@ def run_ours(args, world, rank, local):
         raise RuntimeError(f"device status {bits:#x} after timed steps")
 
     def avg(l, a, b):
-        return float(np.mean([ev[(k, l, a)].elapsed_time(ev[(k, l, b)]) for k in range(K)]))
+        return float(np.mean([ev[(k, l, a)].elapsed_time(ev[(k, l, b)]) for k in range(K1)]))
 
     full_ms = float(np.mean([avg(l, "i0", "i1") for l in full_layers]))
     re_ms = float(np.mean([avg(l, "i0", "i1") for l in re_layers])) if re_layers else 0.0
@@ -259,7 +272,7 @@ def run_ours(args, world, rank, local):
         for l in idx_layers:
             q_idx[l].copy_(q_idx_pin[l], non_blocking=True)
         q.copy_(q_pin, non_blocking=True)
-        step.run(q_idx, q)
+        g_step.replay()
         out_pin.copy_(step.out, non_blocking=True)
         lse_pin.copy_(step.lse, non_blocking=True)
     e1.record(stream)
@@ -286,10 +299,12 @@ def run_ours(args, world, rank, local):
                    "pool": wl.pool_size, "topk": wl.topk,
                    "l2": "no flush: every step streams %.2f GB of indexer keys (> 126 MB L2)"
                          % (fb / 1e9),
+                   "launch": "CUDA graph of the step's libcsa2 calls; per-mode times from "
+                             "per-call graphs",
                    "parallelism": f"replicas x{world}"},
         "per_mode_ms": {"full_index": round(full_ms, 4), "reindex": round(re_ms, 4),
                         "attention": round(attn_ms, 4)},
-        "roofline": {"bound": "hbm", "kernel": "csa2_index(FULL) call: group_prefix_kernel + score_pages_kernel + select_kernel<0>",
+        "roofline": {"bound": "hbm", "kernel": "csa2_index(FULL) call: group_prefix_kernel + score_pages_kernel + select_cta_kernel",
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": fb, "traffic": traffic},
@@ -446,14 +461,14 @@ def workload_of(name: str):
 
 
 def count_launches(wl, step) -> int:
-    """Kernels libcsa2 launches per decode step: Full and Reindex index calls launch a
-    scoring and a selection kernel; Reuse none; attention one kernel plus the split
-    combine when the selected set is split."""
+    """Kernels libcsa2 launches per decode step: Full and Reindex index calls launch the
+    run-list kernel, a scoring kernel and a selection kernel; Reuse none; attention one
+    kernel plus the split combine when the selected set is split."""
     import fp4_compressed_sparse_03_b300 as csa2
     n = 0
     for m in wl.schedule:
         if m != csa2.CSA2_REUSE:
-            n += 2
+            n += 3
     ws = csa2.csa2_attn_workspace_size(step.num_q, step.topk)
     n += len(wl.schedule) * (2 if ws > 0 else 1)
     return n

@@ -112,3 +112,29 @@ class DecodeStep:
 
     def indices(self, l: int):
         return self.idx[self.src[l]]
+
+    # ---- CUDA graphs: the same libcsa2 launches, replayed without per-call host work ----
+    # Every libcsa2 call is an ordered launch sequence on the given stream, so a captured
+    # step replays exactly the kernels of an eager step on the same buffers.  Run the step
+    # eagerly once before capturing (first calls set kernel attributes).
+
+    @staticmethod
+    def _capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            fn()
+        return g
+
+    def capture(self, q_idx, q):
+        """Graph of one whole step reading the device buffers q_idx and q."""
+        return self._capture(lambda: self.run(q_idx, q))
+
+    def capture_calls(self, q_idx, q):
+        """Per-call graphs: {(layer, "index")} for index-producing layers and
+        {(layer, "attn")} for every layer."""
+        graphs = {}
+        for l, m in enumerate(self.schedule):
+            if m != CSA2_REUSE:
+                graphs[(l, "index")] = self._capture(lambda l=l: self.layer_index(l, q_idx[l]))
+            graphs[(l, "attn")] = self._capture(lambda l=l: self.layer_attn(l, q[l]))
+        return graphs

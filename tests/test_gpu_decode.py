@@ -188,6 +188,52 @@ def test_small_ragged_all_modes(drafts):
     check_sampled(wl, range(wl.num_q), step, q_idx, q, min_attn=wl.num_q)
 
 
+def test_graph_replay_matches_eager_step():
+    """The CUDA-graph step (what the benchmark times) replays the same launches: its
+    indices, pools, outputs and lse are bit-identical to the eager step's, and a replay
+    after new queries are copied into the captured buffers matches an eager run on them."""
+    lens = np.array([5000, 64, 300, 2113], np.int32)
+    wl = gen.DecodeWorkload("graph", 31, lens, np.array([2, 1, 1, 3], np.int32),
+                            [gen.FULL, gen.REINDEX, gen.REUSE, gen.REUSE], pool_size=512, topk=128)
+    cache, step, q_idx_h, q_h = run_workload(wl)
+    q_idx, q = dev(q_idx_h), dev(q_h)
+    written = sorted(set(step.src))  # layers whose index output the step writes
+
+    def outputs():
+        return [step.idx[l].clone() for l in written] + [step.pool.clone(), step.out.clone(),
+                                                          step.lse.clone()]
+
+    def clobber():
+        for l in written:
+            step.idx[l].fill_(7)
+        for t in (step.pool, step.out, step.lse):
+            t.fill_(7)
+
+    step.run(q_idx, q)
+    torch.cuda.synchronize()
+    ref = outputs()
+    g = step.capture(q_idx, q)
+    clobber()
+    g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(ref, outputs()):
+        assert torch.equal(a, b)
+    # new queries through the captured buffers
+    q_idx.copy_(torch.flip(q_idx, dims=[1]))
+    q.copy_(torch.flip(q, dims=[1]))
+    clobber()
+    g.replay()
+    torch.cuda.synchronize()
+    got = outputs()
+    clobber()
+    step.run(q_idx, q)
+    torch.cuda.synchronize()
+    for a, b in zip(got, outputs()):
+        assert torch.equal(a, b)
+    status, bits = csa2.csa2_read_status(step.dev_status)
+    assert status == csa2.CSA2_OK, bits
+
+
 def test_two_groups_pool_larger_than_context():
     lens = np.array([700, 3000], np.int32)
     wl = gen.DecodeWorkload("groups", 17, lens, np.ones(2, np.int32),
