@@ -1141,20 +1141,29 @@ __device__ __forceinline__ void big_find(BigShared& sh, uint32_t v, int nb, uint
   __syncthreads();
 }
 
+// kReindex: the query's keys are its P pool entries (n = pool_size), the output is the
+// pool entry's token, and no pool is emitted.
+template <bool kReindex>
 __global__ void __launch_bounds__(kBigThreads, 1)
     select_cta_kernel(const uint32_t* __restrict__ ws, int64_t ws_stride,
                       const int32_t* __restrict__ q_seq, const int32_t* __restrict__ seq_lens,
-                      int32_t num_seqs, int32_t pool_size, int32_t topk,
-                      int32_t* __restrict__ out_idx, int32_t* __restrict__ pool_out,
+                      int32_t num_seqs, const int32_t* __restrict__ pool_in, int32_t pool_size,
+                      int32_t topk, int32_t* __restrict__ out_idx, int32_t* __restrict__ pool_out,
                       int32_t max_ctx) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   BigShared& sh = *reinterpret_cast<BigShared*>(smem_raw);
   const int q = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b = __ldg(q_seq + q);
-  const int n = (b >= 0 && b < num_seqs) ? min(max(0, __ldg(seq_lens + b)), max_ctx) : 0;
-  const bool two = pool_out != nullptr && pool_size > 0;
+  int n;
+  if (kReindex) {
+    n = pool_size;
+  } else {
+    const int b = __ldg(q_seq + q);
+    n = (b >= 0 && b < num_seqs) ? min(max(0, __ldg(seq_lens + b)), max_ctx) : 0;
+  }
+  const bool two = !kReindex && pool_out != nullptr && pool_size > 0;
   const uint32_t* src = ws + (int64_t)q * ws_stride;
+  const int32_t* pin = kReindex ? pool_in + (int64_t)q * pool_size : nullptr;
   int32_t* out0 = out_idx + (int64_t)q * topk;
   int32_t* out1 = two ? pool_out + (int64_t)q * pool_size : nullptr;
 
@@ -1390,7 +1399,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       uint32_t p = base + sel_run + warp_excl(ns, stot);
       for (int e = 0; e < nk; ++e)
         if (selm & (1u << e)) {
-          if (p < want_t) outp[p] = (int32_t)pos[e];
+          if (p < want_t) outp[p] = kReindex ? __ldg(pin + pos[e]) : (int32_t)pos[e];
           ++p;
         }
       tie_run += ttot;
@@ -1532,18 +1541,20 @@ cudaError_t launch_select(bool reindex, const uint32_t* ws, int64_t ws_stride, c
                           int32_t* st, cudaStream_t s, int num_sms) {
   const int32_t n = reindex ? pool_size : pg.max_pages_per_seq * kPage;
   const int32_t want_max = std::max(topk, (!reindex && pool_out) ? pool_size : 0);
-  // FULL over contexts up to 2^18 tokens: one CTA per query, no cluster synchronisation
-  // (measured on B300: 64 queries x 131072 keys took ~90 us in two waves of 8-CTA clusters)
+  // Up to 2^18 keys per query: one CTA per query, no cluster synchronisation (measured on
+  // B300: 64 Full queries x 131072 keys took ~90 us in two waves of 8-CTA clusters, 46 us
+  // this way; 64 Reindex queries x 8192 pool entries 27 us with single-CTA clusters)
   (void)num_sms;
-  if (!reindex && n <= (1 << 18) && want_max <= 8192) {
+  if (n <= (1 << 18) && want_max <= 8192) {
     const size_t smem = sizeof(BigShared);
-    cudaError_t e = cudaFuncSetAttribute(select_cta_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kern = reindex ? select_cta_kernel<true> : select_cta_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return e;
-    select_cta_kernel<<<num_q, kBigThreads, smem, s>>>(ws, ws_stride, q_seq, pg.seq_lens,
-                                                       pg.num_seqs, pool_out ? pool_size : 0,
-                                                       topk, out_idx, pool_out,
-                                                       pg.max_pages_per_seq * kPage);
+    kern<<<num_q, kBigThreads, smem, s>>>(ws, ws_stride, q_seq, pg.seq_lens, pg.num_seqs, pool_in,
+                                          reindex ? pool_size : (pool_out ? pool_size : 0), topk,
+                                          out_idx, reindex ? nullptr : pool_out,
+                                          pg.max_pages_per_seq * kPage);
     return cudaGetLastError();
   }
   const int c = select_cluster(n, want_max);
