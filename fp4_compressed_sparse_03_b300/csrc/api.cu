@@ -11,15 +11,15 @@ cudaError_t launch_quantize(const float*, const int32_t*, uint8_t*, uint8_t*, in
 cudaError_t launch_dequantize(const uint8_t*, const uint8_t*, const int32_t*, float*, int32_t,
                               int32_t, int64_t, int32_t*, cudaStream_t, int);
 cudaError_t launch_score_full(const uint16_t*, const uint16_t*, const int32_t*, int32_t, int32_t,
-                              const csa2_pages&, uint32_t*, int64_t, void*, int32_t*, cudaStream_t,
-                              int);
+                              const csa2_pages&, uint32_t*, int64_t, void*, uint32_t*, int32_t*,
+                              cudaStream_t, int);
 cudaError_t launch_score_reindex(const uint16_t*, const uint16_t*, const int32_t*, int32_t,
                                  const csa2_pages&, const int32_t*, int32_t, uint32_t*, void*,
                                  int32_t*, cudaStream_t, int);
 size_t runlist_bytes(int32_t num_q);
 cudaError_t launch_select(bool, const uint32_t*, int64_t, const int32_t*, const csa2_pages&,
-                          int32_t, const int32_t*, int32_t, int32_t, int32_t*, int32_t*, int32_t*,
-                          cudaStream_t, int);
+                          int32_t, const int32_t*, int32_t, int32_t, int32_t*, int32_t*,
+                          const uint32_t*, int32_t*, cudaStream_t, int);
 cudaError_t launch_attn(const uint16_t*, const uint8_t*, const uint8_t*, const int32_t*,
                         const csa2_pages&, float*, float*, int32_t, const int32_t*, int32_t, float,
                         void*, int32_t*, cudaStream_t, int);
@@ -110,10 +110,16 @@ static size_t scores_bytes(csa2_mode mode, int32_t num_q, int32_t max_pages_per_
   return ((size_t)num_q * n * sizeof(uint32_t) + 255) / 256 * 256;
 }
 
+// FULL: per-query selection histograms (2048 bins) written by the scorer
+static size_t hist_bytes(csa2_mode mode, int32_t num_q) {
+  return mode == CSA2_FULL ? ((size_t)num_q * 2048 * sizeof(uint32_t) + 255) / 256 * 256 : 0;
+}
+
 size_t csa2_index_workspace_size(csa2_mode mode, int32_t num_q, int32_t max_pages_per_seq,
                                  int32_t pool_size) {
   if (num_q <= 0 || (mode != CSA2_FULL && mode != CSA2_REINDEX)) return 0;
-  return scores_bytes(mode, num_q, max_pages_per_seq, pool_size) + runlist_bytes(num_q);
+  return scores_bytes(mode, num_q, max_pages_per_seq, pool_size) + runlist_bytes(num_q) +
+         hist_bytes(mode, num_q);
 }
 
 csa2_status csa2_index(csa2_mode mode, const uint16_t* q_idx, const uint16_t* k_idx, int32_t* pool,
@@ -146,11 +152,12 @@ csa2_status csa2_index(csa2_mode mode, const uint16_t* q_idx, const uint16_t* k_
     const int64_t stride = (int64_t)pages->max_pages_per_seq * kPage;
     void* rl = static_cast<char*>(args->workspace) +
                scores_bytes(mode, args->num_q, pages->max_pages_per_seq, P);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(static_cast<char*>(rl) + runlist_bytes(args->num_q));
     e = launch_score_full(q_idx, k_idx, args->q_seq, args->num_q, args->max_q_per_seq, *pages, ws,
-                          stride, rl, args->dev_status, stream, sms);
+                          stride, rl, hist, args->dev_status, stream, sms);
     if (e != cudaSuccess) return from_cuda(e);
     e = launch_select(false, ws, stride, args->q_seq, *pages, args->num_q, nullptr,
-                      pool ? P : 0, topk, out_idx, pool, args->dev_status, stream, sms);
+                      pool ? P : 0, topk, out_idx, pool, hist, args->dev_status, stream, sms);
     return from_cuda(e);
   }
   // REINDEX
@@ -161,7 +168,7 @@ csa2_status csa2_index(csa2_mode mode, const uint16_t* q_idx, const uint16_t* k_
                            args->dev_status, stream, sms);
   if (e != cudaSuccess) return from_cuda(e);
   e = launch_select(true, ws, P, args->q_seq, *pages, args->num_q, pool, P, topk, out_idx, nullptr,
-                    args->dev_status, stream, sms);
+                    nullptr, args->dev_status, stream, sms);
   return from_cuda(e);
 }
 

@@ -30,6 +30,12 @@ namespace csa2 {
 
 // ------------------------------------------------------------------ scoring -------
 
+// Selection histograms: the top 11 bits of a ranking key (8 exponent + 3 mantissa bits).
+constexpr int kHistBins = 2048;
+__device__ __forceinline__ uint32_t hist_bin(uint32_t key) {
+  return min(key >> 20, (uint32_t)kHistBins - 1);  // finite scores give bins < 2041
+}
+
 constexpr int kScoreThreads = 128;     // Reindex scorer: 4 warps per CTA
 constexpr int kScoreWarps = kScoreThreads / 32;
 constexpr int kGatherCtasPerSm = 3;    // three such CTAs per SM
@@ -351,7 +357,11 @@ struct PageRing {
   int32_t valid[kPageStages]; // 1 if its keys were loaded
   volatile int abort;
 };
-constexpr size_t kTmaSmem = (size_t)kPageStages * kPageBytes + sizeof(PageRing) + 1024;
+constexpr int kMaxDraft = 4;  // query tokens of one sequence scored together
+constexpr size_t kRingOff = (sizeof(PageRing) + 15) / 16 * 16;
+// page ring | ring state | per-query selection histograms of the current run
+constexpr size_t kTmaSmem = (size_t)kPageStages * kPageBytes + kRingOff +
+                            (size_t)kMaxDraft * kHistBins * 4 + 1024;
 
 // Row `row` (0..63), 16-byte chunk `k` (0..15) of a staged page: two 8 KB halves
 // (dims 0-63, 64-127), each 64 rows of 128 bytes with the chunk index XOR-ed by row % 8.
@@ -366,12 +376,14 @@ __device__ __forceinline__ void read_page_row(uint4 (&kv)[4], uint32_t base, int
 __global__ void __launch_bounds__(kTmaThreads, kScoreCtasPerSm)
     score_pages_kernel(const __grid_constant__ CUtensorMap keymap, const uint16_t* __restrict__ q_idx,
                        const int32_t* __restrict__ q_seq, int32_t num_q, ScoreGeom g,
-                       uint32_t* __restrict__ ws, int64_t ws_stride, RunList rl, int32_t* st) {
+                       uint32_t* __restrict__ ws, int64_t ws_stride, RunList rl,
+                       uint32_t* __restrict__ ghist, int32_t* st) {
   extern __shared__ __align__(1024) unsigned char page_smem_raw[];
   unsigned char* data = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(page_smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int S = kPageStages;
   PageRing* ring = reinterpret_cast<PageRing*>(data + S * kPageBytes);
+  uint32_t* shist = reinterpret_cast<uint32_t*>(data + S * kPageBytes + kRingOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, c = lane & 3;
   if (threadIdx.x == 0) {
@@ -436,8 +448,29 @@ __global__ void __launch_bounds__(kTmaThreads, kScoreCtasPerSm)
     const int rr = 16 * warp + ((gq >> 1) | ((gq & 1) << 2));
     int cur_run = -1, rows = 0, q0 = 0, T = 0, NT = 0;
     uint32_t bq[2][4][4];  // [n-tile][j][word]: B fragments of Q^T
+    // Selection histograms (ghist != nullptr): per query of the current run, counts of
+    // the stored ranking keys by top 11 bits, added to the global per-query histograms
+    // when the run ends.  Every consumer warp sees every page, so all of them reach each
+    // flush together (named barrier 1 over the consumer warps).
+    auto consumers_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory"); };
+    auto flush = [&]() {
+      consumers_sync();
+      for (int i = threadIdx.x; i < T * kHistBins; i += kConsumerWarps * 32) {
+        const uint32_t v = shist[i];
+        if (v != 0) {
+          atomicAdd(ghist + (int64_t)(q0 + i / kHistBins) * kHistBins + (i % kHistBins), v);
+          shist[i] = 0;
+        }
+      }
+      consumers_sync();
+    };
+    if (ghist != nullptr) {
+      for (int i = threadIdx.x; i < kMaxDraft * kHistBins; i += kConsumerWarps * 32) shist[i] = 0;
+      consumers_sync();
+    }
     auto enter = [&](int r) {
       if (r == cur_run) return;
+      if (cur_run >= 0 && ghist != nullptr) flush();
       cur_run = r;
       q0 = __ldg(rl.run_q0 + r);
       T = __ldg(rl.run_q0 + r + 1) - q0;
@@ -488,8 +521,13 @@ __global__ void __launch_bounds__(kTmaThreads, kScoreCtasPerSm)
         if ((c & 1) == 0 && t < T) {
           uint32_t* out = ws + (int64_t)(q0 + t) * ws_stride;
           const int ta = page * kPage + ra, tb = page * kPage + rb;
-          if (ta < rows) out[ta] = valid ? rank_key(s0) : 0u;
-          if (tb < rows) out[tb] = valid ? rank_key(s1) : 0u;
+          const uint32_t k0 = valid ? rank_key(s0) : 0u, k1 = valid ? rank_key(s1) : 0u;
+          if (ta < rows) out[ta] = k0;
+          if (tb < rows) out[tb] = k1;
+          if (ghist != nullptr && valid) {
+            if (ta < rows) atomicAdd(&shist[t * kHistBins + hist_bin(k0)], 1u);
+            if (tb < rows) atomicAdd(&shist[t * kHistBins + hist_bin(k1)], 1u);
+          }
         }
       }
     };
@@ -511,6 +549,7 @@ __global__ void __launch_bounds__(kTmaThreads, kScoreCtasPerSm)
       enter(run);
       tile(k0, k1, page, rr, rr + 8, valid);
     }
+    if (cur_run >= 0 && ghist != nullptr) flush();
   }
   __syncthreads();
 }
@@ -1088,8 +1127,8 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kSelThreads, 2)
 constexpr int kBigThreads = 1024;
 constexpr int kBigWarps = kBigThreads / 32;
 constexpr int kBigCap = 512;    // kept keys per warp
-constexpr int kHistBins = 2048;
-constexpr int kBigBatch = 8;    // 16-byte loads in flight per lane in the sweeps
+constexpr int kBigBatch = 8;    // 16-byte loads in flight per lane in the histogram sweep
+constexpr int kFiltBatch = 4;   // 128-key groups in flight per warp in the filtering sweep
 
 struct BigShared {
   uint32_t hist[kHistBins];
@@ -1149,7 +1188,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
                       const int32_t* __restrict__ q_seq, const int32_t* __restrict__ seq_lens,
                       int32_t num_seqs, const int32_t* __restrict__ pool_in, int32_t pool_size,
                       int32_t topk, int32_t* __restrict__ out_idx, int32_t* __restrict__ pool_out,
-                      int32_t max_ctx) {
+                      int32_t max_ctx, const uint32_t* __restrict__ ghist) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   BigShared& sh = *reinterpret_cast<BigShared*>(smem_raw);
   const int q = blockIdx.x;
@@ -1181,15 +1220,23 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     }
   };
 
-  // ---- 1. histogram of the top 11 bits, valid-key count ----
-  for (int i = tid; i < kHistBins; i += kBigThreads) sh.hist[i] = 0;
+  // ---- 1. histogram of the top 11 bits, valid-key count (or the scorer's histogram) ----
   if (tid == 0) {
     sh.nvalid = 0;
     sh.overflow = 0;
   }
-  __syncthreads();
   uint32_t nv = 0;
-  for (int i0 = seg_lo; i0 < seg_hi; i0 += 128 * kBigBatch) {
+  if (ghist != nullptr) {
+    for (int i = tid; i < kHistBins; i += kBigThreads) {
+      const uint32_t v = __ldcg(ghist + (int64_t)q * kHistBins + i);
+      sh.hist[i] = v;
+      nv += v;
+    }
+  } else {
+    for (int i = tid; i < kHistBins; i += kBigThreads) sh.hist[i] = 0;
+  }
+  __syncthreads();
+  for (int i0 = seg_lo; ghist == nullptr && i0 < seg_hi; i0 += 128 * kBigBatch) {
     uint32_t k[kBigBatch][4];
 #pragma unroll
     for (int bb = 0; bb < kBigBatch; ++bb) load4(i0 + 128 * bb + 4 * lane, k[bb]);
@@ -1199,7 +1246,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       for (int e = 0; e < 4; ++e)
         if (k[bb][e] != 0) {
           ++nv;
-          atomicAdd(&sh.hist[min(k[bb][e] >> 20, (uint32_t)kHistBins - 1)], 1u);  // finite: < 2041
+          atomicAdd(&sh.hist[hist_bin(k[bb][e])], 1u);
         }
   }
   nv = __reduce_add_sync(0xffffffffu, nv);
@@ -1248,32 +1295,33 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   if (want1 > 0) bmin = min(bmin, B1);
 
   // ---- 3. ordered sweep: keep keys with bin >= bmin ----
+  // A 128-key group is read slot-major (lane l holds keys l, 32 + l, 64 + l, 96 + l), so
+  // each slot compacts with one ballot: rank = popc(ballot & lanes below).
+  const uint32_t lt = (1u << lane) - 1u;
   uint32_t cnt = 0;
   if (want0 > 0) {
-    for (int i0 = seg_lo; i0 < seg_hi; i0 += 128 * kBigBatch) {
-      uint32_t k[kBigBatch][4];
+    for (int i0 = seg_lo; i0 < seg_hi; i0 += 128 * kFiltBatch) {
+      uint32_t k[kFiltBatch][4];
 #pragma unroll
-      for (int bb = 0; bb < kBigBatch; ++bb) load4(i0 + 128 * bb + 4 * lane, k[bb]);
+      for (int bb = 0; bb < kFiltBatch; ++bb)
 #pragma unroll
-      for (int bb = 0; bb < kBigBatch; ++bb) {
-        const int i = i0 + 128 * bb + 4 * lane;
-        uint32_t m = 0;
+        for (int e = 0; e < 4; ++e) {
+          const int i = i0 + 128 * bb + 32 * e + lane;
+          k[bb][e] = i < seg_hi ? __ldcg(src + i) : 0u;
+        }
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (k[bb][e] != 0 && (k[bb][e] >> 20) >= bmin) m |= 1u << e;
-        uint32_t tot;
-        uint32_t p = cnt + warp_excl(__popc(m), tot);
+      for (int bb = 0; bb < kFiltBatch; ++bb)
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (m & (1u << e)) {
-            if (p < kBigCap) {
-              sh.u.c.pos[warp][p] = (uint32_t)(i + e);
-              sh.u.c.key[warp][p] = k[bb][e];
-            }
-            ++p;
+        for (int e = 0; e < 4; ++e) {
+          const bool m = k[bb][e] != 0 && (k[bb][e] >> 20) >= bmin;
+          const uint32_t bal = __ballot_sync(0xffffffffu, m);
+          const uint32_t p = cnt + __popc(bal & lt);
+          if (m && p < (uint32_t)kBigCap) {
+            sh.u.c.pos[warp][p] = (uint32_t)(i0 + 128 * bb + 32 * e + lane);
+            sh.u.c.key[warp][p] = k[bb][e];
           }
-        cnt += tot;
-      }
+          cnt += __popc(bal);
+        }
     }
     if (lane == 0) {
       sh.wcnt[warp] = cnt;
@@ -1406,14 +1454,20 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       sel_run += stot;
     };
     if (kept) {
-      for (uint32_t j0 = 0; j0 < cnt; j0 += 32) {
+      for (uint32_t j0 = 0; j0 < cnt; j0 += 32) {  // one kept key per lane: ballot ranks
         const uint32_t j = j0 + lane;
-        uint32_t k[1] = {0u}, pos[1] = {0u};
-        if (j < cnt) {
-          k[0] = sh.u.c.key[warp][j];
-          pos[0] = sh.u.c.pos[warp][j];
+        const uint32_t k = j < cnt ? sh.u.c.key[warp][j] : 0u;
+        const bool tie = j < cnt && k == T;
+        const uint32_t tb = __ballot_sync(0xffffffffu, tie);
+        const bool sel = j < cnt && (k > T || (tie && tie_run + __popc(tb & lt) < take));
+        const uint32_t sb = __ballot_sync(0xffffffffu, sel);
+        const uint32_t p = base + sel_run + __popc(sb & lt);
+        if (sel && p < want_t) {
+          const uint32_t pos = sh.u.c.pos[warp][j];
+          outp[p] = kReindex ? __ldg(pin + pos) : (int32_t)pos;
         }
-        emit(k, pos, 1);
+        tie_run += __popc(tb);
+        sel_run += __popc(sb);
       }
     } else {
       for (int i0 = seg_lo; i0 < seg_hi; i0 += 128) {
@@ -1450,8 +1504,8 @@ static RunList make_runlist(void* base, int32_t num_q) {
 
 cudaError_t launch_score_full(const uint16_t* q_idx, const uint16_t* keys, const int32_t* q_seq,
                               int32_t num_q, int32_t max_q_per_seq, const csa2_pages& pg,
-                              uint32_t* ws, int64_t ws_stride, void* runlist, int32_t* st,
-                              cudaStream_t s, int num_sms) {
+                              uint32_t* ws, int64_t ws_stride, void* runlist, uint32_t* ghist,
+                              int32_t* st, cudaStream_t s, int num_sms) {
   ScoreGeom g{pg.seq_lens, pg.page_table, pg.max_pages_per_seq, pg.num_pages, pg.num_seqs};
   RunList rl = make_runlist(runlist, num_q);
   const bool batched = max_q_per_seq > 1;
@@ -1468,8 +1522,12 @@ cudaError_t launch_score_full(const uint16_t* q_idx, const uint16_t* keys, const
   e = cudaFuncSetAttribute(score_pages_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kTmaSmem);
   if (e != cudaSuccess) return e;
+  if (ghist != nullptr) {
+    e = cudaMemsetAsync(ghist, 0, (size_t)num_q * kHistBins * sizeof(uint32_t), s);
+    if (e != cudaSuccess) return e;
+  }
   score_pages_kernel<<<grid, kTmaThreads, kTmaSmem, s>>>(keymap, q_idx, q_seq, num_q, g, ws,
-                                                         ws_stride, rl, st);
+                                                         ws_stride, rl, ghist, st);
   return cudaGetLastError();
 }
 
@@ -1538,7 +1596,7 @@ cudaError_t launch_select_r(int c, const uint32_t* ws, int64_t ws_stride, const 
 cudaError_t launch_select(bool reindex, const uint32_t* ws, int64_t ws_stride, const int32_t* q_seq,
                           const csa2_pages& pg, int32_t num_q, const int32_t* pool_in,
                           int32_t pool_size, int32_t topk, int32_t* out_idx, int32_t* pool_out,
-                          int32_t* st, cudaStream_t s, int num_sms) {
+                          const uint32_t* ghist, int32_t* st, cudaStream_t s, int num_sms) {
   const int32_t n = reindex ? pool_size : pg.max_pages_per_seq * kPage;
   const int32_t want_max = std::max(topk, (!reindex && pool_out) ? pool_size : 0);
   // Up to 2^18 keys per query: one CTA per query, no cluster synchronisation (measured on
@@ -1554,7 +1612,7 @@ cudaError_t launch_select(bool reindex, const uint32_t* ws, int64_t ws_stride, c
     kern<<<num_q, kBigThreads, smem, s>>>(ws, ws_stride, q_seq, pg.seq_lens, pg.num_seqs, pool_in,
                                           reindex ? pool_size : (pool_out ? pool_size : 0), topk,
                                           out_idx, reindex ? nullptr : pool_out,
-                                          pg.max_pages_per_seq * kPage);
+                                          pg.max_pages_per_seq * kPage, reindex ? nullptr : ghist);
     return cudaGetLastError();
   }
   const int c = select_cluster(n, want_max);

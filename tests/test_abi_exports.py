@@ -40,7 +40,8 @@ def test_host_side_checks_without_device():
     assert L.csa2_read_status(None, None, None) == csa2.CSA2_ERR_INVALID_ARGUMENT
     # workspace sizing is host arithmetic
     full = csa2.csa2_index_workspace_size(csa2.CSA2_FULL, 64, 2048, 8192)
-    assert 64 * 2048 * 64 * 4 < full < 64 * 2048 * 64 * 4 + 4096   # scores + run list
+    hist = 64 * 2048 * 4                                             # selection histograms
+    assert 64 * 2048 * 64 * 4 + hist < full < 64 * 2048 * 64 * 4 + hist + 4096  # + scores, run list
     re = csa2.csa2_index_workspace_size(csa2.CSA2_REINDEX, 64, 2048, 8192)
     assert 64 * 8192 * 4 < re < 64 * 8192 * 4 + 4096
     assert csa2.csa2_index_workspace_size(csa2.CSA2_REUSE, 64, 2048, 8192) == 0
