@@ -248,8 +248,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   const int32_t* idx_q = idx + (int64_t)qi * topk + jbeg;
 
-  // ---- resolve every selected entry of this split to its physical row ----
-  for (int e = tid; e < ecount; e += kAttnThreads) {
+  // Q is loaded first: its latency overlaps the index and page-table loads below
+  const uint4* qv = reinterpret_cast<const uint4*>(q + (int64_t)qi * kHq * kDkv);
+  uint4 qr[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) qr[k] = __ldg(qv + tid + kAttnThreads * k);
+
+  // ---- resolve the selected entries to physical rows: the first two tiles first ----
+  auto resolve = [&](int e) {
     const int s = __ldg(idx_q + e);
     int32_t slot = -1;
     if (s >= 0 && s < n_ctx) {
@@ -260,7 +266,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       report(st, CSA2_DEV_BAD_INDEX);
     }
     ctl.slot[e] = slot;
-  }
+  };
+  const int e_first = min(ecount, kRawStages * kTile);
+  for (int e = tid; e < e_first; e += kAttnThreads) resolve(e);
   if (tid == 0) {
     mbar_init(&ctl.bar_s, 1);
     for (int j = 0; j < kPairs; ++j) mbar_init(&ctl.bar_pv[j], 1);
@@ -274,20 +282,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ctl.tmem;
 
-  // start the first gathers before touching Q
+  // start the first gathers, then resolve the remaining entries while they land
 #pragma unroll
   for (int i = 0; i < kRawStages; ++i) {
     if (i < ntiles) issue_tile(raw + i * kRawBytes, i * kTile, ecount, ctl.slot, codes, scales);
     cp_async_commit();
   }
+  for (int e = e_first + tid; e < ecount; e += kAttnThreads) resolve(e);
 
-  // ---- Q: one pass into registers, max |q| -> power-of-two prescale -> f16 chunks ----
-  const uint4* qv = reinterpret_cast<const uint4*>(q + (int64_t)qi * kHq * kDkv);
-  uint4 qr[4];
+  // ---- Q: max |q| -> power-of-two prescale -> f16 chunks (the barrier below also
+  // publishes the remaining slots) ----
   uint32_t mx = 0;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    qr[k] = __ldg(qv + tid + kAttnThreads * k);
     const uint32_t w[4] = {qr[k].x, qr[k].y, qr[k].z, qr[k].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) mx = max(mx, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));

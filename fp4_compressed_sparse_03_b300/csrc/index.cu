@@ -222,21 +222,6 @@ __global__ void __launch_bounds__(kScoreThreads, kGatherCtasPerSm)
   warp_share(__ldg(rl.meta + 1), g0, g1);
   if (g0 >= g1) return;
 
-  // token -> key row of query q (nullptr: skip), with fault reporting
-  auto row_of = [&](int q, int b, int n_ctx, int pos) -> const uint16_t* {
-    if (pos >= pool_size) return nullptr;
-    const int t = __ldg(pool + (int64_t)q * pool_size + pos);
-    if (t < 0 || t >= n_ctx) {
-      if (t != -1 && c == 0) report(st, CSA2_DEV_BAD_INDEX);
-      return nullptr;
-    }
-    const int32_t pg = __ldg(g.page_table + (int64_t)b * g.max_pages + (t >> 6));
-    if (pg < 0 || pg >= g.num_pages) {
-      if (c == 0) report(st, CSA2_DEV_BAD_PAGE);
-      return nullptr;
-    }
-    return keys + ((int64_t)pg * kPage + (t & (kPage - 1))) * kDidx;
-  };
   struct QInfo {
     int q = -1, b = -1, n_ctx = 0;
   };
@@ -250,38 +235,70 @@ __global__ void __launch_bounds__(kScoreThreads, kGatherCtasPerSm)
     }
     return f;
   };
+  // Rows of a group as loaded pool entries: the pool loads of group gg + kGatherRing are
+  // issued one iteration before the group's page-table lookups and copies, so their
+  // latency overlaps the scoring of the current group.
+  struct PoolRows {
+    int b = -1, n_ctx = 0;
+    int ta = -1, tb = -1;  // tokens of rows gq and gq + 8 (-1: none)
+  };
   RunCursor lc, cc;
   cursor_seek(lc, rl, R, g0);
   cc = lc;
   QInfo li = info(lc.r), ci;
+  auto load_pool = [&](int64_t gg) -> PoolRows {
+    PoolRows r;
+    if (gg >= g1) return r;
+    cursor_advance(lc, rl, gg);
+    if (lc.r != li.q) li = info(lc.r);
+    if (li.b < 0) return r;
+    r.b = li.b;
+    r.n_ctx = li.n_ctx;
+    const int pos = (int)(gg - lc.start) * 16 + gq;
+    const int32_t* pq = pool + (int64_t)li.q * pool_size;
+    if (pos < pool_size) r.ta = __ldg(pq + pos);
+    if (pos + 8 < pool_size) r.tb = __ldg(pq + pos + 8);
+    return r;
+  };
+  // token -> key row (nullptr: skip), with fault reporting
+  auto row_of = [&](int b, int n_ctx, int t) -> const uint16_t* {
+    if (t < 0 || t >= n_ctx) {
+      if (t != -1 && c == 0) report(st, CSA2_DEV_BAD_INDEX);
+      return nullptr;
+    }
+    const int32_t pg = __ldg(g.page_table + (int64_t)b * g.max_pages + (t >> 6));
+    if (pg < 0 || pg >= g.num_pages) {
+      if (c == 0) report(st, CSA2_DEV_BAD_PAGE);
+      return nullptr;
+    }
+    return keys + ((int64_t)pg * kPage + (t & (kPage - 1))) * kDidx;
+  };
   uint32_t okmask = 0;  // 2 bits per ring slot: rows gq and gq + 8 of the group loaded
-  auto issue = [&](int64_t gg, int sl) {
+  auto issue = [&](const PoolRows& pr, int sl) {
     okmask &= ~(3u << (2 * sl));
-    if (gg < g1) {
-      cursor_advance(lc, rl, gg);
-      if (lc.r != li.q) li = info(lc.r);
-      if (li.b >= 0) {
-        const int pos = (int)(gg - lc.start) * 16 + gq;
-        const uint32_t slot = ring + sl * kGatherGroup;
-        const uint16_t* ra = row_of(li.q, li.b, li.n_ctx, pos);
-        const uint16_t* rb = row_of(li.q, li.b, li.n_ctx, pos + 8);
+    if (pr.b >= 0) {
+      const uint32_t slot = ring + sl * kGatherGroup;
+      const uint16_t* ra = row_of(pr.b, pr.n_ctx, pr.ta);
+      const uint16_t* rb = row_of(pr.b, pr.n_ctx, pr.tb);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int k = 4 * j + c;
-          if (ra) cp_async16(slot + gq * kKeyRow + ((k ^ sw) << 4), reinterpret_cast<const char*>(ra) + 16 * k);
-          if (rb) cp_async16(slot + (gq + 8) * kKeyRow + ((k ^ sw) << 4), reinterpret_cast<const char*>(rb) + 16 * k);
-        }
-        okmask |= ((ra ? 1u : 0u) | (rb ? 2u : 0u)) << (2 * sl);
+      for (int j = 0; j < 4; ++j) {
+        const int k = 4 * j + c;
+        if (ra) cp_async16(slot + gq * kKeyRow + ((k ^ sw) << 4), reinterpret_cast<const char*>(ra) + 16 * k);
+        if (rb) cp_async16(slot + (gq + 8) * kKeyRow + ((k ^ sw) << 4), reinterpret_cast<const char*>(rb) + 16 * k);
       }
+      okmask |= ((ra ? 1u : 0u) | (rb ? 2u : 0u)) << (2 * sl);
     }
     cp_async_commit();
   };
   uint32_t bq[4][4];
   int slot = 0;
 #pragma unroll
-  for (int i = 0; i < kGatherRing - 1; ++i) issue(g0 + i, i);
+  for (int i = 0; i < kGatherRing - 1; ++i) issue(load_pool(g0 + i), i);
+  PoolRows next = load_pool(g0 + kGatherRing - 1);
   for (int64_t gg = g0; gg < g1; ++gg) {
-    issue(gg + kGatherRing - 1, (slot + kGatherRing - 1) & (kGatherRing - 1));
+    const PoolRows cur = next;
+    next = load_pool(gg + kGatherRing);
+    issue(cur, (slot + kGatherRing - 1) & (kGatherRing - 1));
     cp_async_wait<kGatherRing - 1>();
     cursor_advance(cc, rl, gg);
     if (cc.r != ci.q) {
