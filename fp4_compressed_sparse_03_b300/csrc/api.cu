@@ -19,7 +19,8 @@ cudaError_t launch_score_reindex(const uint16_t*, const uint16_t*, const int32_t
 size_t runlist_bytes(int32_t num_q);
 cudaError_t launch_select(bool, const uint32_t*, int64_t, const int32_t*, const csa2_pages&,
                           int32_t, const int32_t*, int32_t, int32_t, int32_t*, int32_t*,
-                          const uint32_t*, int32_t*, cudaStream_t, int);
+                          const uint32_t*, void*, int32_t*, cudaStream_t, int);
+size_t wide_select_bytes(int32_t num_q, int32_t n);
 cudaError_t launch_attn(const uint16_t*, const uint8_t*, const uint8_t*, const int32_t*,
                         const csa2_pages&, float*, float*, int32_t, const int32_t*, int32_t, float,
                         void*, int32_t*, cudaStream_t, int);
@@ -115,11 +116,18 @@ static size_t hist_bytes(csa2_mode mode, int32_t num_q) {
   return mode == CSA2_FULL ? ((size_t)num_q * 2048 * sizeof(uint32_t) + 255) / 256 * 256 : 0;
 }
 
+// FULL over contexts beyond 2^18 tokens: candidate lists of the wide selection
+static size_t wide_bytes(csa2_mode mode, int32_t num_q, int32_t max_pages_per_seq) {
+  if (mode != CSA2_FULL) return 0;
+  const int64_t n = (int64_t)std::max(0, max_pages_per_seq) * kPage;
+  return (wide_select_bytes(num_q, (int32_t)std::min<int64_t>(n, INT32_MAX)) + 255) / 256 * 256;
+}
+
 size_t csa2_index_workspace_size(csa2_mode mode, int32_t num_q, int32_t max_pages_per_seq,
                                  int32_t pool_size) {
   if (num_q <= 0 || (mode != CSA2_FULL && mode != CSA2_REINDEX)) return 0;
   return scores_bytes(mode, num_q, max_pages_per_seq, pool_size) + runlist_bytes(num_q) +
-         hist_bytes(mode, num_q);
+         hist_bytes(mode, num_q) + wide_bytes(mode, num_q, max_pages_per_seq);
 }
 
 csa2_status csa2_index(csa2_mode mode, const uint16_t* q_idx, const uint16_t* k_idx, int32_t* pool,
@@ -153,11 +161,14 @@ csa2_status csa2_index(csa2_mode mode, const uint16_t* q_idx, const uint16_t* k_
     void* rl = static_cast<char*>(args->workspace) +
                scores_bytes(mode, args->num_q, pages->max_pages_per_seq, P);
     uint32_t* hist = reinterpret_cast<uint32_t*>(static_cast<char*>(rl) + runlist_bytes(args->num_q));
+    void* wide = wide_bytes(mode, args->num_q, pages->max_pages_per_seq) == 0
+                     ? nullptr
+                     : static_cast<void*>(reinterpret_cast<char*>(hist) + hist_bytes(mode, args->num_q));
     e = launch_score_full(q_idx, k_idx, args->q_seq, args->num_q, args->max_q_per_seq, *pages, ws,
                           stride, rl, hist, args->dev_status, stream, sms);
     if (e != cudaSuccess) return from_cuda(e);
     e = launch_select(false, ws, stride, args->q_seq, *pages, args->num_q, nullptr,
-                      pool ? P : 0, topk, out_idx, pool, hist, args->dev_status, stream, sms);
+                      pool ? P : 0, topk, out_idx, pool, hist, wide, args->dev_status, stream, sms);
     return from_cuda(e);
   }
   // REINDEX
@@ -168,7 +179,7 @@ csa2_status csa2_index(csa2_mode mode, const uint16_t* q_idx, const uint16_t* k_
                            args->dev_status, stream, sms);
   if (e != cudaSuccess) return from_cuda(e);
   e = launch_select(true, ws, P, args->q_seq, *pages, args->num_q, pool, P, topk, out_idx, nullptr,
-                    nullptr, args->dev_status, stream, sms);
+                    nullptr, nullptr, args->dev_status, stream, sms);
   return from_cuda(e);
 }
 

@@ -21,6 +21,7 @@
 //                        histograms merged through distributed shared memory, then an
 //                        ordered compaction with warp scans
 #include <cooperative_groups.h>
+#include <cstddef>
 
 #include "async.cuh"
 
@@ -1503,6 +1504,293 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     for (int i = (int)want1 + tid; i < pool_size; i += kBigThreads) out1[i] = -1;
 }
 
+// ------------------------------------------------------------ wide selection (Full) --
+// Contexts beyond 2^18 tokens: the Full scorer's exact histograms give every CTA the
+// boundary bins, so a query's keys are filtered by many CTAs at once.
+//   select_filter_kernel (C CTAs per query): one ordered sweep of the CTA's position
+//     range keeps (position, key) of the keys with bin >= min B_t into per-warp global
+//     lists sized for the whole warp segment (no overflow is possible);
+//   select_finish_kernel (one CTA per query): three radix passes over the boundary-bin
+//     keys of all lists fix T_t, then an ordered emit walks the lists in position order
+//     (CTA-major, then warp-major).
+constexpr int kWideMinKeys = 1 << 16;  // positions per filter CTA at least
+constexpr int kWideMaxCtas = 16;       // filter CTAs per query at most
+constexpr int kMaxWideLists = kWideMaxCtas * kBigWarps;
+
+// Per-CTA position range of the wide filter: a multiple of 4096 (so each warp segment is
+// a multiple of 128) with at most kWideMaxCtas CTAs per query.
+inline int wide_range(int32_t n) {
+  const int64_t per = std::max<int64_t>(kWideMinKeys, ((int64_t)n + kWideMaxCtas - 1) / kWideMaxCtas);
+  return (int)((per + 4095) / 4096 * 4096);
+}
+
+// Boundary bins (B_t) and keys in higher bins (A_t) of both targets from a histogram in
+// shared memory; every thread gets the same values.  Thread t handles bins 2t, 2t + 1.
+__device__ __forceinline__ void boundary_bins(BigShared& sh, uint32_t want0, uint32_t want1,
+                                              uint32_t& B0, uint32_t& A0, uint32_t& B1,
+                                              uint32_t& A1) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t hi = sh.hist[2 * tid + 1], lo = sh.hist[2 * tid];
+  uint32_t x = hi + lo;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_down_sync(0xffffffffu, x, o);
+    if (lane + o < 32) x += y;
+  }
+  if (lane == 0) sh.scan[0][warp] = x;
+  if (tid < 4) sh.res[tid >> 1][tid & 1] = 0;
+  __syncthreads();
+  uint32_t later = 0;
+  for (int w = warp + 1; w < kBigWarps; ++w) later += sh.scan[0][w];
+  const uint32_t above_hi = later + x - (hi + lo), above_lo = above_hi + hi;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const uint32_t want_t = t == 0 ? want0 : want1;
+    if (want_t == 0) continue;
+    if (above_hi < want_t && above_hi + hi >= want_t) {
+      sh.res[t][0] = 2 * tid + 1;
+      sh.res[t][1] = above_hi;
+    } else if (above_lo < want_t && above_lo + lo >= want_t) {
+      sh.res[t][0] = 2 * tid;
+      sh.res[t][1] = above_lo;
+    }
+  }
+  __syncthreads();
+  B0 = sh.res[0][0];
+  A0 = sh.res[0][1];
+  B1 = sh.res[1][0];
+  A1 = sh.res[1][1];
+  __syncthreads();
+}
+
+// Histogram of query q from the scorer into shared memory; returns the valid-key count.
+__device__ __forceinline__ uint32_t load_hist(BigShared& sh, const uint32_t* __restrict__ ghist,
+                                              int q) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid == 0) sh.nvalid = 0;
+  uint32_t nv = 0;
+  for (int i = tid; i < kHistBins; i += kBigThreads) {
+    const uint32_t v = __ldcg(ghist + (int64_t)q * kHistBins + i);
+    sh.hist[i] = v;
+    nv += v;
+  }
+  __syncthreads();
+  nv = __reduce_add_sync(0xffffffffu, nv);
+  if (lane == 0) atomicAdd(&sh.nvalid, nv);
+  __syncthreads();
+  return sh.nvalid;
+}
+
+struct WideLists {
+  uint32_t* pos;   // [num_q][C][32][seg]
+  uint32_t* key;   // [num_q][C][32][seg]
+  uint32_t* cnt;   // [num_q][C][32]
+  int C, seg;
+};
+
+__global__ void __launch_bounds__(kBigThreads, 1)
+    select_filter_kernel(const uint32_t* __restrict__ ws, int64_t ws_stride,
+                         const int32_t* __restrict__ q_seq, const int32_t* __restrict__ seq_lens,
+                         int32_t num_seqs, int32_t pool_size, int32_t topk, int32_t max_ctx,
+                         const uint32_t* __restrict__ ghist, WideLists wl) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  BigShared& sh = *reinterpret_cast<BigShared*>(smem_raw);
+  const int c = blockIdx.x, q = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = __ldg(q_seq + q);
+  const int n = (b >= 0 && b < num_seqs) ? min(max(0, __ldg(seq_lens + b)), max_ctx) : 0;
+  const uint32_t nvalid = load_hist(sh, ghist, q);
+  const uint32_t want0 = min((uint32_t)topk, nvalid);
+  const uint32_t want1 = pool_size > 0 ? min((uint32_t)pool_size, nvalid) : 0u;
+  uint32_t B0, A0, B1, A1;
+  boundary_bins(sh, want0, want1, B0, A0, B1, A1);
+  uint32_t bmin = want0 > 0 ? B0 : 0xFFFFFFFFu;
+  if (want1 > 0) bmin = min(bmin, B1);
+  const int L = wl.seg * kBigWarps;
+  const int lo = min(n, c * L), hi = min(n, lo + L);
+  const int seg_lo = min(hi, lo + warp * wl.seg), seg_hi = min(hi, seg_lo + wl.seg);
+  const uint32_t* src = ws + (int64_t)q * ws_stride;
+  const int64_t list = ((int64_t)q * wl.C + c) * kBigWarps + warp;
+  uint32_t* lpos = wl.pos + list * wl.seg;
+  uint32_t* lkey = wl.key + list * wl.seg;
+  const uint32_t lt = (1u << lane) - 1u;
+  uint32_t cnt = 0;
+  if (want0 > 0) {
+    for (int i0 = seg_lo; i0 < seg_hi; i0 += 128 * kFiltBatch) {
+      uint32_t k[kFiltBatch][4];
+#pragma unroll
+      for (int bb = 0; bb < kFiltBatch; ++bb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = i0 + 128 * bb + 32 * e + lane;
+          k[bb][e] = i < seg_hi ? __ldcg(src + i) : 0u;
+        }
+#pragma unroll
+      for (int bb = 0; bb < kFiltBatch; ++bb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const bool m = k[bb][e] != 0 && (k[bb][e] >> 20) >= bmin;
+          const uint32_t bal = __ballot_sync(0xffffffffu, m);
+          const uint32_t p = cnt + __popc(bal & lt);
+          if (m) {  // p < seg: at most seg keys in the warp's segment
+            lpos[p] = (uint32_t)(i0 + 128 * bb + 32 * e + lane);
+            lkey[p] = k[bb][e];
+          }
+          cnt += __popc(bal);
+        }
+    }
+  }
+  if (lane == 0) wl.cnt[list] = cnt;
+}
+
+// Block-wide exclusive scan of one value per thread (1024 threads); returns the
+// exclusive prefix and sets total.  Uses sh.scan[0].
+__device__ __forceinline__ uint32_t block_excl(BigShared& sh, uint32_t v, uint32_t& total) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh.scan[0][warp] = x;
+  __syncthreads();
+  uint32_t before = 0, all = 0;
+  for (int w = 0; w < kBigWarps; ++w) {
+    const uint32_t s = sh.scan[0][w];
+    before += w < warp ? s : 0u;
+    all += s;
+  }
+  __syncthreads();
+  total = all;
+  return before + x - v;
+}
+
+// The candidate lists of one query, concatenated in position order (list-major), are
+// split into contiguous chunks of `per` elements, one per thread.
+__global__ void __launch_bounds__(kBigThreads, 1)
+    select_finish_kernel(const int32_t* __restrict__ q_seq, int32_t pool_size, int32_t topk,
+                         int32_t* __restrict__ out_idx, int32_t* __restrict__ pool_out,
+                         const uint32_t* __restrict__ ghist, WideLists wl) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  BigShared& sh = *reinterpret_cast<BigShared*>(smem_raw);
+  uint32_t* loff = sh.u.c.pos[0];  // [nlists + 1] offsets of the lists in the concatenation
+  const int q = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int nlists = wl.C * kBigWarps;
+  const bool two = pool_out != nullptr && pool_size > 0;
+  int32_t* out0 = out_idx + (int64_t)q * topk;
+  int32_t* out1 = two ? pool_out + (int64_t)q * pool_size : nullptr;
+  const uint32_t nvalid = load_hist(sh, ghist, q);
+  const uint32_t want0 = min((uint32_t)topk, nvalid);
+  const uint32_t want1 = two ? min((uint32_t)pool_size, nvalid) : 0u;
+  uint32_t B0, A0, B1, A1;
+  boundary_bins(sh, want0, want1, B0, A0, B1, A1);
+  const int64_t list0 = (int64_t)q * nlists;
+
+  // list offsets: nlists <= 512 <= threads
+  uint32_t total;
+  const uint32_t mine = tid < nlists ? __ldcg(wl.cnt + list0 + tid) : 0u;
+  const uint32_t off = block_excl(sh, mine, total);
+  if (tid < nlists) loff[tid] = off;
+  if (tid == 0) loff[nlists] = total;
+  __syncthreads();
+  // list holding concatenated element e: the last l with loff[l] <= e
+  auto list_of = [&](uint32_t e) {
+    int lo = 0, hi = nlists - 1;
+    while (lo < hi) {
+      const int m = (lo + hi + 1) >> 1;
+      if (loff[m] <= e) lo = m; else hi = m - 1;
+    }
+    return lo;
+  };
+  // The concatenated keys are copied into shared memory once (coalesced) when they fit,
+  // so the radix and emit passes below do not wait on L2 element by element.
+  uint32_t* skey = loff + kMaxWideLists + 32;
+  const uint32_t skey_cap =
+      (uint32_t)((sizeof(sh.u) - (kMaxWideLists + 32) * sizeof(uint32_t)) / sizeof(uint32_t));
+  const bool in_smem = total <= skey_cap;
+  if (in_smem) {
+    for (uint32_t e = tid; e < total; e += kBigThreads) {
+      const int l = list_of(e);
+      skey[e] = __ldcg(wl.key + (list0 + l) * wl.seg + (e - loff[l]));
+    }
+    __syncthreads();
+  }
+  const uint32_t per = (total + kBigThreads - 1) / kBigThreads;
+  const uint32_t e_lo = min(total, per * tid), e_hi = min(total, e_lo + per);
+  const int l_first = list_of(e_lo);
+  // visit the chunk's elements in order: f(key, list, index in list)
+  auto walk = [&](auto f) {
+    int l = l_first;
+    for (uint32_t e = e_lo; e < e_hi; ++e) {
+      while (loff[l + 1] <= e) ++l;
+      const uint32_t j = e - loff[l];
+      f(in_smem ? skey[e] : __ldcg(wl.key + (list0 + l) * wl.seg + j), l, j);
+    }
+  };
+
+  // ---- exact boundary keys: three radix passes over the boundary-bin keys ----
+  uint32_t pre[2] = {B0, B1}, abv[2] = {A0, A1};
+  const uint32_t want[2] = {want0, want1};
+  if (want0 > 0) {
+    for (int pass = 0; pass < 3; ++pass) {
+      const int shift = pass == 0 ? 12 : pass == 1 ? 4 : 0, width = pass == 2 ? 4 : 8;
+      const uint32_t dmask = (1u << width) - 1u;
+      for (int i = tid; i < 2 * 256; i += kBigThreads) sh.rh[i >> 8][i & 255] = 0;
+      __syncthreads();
+      walk([&](uint32_t k, int, uint32_t) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (want[t] > 0 && (k >> (shift + width)) == pre[t])
+            atomicAdd(&sh.rh[t][(k >> shift) & dmask], 1u);
+      });
+      __syncthreads();
+      const uint32_t v = tid < 512 ? sh.rh[tid >> 8][tid & 255] : 0u;
+      big_find(sh, v, 256, want[0], want[1], abv[0], abv[1]);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if (want[t] > 0) {
+          pre[t] = (pre[t] << width) | sh.res[t][0];
+          abv[t] = sh.res[t][1];
+        }
+      __syncthreads();
+    }
+  }
+
+  // ---- ordered emit ----
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const uint32_t want_t = want[t];
+    if (want_t == 0) continue;
+    const uint32_t T = pre[t], quota = want_t - abv[t];
+    int32_t* outp = t == 0 ? out0 : out1;
+    uint32_t gt = 0, eq = 0;
+    walk([&](uint32_t k, int, uint32_t) {
+      gt += k > T;
+      eq += k == T;
+    });
+    uint32_t tie_all, sel_all;
+    const uint32_t ties_before = block_excl(sh, eq, tie_all);
+    const uint32_t take = quota > ties_before ? min(quota - ties_before, eq) : 0u;
+    uint32_t p = block_excl(sh, gt + take, sel_all);  // output base of this chunk
+    uint32_t tie_rank = 0;
+    walk([&](uint32_t k, int l, uint32_t j) {
+      const bool tie = k == T;
+      if (k > T || (tie && tie_rank < take)) {
+        if (p < want_t) outp[p] = (int32_t)__ldcg(wl.pos + (list0 + l) * wl.seg + j);
+        ++p;
+      }
+      tie_rank += tie;
+    });
+    __syncthreads();
+  }
+  for (int i = (int)want0 + tid; i < topk; i += kBigThreads) out0[i] = -1;
+  if (two)
+    for (int i = (int)want1 + tid; i < pool_size; i += kBigThreads) out1[i] = -1;
+  (void)q_seq;
+}
+
 // ------------------------------------------------------------------ launchers -----
 
 size_t select_smem_bytes() { return kSelCacheOff + (size_t)kSelCacheKeys * 4; }
@@ -1610,12 +1898,46 @@ cudaError_t launch_select_r(int c, const uint32_t* ws, int64_t ws_stride, const 
   }
 }
 
+// Bytes of the wide selection's candidate lists for FULL over contexts of n > 2^18 tokens.
+size_t wide_select_bytes(int32_t num_q, int32_t n) {
+  if (n <= (1 << 18)) return 0;
+  const int L = wide_range(n);
+  const int64_t C = ((int64_t)n + L - 1) / L;
+  return (size_t)num_q * C * ((size_t)L * 8 + kBigWarps * 4);
+}
+
 cudaError_t launch_select(bool reindex, const uint32_t* ws, int64_t ws_stride, const int32_t* q_seq,
                           const csa2_pages& pg, int32_t num_q, const int32_t* pool_in,
                           int32_t pool_size, int32_t topk, int32_t* out_idx, int32_t* pool_out,
-                          const uint32_t* ghist, int32_t* st, cudaStream_t s, int num_sms) {
+                          const uint32_t* ghist, void* wide_ws, int32_t* st, cudaStream_t s,
+                          int num_sms) {
   const int32_t n = reindex ? pool_size : pg.max_pages_per_seq * kPage;
   const int32_t want_max = std::max(topk, (!reindex && pool_out) ? pool_size : 0);
+  // FULL beyond 2^18 tokens with the scorer's histograms: C filter CTAs per query, then
+  // one finishing CTA per query (the cluster kernel took ~265 us for 4 x 2^20 keys)
+  if (!reindex && n > (1 << 18) && ghist != nullptr && wide_ws != nullptr) {
+    const int L = wide_range(n);
+    const int C = (int)(((int64_t)n + L - 1) / L);
+    WideLists wl;
+    wl.C = C;
+    wl.seg = L / kBigWarps;
+    const size_t lists = (size_t)num_q * C * L;
+    wl.pos = static_cast<uint32_t*>(wide_ws);
+    wl.key = wl.pos + lists;
+    wl.cnt = wl.key + lists;
+    const size_t fsmem = offsetof(BigShared, u), bsmem = sizeof(BigShared);
+    cudaError_t e = cudaFuncSetAttribute(select_finish_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bsmem);
+    if (e != cudaSuccess) return e;
+    const int32_t P = pool_out ? pool_size : 0;
+    select_filter_kernel<<<dim3(C, num_q), kBigThreads, fsmem, s>>>(
+        ws, ws_stride, q_seq, pg.seq_lens, pg.num_seqs, P, topk, n, ghist, wl);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    select_finish_kernel<<<num_q, kBigThreads, bsmem, s>>>(q_seq, P, topk, out_idx, pool_out,
+                                                           ghist, wl);
+    return cudaGetLastError();
+  }
   // Up to 2^18 keys per query: one CTA per query, no cluster synchronisation (measured on
   // B300: 64 Full queries x 131072 keys took ~90 us in two waves of 8-CTA clusters, 46 us
   // this way; 64 Reindex queries x 8192 pool entries 27 us with single-CTA clusters)

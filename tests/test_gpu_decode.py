@@ -234,6 +234,16 @@ def test_graph_replay_matches_eager_step():
     assert status == csa2.CSA2_OK, bits
 
 
+def test_wide_selection_beyond_2_18_tokens():
+    """Contexts beyond 2^18 tokens take the multi-CTA filter + finishing selection; a
+    shorter sequence in the same batch leaves some filter CTAs without positions."""
+    lens = np.array([300000, 70000], np.int32)
+    wl = gen.DecodeWorkload("wide", 37, lens, np.array([2, 1], np.int32),
+                            [gen.FULL, gen.REINDEX, gen.REUSE], pool_size=4096, topk=1024)
+    _, step, q_idx, q = run_workload(wl)
+    check_sampled(wl, range(wl.num_q), step, q_idx, q, min_attn=wl.num_q)
+
+
 def test_two_groups_pool_larger_than_context():
     lens = np.array([700, 3000], np.int32)
     wl = gen.DecodeWorkload("groups", 17, lens, np.ones(2, np.int32),
