@@ -1510,9 +1510,11 @@ __global__ void __launch_bounds__(kBigThreads, 1)
 //   select_filter_kernel (C CTAs per query): one ordered sweep of the CTA's position
 //     range keeps (position, key) of the keys with bin >= min B_t into per-warp global
 //     lists sized for the whole warp segment (no overflow is possible);
-//   select_finish_kernel (one CTA per query): three radix passes over the boundary-bin
-//     keys of all lists fix T_t, then an ordered emit walks the lists in position order
-//     (CTA-major, then warp-major).
+//   select_resolve_kernel (one CTA per query): three radix passes over the boundary-bin
+//     keys of all lists fix T_t; per-list output bases and tie quotas follow in list
+//     order, which is position order (CTA-major, then warp-major);
+//   select_emit_kernel (the filter's grid, one warp per list): each list writes its
+//     selected positions at its base.
 constexpr int kWideMinKeys = 1 << 16;  // positions per filter CTA at least
 constexpr int kWideMaxCtas = 16;       // filter CTAs per query at most
 constexpr int kMaxWideLists = kWideMaxCtas * kBigWarps;
@@ -1585,8 +1587,12 @@ struct WideLists {
   uint32_t* pos;   // [num_q][C][32][seg]
   uint32_t* key;   // [num_q][C][32][seg]
   uint32_t* cnt;   // [num_q][C][32]
+  uint32_t* meta;  // [num_q][kWideMeta]: per target T, want, then per-list base and take
   int C, seg;
 };
+// meta layout per query: [0..1] T_t, [2..3] want_t, then base[2][kMaxWideLists],
+// take[2][kMaxWideLists]
+constexpr int kWideMeta = 4 + 4 * kMaxWideLists;
 
 __global__ void __launch_bounds__(kBigThreads, 1)
     select_filter_kernel(const uint32_t* __restrict__ ws, int64_t ws_stride,
@@ -1666,37 +1672,38 @@ __device__ __forceinline__ uint32_t block_excl(BigShared& sh, uint32_t v, uint32
   return before + x - v;
 }
 
-// The candidate lists of one query, concatenated in position order (list-major), are
-// split into contiguous chunks of `per` elements, one per thread.
+// Resolve (one CTA per query): the candidate lists of the query, concatenated in
+// position order (list-major), are staged in shared memory when they fit and split into
+// contiguous per-thread chunks for three radix passes over the boundary-bin keys; the
+// exact boundary keys, the per-list output bases and tie quotas go to the query's meta.
 __global__ void __launch_bounds__(kBigThreads, 1)
-    select_finish_kernel(const int32_t* __restrict__ q_seq, int32_t pool_size, int32_t topk,
-                         int32_t* __restrict__ out_idx, int32_t* __restrict__ pool_out,
-                         const uint32_t* __restrict__ ghist, WideLists wl) {
+    select_resolve_kernel(int32_t pool_size, int32_t topk, const uint32_t* __restrict__ ghist,
+                          WideLists wl) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   BigShared& sh = *reinterpret_cast<BigShared*>(smem_raw);
-  uint32_t* loff = sh.u.c.pos[0];  // [nlists + 1] offsets of the lists in the concatenation
+  uint32_t* loff = sh.u.c.pos[0];                 // [nlists + 1] list offsets
+  uint32_t* lgt = loff + kMaxWideLists + 32;      // [nlists] keys > T_t per list
+  uint32_t* leq = lgt + kMaxWideLists;            // [nlists] keys == T_t per list
+  uint32_t* skey = leq + kMaxWideLists;           // staged keys
   const int q = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nlists = wl.C * kBigWarps;
-  const bool two = pool_out != nullptr && pool_size > 0;
-  int32_t* out0 = out_idx + (int64_t)q * topk;
-  int32_t* out1 = two ? pool_out + (int64_t)q * pool_size : nullptr;
+  const bool two = pool_size > 0;
   const uint32_t nvalid = load_hist(sh, ghist, q);
   const uint32_t want0 = min((uint32_t)topk, nvalid);
   const uint32_t want1 = two ? min((uint32_t)pool_size, nvalid) : 0u;
   uint32_t B0, A0, B1, A1;
   boundary_bins(sh, want0, want1, B0, A0, B1, A1);
   const int64_t list0 = (int64_t)q * nlists;
+  uint32_t* meta = wl.meta + (int64_t)q * kWideMeta;
 
-  // list offsets: nlists <= 512 <= threads
   uint32_t total;
   const uint32_t mine = tid < nlists ? __ldcg(wl.cnt + list0 + tid) : 0u;
   const uint32_t off = block_excl(sh, mine, total);
   if (tid < nlists) loff[tid] = off;
   if (tid == 0) loff[nlists] = total;
   __syncthreads();
-  // list holding concatenated element e: the last l with loff[l] <= e
-  auto list_of = [&](uint32_t e) {
+  auto list_of = [&](uint32_t e) {  // the last l with loff[l] <= e
     int lo = 0, hi = nlists - 1;
     while (lo < hi) {
       const int m = (lo + hi + 1) >> 1;
@@ -1704,11 +1711,8 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     }
     return lo;
   };
-  // The concatenated keys are copied into shared memory once (coalesced) when they fit,
-  // so the radix and emit passes below do not wait on L2 element by element.
-  uint32_t* skey = loff + kMaxWideLists + 32;
-  const uint32_t skey_cap =
-      (uint32_t)((sizeof(sh.u) - (kMaxWideLists + 32) * sizeof(uint32_t)) / sizeof(uint32_t));
+  const uint32_t skey_cap = (uint32_t)((sizeof(sh.u) - (3 * kMaxWideLists + 32) * sizeof(uint32_t)) /
+                                       sizeof(uint32_t));
   const bool in_smem = total <= skey_cap;
   if (in_smem) {
     for (uint32_t e = tid; e < total; e += kBigThreads) {
@@ -1720,17 +1724,14 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   const uint32_t per = (total + kBigThreads - 1) / kBigThreads;
   const uint32_t e_lo = min(total, per * tid), e_hi = min(total, e_lo + per);
   const int l_first = list_of(e_lo);
-  // visit the chunk's elements in order: f(key, list, index in list)
   auto walk = [&](auto f) {
     int l = l_first;
     for (uint32_t e = e_lo; e < e_hi; ++e) {
       while (loff[l + 1] <= e) ++l;
-      const uint32_t j = e - loff[l];
-      f(in_smem ? skey[e] : __ldcg(wl.key + (list0 + l) * wl.seg + j), l, j);
+      f(in_smem ? skey[e] : __ldcg(wl.key + (list0 + l) * wl.seg + (e - loff[l])));
     }
   };
 
-  // ---- exact boundary keys: three radix passes over the boundary-bin keys ----
   uint32_t pre[2] = {B0, B1}, abv[2] = {A0, A1};
   const uint32_t want[2] = {want0, want1};
   if (want0 > 0) {
@@ -1739,7 +1740,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       const uint32_t dmask = (1u << width) - 1u;
       for (int i = tid; i < 2 * 256; i += kBigThreads) sh.rh[i >> 8][i & 255] = 0;
       __syncthreads();
-      walk([&](uint32_t k, int, uint32_t) {
+      walk([&](uint32_t k) {
 #pragma unroll
         for (int t = 0; t < 2; ++t)
           if (want[t] > 0 && (k >> (shift + width)) == pre[t])
@@ -1757,38 +1758,88 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       __syncthreads();
     }
   }
-
-  // ---- ordered emit ----
+  if (tid < 2) {
+    meta[tid] = pre[tid];
+    meta[2 + tid] = want[tid];
+  }
+  // per-list counts, then bases and tie quotas in list (= position) order
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
-    const uint32_t want_t = want[t];
-    if (want_t == 0) continue;
-    const uint32_t T = pre[t], quota = want_t - abv[t];
-    int32_t* outp = t == 0 ? out0 : out1;
-    uint32_t gt = 0, eq = 0;
-    walk([&](uint32_t k, int, uint32_t) {
-      gt += k > T;
-      eq += k == T;
-    });
-    uint32_t tie_all, sel_all;
-    const uint32_t ties_before = block_excl(sh, eq, tie_all);
-    const uint32_t take = quota > ties_before ? min(quota - ties_before, eq) : 0u;
-    uint32_t p = block_excl(sh, gt + take, sel_all);  // output base of this chunk
-    uint32_t tie_rank = 0;
-    walk([&](uint32_t k, int l, uint32_t j) {
-      const bool tie = k == T;
-      if (k > T || (tie && tie_rank < take)) {
-        if (p < want_t) outp[p] = (int32_t)__ldcg(wl.pos + (list0 + l) * wl.seg + j);
-        ++p;
+    if (want[t] == 0) continue;
+    const uint32_t T = pre[t], quota = want[t] - abv[t];
+    for (int l = warp; l < nlists; l += kBigWarps) {
+      uint32_t gt = 0, eq = 0;
+      for (uint32_t e = loff[l] + lane; e < loff[l + 1]; e += 32) {
+        const uint32_t k = in_smem ? skey[e] : __ldcg(wl.key + (list0 + l) * wl.seg + (e - loff[l]));
+        gt += k > T;
+        eq += k == T;
       }
-      tie_rank += tie;
-    });
+      gt = __reduce_add_sync(0xffffffffu, gt);
+      eq = __reduce_add_sync(0xffffffffu, eq);
+      if (lane == 0) {
+        lgt[l] = gt;
+        leq[l] = eq;
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t base = 0, ties_before = 0;
+      for (int l = 0; l < nlists; ++l) {
+        const uint32_t take = quota > ties_before ? min(quota - ties_before, leq[l]) : 0u;
+        meta[4 + t * kMaxWideLists + l] = base;
+        meta[4 + (2 + t) * kMaxWideLists + l] = take;
+        base += lgt[l] + take;
+        ties_before += leq[l];
+      }
+    }
     __syncthreads();
   }
-  for (int i = (int)want0 + tid; i < topk; i += kBigThreads) out0[i] = -1;
-  if (two)
-    for (int i = (int)want1 + tid; i < pool_size; i += kBigThreads) out1[i] = -1;
-  (void)q_seq;
+}
+
+// Emit (the filter's grid, one warp per list): keys > T_t, then ties of T_t up to the
+// list's quota, written at the list's base; CTA 0 of a query writes the -1 padding.
+__global__ void __launch_bounds__(kBigThreads, 1)
+    select_emit_kernel(int32_t pool_size, int32_t topk, int32_t* __restrict__ out_idx,
+                       int32_t* __restrict__ pool_out, WideLists wl) {
+  const int c = blockIdx.x, q = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t list = ((int64_t)q * wl.C + c) * kBigWarps + warp;
+  const int l = c * kBigWarps + warp;
+  const uint32_t* meta = wl.meta + (int64_t)q * kWideMeta;
+  const uint32_t cn = __ldcg(wl.cnt + list);
+  const uint32_t* lk = wl.key + list * wl.seg;
+  const uint32_t* lp = wl.pos + list * wl.seg;
+  const uint32_t lt = (1u << lane) - 1u;
+  const bool two = pool_out != nullptr && pool_size > 0;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const uint32_t want_t = __ldcg(meta + 2 + t);
+    if (want_t == 0) continue;
+    const uint32_t T = __ldcg(meta + t);
+    const uint32_t base = __ldcg(meta + 4 + t * kMaxWideLists + l);
+    const uint32_t take = __ldcg(meta + 4 + (2 + t) * kMaxWideLists + l);
+    int32_t* outp = t == 0 ? out_idx + (int64_t)q * topk : pool_out + (int64_t)q * pool_size;
+    uint32_t tie_run = 0, sel_run = 0;
+    for (uint32_t j0 = 0; j0 < cn; j0 += 32) {
+      const uint32_t j = j0 + lane;
+      const uint32_t k = j < cn ? __ldcg(lk + j) : 0u;
+      const bool tie = j < cn && k == T;
+      const uint32_t tb = __ballot_sync(0xffffffffu, tie);
+      const bool sel = j < cn && (k > T || (tie && tie_run + __popc(tb & lt) < take));
+      const uint32_t sb = __ballot_sync(0xffffffffu, sel);
+      const uint32_t p = base + sel_run + __popc(sb & lt);
+      if (sel && p < want_t) outp[p] = (int32_t)__ldcg(lp + j);
+      tie_run += __popc(tb);
+      sel_run += __popc(sb);
+    }
+  }
+  if (c == 0) {
+    const uint32_t want0 = __ldcg(meta + 2), want1 = __ldcg(meta + 3);
+    for (int i = (int)want0 + tid; i < topk; i += kBigThreads) out_idx[(int64_t)q * topk + i] = -1;
+    if (two)
+      for (int i = (int)want1 + tid; i < pool_size; i += kBigThreads)
+        pool_out[(int64_t)q * pool_size + i] = -1;
+  }
 }
 
 // ------------------------------------------------------------------ launchers -----
@@ -1903,7 +1954,7 @@ size_t wide_select_bytes(int32_t num_q, int32_t n) {
   if (n <= (1 << 18)) return 0;
   const int L = wide_range(n);
   const int64_t C = ((int64_t)n + L - 1) / L;
-  return (size_t)num_q * C * ((size_t)L * 8 + kBigWarps * 4);
+  return (size_t)num_q * (C * ((size_t)L * 8 + kBigWarps * 4) + (size_t)kWideMeta * 4);
 }
 
 cudaError_t launch_select(bool reindex, const uint32_t* ws, int64_t ws_stride, const int32_t* q_seq,
@@ -1925,8 +1976,9 @@ cudaError_t launch_select(bool reindex, const uint32_t* ws, int64_t ws_stride, c
     wl.pos = static_cast<uint32_t*>(wide_ws);
     wl.key = wl.pos + lists;
     wl.cnt = wl.key + lists;
+    wl.meta = wl.cnt + (size_t)num_q * C * kBigWarps;
     const size_t fsmem = offsetof(BigShared, u), bsmem = sizeof(BigShared);
-    cudaError_t e = cudaFuncSetAttribute(select_finish_kernel,
+    cudaError_t e = cudaFuncSetAttribute(select_resolve_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bsmem);
     if (e != cudaSuccess) return e;
     const int32_t P = pool_out ? pool_size : 0;
@@ -1934,8 +1986,10 @@ cudaError_t launch_select(bool reindex, const uint32_t* ws, int64_t ws_stride, c
         ws, ws_stride, q_seq, pg.seq_lens, pg.num_seqs, P, topk, n, ghist, wl);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    select_finish_kernel<<<num_q, kBigThreads, bsmem, s>>>(q_seq, P, topk, out_idx, pool_out,
-                                                           ghist, wl);
+    select_resolve_kernel<<<num_q, kBigThreads, bsmem, s>>>(P, topk, ghist, wl);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    select_emit_kernel<<<dim3(C, num_q), kBigThreads, 0, s>>>(P, topk, out_idx, pool_out, wl);
     return cudaGetLastError();
   }
   // Up to 2^18 keys per query: one CTA per query, no cluster synchronisation (measured on
