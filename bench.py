@@ -649,9 +649,13 @@ def main():
                     choices=["decode_batch", "decode_batch16", "long_context", "ragged", "tiny",
                              "ced_write"])
     ap.add_argument("--e2e-steps", type=int, default=100)
-    ap.add_argument("--cpu-sample", type=int, default=32, help="queries timed on the oracle")
+    ap.add_argument("--cpu-sample", type=int, default=None,
+                    help="queries (decode) or token rows (ced_write) timed on the oracle; "
+                         "default 32 queries / 256 rows, about 10-30 s of CPU work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.cpu_sample is None:
+        args.cpu_sample = 256 if args.workload == "ced_write" else 32
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
