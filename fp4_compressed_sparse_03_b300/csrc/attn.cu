@@ -5,79 +5,83 @@
 // "Reuse Mode": sparse attention runs directly over the inherited top-K entries.
 // MQA over the shared latent: K = V = c_hat (512 channels), 16 query heads.
 //
-// One CTA (8 warps, one per SM) handles one (query, split) pair: up to `split_len`
-// selected entries in tiles of 128 tokens, on the 5th-generation tensor cores:
-//   1. cp.async gathers the tile's 128 x (256 B codes + 32 B scales) into a 2-stage
-//      staging ring (1D bulk copies were measured slower: the copy engine took ~50
-//      cycles per 256-byte row);
-//   2. the warps dequantise the tile into an f16 tile C [128 tokens][512 channels]
-//      laid out as eight 128-byte-swizzled [128][64] chunks (E2M1 x E4M3 is exact in
-//      f16: at most 6 significant bits, magnitudes 2^-10 .. 2688);
-//   3. S^T = C . Q^T: tcgen05.mma M=128 (tokens) x N=16 (heads) x K=512, C K-major,
-//      fp32 accumulator in TMEM;
-//   4. fp32 softmax in the exp2 domain with a lazily moved reference max per head: the
-//      reference only moves (and the TMEM accumulator is rescaled) when a tile's max
-//      exceeds it by more than 2^8, so every weight is at most 2^8;
-//   5. O^T += C^T . P^T: M=128 (channels) x N=16 (heads) x K=128 (tokens) per 128-channel
-//      block, reading the same C tile as an MN-major operand; P^T is f16, and the
-//      normaliser sums the same f16-rounded weights.
-// Steps 5 (tile t) and 2-3 (tile t+1) are pipelined by 128-channel chunk pairs: block
-// j of the P.C product commits its own mbarrier, the next tile's chunk pair j is
-// dequantised as soon as block j is done, and its logit MMAs are issued right after.
-// Q is converted to f16 after a per-query power-of-two prescale (exact for every
-// value within 2^28 of the largest |q|); the scale is undone in the logit factor.
-// Several splits per query are merged by a log-sum-exp combine kernel.
+// One CTA (8 warps) handles one (query, split) pair: up to `split_len` selected entries
+// in tiles of 128 tokens.  Warp w owns latent channels 64 w .. 64 w + 63 for the whole
+// tile, so every code is dequantised exactly once per product, from the staged bytes
+// straight into tensor-core operand registers (E2M1 x E4M3 is exact in f16: at most 6
+// significant bits, magnitudes 2^-10 .. 2688):
+//   1. cp.async gathers the tile's 128 x (256 B codes + 32 B scales) into a 3-stage
+//      ring; codes are laid out [channel slice][row][32 B], and rows that are not
+//      selected (skipped entries, the ragged end of the split) are zero-filled;
+//   2. S^T partial = Q_w . C_w^T over the warp's 64 channels (mma.sync m16n8k16, f16
+//      operands, fp32 accumulation; M = 16 heads, N = 8 tokens per instruction); the
+//      eight partials are summed through shared memory;
+//   3. fp32 softmax in the exp2 domain, 16 threads per head, with a lazily moved
+//      reference max per head: it only moves (and the output accumulators are
+//      rescaled) when a tile's max exceeds it by more than 2^8, so every weight is at
+//      most 2^8; P is rounded to f16 and the normaliser sums the rounded weights;
+//   4. O_w += P . C_w (M = 16 heads, N = the warp's 64 channels, K = 16 tokens per
+//      instruction), with the two-token operand pairs assembled from the same bytes.
+// Q is converted to f16 after a per-query power-of-two prescale (exact for every value
+// within 2^28 of the largest |q|); the scale is undone in the logit factor.  Several
+// splits per query are merged by a log-sum-exp combine kernel.
+//
+// A 128-token tile holds only 2 M multiply-adds per product, so the kernel is bound by
+// the dequantisation arithmetic and per-tile latency, not by tensor throughput; operands
+// built in registers avoid writing a dequantised f16 tile to shared memory and reading
+// it back for each product.
+#include <algorithm>
 #include <cstddef>
 
-#include "tcgen05.cuh"
+#include "common.cuh"
 
 namespace csa2 {
 
-constexpr int kAttnThreads = 256;   // 8 warps
+constexpr int kAttnThreads = 256;  // 8 warps
 constexpr int kAttnWarps = kAttnThreads / 32;
-constexpr int kTile = 128;           // tokens per tile = UMMA M
-constexpr int kRawStages = 2;        // cp.async staging ring
-constexpr int kMaxSplit = 1024;      // selected entries per CTA at most
-constexpr int kChunkBytes = kTile * 128;        // one 64-channel chunk of C: 16 KB
-constexpr int kCBytes = (kDkv / 64) * kChunkBytes;  // 128 KB
-constexpr int kQChunk = kHq * 128;              // one 64-channel chunk of Q: 2 KB
-constexpr int kQBytes = (kDkv / 64) * kQChunk;  // 16 KB
-constexpr int kPBytes = (kTile / 64) * kQChunk; // P^T [16 heads][128 tokens]: 4 KB
-constexpr int kRawCodeBytes = kTile * kCodeRow;             // 32 KB
-constexpr int kRawBytes = kRawCodeBytes + kTile * kScaleRow;  // 36 KB
-constexpr uint32_t kTmemCols = 128;  // S^T at columns 0..15, O^T blocks at 32 + 16 j
-constexpr uint32_t kOCol = 32;
-constexpr float kRescaleGap = 8.0f;  // log2 units
+constexpr int kTile = 128;         // tokens per tile
+constexpr int kStages = 3;         // cp.async ring: two tiles in flight ahead of the current one
+constexpr int kMaxSplit = 1024;    // selected entries per CTA at most
+constexpr int kSliceCh = kDkv / kAttnWarps;           // 64 channels per warp
+constexpr int kSliceBytes = kSliceCh / 2;             // 32 code bytes per row and warp
+constexpr int kSliceStride = kTile * kSliceBytes;     // 4 KB per channel slice of a stage
+constexpr int kStageCodes = kTile * kCodeRow;         // 32 KB: [slice][row][32 B]
+constexpr int kScaleHalf = kTile * 16;                // scales: [half][row][16 B]
+constexpr int kStageBytes = kStageCodes + 2 * kScaleHalf;  // 36 KB
+constexpr int kRedStride = kTile + 8;   // floats per (warp, head) row of S partials
+constexpr int kOStride = kDkv + 4;      // floats per head row of the output staging
+constexpr float kRescaleGap = 8.0f;     // log2 units
 
-constexpr int kPairs = kDkv / 128;  // 128-channel chunk pairs = O^T blocks
+static_assert(kSliceCh == 64 && kAttnThreads == 2 * kTile, "layout assumes 8 warps, 128-token tiles");
 
-struct AttnCtl {
-  alignas(16) float red_max[kHq][4];  // read back as float4 per head
-  alignas(16) float red_sum[kHq][4];
-  uint64_t bar_s, bar_fin;
-  uint64_t bar_pv[kPairs];  // block j of the current tile's P.C product (and all before it)
-  uint32_t tmem;
-  volatile int abort;
+struct AttnSmem {
+  unsigned char stage[kStages][kStageBytes];
+  float red[kAttnWarps][kHq][kRedStride];  // S^T partials; reused to stage the output
+  uint16_t p[kHq][kTile];                  // P (f16): 16-byte units XOR-swizzled by head
+  float alpha[kHq];
+  float m_fin[kHq], l_fin[kHq];
   uint32_t qmax[kAttnWarps];
   int32_t slot[kMaxSplit];  // physical row of each selected entry, -1 if skipped
 };
-static_assert(offsetof(AttnCtl, red_max) % 16 == 0 && offsetof(AttnCtl, red_sum) % 16 == 0,
-              "per-head reductions are read as float4");
-static_assert(offsetof(AttnCtl, bar_s) % 8 == 0 && offsetof(AttnCtl, bar_pv) % 8 == 0,
-              "mbarriers need 8-byte alignment");
-constexpr size_t kAttnSmem = 1024 + kCBytes + kQBytes + kPBytes + kRawStages * kRawBytes + sizeof(AttnCtl);
+static_assert(offsetof(AttnSmem, red) % 16 == 0 && offsetof(AttnSmem, p) % 16 == 0,
+              "vector accesses need 16-byte alignment");
+static_assert(kHq * kOStride <= kAttnWarps * kHq * kRedStride, "output staging fits the partials");
+constexpr size_t kAttnSmem = sizeof(AttnSmem);
 static_assert(kAttnSmem <= 232448, "sparse attention needs more than 227 KB of shared memory");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src));
+// 16-byte cp.async; `valid` false writes 16 zero bytes without reading global memory.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N));
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // 2^x by the MUFU ex2 instruction (flushes subnormal results to zero; 2^-inf = 0).
@@ -87,12 +91,35 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Bounded wait on an mbarrier phase that ignores the CTA's abort flag (used to drain).
-__device__ __forceinline__ bool mbar_drain(uint64_t* b, uint32_t parity, uint32_t limit) {
-  for (uint32_t i = 0; i < limit; ++i)
-    if (mbar_try(b, parity)) return true;
-  return false;
+// Two E4M3 bytes (low byte -> low half) -> f16x2, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)(two & 0xFFFFu)));
+  return h2;
 }
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// D += A . B, m16n8k16, f16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+// Stage position of tile row r: rows 4..7 of every group of 8 are stored in reverse
+// order, so that both the S-phase reads (8 consecutive rows, 8 bytes each) and the
+// O-phase reads (rows 2i or 2i + 1, i = 0..3, of a group) hit distinct banks.
+__device__ __forceinline__ int stage_row(int r) { return r ^ (((r >> 2) & 1) * 3); }
 
 struct AttnGeom {
   const int32_t* seq_lens;
@@ -102,120 +129,22 @@ struct AttnGeom {
   int32_t num_seqs;
 };
 
-// Gather the codes and scales of the tile starting at local entry `e0` into `stage`:
-// thread -> row tid / 2; the two threads of a row take the 16-byte parts of even and odd
-// index (16 code parts, then 2 scale parts), so each pair of lanes moves 32 contiguous bytes.
-// Codes are staged chunk-pair-major, [pair j][row][64 B] (code bytes 64 j .. 64 j + 63 of
-// each row), so that the dequantiser's four rows per load instruction are contiguous;
-// scales are staged [row][32 B].
+// Gather the tile starting at local entry `e0`: thread -> row tid / 2, the two threads
+// of a row take the two 16-byte halves of each warp's 32-byte code slice, and one
+// 16-byte half of the row's scales.
 __device__ __forceinline__ void issue_tile(unsigned char* stage, int e0, int ecount,
                                            const int32_t* slot, const uint8_t* __restrict__ codes,
                                            const uint8_t* __restrict__ scales) {
   const int r = threadIdx.x >> 1, h = threadIdx.x & 1;
   const int e = e0 + r;
   const int32_t sl = e < ecount ? slot[e] : -1;
-  if (sl < 0) return;
-  const uint8_t* src = codes + (int64_t)sl * kCodeRow;
-  unsigned char* dst = stage + r * 64;
+  const bool ok = sl >= 0;
+  const uint8_t* src = codes + (ok ? (int64_t)sl * kCodeRow : 0);
+  unsigned char* dst = stage + stage_row(r) * kSliceBytes + 16 * h;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int part = 2 * j + h;  // bytes 16 part .. +15 = pair part / 4, offset 16 (part % 4)
-    cp_async16(dst + (part >> 2) * (kTile * 64) + 16 * (part & 3), src + 16 * part);
-  }
-  cp_async16(stage + kRawCodeBytes + r * kScaleRow + 16 * h, scales + (int64_t)sl * kScaleRow + 16 * h);
-}
-static_assert(kAttnThreads == 2 * kTile, "issue_tile maps two threads to each row of a tile");
-
-// Staged tile -> chunks 2j, 2j + 1 (channels 128 j .. 128 j + 127) of the f16 tile C.
-// Lane -> (row sub-index lane / 8, scale group 8 j + lane % 8 = 16 channels = code bytes
-// 64 j + 8 (lane % 8) .. +7); warp w takes rows 4 (w + 8 i) + lane / 8, i = 0..3, so each
-// 8-byte load instruction reads 256 contiguous staged bytes.  The
-// group's 16 channels are units 2 (lane % 4), +1 of chunk 2 j + (lane % 8) / 4, stored at
-// unit u ^ (row % 8); lanes of the odd chunk store their two units in the opposite
-// order, so each quarter-warp store phase covers all eight units of a 128-byte row
-// segment.  All loads are issued before any store.  Invalid rows become zeros.
-__device__ __forceinline__ void dequant_pair(const unsigned char* stage, unsigned char* Cs, int j,
-                                             int e0, int ecount, const int32_t* slot, int warp,
-                                             int lane) {
-  constexpr int kIter = kTile / (4 * kAttnWarps);  // 4
-  const unsigned char* rc = stage;
-  const unsigned char* rs = stage + kRawCodeBytes;
-  const int l8 = lane & 7, rsub = lane >> 3;
-  const int ch = 2 * j + (l8 >> 2), u0 = 2 * (l8 & 3), swap = l8 >> 2;
-  unsigned char* cbase = Cs + ch * kChunkBytes;
-  uint2 cw[kIter];
-  uint32_t sb[kIter];
-  bool ok[kIter];
-#pragma unroll
-  for (int i = 0; i < kIter; ++i) {
-    const int r = 4 * (warp + kAttnWarps * i) + rsub;
-    const int e = e0 + r;
-    ok[i] = e < ecount && slot[e] >= 0;
-    cw[i] = *reinterpret_cast<const uint2*>(rc + j * (kTile * 64) + r * 64 + 8 * l8);
-    sb[i] = rs[r * kScaleRow + 8 * j + l8];
-  }
-#pragma unroll
-  for (int i = 0; i < kIter; ++i) {
-    const int r = 4 * (warp + kAttnWarps * i) + rsub;
-    uint32_t hv[8];
-    if (ok[i]) {
-      uint32_t s2;
-      const uint16_t sp = (uint16_t)(sb[i] | (sb[i] << 8));
-      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"(sp));
-      const uint32_t w[2] = {cw[i].x, cw[i].y};
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t c2 = e2m1x2_to_f16x2((w[k >> 2] >> (8 * (k & 3))) & 0xFFu);
-        const __half2 x = __hmul2(*reinterpret_cast<const __half2*>(&c2),
-                                  *reinterpret_cast<const __half2*>(&s2));
-        hv[k] = *reinterpret_cast<const uint32_t*>(&x);
-      }
-    } else {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) hv[k] = 0u;
-    }
-    unsigned char* row = cbase + r * 128;
-    const int x7 = r & 7;
-    const uint4 a = make_uint4(hv[0], hv[1], hv[2], hv[3]), c = make_uint4(hv[4], hv[5], hv[6], hv[7]);
-    if (swap) {
-      *reinterpret_cast<uint4*>(row + (((u0 + 1) ^ x7) << 4)) = c;
-      *reinterpret_cast<uint4*>(row + ((u0 ^ x7) << 4)) = a;
-    } else {
-      *reinterpret_cast<uint4*>(row + ((u0 ^ x7) << 4)) = a;
-      *reinterpret_cast<uint4*>(row + (((u0 + 1) ^ x7) << 4)) = c;
-    }
-  }
-}
-
-// Butterfly over the warp: lane l ends with the reduction, over all 32 lanes, of value
-// (l >> 2) & 7 of the 8 each lane holds.
-template <bool kMax>
-__device__ __forceinline__ float warp_reduce8(float (&v)[8], int lane) {
-  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const bool hi = lane & 16;
-    const float send = hi ? v[i] : v[i + 4];
-    const float keep = hi ? v[i + 4] : v[i];
-    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const bool hi = lane & 8;
-    const float send = hi ? v[i] : v[i + 2];
-    const float keep = hi ? v[i + 2] : v[i];
-    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
-  }
-  {
-    const bool hi = lane & 4;
-    const float send = hi ? v[0] : v[1];
-    const float keep = hi ? v[1] : v[0];
-    v[0] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
-  }
-  float x = v[0];
-  x = op(x, __shfl_xor_sync(0xffffffffu, x, 2));
-  x = op(x, __shfl_xor_sync(0xffffffffu, x, 1));
-  return x;
+  for (int w = 0; w < kAttnWarps; ++w) cp_async16(dst + w * kSliceStride, src + 32 * w + 16 * h, ok);
+  cp_async16(stage + kStageCodes + h * kScaleHalf + stage_row(r) * 16,
+             scales + (ok ? (int64_t)sl * kScaleRow : 0) + 16 * h, ok);
 }
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -224,16 +153,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                        AttnGeom g, const int32_t* __restrict__ q_seq, int32_t topk, int32_t split_len,
                        float softmax_scale, float* __restrict__ out, float* __restrict__ lse,
                        float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* st) {
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* Cs = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* Qs = Cs + kCBytes;
-  unsigned char* Ps = Qs + kQBytes;
-  unsigned char* raw = Ps + kPBytes;
-  AttnCtl& ctl = *reinterpret_cast<AttnCtl*>(raw + kRawStages * kRawBytes);
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  AttnSmem& sm = *reinterpret_cast<AttnSmem*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int sp = warp & 3;   // TMEM sub-partition: lanes 32 sp .. 32 sp + 31
-  const int hg = warp >> 2;  // heads 8 hg .. 8 hg + 7 in the softmax; O blocks 2 hg, 2 hg + 1
+  const int gq = lane >> 2, iq = lane & 3;  // mma fragment: row group, column pair
   const int qi = blockIdx.y, split = blockIdx.x, nsplit = gridDim.x;
   const int jbeg = split * split_len;
   const int ecount = max(0, min(topk, jbeg + split_len) - jbeg);
@@ -248,13 +171,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   const int32_t* idx_q = idx + (int64_t)qi * topk + jbeg;
 
-  // Q is loaded first: its latency overlaps the index and page-table loads below
-  const uint4* qv = reinterpret_cast<const uint4*>(q + (int64_t)qi * kHq * kDkv);
+  // Q first (its latency overlaps the index and page-table loads): heads gq and gq + 8,
+  // channels 64 warp + 16 iq .. + 15 -- the operand channels of this thread
+  const uint4* qg = reinterpret_cast<const uint4*>(q + (int64_t)qi * kHq * kDkv + gq * kDkv +
+                                                   warp * kSliceCh + 16 * iq);
   uint4 qr[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) qr[k] = __ldg(qv + tid + kAttnThreads * k);
+  qr[0] = __ldg(qg);
+  qr[1] = __ldg(qg + 1);
+  qr[2] = __ldg(qg + 8 * kDkv * 2 / 16);  // head gq + 8
+  qr[3] = __ldg(qg + 8 * kDkv * 2 / 16 + 1);
 
-  // ---- resolve the selected entries to physical rows: the first two tiles first ----
+  // ---- resolve the selected entries to physical rows: the first tiles first ----
   auto resolve = [&](int e) {
     const int s = __ldg(idx_q + e);
     int32_t slot = -1;
@@ -265,33 +192,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     } else if (s != -1) {
       report(st, CSA2_DEV_BAD_INDEX);
     }
-    ctl.slot[e] = slot;
+    sm.slot[e] = slot;
   };
-  const int e_first = min(ecount, kRawStages * kTile);
+  const int e_first = min(ecount, (kStages - 1) * kTile);
   for (int e = tid; e < e_first; e += kAttnThreads) resolve(e);
-  if (tid == 0) {
-    mbar_init(&ctl.bar_s, 1);
-    for (int j = 0; j < kPairs; ++j) mbar_init(&ctl.bar_pv[j], 1);
-    mbar_init(&ctl.bar_fin, 1);
-    ctl.abort = 0;
-    mbar_fence_init();
-  }
-  if (warp == 0) tmem_alloc(&ctl.tmem, kTmemCols);
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = ctl.tmem;
-
-  // start the first gathers, then resolve the remaining entries while they land
 #pragma unroll
-  for (int i = 0; i < kRawStages; ++i) {
-    if (i < ntiles) issue_tile(raw + i * kRawBytes, i * kTile, ecount, ctl.slot, codes, scales);
+  for (int i = 0; i < kStages - 1; ++i) {
+    if (i < ntiles) issue_tile(sm.stage[i], i * kTile, ecount, sm.slot, codes, scales);
     cp_async_commit();
   }
   for (int e = e_first + tid; e < ecount; e += kAttnThreads) resolve(e);
 
-  // ---- Q: max |q| -> power-of-two prescale -> f16 chunks (the barrier below also
-  // publishes the remaining slots) ----
+  // ---- Q: max |q| -> power-of-two prescale -> f16 operand fragments (the barrier
+  // below also publishes the remaining slots) ----
   uint32_t mx = 0;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -300,11 +214,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int e = 0; e < 4; ++e) mx = max(mx, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
   }
   mx = __reduce_max_sync(0xffffffffu, mx);
-  if (lane == 0) ctl.qmax[warp] = mx;
+  if (lane == 0) sm.qmax[warp] = mx;
   __syncthreads();
   uint32_t mxa = 0;
 #pragma unroll
-  for (int w = 0; w < kAttnWarps; ++w) mxa = max(mxa, ctl.qmax[w]);
+  for (int w = 0; w < kAttnWarps; ++w) mxa = max(mxa, sm.qmax[w]);
   int sh = 0;
   if (mxa != 0) {
     const int e = (int)((mxa >> 7) & 0xFF) - 127;  // bf16 exponent of max |q|
@@ -313,214 +227,199 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const float pre = __uint_as_float((uint32_t)(127 + sh) << 23);   // 2^sh
   const float post = __uint_as_float((uint32_t)(127 - sh) << 23);  // 2^-sh
   const float kq = softmax_scale * 1.4426950408889634f * post;  // logits in the exp2 domain
+  // k-step kk covers channels 16 iq + 4 kk .. + 3 of this thread: a0/a1 the first pair
+  // (heads gq / gq + 8), a2/a3 the second -- the byte order of the staged codes
+  uint32_t qa[4][4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int i = tid + kAttnThreads * k;  // 8 channels 8i .. 8i + 7
-    const int hd = (8 * i) / kDkv, c = (8 * i) % kDkv;
-    const uint32_t w[4] = {qr[k].x, qr[k].y, qr[k].z, qr[k].w};
-    uint32_t hv[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const __half2 h = __floats2half2_rn(bf16lo(w[e]) * pre, bf16hi(w[e]) * pre);
-      hv[e] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-    const int u = (c & 63) >> 3;
-    *reinterpret_cast<uint4*>(Qs + (c >> 6) * kQChunk + hd * 128 + ((u ^ (hd & 7)) << 4)) =
-        make_uint4(hv[0], hv[1], hv[2], hv[3]);
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t wl = (&qr[j >> 2].x)[j & 3], wh = (&qr[2 + (j >> 2)].x)[j & 3];
+    const __half2 hl = __floats2half2_rn(bf16lo(wl) * pre, bf16hi(wl) * pre);
+    const __half2 hh = __floats2half2_rn(bf16lo(wh) * pre, bf16hi(wh) * pre);
+    qa[j >> 1][2 * (j & 1)] = *reinterpret_cast<const uint32_t*>(&hl);
+    qa[j >> 1][2 * (j & 1) + 1] = *reinterpret_cast<const uint32_t*>(&hh);
   }
-  fence_proxy_async_smem();
 
-  // per-head reference max (log2 units) and normaliser, identical in every thread
-  float m_used[kHq], l_run[kHq];
+  // softmax ownership: thread -> head sh_h, tokens 4 sk .. + 3 and 64 + 4 sk .. + 3
+  const int sh_h = tid >> 4, sk = tid & 15;
+  float m_ref = -INFINITY, l_run = 0.0f;
+  float oacc[8][4];
 #pragma unroll
-  for (int h = 0; h < kHq; ++h) {
-    m_used[h] = -INFINITY;
-    l_run[h] = 0.0f;
-  }
-  const uint32_t idesc_s = umma_idesc_f16(kTile, kHq, false, false, false);
-  const uint32_t idesc_o = umma_idesc_f16(128, kHq, false, true, false);
-  const uint32_t cs_addr = smem_u32(Cs), qs_addr = smem_u32(Qs), ps_addr = smem_u32(Ps);
-  const int tt = 32 * sp + lane;  // this thread's token row of the S tile
+  for (int n = 0; n < 8; ++n) oacc[n][0] = oacc[n][1] = oacc[n][2] = oacc[n][3] = 0.0f;
+  const uint32_t p_base = smem_u32(&sm.p[0][0]);
+  const int lrow = (lane & 7) + 8 * ((lane >> 3) & 1), lhi = lane >> 4;  // ldmatrix source rows
 
-  // Build C for tile u from its staged rows, chunk pair by chunk pair, issuing the logit
-  // MMAs of each pair as soon as it is written.  For u > 0, pair j is overwritten only
-  // after block j of tile u - 1's P.C product has completed.  Returns false on abort.
-  auto build_tile = [&](int u) -> bool {
-    unsigned char* stage = raw + (u % kRawStages) * kRawBytes;
-    if (u > 0) {  // tile u + 1 goes into the stage tile u - 1 has released
-      if (u + 1 < ntiles)
-        issue_tile(raw + ((u + 1) % kRawStages) * kRawBytes, (u + 1) * kTile, ecount, ctl.slot,
-                   codes, scales);
+  for (int t = 0; t < ntiles; ++t) {
+    cp_async_wait<kStages - 2>();  // this thread's copies of tile t have landed
+    __syncthreads();               // everyone's; and every warp is done with tile t - 1
+    {
+      const int tn = t + kStages - 1;
+      if (tn < ntiles) issue_tile(sm.stage[tn % kStages], tn * kTile, ecount, sm.slot, codes, scales);
       cp_async_commit();
     }
-    cp_async_wait<1>();  // every group but the newest has landed: tile u is staged
-    const uint32_t par = (uint32_t)((u - 1) & 1);
-    if (tid == 0 && u > 0) (void)mbar_wait(&ctl.abort, &ctl.bar_pv[0], par, st);
+    const unsigned char* cs = sm.stage[t % kStages] + warp * kSliceStride;
+    const unsigned char* ss = sm.stage[t % kStages] + kStageCodes + (warp >> 2) * kScaleHalf + 4 * (warp & 3);
+
+    // ---- S^T partial over this warp's channels: 16 n-tiles of 8 tokens ----
+#pragma unroll 4
+    for (int n = 0; n < kTile / 8; ++n) {
+      const int r = stage_row(8 * n + gq);
+      const uint2 cw = *reinterpret_cast<const uint2*>(cs + r * kSliceBytes + 8 * iq);
+      const uint32_t sb = ss[r * 16 + iq];  // one scale: these 16 channels are one group
+      const uint32_t s2 = e4m3x2_to_f16x2(sb | (sb << 8));
+      uint32_t bf[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        bf[k] = hmul2(e2m1x2_to_f16x2(((k < 4 ? cw.x : cw.y) >> (8 * (k & 3))) & 0xFFu), s2);
+      float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) mma16816(c, qa[kk], bf[2 * kk], bf[2 * kk + 1]);
+      *reinterpret_cast<float2*>(&sm.red[warp][gq][8 * n + 2 * iq]) = make_float2(c[0], c[1]);
+      *reinterpret_cast<float2*>(&sm.red[warp][gq + 8][8 * n + 2 * iq]) = make_float2(c[2], c[3]);
+    }
     __syncthreads();
-    if (ctl.abort) return false;
-    for (int j = 0; j < kPairs; ++j) {
-      dequant_pair(stage, Cs, j, u * kTile, ecount, ctl.slot, warp, lane);
-      fence_proxy_async_smem();
-      if (tid == 0 && u > 0 && j + 1 < kPairs)
-        (void)mbar_wait(&ctl.abort, &ctl.bar_pv[j + 1], par, st);
-      __syncthreads();
-      if (ctl.abort) return false;
-      if (tid == 0) {
-        tc_fence_after();
+
+    // ---- softmax ----
+    {
+      float s[8];
+      {
+        const float4 a = *reinterpret_cast<const float4*>(&sm.red[0][sh_h][4 * sk]);
+        const float4 c = *reinterpret_cast<const float4*>(&sm.red[0][sh_h][64 + 4 * sk]);
+        s[0] = a.x; s[1] = a.y; s[2] = a.z; s[3] = a.w;
+        s[4] = c.x; s[5] = c.y; s[6] = c.z; s[7] = c.w;
+      }
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          const int kc = 2 * j + c2;
+      for (int w = 1; w < kAttnWarps; ++w) {
+        const float4 a = *reinterpret_cast<const float4*>(&sm.red[w][sh_h][4 * sk]);
+        const float4 c = *reinterpret_cast<const float4*>(&sm.red[w][sh_h][64 + 4 * sk]);
+        s[0] += a.x; s[1] += a.y; s[2] += a.z; s[3] += a.w;
+        s[4] += c.x; s[5] += c.y; s[6] += c.z; s[7] += c.w;
+      }
+      float mt = -INFINITY;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_f16(tmem, umma_desc_sw128(cs_addr + kc * kChunkBytes, 16, 1024) + 2 * kk,
-                     umma_desc_sw128(qs_addr + kc * kQChunk, 16, 1024) + 2 * kk, idesc_s,
-                     (kc | kk) != 0 ? 1u : 0u);
+      for (int j = 0; j < 8; ++j) {
+        const int e = t * kTile + (j < 4 ? 4 * sk + j : 64 + 4 * sk + j - 4);
+        const bool valid = e < ecount && sm.slot[e] >= 0;
+        s[j] = valid ? s[j] * kq : -INFINITY;
+        mt = fmaxf(mt, s[j]);
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+      float mn = m_ref;
+      if (m_ref == -INFINITY || mt > m_ref + kRescaleGap) mn = fmaxf(m_ref, mt);
+      const float alpha = (mn != m_ref) ? ex2(m_ref - mn) : 1.0f;
+      m_ref = mn;
+      const float mh = (m_ref == -INFINITY) ? 0.0f : m_ref;  // no valid entry yet: all s are -inf
+      uint32_t pw[4];
+      float psum = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const __half2 ph = __floats2half2_rn(ex2(s[2 * j] - mh), ex2(s[2 * j + 1] - mh));
+        pw[j] = *reinterpret_cast<const uint32_t*>(&ph);
+        psum += __low2float(ph) + __high2float(ph);
+      }
+      unsigned char* prow = reinterpret_cast<unsigned char*>(&sm.p[sh_h][0]);
+      const int x7 = sh_h & 7;
+      *reinterpret_cast<uint2*>(prow + (((sk >> 1) ^ x7) << 4) + 8 * (sk & 1)) = make_uint2(pw[0], pw[1]);
+      *reinterpret_cast<uint2*>(prow + (((8 + (sk >> 1)) ^ x7) << 4) + 8 * (sk & 1)) =
+          make_uint2(pw[2], pw[3]);
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
+      l_run = l_run * alpha + psum;
+      if (sk == 0) sm.alpha[sh_h] = alpha;
+    }
+    __syncthreads();
+
+    // ---- O += P . C over this warp's channels ----
+    {
+      const float a_lo = sm.alpha[gq], a_hi = sm.alpha[gq + 8];
+      if (a_lo != 1.0f || a_hi != 1.0f) {
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+          oacc[n][0] *= a_lo;
+          oacc[n][1] *= a_lo;
+          oacc[n][2] *= a_hi;
+          oacc[n][3] *= a_hi;
         }
       }
     }
-    if (tid == 0) umma_commit(&ctl.bar_s);
-    return true;
-  };
-
-  bool ok = ntiles == 0 || build_tile(0);
-  for (int t = 0; ok && t < ntiles; ++t) {
-    // ---- wait for S^T of tile t ----
-    if (tid == 0) (void)mbar_wait(&ctl.abort, &ctl.bar_s, (uint32_t)(t & 1), st);
-    __syncthreads();
-    if (ctl.abort) break;
-    tc_fence_after();
-
-    // ---- softmax: thread -> token tt, heads 8 hg .. 8 hg + 7 ----
-    uint32_t sr[8];
-    tmem_ld8(tmem + ((uint32_t)(32 * sp) << 16) + (uint32_t)(8 * hg), sr);
-    const int e = t * kTile + tt;
-    const bool valid = e < ecount && ctl.slot[e] >= 0;
-    float s[8], v[8];
+#pragma unroll 2
+    for (int ks = 0; ks < kTile / 16; ++ks) {
+      uint32_t a[4];
+      const int unit = 2 * ks + lhi;
+      ldmatrix_x4(a, p_base + lrow * (kTile * 2) + ((unit ^ (lrow & 7)) << 4));
+      const int t0 = 16 * ks + 2 * iq;
+      const int r0 = stage_row(t0), r1 = stage_row(t0 + 1), r8 = stage_row(t0 + 8),
+                r9 = stage_row(t0 + 9);
+      const uint32_t x0 = *reinterpret_cast<const uint32_t*>(cs + r0 * kSliceBytes + 4 * gq);
+      const uint32_t x1 = *reinterpret_cast<const uint32_t*>(cs + r1 * kSliceBytes + 4 * gq);
+      const uint32_t x8 = *reinterpret_cast<const uint32_t*>(cs + r8 * kSliceBytes + 4 * gq);
+      const uint32_t x9 = *reinterpret_cast<const uint32_t*>(cs + r9 * kSliceBytes + 4 * gq);
+      const int sg = gq >> 1;  // scale group of this thread's channels 8 gq .. 8 gq + 7
+      const uint32_t s01 = e4m3x2_to_f16x2(ss[r0 * 16 + sg] | ((uint32_t)ss[r1 * 16 + sg] << 8));
+      const uint32_t s89 = e4m3x2_to_f16x2(ss[r8 * 16 + sg] | ((uint32_t)ss[r9 * 16 + sg] << 8));
+      // byte p of lo: the even channel of code byte 4 gq + p for the two tokens (first
+      // token in the low nibble); hi: the odd channel
+      const uint32_t lo01 = (x0 & 0x0F0F0F0Fu) | ((x1 << 4) & 0xF0F0F0F0u);
+      const uint32_t hi01 = ((x0 >> 4) & 0x0F0F0F0Fu) | (x1 & 0xF0F0F0F0u);
+      const uint32_t lo89 = (x8 & 0x0F0F0F0Fu) | ((x9 << 4) & 0xF0F0F0F0u);
+      const uint32_t hi89 = ((x8 >> 4) & 0x0F0F0F0Fu) | (x9 & 0xF0F0F0F0u);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      s[i] = valid ? __uint_as_float(sr[i]) * kq : -INFINITY;
-      v[i] = s[i];
-    }
-    const int hl = (lane >> 2) & 7;
-    const float wmax = warp_reduce8<true>(v, lane);
-    if ((lane & 3) == 0) ctl.red_max[8 * hg + hl][sp] = wmax;
-    __syncthreads();
-    float alpha[kHq];
-    bool moved = false;
-#pragma unroll
-    for (int h = 0; h < kHq; ++h) {
-      const float4 r = *reinterpret_cast<const float4*>(ctl.red_max[h]);
-      const float mt = fmaxf(fmaxf(r.x, r.y), fmaxf(r.z, r.w));
-      const float mu = m_used[h];
-      float mn = mu;
-      if (mu == -INFINITY || mt > mu + kRescaleGap) mn = fmaxf(mu, mt);
-      alpha[h] = 1.0f;
-      if (mn != mu) {  // uniform: every thread holds the same reference maxima
-        alpha[h] = ex2(mu - mn);
-        moved = true;
-      }
-      m_used[h] = mn;
-    }
-    const int tk = tt & 63, pu = tk >> 3;
-    unsigned char* prow = Ps + (tt >> 6) * kQChunk;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float mh = hg ? m_used[8 + i] : m_used[i];
-      if (mh == -INFINITY) mh = 0.0f;  // no valid entry yet: every s is -inf as well
-      const __half ph = __float2half_rn(ex2(s[i] - mh));  // 2^-inf = 0 for skipped entries
-      *reinterpret_cast<__half*>(prow + (8 * hg + i) * 128 + ((pu ^ i) << 4) + (tk & 7) * 2) = ph;
-      v[i] = __half2float(ph);
-    }
-    const float wsum = warp_reduce8<false>(v, lane);
-    if ((lane & 3) == 0) ctl.red_sum[8 * hg + hl][sp] = wsum;
-    if (moved && t > 0) {  // move the accumulated O^T to the new reference
-      uint32_t o[32];
-      const uint32_t ta = tmem + ((uint32_t)(32 * sp) << 16) + kOCol + (uint32_t)(32 * hg);
-      tmem_ld32(ta, o);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha[i & 15]);
-      tmem_st32(ta, o);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-#pragma unroll
-    for (int h = 0; h < kHq; ++h) {
-      const float4 r = *reinterpret_cast<const float4*>(ctl.red_sum[h]);
-      l_run[h] = l_run[h] * alpha[h] + ((r.x + r.y) + (r.z + r.w));
-    }
-
-    // ---- O^T += C^T . P^T, one 128-channel block at a time, one barrier per block ----
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int j = 0; j < kPairs; ++j) {
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_f16(tmem + kOCol + 16 * j,
-                   umma_desc_sw128(cs_addr + 2 * j * kChunkBytes + kk * 2048, kChunkBytes, 1024),
-                   umma_desc_sw128(ps_addr + (kk >> 2) * kQChunk, 16, 1024) + 2 * (kk & 3),
-                   idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&ctl.bar_pv[j]);
+      for (int p = 0; p < 4; ++p) {
+        mma16816(oacc[2 * p], a, hmul2(e2m1x2_to_f16x2((lo01 >> (8 * p)) & 0xFFu), s01),
+                 hmul2(e2m1x2_to_f16x2((lo89 >> (8 * p)) & 0xFFu), s89));
+        mma16816(oacc[2 * p + 1], a, hmul2(e2m1x2_to_f16x2((hi01 >> (8 * p)) & 0xFFu), s01),
+                 hmul2(e2m1x2_to_f16x2((hi89 >> (8 * p)) & 0xFFu), s89));
       }
     }
-    if (t + 1 < ntiles) ok = build_tile(t + 1);
   }
-  cp_async_wait<0>();
-  if (tid == 0) {
-    if (ntiles > 0 && !ctl.abort)
-      (void)mbar_wait(&ctl.abort, &ctl.bar_pv[kPairs - 1], (uint32_t)((ntiles - 1) & 1), st);
-    // every MMA this thread issued has completed before TMEM is read or released
-    umma_commit(&ctl.bar_fin);
-    (void)mbar_drain(&ctl.bar_fin, 0, 1u << 20);
+  cp_async_wait<0>();  // only empty groups remain; drained before the stages are reused
+  __syncthreads();     // every warp is done with the partials and P
+
+  // ---- epilogue: stage the 16 x 512 output through shared memory ----
+  // n-tile 2 p + hb, column c <-> channel 64 warp + 8 c + 2 p + hb
+  float* ob = &sm.red[0][0][0];
+#pragma unroll
+  for (int n = 0; n < 8; ++n) {
+    const int ch = warp * kSliceCh + 16 * iq + 2 * (n >> 1) + (n & 1);
+    ob[gq * kOStride + ch] = oacc[n][0];
+    ob[gq * kOStride + ch + 8] = oacc[n][1];
+    ob[(gq + 8) * kOStride + ch] = oacc[n][2];
+    ob[(gq + 8) * kOStride + ch + 8] = oacc[n][3];
+  }
+  if (sk == 0) {
+    sm.m_fin[sh_h] = m_ref;
+    sm.l_fin[sh_h] = l_run;
   }
   __syncthreads();
-  tc_fence_after();
-  const bool have = ntiles > 0 && !ctl.abort;
-
-  // ---- epilogue: thread -> channel 128 j + 32 sp + lane of blocks j = 2 hg, 2 hg + 1 ----
-  uint32_t o[32];
-  if (have) {
-    tmem_ld32(tmem + ((uint32_t)(32 * sp) << 16) + kOCol + (uint32_t)(32 * hg), o);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) o[i] = 0u;
-  }
   if (nsplit == 1) {
-    float* ob = out + (int64_t)qi * kHq * kDkv;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int h = i & 15, ch = 128 * (2 * hg + (i >> 4)) + 32 * sp + lane;
-      const float l = l_run[h];
-      ob[h * kDkv + ch] = l > 0.f ? __uint_as_float(o[i]) / l : 0.f;
+    float* obase = out + (int64_t)qi * kHq * kDkv;
+    for (int f = tid; f < kHq * kDkv / 4; f += kAttnThreads) {
+      const int h = f / (kDkv / 4), c4 = f % (kDkv / 4);
+      const float l = sm.l_fin[h];
+      float4 v = *reinterpret_cast<const float4*>(ob + h * kOStride + 4 * c4);
+      if (l > 0.0f) {
+        v.x /= l; v.y /= l; v.z /= l; v.w /= l;
+      } else {
+        v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+      reinterpret_cast<float4*>(obase + h * kDkv)[c4] = v;
     }
-    if (lse != nullptr) {
-#pragma unroll
-      for (int h = 0; h < kHq; ++h)
-        if (tid == h)
-          lse[(int64_t)qi * kHq + h] =
-              l_run[h] > 0.f ? m_used[h] * 0.6931471805599453f + logf(l_run[h]) : -INFINITY;
+    if (lse != nullptr && tid < kHq) {
+      const float l = sm.l_fin[tid];
+      lse[(int64_t)qi * kHq + tid] = l > 0.0f ? sm.m_fin[tid] * 0.6931471805599453f + logf(l) : -INFINITY;
     }
   } else {
-    float* ob = part_o + ((int64_t)qi * nsplit + split) * kHq * kDkv;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int h = i & 15, ch = 128 * (2 * hg + (i >> 4)) + 32 * sp + lane;
-      ob[h * kDkv + ch] = __uint_as_float(o[i]);
+    float* obase = part_o + ((int64_t)qi * nsplit + split) * kHq * kDkv;
+    for (int f = tid; f < kHq * kDkv / 4; f += kAttnThreads) {
+      const int h = f / (kDkv / 4), c4 = f % (kDkv / 4);
+      reinterpret_cast<float4*>(obase + h * kDkv)[c4] =
+          *reinterpret_cast<const float4*>(ob + h * kOStride + 4 * c4);
     }
-    float* ml = part_ml + ((int64_t)qi * nsplit + split) * 2 * kHq;
-#pragma unroll
-    for (int h = 0; h < kHq; ++h)
-      if (tid == h) {
-        ml[h] = m_used[h];
-        ml[kHq + h] = l_run[h];
-      }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    if (tid < kHq) {
+      float* ml = part_ml + ((int64_t)qi * nsplit + split) * 2 * kHq;
+      ml[tid] = sm.m_fin[tid];
+      ml[kHq + tid] = sm.l_fin[tid];
+    }
   }
 }
 
