@@ -5,23 +5,25 @@
 // "Reuse Mode": sparse attention runs directly over the inherited top-K entries.
 // MQA over the shared latent: K = V = c_hat (512 channels), 16 query heads.
 //
-// One CTA (8 warps) handles one (query, split) pair: up to `split_len` selected entries
-// in tiles of 128 tokens.  Warp w owns latent channels 64 w .. 64 w + 63 for the whole
-// tile, so every code is dequantised exactly once per product, from the staged bytes
-// straight into tensor-core operand registers (E2M1 x E4M3 is exact in f16: at most 6
-// significant bits, magnitudes 2^-10 .. 2688):
-//   1. cp.async gathers the tile's 128 x (256 B codes + 32 B scales) into a 3-stage
-//      ring; codes are laid out [channel slice][row][32 B], and rows that are not
-//      selected (skipped entries, the ragged end of the split) are zero-filled;
-//   2. S^T partial = Q_w . C_w^T over the warp's 64 channels (mma.sync m16n8k16, f16
-//      operands, fp32 accumulation; M = 16 heads, N = 8 tokens per instruction); the
-//      eight partials are summed through shared memory;
+// One CTA (8 warps, two CTAs per SM) handles one (query, split) pair: up to
+// `split_len` selected entries in tiles of 128 tokens.  Every code is dequantised once
+// per product, from the staged bytes straight into tensor-core operand registers
+// (E2M1 x E4M3 is exact in f16: at most 6 significant bits, magnitudes 2^-10 .. 2688):
+//   1. cp.async gathers the tile's 128 x (256 B codes + 32 B scales) into a 2-stage
+//      ring, 16 lanes per row; codes are laid out [64-channel slice][row][32 B], and
+//      rows that are not selected (skipped entries, the ragged end of the split) are
+//      zero-filled;
+//   2. S^T partial = Q_c . C_c^T: warp w takes channels 128 (w % 4) .. + 127 of tokens
+//      64 (w / 4) .. + 63 (mma.sync m16n8k16, f16 operands, fp32 accumulation; M = 16
+//      heads, N = 8 tokens per instruction); the four channel partials are summed
+//      through shared memory;
 //   3. fp32 softmax in the exp2 domain, 16 threads per head, with a lazily moved
 //      reference max per head: it only moves (and the output accumulators are
 //      rescaled) when a tile's max exceeds it by more than 2^8, so every weight is at
 //      most 2^8; P is rounded to f16 and the normaliser sums the rounded weights;
-//   4. O_w += P . C_w (M = 16 heads, N = the warp's 64 channels, K = 16 tokens per
-//      instruction), with the two-token operand pairs assembled from the same bytes.
+//   4. O_w += P . C_w: warp w owns channels 64 w .. 64 w + 63 of the output (M = 16
+//      heads, N = 8 channels, K = 16 tokens per instruction), with the two-token operand
+//      pairs assembled from the same staged bytes.
 // Q is converted to f16 after a per-query power-of-two prescale (exact for every value
 // within 2^28 of the largest |q|); the scale is undone in the logit factor.  Several
 // splits per query are merged by a log-sum-exp combine kernel.
@@ -39,16 +41,18 @@ namespace csa2 {
 
 constexpr int kAttnThreads = 256;  // 8 warps
 constexpr int kAttnWarps = kAttnThreads / 32;
+constexpr int kAttnCtasPerSm = 2;
 constexpr int kTile = 128;         // tokens per tile
-constexpr int kStages = 3;         // cp.async ring: two tiles in flight ahead of the current one
-constexpr int kMaxSplit = 1024;    // selected entries per CTA at most
-constexpr int kSliceCh = kDkv / kAttnWarps;           // 64 channels per warp
-constexpr int kSliceBytes = kSliceCh / 2;             // 32 code bytes per row and warp
+constexpr int kStages = 2;         // cp.async ring: one tile in flight ahead of the current one
+constexpr int kMaxSplit = 512;     // selected entries per CTA at most
+constexpr int kSliceCh = kDkv / kAttnWarps;           // 64 output channels per warp
+constexpr int kSliceBytes = kSliceCh / 2;             // 32 code bytes per row and slice
+constexpr int kKSplit = 4;                            // S partials: 128-channel quarters
 constexpr int kSliceStride = kTile * kSliceBytes;     // 4 KB per channel slice of a stage
 constexpr int kStageCodes = kTile * kCodeRow;         // 32 KB: [slice][row][32 B]
 constexpr int kScaleHalf = kTile * 16;                // scales: [half][row][16 B]
 constexpr int kStageBytes = kStageCodes + 2 * kScaleHalf;  // 36 KB
-constexpr int kRedStride = kTile + 8;   // floats per (warp, head) row of S partials
+constexpr int kRedStride = kTile + 8;   // floats per (quarter, head) row of S partials
 constexpr int kOStride = kDkv + 4;      // floats per head row of the output staging
 constexpr float kRescaleGap = 8.0f;     // log2 units
 
@@ -56,7 +60,7 @@ static_assert(kSliceCh == 64 && kAttnThreads == 2 * kTile, "layout assumes 8 war
 
 struct AttnSmem {
   unsigned char stage[kStages][kStageBytes];
-  float red[kAttnWarps][kHq][kRedStride];  // S^T partials; reused to stage the output
+  float red[kKSplit][kHq][kRedStride];     // S^T partials; reused to stage the output
   uint16_t p[kHq][kTile];                  // P (f16): 16-byte units XOR-swizzled by head
   float alpha[kHq];
   float m_fin[kHq], l_fin[kHq];
@@ -65,9 +69,10 @@ struct AttnSmem {
 };
 static_assert(offsetof(AttnSmem, red) % 16 == 0 && offsetof(AttnSmem, p) % 16 == 0,
               "vector accesses need 16-byte alignment");
-static_assert(kHq * kOStride <= kAttnWarps * kHq * kRedStride, "output staging fits the partials");
+static_assert(kHq * kOStride <= kKSplit * kHq * kRedStride, "output staging fits the partials");
 constexpr size_t kAttnSmem = sizeof(AttnSmem);
-static_assert(kAttnSmem <= 232448, "sparse attention needs more than 227 KB of shared memory");
+static_assert(kAttnCtasPerSm * (kAttnSmem + 1024) <= 233472,
+              "sparse attention CTAs do not fit an SM's shared memory");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -116,10 +121,13 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
                : "memory");
 }
 
-// Stage position of tile row r: rows 4..7 of every group of 8 are stored in reverse
-// order, so that both the S-phase reads (8 consecutive rows, 8 bytes each) and the
-// O-phase reads (rows 2i or 2i + 1, i = 0..3, of a group) hit distinct banks.
+// Position of tile row r in code slice s: rows 4..7 of every group of 8 are stored in
+// reverse order, so that both the S-phase reads (8 consecutive rows, 8 bytes each) and
+// the O-phase reads (rows 2i or 2i + 1, i = 0..3, of a group) hit distinct banks; the
+// slice index rotates rows within aligned groups of 4, so that the 16 pieces of one row
+// written by a gather instruction spread over the banks.
 __device__ __forceinline__ int stage_row(int r) { return r ^ (((r >> 2) & 1) * 3); }
+__device__ __forceinline__ int slice_row(int r, int s) { return stage_row(r) ^ (s & 3); }
 
 struct AttnGeom {
   const int32_t* seq_lens;
@@ -129,25 +137,31 @@ struct AttnGeom {
   int32_t num_seqs;
 };
 
-// Gather the tile starting at local entry `e0`: thread -> row tid / 2, the two threads
-// of a row take the two 16-byte halves of each warp's 32-byte code slice, and one
-// 16-byte half of the row's scales.
+// Gather the tile starting at local entry `e0`.  Codes: 16 lanes per row, lane -> one
+// 16-byte piece, so each warp instruction reads two whole 256-byte rows.  Scales: two
+// lanes per row.
 __device__ __forceinline__ void issue_tile(unsigned char* stage, int e0, int ecount,
                                            const int32_t* slot, const uint8_t* __restrict__ codes,
                                            const uint8_t* __restrict__ scales) {
+  const int piece = threadIdx.x & 15, sl_i = piece >> 1;
+#pragma unroll
+  for (int k = 0; k < kTile / 16; ++k) {
+    const int r = 16 * k + (threadIdx.x >> 4);
+    const int e = e0 + r;
+    const int32_t sl = e < ecount ? slot[e] : -1;
+    const bool ok = sl >= 0;
+    cp_async16(stage + sl_i * kSliceStride + slice_row(r, sl_i) * kSliceBytes + 16 * (piece & 1),
+               codes + (ok ? (int64_t)sl * kCodeRow : 0) + 16 * piece, ok);
+  }
   const int r = threadIdx.x >> 1, h = threadIdx.x & 1;
   const int e = e0 + r;
   const int32_t sl = e < ecount ? slot[e] : -1;
   const bool ok = sl >= 0;
-  const uint8_t* src = codes + (ok ? (int64_t)sl * kCodeRow : 0);
-  unsigned char* dst = stage + stage_row(r) * kSliceBytes + 16 * h;
-#pragma unroll
-  for (int w = 0; w < kAttnWarps; ++w) cp_async16(dst + w * kSliceStride, src + 32 * w + 16 * h, ok);
   cp_async16(stage + kStageCodes + h * kScaleHalf + stage_row(r) * 16,
              scales + (ok ? (int64_t)sl * kScaleRow : 0) + 16 * h, ok);
 }
 
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     sparse_attn_kernel(const uint16_t* __restrict__ q, const uint8_t* __restrict__ codes,
                        const uint8_t* __restrict__ scales, const int32_t* __restrict__ idx,
                        AttnGeom g, const int32_t* __restrict__ q_seq, int32_t topk, int32_t split_len,
@@ -172,14 +186,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int32_t* idx_q = idx + (int64_t)qi * topk + jbeg;
 
   // Q first (its latency overlaps the index and page-table loads): heads gq and gq + 8,
-  // channels 64 warp + 16 iq .. + 15 -- the operand channels of this thread
+  // channels 64 s + 16 iq .. + 15 of code slices s = 2 (warp % 4) + j, j = 0, 1 -- the
+  // S-operand channels of this thread.  qr[4 hh + 2 j + v]: head gq + 8 hh, slice j, half v.
+  const int quarter = warp & 3, thalf = warp >> 2;
   const uint4* qg = reinterpret_cast<const uint4*>(q + (int64_t)qi * kHq * kDkv + gq * kDkv +
-                                                   warp * kSliceCh + 16 * iq);
-  uint4 qr[4];
-  qr[0] = __ldg(qg);
-  qr[1] = __ldg(qg + 1);
-  qr[2] = __ldg(qg + 8 * kDkv * 2 / 16);  // head gq + 8
-  qr[3] = __ldg(qg + 8 * kDkv * 2 / 16 + 1);
+                                                   2 * quarter * kSliceCh + 16 * iq);
+  uint4 qr[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    qr[k] = __ldg(qg + (k >> 2) * (8 * kDkv * 2 / 16) + ((k >> 1) & 1) * (kSliceCh * 2 / 16) + (k & 1));
 
   // ---- resolve the selected entries to physical rows: the first tiles first ----
   auto resolve = [&](int e) {
@@ -208,7 +223,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // below also publishes the remaining slots) ----
   uint32_t mx = 0;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < 8; ++k) {
     const uint32_t w[4] = {qr[k].x, qr[k].y, qr[k].z, qr[k].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) mx = max(mx, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
@@ -227,12 +242,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const float pre = __uint_as_float((uint32_t)(127 + sh) << 23);   // 2^sh
   const float post = __uint_as_float((uint32_t)(127 - sh) << 23);  // 2^-sh
   const float kq = softmax_scale * 1.4426950408889634f * post;  // logits in the exp2 domain
-  // k-step kk covers channels 16 iq + 4 kk .. + 3 of this thread: a0/a1 the first pair
+  // k-step 4 j + kk covers channels 16 iq + 4 kk .. + 3 of slice j: a0/a1 the first pair
   // (heads gq / gq + 8), a2/a3 the second -- the byte order of the staged codes
-  uint32_t qa[4][4];
+  uint32_t qa[8][4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t wl = (&qr[j >> 2].x)[j & 3], wh = (&qr[2 + (j >> 2)].x)[j & 3];
+  for (int j = 0; j < 16; ++j) {  // f16x2 word j of the thread's 32 channels
+    const uint32_t wl = (&qr[j >> 2].x)[j & 3], wh = (&qr[4 + (j >> 2)].x)[j & 3];
     const __half2 hl = __floats2half2_rn(bf16lo(wl) * pre, bf16hi(wl) * pre);
     const __half2 hh = __floats2half2_rn(bf16lo(wh) * pre, bf16hi(wh) * pre);
     qa[j >> 1][2 * (j & 1)] = *reinterpret_cast<const uint32_t*>(&hl);
@@ -256,25 +271,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (tn < ntiles) issue_tile(sm.stage[tn % kStages], tn * kTile, ecount, sm.slot, codes, scales);
       cp_async_commit();
     }
-    const unsigned char* cs = sm.stage[t % kStages] + warp * kSliceStride;
-    const unsigned char* ss = sm.stage[t % kStages] + kStageCodes + (warp >> 2) * kScaleHalf + 4 * (warp & 3);
+    const unsigned char* stg = sm.stage[t % kStages];
 
-    // ---- S^T partial over this warp's channels: 16 n-tiles of 8 tokens ----
-#pragma unroll 4
-    for (int n = 0; n < kTile / 8; ++n) {
-      const int r = stage_row(8 * n + gq);
-      const uint2 cw = *reinterpret_cast<const uint2*>(cs + r * kSliceBytes + 8 * iq);
-      const uint32_t sb = ss[r * 16 + iq];  // one scale: these 16 channels are one group
-      const uint32_t s2 = e4m3x2_to_f16x2(sb | (sb << 8));
-      uint32_t bf[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        bf[k] = hmul2(e2m1x2_to_f16x2(((k < 4 ? cw.x : cw.y) >> (8 * (k & 3))) & 0xFFu), s2);
+    // ---- S^T partial over channel quarter `quarter`, tokens 64 thalf .. + 63 ----
+#pragma unroll 2
+    for (int n = 0; n < kTile / 16; ++n) {
+      const int tok = 64 * thalf + 8 * n + gq;
       float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) mma16816(c, qa[kk], bf[2 * kk], bf[2 * kk + 1]);
-      *reinterpret_cast<float2*>(&sm.red[warp][gq][8 * n + 2 * iq]) = make_float2(c[0], c[1]);
-      *reinterpret_cast<float2*>(&sm.red[warp][gq + 8][8 * n + 2 * iq]) = make_float2(c[2], c[3]);
+      for (int j = 0; j < 2; ++j) {
+        const int sl_i = 2 * quarter + j;
+        const uint2 cw = *reinterpret_cast<const uint2*>(stg + sl_i * kSliceStride +
+                                                         slice_row(tok, sl_i) * kSliceBytes + 8 * iq);
+        // one scale: these 16 channels are one group
+        const uint32_t sb = stg[kStageCodes + (sl_i >> 2) * kScaleHalf + stage_row(tok) * 16 +
+                                4 * (sl_i & 3) + iq];
+        const uint32_t s2 = e4m3x2_to_f16x2(sb | (sb << 8));
+        uint32_t bf[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          bf[k] = hmul2(e2m1x2_to_f16x2(((k < 4 ? cw.x : cw.y) >> (8 * (k & 3))) & 0xFFu), s2);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma16816(c, qa[4 * j + kk], bf[2 * kk], bf[2 * kk + 1]);
+      }
+      const int col = 64 * thalf + 8 * n + 2 * iq;
+      *reinterpret_cast<float2*>(&sm.red[quarter][gq][col]) = make_float2(c[0], c[1]);
+      *reinterpret_cast<float2*>(&sm.red[quarter][gq + 8][col]) = make_float2(c[2], c[3]);
     }
     __syncthreads();
 
@@ -288,7 +310,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         s[4] = c.x; s[5] = c.y; s[6] = c.z; s[7] = c.w;
       }
 #pragma unroll
-      for (int w = 1; w < kAttnWarps; ++w) {
+      for (int w = 1; w < kKSplit; ++w) {
         const float4 a = *reinterpret_cast<const float4*>(&sm.red[w][sh_h][4 * sk]);
         const float4 c = *reinterpret_cast<const float4*>(&sm.red[w][sh_h][64 + 4 * sk]);
         s[0] += a.x; s[1] += a.y; s[2] += a.z; s[3] += a.w;
@@ -342,6 +364,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
       }
     }
+    const unsigned char* cs = stg + warp * kSliceStride;
+    const unsigned char* ss = stg + kStageCodes + (warp >> 2) * kScaleHalf + 4 * (warp & 3);
 #pragma unroll 2
     for (int ks = 0; ks < kTile / 16; ++ks) {
       uint32_t a[4];
@@ -350,10 +374,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int t0 = 16 * ks + 2 * iq;
       const int r0 = stage_row(t0), r1 = stage_row(t0 + 1), r8 = stage_row(t0 + 8),
                 r9 = stage_row(t0 + 9);
-      const uint32_t x0 = *reinterpret_cast<const uint32_t*>(cs + r0 * kSliceBytes + 4 * gq);
-      const uint32_t x1 = *reinterpret_cast<const uint32_t*>(cs + r1 * kSliceBytes + 4 * gq);
-      const uint32_t x8 = *reinterpret_cast<const uint32_t*>(cs + r8 * kSliceBytes + 4 * gq);
-      const uint32_t x9 = *reinterpret_cast<const uint32_t*>(cs + r9 * kSliceBytes + 4 * gq);
+      const int xs = warp & 3;  // the slice's row rotation
+      const uint32_t x0 = *reinterpret_cast<const uint32_t*>(cs + (r0 ^ xs) * kSliceBytes + 4 * gq);
+      const uint32_t x1 = *reinterpret_cast<const uint32_t*>(cs + (r1 ^ xs) * kSliceBytes + 4 * gq);
+      const uint32_t x8 = *reinterpret_cast<const uint32_t*>(cs + (r8 ^ xs) * kSliceBytes + 4 * gq);
+      const uint32_t x9 = *reinterpret_cast<const uint32_t*>(cs + (r9 ^ xs) * kSliceBytes + 4 * gq);
       const int sg = gq >> 1;  // scale group of this thread's channels 8 gq .. 8 gq + 7
       const uint32_t s01 = e4m3x2_to_f16x2(ss[r0 * 16 + sg] | ((uint32_t)ss[r1 * 16 + sg] << 8));
       const uint32_t s89 = e4m3x2_to_f16x2(ss[r8 * 16 + sg] | ((uint32_t)ss[r9 * 16 + sg] << 8));
@@ -482,8 +507,9 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restri
       make_float4(a.x * iv, a.y * iv, a.z * iv, a.w * iv);
 }
 
-// Splits per query: the count that minimises (waves of one CTA per SM) x (tiles per
-// CTA + a fixed start-up cost of ~2 tiles), with at most kMaxSplit entries per CTA.
+// Splits per query: the count that minimises (waves of kAttnCtasPerSm CTAs per SM) x
+// (tiles per CTA + a fixed start-up cost of ~2 tiles), with at most kMaxSplit entries
+// per CTA.
 int attn_splits(int32_t num_q, int32_t topk, int num_sms) {
   const int tiles = std::max(1, (topk + kTile - 1) / kTile);
   const int min_splits = (tiles * kTile + kMaxSplit - 1) / kMaxSplit;
@@ -494,7 +520,8 @@ int attn_splits(int32_t num_q, int32_t topk, int num_sms) {
     const int per = (tiles + sp - 1) / sp;     // tiles per split
     const int real = (tiles + per - 1) / per;  // splits actually used
     const int64_t ctas = (int64_t)num_q * real;
-    const int64_t waves = (ctas + num_sms - 1) / num_sms;
+    const int64_t slots = (int64_t)num_sms * kAttnCtasPerSm;
+    const int64_t waves = (ctas + slots - 1) / slots;
     const double cost = (double)waves * (per + 2);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;

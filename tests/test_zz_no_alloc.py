@@ -54,8 +54,9 @@ def test_static_scratch_matches_workspace_on_consecutive_calls():
 
 
 def test_static_scratch_rejects_oversized_requests():
-    # 8 queries over 65536 selected entries need 64 splits of 16 x 512 fp32 partials each:
-    # 16.06 MiB, over the 16 MiB array.  Refused before any device work.
+    # 8 queries over 65536 selected entries need at least 128 splits (512 entries each) of
+    # 16 x 512 fp32 partials: 32.1 MiB, over the 16 MiB array.  Refused before any device
+    # work.
     assert csa2.csa2_attn_workspace_size(8, 65536) > csa2.ATTN_STATIC_SCRATCH_BYTES
     pages = csa2.Csa2Pages(1, None, None, 1, 1, 64)
     assert csa2.csa2_sparse_attn_static(None, None, None, None, pages, None, None, 8, None, 65536,
