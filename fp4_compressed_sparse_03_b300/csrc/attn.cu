@@ -102,6 +102,16 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)(two & 0xFFFFu)));
   return h2;
 }
+// The four bytes of `w` (two E2M1 codes each) -> four f16x2: byte k -> h_k, low nibble
+// -> low half; exact.  Unpacking the word in one step feeds the conversions directly.
+__device__ __forceinline__ void e2m1x4_unpack(uint32_t w, uint32_t& h0, uint32_t& h1, uint32_t& h2,
+                                              uint32_t& h3) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+      : "r"(w));
+}
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -288,9 +298,10 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                                 4 * (sl_i & 3) + iq];
         const uint32_t s2 = e4m3x2_to_f16x2(sb | (sb << 8));
         uint32_t bf[8];
+        e2m1x4_unpack(cw.x, bf[0], bf[1], bf[2], bf[3]);
+        e2m1x4_unpack(cw.y, bf[4], bf[5], bf[6], bf[7]);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          bf[k] = hmul2(e2m1x2_to_f16x2(((k < 4 ? cw.x : cw.y) >> (8 * (k & 3))) & 0xFFu), s2);
+        for (int k = 0; k < 8; ++k) bf[k] = hmul2(bf[k], s2);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma16816(c, qa[4 * j + kk], bf[2 * kk], bf[2 * kk + 1]);
       }
@@ -388,12 +399,15 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
       const uint32_t hi01 = ((x0 >> 4) & 0x0F0F0F0Fu) | (x1 & 0xF0F0F0F0u);
       const uint32_t lo89 = (x8 & 0x0F0F0F0Fu) | ((x9 << 4) & 0xF0F0F0F0u);
       const uint32_t hi89 = ((x8 >> 4) & 0x0F0F0F0Fu) | (x9 & 0xF0F0F0F0u);
+      uint32_t L01[4], H01[4], L89[4], H89[4];
+      e2m1x4_unpack(lo01, L01[0], L01[1], L01[2], L01[3]);
+      e2m1x4_unpack(hi01, H01[0], H01[1], H01[2], H01[3]);
+      e2m1x4_unpack(lo89, L89[0], L89[1], L89[2], L89[3]);
+      e2m1x4_unpack(hi89, H89[0], H89[1], H89[2], H89[3]);
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
-        mma16816(oacc[2 * p], a, hmul2(e2m1x2_to_f16x2((lo01 >> (8 * p)) & 0xFFu), s01),
-                 hmul2(e2m1x2_to_f16x2((lo89 >> (8 * p)) & 0xFFu), s89));
-        mma16816(oacc[2 * p + 1], a, hmul2(e2m1x2_to_f16x2((hi01 >> (8 * p)) & 0xFFu), s01),
-                 hmul2(e2m1x2_to_f16x2((hi89 >> (8 * p)) & 0xFFu), s89));
+        mma16816(oacc[2 * p], a, hmul2(L01[p], s01), hmul2(L89[p], s89));
+        mma16816(oacc[2 * p + 1], a, hmul2(H01[p], s01), hmul2(H89[p], s89));
       }
     }
   }
