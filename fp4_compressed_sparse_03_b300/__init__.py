@@ -71,6 +71,7 @@ _attn_static = _sig("csa2_sparse_attn_static", ctypes.c_int,
                     [_vp, _vp, _vp, _vp, ctypes.POINTER(Csa2Pages), _vp, _vp, _i32, _vp, _i32,
                      ctypes.c_float, _vp, _vp])
 ATTN_STATIC_SCRATCH_BYTES = 16 << 20  # CSA2_ATTN_STATIC_SCRATCH_BYTES
+ATTN_MAX_TOPK = 65536  # CSA2_ATTN_MAX_TOPK
 _quantize = _sig("csa2_quantize", ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp])
 _dequantize = _sig("csa2_dequantize", ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp])
 _read_status = _sig("csa2_read_status", ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp])

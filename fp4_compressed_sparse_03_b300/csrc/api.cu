@@ -200,7 +200,7 @@ csa2_status csa2_sparse_attn(const uint16_t* q, const uint8_t* codes, const uint
   if (!al16(q) || !al16(codes) || !al16(scales) || (reinterpret_cast<uintptr_t>(out) & 7u))
     return CSA2_ERR_INVALID_ARGUMENT;
   if (!(softmax_scale == softmax_scale)) return CSA2_ERR_INVALID_ARGUMENT;
-  if (num_q > 65535) return CSA2_ERR_UNSUPPORTED;
+  if (num_q > 65535 || topk > CSA2_ATTN_MAX_TOPK) return CSA2_ERR_UNSUPPORTED;
   const int sms = device_sms();
   const size_t need = attn_workspace_bytes(num_q, topk, sms);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need || !al16(workspace)))

@@ -45,6 +45,8 @@ constexpr int kAttnCtasPerSm = 2;
 constexpr int kTile = 128;         // tokens per tile
 constexpr int kStages = 2;         // cp.async ring: one tile in flight ahead of the current one
 constexpr int kMaxSplit = 512;     // selected entries per CTA at most
+constexpr int kMaxSplits = CSA2_ATTN_MAX_TOPK / kMaxSplit;  // splits per query at most
+static_assert(kMaxSplits >= 64, "the split search goes up to 64 splits");
 constexpr int kSliceCh = kDkv / kAttnWarps;           // 64 output channels per warp
 constexpr int kSliceBytes = kSliceCh / 2;             // 32 code bytes per row and slice
 constexpr int kKSplit = 4;                            // S partials: 128-channel quarters
@@ -177,6 +179,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                        AttnGeom g, const int32_t* __restrict__ q_seq, int32_t topk, int32_t split_len,
                        float softmax_scale, float* __restrict__ out, float* __restrict__ lse,
                        float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* st) {
+  grid_dep_wait();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   AttnSmem& sm = *reinterpret_cast<AttnSmem*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -467,8 +470,9 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restri
                                                            const float* __restrict__ part_ml,
                                                            int nsplit, float* __restrict__ out,
                                                            float* __restrict__ lse) {
+  grid_dep_wait();
   const int qi = blockIdx.x, h = blockIdx.y;
-  __shared__ float wgt[64];
+  __shared__ float wgt[kMaxSplits];
   __shared__ float inv;
   const float* ml = part_ml + (int64_t)qi * nsplit * 2 * kHq;
   if (threadIdx.x < 32) {
@@ -569,15 +573,12 @@ cudaError_t launch_attn(const uint16_t* q, const uint8_t* codes, const uint8_t* 
   float* part_o = reinterpret_cast<float*>(ws);
   float* part_ml = part_o + (int64_t)num_q * splits * kHq * kDkv;
   dim3 grid(splits, num_q);
-  sparse_attn_kernel<<<grid, kAttnThreads, smem, s>>>(q, codes, scales, idx, g, q_seq, topk,
-                                                      split_len, softmax_scale, out, lse, part_o,
-                                                      part_ml, st);
-  e = cudaGetLastError();
+  e = launch_pdl(sparse_attn_kernel, grid, dim3(kAttnThreads), smem, s, q, codes, scales, idx, g,
+                 q_seq, topk, split_len, softmax_scale, out, lse, part_o, part_ml, st);
   if (e != cudaSuccess) return e;
-  if (splits > 1) {
-    attn_combine_kernel<<<dim3(num_q, kHq), 128, 0, s>>>(part_o, part_ml, splits, out, lse);
-    e = cudaGetLastError();
-  }
+  if (splits > 1)
+    e = launch_pdl(attn_combine_kernel, dim3(num_q, kHq), dim3(128), 0, s, (const float*)part_o,
+                   (const float*)part_ml, splits, out, lse);
   return e;
 }
 

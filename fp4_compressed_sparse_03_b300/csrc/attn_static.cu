@@ -54,6 +54,7 @@ extern "C" csa2_status csa2_sparse_attn_static(const uint16_t* q, const uint8_t*
                                                 float softmax_scale, int32_t* dev_status,
                                                 cudaStream_t stream) {
   if (num_q < 1 || topk < 1) return CSA2_ERR_INVALID_ARGUMENT;
+  if (topk > CSA2_ATTN_MAX_TOPK) return CSA2_ERR_UNSUPPORTED;
   if (csa2_attn_workspace_size(num_q, topk) > (size_t)CSA2_ATTN_STATIC_SCRATCH_BYTES)
     return CSA2_ERR_UNSUPPORTED;
   void* scratch = nullptr;

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/csa2.h"
 
 namespace csa2 {
@@ -21,6 +23,29 @@ constexpr int kKeyRow = kDidx * 2;      // 256 B of bf16 key per token
 // Iteration limit of every bounded spin (mbarrier try_wait loops).  try_wait itself
 // suspends for a hardware-chosen interval, so this is seconds of real time.
 constexpr uint32_t kSpinLimit = 1u << 26;
+
+// ---- programmatic dependent launch ----
+// Every kernel of the index and attention calls begins with grid_dep_wait() and is
+// launched by launch_pdl.  The launch may then be processed while the previous kernel in
+// the stream is still finishing; the wait (a no-op after an ordinary launch) returns once
+// that kernel has completed and its writes are visible, so stream order is unchanged.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 __device__ __forceinline__ void report(int32_t* st, int bits) {
   if (st) atomicOr(st, bits);

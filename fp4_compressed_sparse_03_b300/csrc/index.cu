@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(1024) group_prefix_kernel(bool batched, bool r
                                                             int32_t pool_size, int32_t unit_rows,
                                                             int64_t* meta, int64_t* prefix,
                                                             int32_t* run_q0) {
+  grid_dep_wait();
   __shared__ int64_t wsum[32];
   __shared__ int64_t carry_s;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -211,6 +212,7 @@ __global__ void __launch_bounds__(kScoreThreads, kGatherCtasPerSm)
                         const int32_t* __restrict__ q_seq, int32_t num_q, ScoreGeom g,
                         const int32_t* __restrict__ pool, int32_t pool_size,
                         uint32_t* __restrict__ ws, RunList rl, int32_t* st) {
+  grid_dep_wait();
   extern __shared__ __align__(128) unsigned char gather_smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gq = lane >> 2, c = lane & 3;
@@ -396,6 +398,7 @@ __global__ void __launch_bounds__(kTmaThreads, kScoreCtasPerSm)
                        const int32_t* __restrict__ q_seq, int32_t num_q, ScoreGeom g,
                        uint32_t* __restrict__ ws, int64_t ws_stride, RunList rl,
                        uint32_t* __restrict__ ghist, int32_t* st) {
+  grid_dep_wait();
   extern __shared__ __align__(1024) unsigned char page_smem_raw[];
   unsigned char* data = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(page_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -686,6 +689,7 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kSelThreads, 2)
                   int32_t num_seqs, const int32_t* __restrict__ pool_in, int32_t pool_size,
                   int32_t topk, int32_t* __restrict__ out_idx, int32_t* __restrict__ pool_out,
                   int32_t max_ctx, int32_t* st) {
+  grid_dep_wait();
   constexpr int kS = C * kSamplesPerCta;  // samples per query
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
@@ -1207,6 +1211,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
                       int32_t num_seqs, const int32_t* __restrict__ pool_in, int32_t pool_size,
                       int32_t topk, int32_t* __restrict__ out_idx, int32_t* __restrict__ pool_out,
                       int32_t max_ctx, const uint32_t* __restrict__ ghist) {
+  grid_dep_wait();
   extern __shared__ __align__(128) unsigned char smem_raw[];
   BigShared& sh = *reinterpret_cast<BigShared*>(smem_raw);
   const int q = blockIdx.x;
@@ -1599,6 +1604,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
                          const int32_t* __restrict__ q_seq, const int32_t* __restrict__ seq_lens,
                          int32_t num_seqs, int32_t pool_size, int32_t topk, int32_t max_ctx,
                          const uint32_t* __restrict__ ghist, WideLists wl) {
+  grid_dep_wait();
   extern __shared__ __align__(128) unsigned char smem_raw[];
   BigShared& sh = *reinterpret_cast<BigShared*>(smem_raw);
   const int c = blockIdx.x, q = blockIdx.y;
@@ -1679,6 +1685,7 @@ __device__ __forceinline__ uint32_t block_excl(BigShared& sh, uint32_t v, uint32
 __global__ void __launch_bounds__(kBigThreads, 1)
     select_resolve_kernel(int32_t pool_size, int32_t topk, const uint32_t* __restrict__ ghist,
                           WideLists wl) {
+  grid_dep_wait();
   extern __shared__ __align__(128) unsigned char smem_raw[];
   BigShared& sh = *reinterpret_cast<BigShared*>(smem_raw);
   uint32_t* loff = sh.u.c.pos[0];                 // [nlists + 1] list offsets
@@ -1801,6 +1808,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
 __global__ void __launch_bounds__(kBigThreads, 1)
     select_emit_kernel(int32_t pool_size, int32_t topk, int32_t* __restrict__ out_idx,
                        int32_t* __restrict__ pool_out, WideLists wl) {
+  grid_dep_wait();
   const int c = blockIdx.x, q = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t list = ((int64_t)q * wl.C + c) * kBigWarps + warp;
@@ -1865,11 +1873,9 @@ cudaError_t launch_score_full(const uint16_t* q_idx, const uint16_t* keys, const
   ScoreGeom g{pg.seq_lens, pg.page_table, pg.max_pages_per_seq, pg.num_pages, pg.num_seqs};
   RunList rl = make_runlist(runlist, num_q);
   const bool batched = max_q_per_seq > 1;
-  group_prefix_kernel<<<1, 1024, 0, s>>>(batched, false, q_seq, num_q, g, 0, kPage,
-                                         const_cast<int64_t*>(rl.meta),
-                                         const_cast<int64_t*>(rl.prefix),
-                                         const_cast<int32_t*>(rl.run_q0));
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(group_prefix_kernel, dim3(1), dim3(1024), 0, s, batched, false, q_seq,
+                             num_q, g, 0, kPage, const_cast<int64_t*>(rl.meta),
+                             const_cast<int64_t*>(rl.prefix), const_cast<int32_t*>(rl.run_q0));
   if (e != cudaSuccess) return e;
   CUtensorMap keymap;
   if (!make_bf16_map(&keymap, keys, (int64_t)pg.num_pages * kPage, kDidx, 64, kPage))
@@ -1882,9 +1888,8 @@ cudaError_t launch_score_full(const uint16_t* q_idx, const uint16_t* keys, const
     e = cudaMemsetAsync(ghist, 0, (size_t)num_q * kHistBins * sizeof(uint32_t), s);
     if (e != cudaSuccess) return e;
   }
-  score_pages_kernel<<<grid, kTmaThreads, kTmaSmem, s>>>(keymap, q_idx, q_seq, num_q, g, ws,
-                                                         ws_stride, rl, ghist, st);
-  return cudaGetLastError();
+  return launch_pdl(score_pages_kernel, dim3(grid), dim3(kTmaThreads), kTmaSmem, s, keymap, q_idx,
+                    q_seq, num_q, g, ws, ws_stride, rl, ghist, st);
 }
 
 cudaError_t launch_score_reindex(const uint16_t* q_idx, const uint16_t* keys, const int32_t* q_seq,
@@ -1893,19 +1898,16 @@ cudaError_t launch_score_reindex(const uint16_t* q_idx, const uint16_t* keys, co
                                  cudaStream_t s, int num_sms) {
   ScoreGeom g{pg.seq_lens, pg.page_table, pg.max_pages_per_seq, pg.num_pages, pg.num_seqs};
   RunList rl = make_runlist(runlist, num_q);
-  group_prefix_kernel<<<1, 1024, 0, s>>>(false, true, q_seq, num_q, g, pool_size, 16,
-                                         const_cast<int64_t*>(rl.meta),
-                                         const_cast<int64_t*>(rl.prefix),
-                                         const_cast<int32_t*>(rl.run_q0));
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(group_prefix_kernel, dim3(1), dim3(1024), 0, s, false, true, q_seq,
+                             num_q, g, pool_size, 16, const_cast<int64_t*>(rl.meta),
+                             const_cast<int64_t*>(rl.prefix), const_cast<int32_t*>(rl.run_q0));
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(score_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kGatherSmem);
   if (e != cudaSuccess) return e;
   const int grid = std::max(1, kGatherCtasPerSm * num_sms);
-  score_gather_kernel<<<grid, kScoreThreads, kGatherSmem, s>>>(q_idx, keys, q_seq, num_q, g, pool,
-                                                              pool_size, ws, rl, st);
-  return cudaGetLastError();
+  return launch_pdl(score_gather_kernel, dim3(grid), dim3(kScoreThreads), kGatherSmem, s, q_idx,
+                    keys, q_seq, num_q, g, pool, pool_size, ws, rl, st);
 }
 
 // CTAs per query: enough kept-key capacity (4096 per CTA and target) for twice the
@@ -1930,10 +1932,9 @@ cudaError_t launch_select_c(const uint32_t* ws, int64_t ws_stride, const int32_t
   cudaError_t e = cudaFuncSetAttribute(select_kernel<R, C>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  select_kernel<R, C><<<dim3(C, num_q), kSelThreads, smem, s>>>(
-      ws, ws_stride, q_seq, pg.seq_lens, pg.num_seqs, pool_in, pool_size, topk, out_idx, pool_out,
-      pg.max_pages_per_seq * kPage, st);
-  return cudaGetLastError();
+  return launch_pdl(select_kernel<R, C>, dim3(C, num_q), dim3(kSelThreads), smem, s, ws,
+                    ws_stride, q_seq, pg.seq_lens, pg.num_seqs, pool_in, pool_size, topk, out_idx,
+                    pool_out, pg.max_pages_per_seq * kPage, st);
 }
 
 template <bool R>
@@ -1982,15 +1983,13 @@ cudaError_t launch_select(bool reindex, const uint32_t* ws, int64_t ws_stride, c
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bsmem);
     if (e != cudaSuccess) return e;
     const int32_t P = pool_out ? pool_size : 0;
-    select_filter_kernel<<<dim3(C, num_q), kBigThreads, fsmem, s>>>(
-        ws, ws_stride, q_seq, pg.seq_lens, pg.num_seqs, P, topk, n, ghist, wl);
-    e = cudaGetLastError();
+    e = launch_pdl(select_filter_kernel, dim3(C, num_q), dim3(kBigThreads), fsmem, s, ws, ws_stride,
+                   q_seq, pg.seq_lens, pg.num_seqs, P, topk, n, ghist, wl);
     if (e != cudaSuccess) return e;
-    select_resolve_kernel<<<num_q, kBigThreads, bsmem, s>>>(P, topk, ghist, wl);
-    e = cudaGetLastError();
+    e = launch_pdl(select_resolve_kernel, dim3(num_q), dim3(kBigThreads), bsmem, s, P, topk, ghist, wl);
     if (e != cudaSuccess) return e;
-    select_emit_kernel<<<dim3(C, num_q), kBigThreads, 0, s>>>(P, topk, out_idx, pool_out, wl);
-    return cudaGetLastError();
+    return launch_pdl(select_emit_kernel, dim3(C, num_q), dim3(kBigThreads), 0, s, P, topk, out_idx,
+                      pool_out, wl);
   }
   // Up to 2^18 keys per query: one CTA per query, no cluster synchronisation (measured on
   // B300: 64 Full queries x 131072 keys took ~90 us in two waves of 8-CTA clusters, 46 us
@@ -2002,11 +2001,11 @@ cudaError_t launch_select(bool reindex, const uint32_t* ws, int64_t ws_stride, c
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<num_q, kBigThreads, smem, s>>>(ws, ws_stride, q_seq, pg.seq_lens, pg.num_seqs, pool_in,
-                                          reindex ? pool_size : (pool_out ? pool_size : 0), topk,
-                                          out_idx, reindex ? nullptr : pool_out,
-                                          pg.max_pages_per_seq * kPage, reindex ? nullptr : ghist);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(num_q), dim3(kBigThreads), smem, s, ws, ws_stride, q_seq,
+                      pg.seq_lens, pg.num_seqs, pool_in,
+                      reindex ? pool_size : (pool_out ? pool_size : 0), topk, out_idx,
+                      reindex ? nullptr : pool_out, pg.max_pages_per_seq * kPage,
+                      reindex ? nullptr : ghist);
   }
   const int c = select_cluster(n, want_max);
   if (reindex)

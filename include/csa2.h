@@ -173,12 +173,14 @@ CSA2_API size_t csa2_index_workspace_size(csa2_mode mode, int32_t num_q, int32_t
  *
  *   q      bf16 [num_q][16][512]
  *   codes, scales  the Full layer's pools (layout above)
- *   idx    int32 [num_q][topk], entries in [-1, seq_len)
+ *   idx    int32 [num_q][topk], entries in [-1, seq_len); 1 <= topk <= CSA2_ATTN_MAX_TOPK
+ *          (CSA2_ERR_UNSUPPORTED above it)
  *   out    fp32 [num_q][16][512];  lse fp32 [num_q][16] (nullable)
  *   q_seq  int32 [num_q]
  * Workspace: csa2_attn_workspace_size(num_q, topk) bytes (may be 0).
  * fp32 online softmax, split over the selected set, merged by log-sum-exp.
  */
+#define CSA2_ATTN_MAX_TOPK 65536
 CSA2_API csa2_status csa2_sparse_attn(const uint16_t* q, const uint8_t* codes, const uint8_t* scales,
                              const int32_t* idx, const csa2_pages* pages, float* out, float* lse,
                              int32_t num_q, const int32_t* q_seq, int32_t topk, float softmax_scale,

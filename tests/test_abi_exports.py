@@ -38,6 +38,15 @@ def test_host_side_checks_without_device():
     assert L.csa2_kv_write(None, None, None, None, None, 4, 64, 1, 0, None, 4, None, None) == \
         csa2.CSA2_ERR_INVALID_ARGUMENT
     assert L.csa2_read_status(None, None, None) == csa2.CSA2_ERR_INVALID_ARGUMENT
+    # attention over more than CSA2_ATTN_MAX_TOPK entries per query is refused on the host
+    # (fake aligned addresses: nothing is dereferenced before the check)
+    fake = 1 << 12
+    pages = csa2.Csa2Pages(1, fake, fake, 1, 1, 64)
+    for f in (lambda k: L.csa2_sparse_attn(fake, fake, fake, fake, ctypes.byref(pages), fake, None, 1,
+                                           fake, k, 0.04, None, 0, None, None),
+              lambda k: L.csa2_sparse_attn_static(fake, fake, fake, fake, ctypes.byref(pages), fake,
+                                                  None, 1, fake, k, 0.04, None, None)):
+        assert f(65536 + 1) == csa2.CSA2_ERR_UNSUPPORTED
     # workspace sizing is host arithmetic
     full = csa2.csa2_index_workspace_size(csa2.CSA2_FULL, 64, 2048, 8192)
     hist = 64 * 2048 * 4                                             # selection histograms

@@ -255,11 +255,12 @@ def test_two_groups_pool_larger_than_context():
 
 def test_attention_random_index_sets():
     """Attention alone on seeded random selections (with -1 padding and an empty set),
-    single- and multi-split launches."""
+    single- and multi-split launches (up to 36 splits of 128 entries, most of them empty
+    for the 100-token sequence)."""
     lens = np.array([3000, 100, 5000], np.int32)
     wl = gen.DecodeWorkload("attn", 23, lens, np.ones(3, np.int32), [gen.FULL], 0, 16)
     cache = fill_decode_cache(wl)
-    for topk, nq in [(256, 3), (2048, 3), (64, 3)]:
+    for topk, nq in [(256, 3), (2048, 3), (64, 3), (4608, 3)]:
         q_seq = np.array([0, 1, 2][:nq], np.int32)
         idx = np.stack([gen.random_index_set(23, 100 * topk + i, int(lens[b]), topk,
                                              n_invalid=(7 if i == 0 else 0))
