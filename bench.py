@@ -494,14 +494,18 @@ def workload_of(name: str):
 
 
 def count_launches(wl, step) -> int:
-    """Kernels libcsa2 launches per decode step: Full and Reindex index calls launch the
-    run-list kernel, a scoring kernel and a selection kernel; Reuse none; attention one
-    kernel plus the split combine when the selected set is split."""
+    """Kernels libcsa2 launches per decode step.  Full index call: the run-list kernel, the
+    page scorer and one selection kernel (three, filter / resolve / emit, beyond 2^18
+    tokens of context); Reindex: the gather scorer and one selection kernel; Reuse: none;
+    attention: one kernel, plus the split combine when the selected set is split."""
     import fp4_compressed_sparse_03_b300 as csa2
+    wide = step.cache.page_table.shape[1] * 64 > (1 << 18)
     n = 0
     for m in wl.schedule:
-        if m != csa2.CSA2_REUSE:
-            n += 3
+        if m == csa2.CSA2_FULL:
+            n += 2 + (3 if wide else 1)
+        elif m == csa2.CSA2_REINDEX:
+            n += 2
     ws = csa2.csa2_attn_workspace_size(step.num_q, step.topk)
     n += len(wl.schedule) * (2 if ws > 0 else 1)
     return n

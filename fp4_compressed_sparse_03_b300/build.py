@@ -9,7 +9,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libcsa2.so")
 SOURCES = ["api.cu", "codec.cu", "index.cu", "attn.cu", "kv_write.cu", "tensor_map.cu",
            "attn_static.cu"]
-HEADERS = ["common.cuh", "async.cuh", "tcgen05.cuh"]
+HEADERS = ["common.cuh", "async.cuh"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 
 FLAGS = [

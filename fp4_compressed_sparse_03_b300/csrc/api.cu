@@ -14,8 +14,8 @@ cudaError_t launch_score_full(const uint16_t*, const uint16_t*, const int32_t*, 
                               const csa2_pages&, uint32_t*, int64_t, void*, uint32_t*, int32_t*,
                               cudaStream_t, int);
 cudaError_t launch_score_reindex(const uint16_t*, const uint16_t*, const int32_t*, int32_t,
-                                 const csa2_pages&, const int32_t*, int32_t, uint32_t*, void*,
-                                 int32_t*, cudaStream_t, int);
+                                 const csa2_pages&, const int32_t*, int32_t, uint32_t*, int32_t*,
+                                 cudaStream_t, int);
 size_t runlist_bytes(int32_t num_q);
 cudaError_t launch_select(bool, const uint32_t*, int64_t, const int32_t*, const csa2_pages&,
                           int32_t, const int32_t*, int32_t, int32_t, int32_t*, int32_t*,
@@ -102,8 +102,8 @@ csa2_status csa2_dequantize(const uint8_t* codes, const uint8_t* scales,
                                      stream, device_sms()));
 }
 
-// Scores (one 32-bit key per candidate) followed, at a 256-byte boundary, by the
-// scorer's run list.
+// Scores (one 32-bit key per candidate) followed, at a 256-byte boundary, by the FULL
+// scorer's run list (the REINDEX work list is arithmetic).
 static size_t scores_bytes(csa2_mode mode, int32_t num_q, int32_t max_pages_per_seq,
                            int32_t pool_size) {
   const size_t n = mode == CSA2_FULL ? (size_t)std::max(0, max_pages_per_seq) * kPage
@@ -126,8 +126,9 @@ static size_t wide_bytes(csa2_mode mode, int32_t num_q, int32_t max_pages_per_se
 size_t csa2_index_workspace_size(csa2_mode mode, int32_t num_q, int32_t max_pages_per_seq,
                                  int32_t pool_size) {
   if (num_q <= 0 || (mode != CSA2_FULL && mode != CSA2_REINDEX)) return 0;
-  return scores_bytes(mode, num_q, max_pages_per_seq, pool_size) + runlist_bytes(num_q) +
-         hist_bytes(mode, num_q) + wide_bytes(mode, num_q, max_pages_per_seq);
+  return scores_bytes(mode, num_q, max_pages_per_seq, pool_size) +
+         (mode == CSA2_FULL ? runlist_bytes(num_q) : 0) + hist_bytes(mode, num_q) +
+         wide_bytes(mode, num_q, max_pages_per_seq);
 }
 
 csa2_status csa2_index(csa2_mode mode, const uint16_t* q_idx, const uint16_t* k_idx, int32_t* pool,
@@ -173,9 +174,7 @@ csa2_status csa2_index(csa2_mode mode, const uint16_t* q_idx, const uint16_t* k_
   }
   // REINDEX
   if (pool == nullptr || P < 1) return CSA2_ERR_INVALID_ARGUMENT;
-  void* rl = static_cast<char*>(args->workspace) +
-             scores_bytes(mode, args->num_q, pages->max_pages_per_seq, P);
-  e = launch_score_reindex(q_idx, k_idx, args->q_seq, args->num_q, *pages, pool, P, ws, rl,
+  e = launch_score_reindex(q_idx, k_idx, args->q_seq, args->num_q, *pages, pool, P, ws,
                            args->dev_status, stream, sms);
   if (e != cudaSuccess) return from_cuda(e);
   e = launch_select(true, ws, P, args->q_seq, *pages, args->num_q, pool, P, topk, out_idx, nullptr,

@@ -57,16 +57,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, ui
       : "memory");
 }
 
-// 1D bulk copy global -> shared (TMA engine), completing `bytes` on `bar`.  Both
-// addresses 16-byte aligned, `bytes` a multiple of 16.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          saddr(dst)),
-      "l"(src), "r"(bytes), "r"(saddr(bar))
-      : "memory");
-}
-
 // Host: 2D bf16 tensor map over a row-major [rows][cols] array, boxes of
 // [box_rows][box_cols] with 128-byte swizzle (box_cols * 2 must be <= 128).
 bool make_bf16_map(CUtensorMap* tm, const void* ptr, int64_t rows, int64_t cols, int box_cols,

@@ -210,8 +210,9 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     qr[k] = __ldg(qg + (k >> 2) * (8 * kDkv * 2 / 16) + ((k >> 1) & 1) * (kSliceCh * 2 / 16) + (k & 1));
 
   // ---- resolve the selected entries to physical rows: the first tiles first ----
-  auto resolve = [&](int e) {
-    const int s = __ldg(idx_q + e);
+  // the index load of an entry is issued separately from its page-table lookup, so that
+  // a thread's loads of several entries are in flight together
+  auto resolve = [&](int e, int s) {
     int32_t slot = -1;
     if (s >= 0 && s < n_ctx) {
       const int32_t pg = __ldg(g.page_table + (int64_t)b * g.max_pages + (s >> 6));
@@ -223,14 +224,26 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     sm.slot[e] = slot;
   };
   const int e_first = min(ecount, (kStages - 1) * kTile);
-  for (int e = tid; e < e_first; e += kAttnThreads) resolve(e);
+  static_assert((kStages - 1) * kTile <= kAttnThreads, "one first-tile entry per thread");
+  if (tid < e_first) resolve(tid, __ldg(idx_q + tid));
+  constexpr int kRest = (kMaxSplit - (kStages - 1) * kTile + kAttnThreads - 1) / kAttnThreads;
+  int rest_s[kRest];
+#pragma unroll
+  for (int i = 0; i < kRest; ++i) {
+    const int e = e_first + tid + i * kAttnThreads;
+    rest_s[i] = e < ecount ? __ldg(idx_q + e) : -1;
+  }
   __syncthreads();
 #pragma unroll
   for (int i = 0; i < kStages - 1; ++i) {
     if (i < ntiles) issue_tile(sm.stage[i], i * kTile, ecount, sm.slot, codes, scales);
     cp_async_commit();
   }
-  for (int e = e_first + tid; e < ecount; e += kAttnThreads) resolve(e);
+#pragma unroll
+  for (int i = 0; i < kRest; ++i) {
+    const int e = e_first + tid + i * kAttnThreads;
+    if (e < ecount) resolve(e, rest_s[i]);
+  }
 
   // ---- Q: max |q| -> power-of-two prescale -> f16 operand fragments (the barrier
   // below also publishes the remaining slots) ----

@@ -191,7 +191,8 @@ __device__ __forceinline__ void cursor_advance(RunCursor& cu, const RunList& rl,
   }
 }
 
-// REINDEX: each query's P pool positions are a run of 16-row groups; the rows are
+// REINDEX: query q's P pool positions are groups [q u, (q + 1) u) of 16 rows, u =
+// ceil(P / 16), so the work list is plain arithmetic; the rows are
 // gathered (pool entry -> page table -> slot) through the per-lane cp.async ring and
 // scored on the tensor cores exactly like the page scorer (M = 16 gathered keys,
 // N = 8 columns holding the query's 4 heads, K = 128 dims in the shared permuted order).
@@ -211,7 +212,7 @@ __global__ void __launch_bounds__(kScoreThreads, kGatherCtasPerSm)
     score_gather_kernel(const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ keys,
                         const int32_t* __restrict__ q_seq, int32_t num_q, ScoreGeom g,
                         const int32_t* __restrict__ pool, int32_t pool_size,
-                        uint32_t* __restrict__ ws, RunList rl, int32_t* st) {
+                        uint32_t* __restrict__ ws, int32_t* st) {
   grid_dep_wait();
   extern __shared__ __align__(128) unsigned char gather_smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -220,9 +221,9 @@ __global__ void __launch_bounds__(kScoreThreads, kGatherCtasPerSm)
   // (gq = 2p, 2p + 1) get masks p and p + 4, so their 16-byte chunks fill all 32 banks
   const int sw = (gq >> 1) | ((gq & 1) << 2);
   const uint32_t ring = smem_addr(gather_smem) + warp * kGatherRing * kGatherGroup;
-  const int R = (int)__ldg(rl.meta);
+  const int64_t used = (pool_size + 15) / 16;  // groups per query
   int64_t g0, g1;
-  warp_share(__ldg(rl.meta + 1), g0, g1);
+  warp_share((int64_t)num_q * used, g0, g1);
   if (g0 >= g1) return;
 
   struct QInfo {
@@ -245,14 +246,24 @@ __global__ void __launch_bounds__(kScoreThreads, kGatherCtasPerSm)
     int b = -1, n_ctx = 0;
     int ta = -1, tb = -1;  // tokens of rows gq and gq + 8 (-1: none)
   };
+  // cursor over the queries: query r owns groups [start, start + used)
+  auto advance = [&](RunCursor& cu, int64_t gg) {
+    while (gg >= cu.end) {
+      ++cu.r;
+      cu.start = cu.end;
+      cu.end = cu.start + used;
+    }
+  };
   RunCursor lc, cc;
-  cursor_seek(lc, rl, R, g0);
+  lc.r = (int)(g0 / used);
+  lc.start = (int64_t)lc.r * used;
+  lc.end = lc.start + used;
   cc = lc;
   QInfo li = info(lc.r), ci;
   auto load_pool = [&](int64_t gg) -> PoolRows {
     PoolRows r;
     if (gg >= g1) return r;
-    cursor_advance(lc, rl, gg);
+    advance(lc, gg);
     if (lc.r != li.q) li = info(lc.r);
     if (li.b < 0) return r;
     r.b = li.b;
@@ -303,7 +314,7 @@ __global__ void __launch_bounds__(kScoreThreads, kGatherCtasPerSm)
     next = load_pool(gg + kGatherRing);
     issue(cur, (slot + kGatherRing - 1) & (kGatherRing - 1));
     cp_async_wait<kGatherRing - 1>();
-    cursor_advance(cc, rl, gg);
+    advance(cc, gg);
     if (cc.r != ci.q) {
       ci = info(cc.r);
       if (ci.b < 0 && lane == 0) report(st, CSA2_DEV_BAD_QSEQ);
@@ -1894,20 +1905,15 @@ cudaError_t launch_score_full(const uint16_t* q_idx, const uint16_t* keys, const
 
 cudaError_t launch_score_reindex(const uint16_t* q_idx, const uint16_t* keys, const int32_t* q_seq,
                                  int32_t num_q, const csa2_pages& pg, const int32_t* pool,
-                                 int32_t pool_size, uint32_t* ws, void* runlist, int32_t* st,
-                                 cudaStream_t s, int num_sms) {
+                                 int32_t pool_size, uint32_t* ws, int32_t* st, cudaStream_t s,
+                                 int num_sms) {
   ScoreGeom g{pg.seq_lens, pg.page_table, pg.max_pages_per_seq, pg.num_pages, pg.num_seqs};
-  RunList rl = make_runlist(runlist, num_q);
-  cudaError_t e = launch_pdl(group_prefix_kernel, dim3(1), dim3(1024), 0, s, false, true, q_seq,
-                             num_q, g, pool_size, 16, const_cast<int64_t*>(rl.meta),
-                             const_cast<int64_t*>(rl.prefix), const_cast<int32_t*>(rl.run_q0));
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(score_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kGatherSmem);
+  cudaError_t e = cudaFuncSetAttribute(score_gather_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kGatherSmem);
   if (e != cudaSuccess) return e;
   const int grid = std::max(1, kGatherCtasPerSm * num_sms);
   return launch_pdl(score_gather_kernel, dim3(grid), dim3(kScoreThreads), kGatherSmem, s, q_idx,
-                    keys, q_seq, num_q, g, pool, pool_size, ws, rl, st);
+                    keys, q_seq, num_q, g, pool, pool_size, ws, st);
 }
 
 // CTAs per query: enough kept-key capacity (4096 per CTA and target) for twice the
