@@ -489,6 +489,11 @@ def workload_of(name: str):
         wl = gen.config_decode_batch()
         return gen.DecodeWorkload("decode_batch_16x131072", wl.seed, wl.seq_lens[:16],
                                   wl.q_per_seq[:16], wl.schedule, wl.pool_size, wl.topk)
+    if name == "decode_short":     # the decode batch's 64 queries over 16384-token contexts:
+        wl = gen.config_decode_batch()   # the attention launch shape at profiling size
+        return gen.DecodeWorkload("decode_batch_64x16384", wl.seed,
+                                  np.full(len(wl.seq_lens), 16384, np.int32), wl.q_per_seq,
+                                  wl.schedule, wl.pool_size, wl.topk)
     return {"decode_batch": gen.config_decode_batch, "long_context": gen.config_long_context,
             "ragged": gen.config_ragged, "tiny": gen.config_tiny}[name]()
 
@@ -650,7 +655,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_batch",
-                    choices=["decode_batch", "decode_batch16", "long_context", "ragged", "tiny",
+                    choices=["decode_batch", "decode_batch16", "decode_short", "long_context", "ragged", "tiny",
                              "ced_write"])
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-sample", type=int, default=None,

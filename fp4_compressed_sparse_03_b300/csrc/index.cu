@@ -1521,8 +1521,8 @@ __global__ void __launch_bounds__(kBigThreads, 1)
 }
 
 // ------------------------------------------------------------ wide selection (Full) --
-// Contexts beyond 2^18 tokens: the Full scorer's exact histograms give every CTA the
-// boundary bins, so a query's keys are filtered by many CTAs at once.
+// Contexts beyond kWideThreshold tokens: the Full scorer's exact histograms give every
+// CTA the boundary bins, so a query's keys are filtered by several CTAs at once.
 //   select_filter_kernel (C CTAs per query): one ordered sweep of the CTA's position
 //     range keeps (position, key) of the keys with bin >= min B_t into per-warp global
 //     lists sized for the whole warp segment (no overflow is possible);
@@ -1531,6 +1531,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
 //     order, which is position order (CTA-major, then warp-major);
 //   select_emit_kernel (the filter's grid, one warp per list): each list writes its
 //     selected positions at its base.
+constexpr int kWideThreshold = 1 << 18;  // Full contexts longer than this use the wide path
 constexpr int kWideMinKeys = 1 << 16;  // positions per filter CTA at least
 constexpr int kWideMaxCtas = 16;       // filter CTAs per query at most
 constexpr int kMaxWideLists = kWideMaxCtas * kBigWarps;
@@ -1956,9 +1957,9 @@ cudaError_t launch_select_r(int c, const uint32_t* ws, int64_t ws_stride, const 
   }
 }
 
-// Bytes of the wide selection's candidate lists for FULL over contexts of n > 2^18 tokens.
+// Bytes of the wide selection's candidate lists for FULL over contexts of n > kWideThreshold.
 size_t wide_select_bytes(int32_t num_q, int32_t n) {
-  if (n <= (1 << 18)) return 0;
+  if (n <= kWideThreshold) return 0;
   const int L = wide_range(n);
   const int64_t C = ((int64_t)n + L - 1) / L;
   return (size_t)num_q * (C * ((size_t)L * 8 + kBigWarps * 4) + (size_t)kWideMeta * 4);
@@ -1973,7 +1974,7 @@ cudaError_t launch_select(bool reindex, const uint32_t* ws, int64_t ws_stride, c
   const int32_t want_max = std::max(topk, (!reindex && pool_out) ? pool_size : 0);
   // FULL beyond 2^18 tokens with the scorer's histograms: C filter CTAs per query, then
   // one finishing CTA per query (the cluster kernel took ~265 us for 4 x 2^20 keys)
-  if (!reindex && n > (1 << 18) && ghist != nullptr && wide_ws != nullptr) {
+  if (!reindex && n > kWideThreshold && ghist != nullptr && wide_ws != nullptr) {
     const int L = wide_range(n);
     const int C = (int)(((int64_t)n + L - 1) / L);
     WideLists wl;

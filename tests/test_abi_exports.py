@@ -48,9 +48,13 @@ def test_host_side_checks_without_device():
                                                   None, 1, fake, k, 0.04, None, None)):
         assert f(65536 + 1) == csa2.CSA2_ERR_UNSUPPORTED
     # workspace sizing is host arithmetic
-    full = csa2.csa2_index_workspace_size(csa2.CSA2_FULL, 64, 2048, 8192)
+    full = csa2.csa2_index_workspace_size(csa2.CSA2_FULL, 64, 1024, 8192)
     hist = 64 * 2048 * 4                                             # selection histograms
-    assert 64 * 2048 * 64 * 4 + hist < full < 64 * 2048 * 64 * 4 + hist + 4096  # + scores, run list
+    assert 64 * 1024 * 64 * 4 + hist < full < 64 * 1024 * 64 * 4 + hist + 4096  # + scores, run list
+    # beyond 2^18 tokens the wide selection adds (position, key) lists covering every
+    # position of the context
+    wide = csa2.csa2_index_workspace_size(csa2.CSA2_FULL, 4, 16384, 8192)
+    assert wide >= 4 * 16384 * 64 * (4 + 8) + 4 * 2048 * 4
     re = csa2.csa2_index_workspace_size(csa2.CSA2_REINDEX, 64, 2048, 8192)
     assert re == 64 * 8192 * 4                                       # scores only
     assert csa2.csa2_index_workspace_size(csa2.CSA2_REUSE, 64, 2048, 8192) == 0
