@@ -353,9 +353,14 @@ def run_ours(args, world, rank, local):
 
 
 def run_write(args, world, rank, local):
-    """The CED write path alone: one csa2_kv_write over the whole write workload per step
-    (H [32768, 4096] bf16 times 20 latent + 20 indexer-key projections, quantised on
-    write).  The roofline is the tensor pipe: 2 T d n_out flops per call."""
+    """The CED write path alone: one csa2_kv_write per step.
+    ced_write: the whole prefill write (H [32768, 4096] bf16 times 20 latent + 20
+    indexer-key projections, quantised on write); roofline the tensor pipe, 2 T d n_out
+    flops per call.
+    decode_append: the new token of each of 64 sequences through the same projections;
+    roofline HBM, the 105 MB of projection weights streamed per call.  The weights fit
+    in L2, so L2 is flushed (a 256 MB buffer written) before every timed call, and each
+    call is timed by its own events."""
     import torch
     import csa2_inputs as gen
     import fp4_compressed_sparse_03_b300 as csa2
@@ -363,8 +368,10 @@ def run_write(args, world, rank, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    ww = gen.config_write()
+    append = args.workload == "decode_append"
+    ww = gen.config_append() if append else gen.config_write()
     H, Wt, slots = fill_write_inputs(ww, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if append else None
     num_slots = ww.num_pages * 64
     codes = torch.empty((ww.n_kv_proj, num_slots, 256), dtype=torch.uint8, device=dev)
     scales = torch.empty((ww.n_kv_proj, num_slots, 32), dtype=torch.uint8, device=dev)
@@ -391,6 +398,8 @@ def run_write(args, world, rank, local):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for k in range(K):
+        if flush is not None:
+            flush.fill_(k & 0xFF)
         evs[k][0].record(stream)
         call()
         evs[k][1].record(stream)
@@ -401,21 +410,31 @@ def run_write(args, world, rank, local):
     status, bits = csa2.csa2_read_status(st)
     if status != csa2.CSA2_OK:
         raise RuntimeError(f"device status {bits:#x} after timed steps")
-    ms_step = reduce_max(t0.elapsed_time(t1) / K, world, dev)
     kern_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    # with L2 flushes between calls the step is the call itself
+    ms_step = reduce_max(kern_ms if append else t0.elapsed_time(t1) / K, world, dev)
     units = ww.T * world
     value = units / (ms_step / 1e3)
     flops = 2.0 * ww.T * ww.d_model * ww.n_out
-    _, tc_peak, peak_src = load_peaks()
+    hbm_peak, tc_peak, peak_src = load_peaks()
     achieved = flops / (kern_ms / 1e3) / 1e12
+    # algorithmic bytes of one call: weights and H read, codes + scales + keys written
+    out_row = ww.n_kv_proj * (256 + 32) + ww.n_idx_proj * 128 * 2
+    abytes = ww.n_out * ww.d_model * 2 + ww.T * ww.d_model * 2 + ww.T * (out_row + 4)
+    achieved_gbs = abytes / (kern_ms / 1e3) / 1e9
 
-    # end to end: H from pinned host memory in, every code, scale and key back out
+    # end to end: H from pinned host memory in, every code, scale and key back out (for
+    # decode_append the step's result is the new rows only: gathered, then read back)
     H_pin = torch.empty(H.shape, dtype=H.dtype).pin_memory()
     H_pin.copy_(H)
-    c_pin = torch.empty(codes.shape, dtype=codes.dtype).pin_memory()
-    s_pin = torch.empty(scales.shape, dtype=scales.dtype).pin_memory()
-    k_pin = torch.empty(keys.shape, dtype=keys.dtype).pin_memory()
+    rows = ww.T if append else codes.shape[1]
+    c_pin = torch.empty((codes.shape[0], rows, 256), dtype=codes.dtype).pin_memory()
+    s_pin = torch.empty((scales.shape[0], rows, 32), dtype=scales.dtype).pin_memory()
+    k_pin = torch.empty((keys.shape[0], rows, 128), dtype=keys.dtype).pin_memory()
     H_dev = torch.empty_like(H)
+    sl_long = slots.long()
+    if append:  # first use of the gathers outside the timed region
+        c_pin.copy_(codes.index_select(1, sl_long))
     K2 = max(1, min(K, args.e2e_steps, 10))
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
@@ -423,35 +442,52 @@ def run_write(args, world, rank, local):
     w0 = time.perf_counter()
     e0.record(stream)
     for _ in range(K2):
+        if flush is not None:
+            flush.fill_(7)
         H_dev.copy_(H_pin, non_blocking=True)
         call(H_dev)
-        c_pin.copy_(codes, non_blocking=True)
-        s_pin.copy_(scales, non_blocking=True)
-        k_pin.copy_(keys, non_blocking=True)
+        if append:
+            c_pin.copy_(codes.index_select(1, sl_long), non_blocking=True)
+            s_pin.copy_(scales.index_select(1, sl_long), non_blocking=True)
+            k_pin.copy_(keys.index_select(1, sl_long), non_blocking=True)
+        else:
+            c_pin.copy_(codes, non_blocking=True)
+            s_pin.copy_(scales, non_blocking=True)
+            k_pin.copy_(keys, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     wall = (time.perf_counter() - w0) / K2 * 1e3
     ms_e2e = reduce_max(max(e0.elapsed_time(e1) / K2, wall), world, dev)
     h2d = H.numel() * 2
-    d2h = codes.numel() + scales.numel() + keys.numel() * 2
+    d2h = c_pin.numel() + s_pin.numel() + k_pin.numel() * 2
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline_write(ww, args.cpu_sample)
+    if append:
+        roof = {"bound": "hbm", "kernel": "csa2_kv_write: kv_write_kernel",
+                "achieved": round(achieved_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved_gbs / hbm_peak, 4), "peak_source": peak_src + " HBM copy",
+                "algorithmic_bytes_per_launch": int(abytes), "traffic": None}
+        l2 = "flushed before every call (256 MB written): the 105 MB of weights fit in L2"
+    else:
+        roof = {"bound": "tensor", "kernel": "csa2_kv_write: kv_write_kernel",
+                "achieved": round(achieved, 1), "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": round(achieved / tc_peak, 4), "peak_source": peak_src + " bf16 burst",
+                "algorithmic_flops_per_launch": flops, "traffic": None}
+        l2 = "no flush: H is %.0f MB (> 126 MB L2)" % (H.numel() * 2 / 1e6)
     line = {
-        "metric": "CED write path: tokens/s projected and quantised on write", "value": round(value, 1),
+        "metric": ("decode-time append: new tokens/s projected and quantised into the paged cache"
+                   if append else "CED write path: tokens/s projected and quantised on write"),
+        "value": round(value, 1),
         "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 operands, f32 accumulate, fp4-e2m1/e4m3 + bf16 out",
         "data": "synthetic (seeded counter-based generator)",
         "config": {"workload": ww.name, "tokens": ww.T, "d_model": ww.d_model,
                    "latent_projections": ww.n_kv_proj, "key_projections": ww.n_idx_proj,
-                   "l2": "no flush: H is %.0f MB (> 126 MB L2)" % (H.numel() * 2 / 1e6),
-                   "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "tensor", "kernel": "csa2_kv_write: kv_write_kernel",
-                     "achieved": round(achieved, 1), "peak": tc_peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / tc_peak, 4), "peak_source": peak_src + " bf16 burst",
-                     "algorithmic_flops_per_launch": flops, "traffic": None},
+                   "l2": l2, "parallelism": f"replicas x{world}"},
+        "roofline": roof,
         "e2e": {"value": round(units / (ms_e2e / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": K2},
         "gpu_launches": K,
@@ -593,7 +629,7 @@ def run_reference(args, world, rank):
     import csa2_inputs as gen
     if rank != 0:
         return
-    if args.workload == "ced_write":
+    if args.workload in ("ced_write", "decode_append"):
         return run_reference_write(args, world)
     wl = workload_of(args.workload)
     per_step = max(1, args.cpu_sample // max(1, args.steps))
@@ -624,7 +660,8 @@ def run_reference(args, world, rank):
 
 def run_reference_write(args, world):
     import csa2_inputs as gen
-    ww = gen.config_write()
+    append = args.workload == "decode_append"
+    ww = gen.config_append() if append else gen.config_write()
     per_step = max(1, args.cpu_sample // max(1, args.steps))
     vals = []
     t0 = time.perf_counter()
@@ -635,7 +672,9 @@ def run_reference_write(args, world):
     cb = dict(vals[-1])
     cb["value"] = round(v, 3)
     cb["sample"] = f"{args.steps} steps x {per_step} token rows of {ww.name}"
-    line = {"impl": "reference", "metric": "CED write path: tokens/s projected and quantised on write",
+    line = {"impl": "reference",
+            "metric": ("decode-time append: new tokens/s projected and quantised into the paged cache"
+                       if append else "CED write path: tokens/s projected and quantised on write"),
             "value": round(v, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -656,19 +695,20 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_batch",
                     choices=["decode_batch", "decode_batch16", "decode_short", "long_context", "ragged", "tiny",
-                             "ced_write"])
+                             "ced_write", "decode_append"])
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-sample", type=int, default=None,
-                    help="queries (decode) or token rows (ced_write) timed on the oracle; "
-                         "default 32 queries / 256 rows, about 10-30 s of CPU work")
+                    help="queries (decode) or token rows (write workloads) timed on the oracle; "
+                         "default 32 queries / 256 rows (all 64 for decode_append), about "
+                         "10-30 s of CPU work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.cpu_sample is None:
-        args.cpu_sample = 256 if args.workload == "ced_write" else 32
+        args.cpu_sample = {"ced_write": 256, "decode_append": 64}.get(args.workload, 32)
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
-    elif args.workload == "ced_write":
+    elif args.workload in ("ced_write", "decode_append"):
         args.warmup = max(3, args.warmup)
         run_write(args, world, rank, local)
     else:

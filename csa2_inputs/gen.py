@@ -316,6 +316,7 @@ class WriteWorkload:
     n_kv_proj: int
     n_idx_proj: int
     shuffle: bool = True
+    append_pos: int = -1  # >= 0: token t is the new token of sequence t, at this position
 
     @property
     def n_out(self) -> int:
@@ -323,11 +324,15 @@ class WriteWorkload:
 
     @property
     def num_pages(self) -> int:
+        if self.append_pos >= 0:
+            return self.T  # one (current) page per sequence
         return (self.T + PAGE - 1) // PAGE
 
     def slot_of_token(self) -> np.ndarray:
         perm = page_permutation(self.seed, self.num_pages, self.shuffle)
         t = np.arange(self.T, dtype=np.int64)
+        if self.append_pos >= 0:  # sequence t's current page, at the new position's offset
+            return (perm[t].astype(np.int64) * PAGE + self.append_pos % PAGE).astype(np.int32)
         return (perm[t // PAGE].astype(np.int64) * PAGE + t % PAGE).astype(np.int32)
 
     def h_rows(self, rows) -> np.ndarray:
@@ -355,6 +360,14 @@ def config_write(seed: int = 2) -> WriteWorkload:
     """H [32768, 4096] ~N(0,1); 20 KV projections [4096, 512] and 20 indexer-key
     projections [4096, 128] ~N(0, 1/4096); 512 shuffled pages of 64 tokens."""
     return WriteWorkload("ced_write_32768x4096_20x512_20x128", seed, 32768, 4096, 20, 20)
+
+
+def config_append(seed: int = 5) -> WriteWorkload:
+    """Decode-time append: the new token of each of the decode batch's 64 sequences (at
+    position 131072, the first slot of a fresh page), projected by the same 20 latent and
+    20 indexer-key projections of d_model 4096."""
+    return WriteWorkload("decode_append_64x4096_20x512_20x128", seed, 64, 4096, 20, 20,
+                         append_pos=131072)
 
 
 def d_model_pow2_scale(d_model: int) -> int:

@@ -221,7 +221,7 @@ csa2_status csa2_kv_write(const uint16_t* H, const uint16_t* Wt, uint8_t* codes,
   if (!al16(H) || !al16(Wt) || (codes && (reinterpret_cast<uintptr_t>(codes) & 7u)) ||
       (k_idx && !al16(k_idx)))
     return CSA2_ERR_INVALID_ARGUMENT;
-  if (T % 128 != 0 || d_model % 64 != 0) return CSA2_ERR_UNSUPPORTED;
+  if (d_model % 64 != 0) return CSA2_ERR_UNSUPPORTED;
   return from_cuda(launch_kv_write(H, Wt, codes, scales, k_idx, T, d_model, n_kv_proj, n_idx_proj,
                                    slot_of_token, num_slots, dev_status, stream, device_sms()));
 }

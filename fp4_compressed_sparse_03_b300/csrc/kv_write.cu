@@ -18,6 +18,8 @@
 //     projections), or bf16 RNE (indexer-key projections), stored at the token's slot;
 //   - tile order: groups of 16 M-tiles swept across all N-tiles, so the A tiles of a
 //     group stay in L2 while the B slices stream;
+//   - any T: rows of the last M-tile beyond T are zero-filled by the TMA load and not
+//     stored (decode-time append writes T = one token per sequence);
 //   - every mbarrier wait is bounded; on expiry the CTA raises CSA2_DEV_TIMEOUT, stops
 //     issuing, waits (bounded) for its own copies and MMAs, frees TMEM and returns.
 #include "async.cuh"
@@ -158,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  const int num_m = p.T / BM;
+  const int num_m = (p.T + BM - 1) / BM;
   const int num_n = (p.n_out + BN - 1) / BN;
   const int num_tiles = num_m * num_n;
   const int kblocks = p.d_model / BK;
@@ -244,9 +246,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&bars->abort, &bars->tfull[acc], acc_phase, p.st)) break;
       fence_after();
       const int t = m * BM + row;
-      const int32_t slot = __ldg(p.slot_of_token + t);
-      const bool slot_ok = slot >= 0 && slot < p.num_slots;
-      if (!slot_ok) report(p.st, CSA2_DEV_BAD_SLOT);
+      const bool in_t = t < p.T;  // rows past T are padding of the last M-tile
+      const int32_t slot = in_t ? __ldg(p.slot_of_token + t) : -1;
+      const bool slot_ok = in_t && slot >= 0 && slot < p.num_slots;
+      if (in_t && !slot_ok) report(p.st, CSA2_DEV_BAD_SLOT);
       const uint32_t tbase = tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(acc * BN);
       uint32_t sc[4] = {0, 0, 0, 0};
       const int col0 = n * BN;
@@ -326,7 +329,7 @@ cudaError_t launch_kv_write(const uint16_t* H, const uint16_t* Wt, uint8_t* code
   cudaError_t e = cudaFuncSetAttribute(kv_write_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  const int tiles = (T / BM) * ((n_out + BN - 1) / BN);
+  const int tiles = ((T + BM - 1) / BM) * ((n_out + BN - 1) / BN);
   const int grid = std::max(1, std::min(tiles, num_sms));
   kv_write_kernel<<<grid, kThreads, smem, s>>>(ta, tb, p);
   return cudaGetLastError();

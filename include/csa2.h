@@ -126,8 +126,9 @@ typedef struct {
  * Arithmetic: C = H.W with fp32 accumulation on the tensor cores; per token and
  * 16-channel block s = E4M3_RNE_satfinite(amax/6), codes = E2M1_RNE_sat(C/s) (IEEE
  * division, sign kept, s == 0 gives zero codes); indexer keys = bf16_RNE(C).
- * Requires T % 128 == 0, d_model % 64 == 0, 16-B aligned H and Wt.  Tokens whose slot
- * is out of range are skipped (CSA2_DEV_BAD_SLOT).
+ * Any T >= 1 (the prefill of a whole prompt, or decode-time append of one new token per
+ * sequence, each at its own slot); requires d_model % 64 == 0, 16-B aligned H and Wt.
+ * Tokens whose slot is out of range are skipped (CSA2_DEV_BAD_SLOT).
  */
 CSA2_API csa2_status csa2_kv_write(const uint16_t* H, const uint16_t* Wt, uint8_t* codes, uint8_t* scales,
                           uint16_t* k_idx, int32_t T, int32_t d_model, int32_t n_kv_proj,

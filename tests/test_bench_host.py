@@ -70,6 +70,19 @@ def test_reference_arm_line_on_tiny_workload():
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["unit"] == bench.UNIT
 
 
+def test_reference_arm_line_on_decode_append():
+    """The write path's reference arm on the decode-time append workload (2 of its 64 new
+    tokens through all 12800 projection columns)."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", "decode_append", "--steps", "1", "--warmup", "0",
+                          "--cpu-sample", "2"], capture_output=True, text=True, timeout=600,
+                         cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "tokens/s"
+    assert line["config"]["workload"].startswith("decode_append") and line["config"]["tokens"] == 64
+
+
 @pytest.mark.parametrize("world", [2])
 def test_reference_arm_under_torchrun_prints_once(world):
     env = dict(os.environ, CSA2_BENCH_BACKEND="gloo")
