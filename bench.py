@@ -552,12 +552,17 @@ def count_launches(wl, step) -> int:
     return n
 
 
+# Sources of the Full index call's kernels (the roofline line's kernels)
+INDEX_SOURCES = ("index.cu", "async.cuh", "common.cuh")
+
+
 def kernel_hash() -> str:
-    """Hash of the CUDA sources; traffic counters are only reported for this exact build."""
+    """Hash of the sources the Full index call's kernels are built from; its traffic
+    counters are only reported for this exact build of them."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp4_compressed_sparse_03_b300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in INDEX_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
