@@ -48,6 +48,12 @@ def lib():
         L.orc_select_topk.argtypes = [_f64p, _i32p, ctypes.c_int64, ctypes.c_int32, _i32p]
         L.orc_sparse_attention.argtypes = [_u16p, _f64p, ctypes.c_int64, ctypes.c_float, _f32p, _f32p]
         L.orc_e2m1_encode_array.argtypes = [_f32p, ctypes.c_int64, _u8p]
+        L.orc_e8m0_scale_for.restype = ctypes.c_uint8
+        L.orc_e8m0_scale_for.argtypes = [ctypes.c_float]
+        L.orc_e8m0_decode.restype = ctypes.c_double
+        L.orc_e8m0_decode.argtypes = [ctypes.c_uint8]
+        L.orc_mx_quantize_rows.argtypes = [_f32p, ctypes.c_int64, ctypes.c_int32, _u8p, _u8p]
+        L.orc_mx_dequantize_rows.argtypes = [_u8p, _u8p, ctypes.c_int64, ctypes.c_int32, _f64p]
         L.orc_e4m3_encode_array.argtypes = [_f32p, ctypes.c_int64, _u8p]
         _lib = L
     return _lib
@@ -99,6 +105,38 @@ def dequantize(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     T, half = codes.shape
     out = np.empty((T, half * 2), np.float64)
     lib().orc_dequantize_rows(_p(codes, _u8p), _p(scales, _u8p), T, half * 2, _p(out, _f64p))
+    return out
+
+
+# -------------------------------------------------------------- MXFP4 variant --
+# Tech-report digest, "FP4 メイン KV Cache と SWA Bounded Replay" (OCP-standard MXFP4,
+# E2M1 elements), read as OCP MX: E8M0 scale per 32 channels (see csa2_oracle.c).
+
+def e8m0_scale_for(amax: float) -> int:
+    return int(lib().orc_e8m0_scale_for(float(amax)))
+
+
+def e8m0_decode(b) -> np.ndarray:
+    return np.array([lib().orc_e8m0_decode(int(c)) for c in np.ravel(b)], dtype=np.float64)
+
+
+def mx_quantize(x: np.ndarray):
+    """fp32 [T, D] -> (codes u8 [T, D/2], E8M0 scales u8 [T, D/32])."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    T, D = x.shape
+    assert D % 32 == 0
+    codes = np.zeros((T, D // 2), np.uint8)
+    scales = np.zeros((T, D // 32), np.uint8)
+    lib().orc_mx_quantize_rows(_p(x, _f32p), T, D, _p(codes, _u8p), _p(scales, _u8p))
+    return codes, scales
+
+
+def mx_dequantize(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    T, half = codes.shape
+    out = np.empty((T, half * 2), np.float64)
+    lib().orc_mx_dequantize_rows(_p(codes, _u8p), _p(scales, _u8p), T, half * 2, _p(out, _f64p))
     return out
 
 

@@ -34,6 +34,16 @@ void orc_quantize_rows(const float* x, int64_t T, int32_t D, uint8_t* codes, uin
 void orc_dequantize_rows(const uint8_t* codes, const uint8_t* scales, int64_t T, int32_t D,
                          double* out);
 
+/* MXFP4 variant (tech-report digest "FP4 メイン KV Cache": OCP-standard MXFP4, E2M1),
+ * read as OCP MX: one E8M0 scale per 32 channels, X = 2^(floor(log2 amax) - 2) clamped to
+ * 2^-127..2^127; codes = E2M1_RNE_sat(x / X); zero block -> scale byte 0, zero codes.
+ * Codes [T][D/2] as above, scales [T][D/32]; D a multiple of 32. */
+uint8_t orc_e8m0_scale_for(float amax);
+double orc_e8m0_decode(uint8_t b);
+void orc_mx_quantize_rows(const float* x, int64_t T, int32_t D, uint8_t* codes, uint8_t* scales);
+void orc_mx_dequantize_rows(const uint8_t* codes, const uint8_t* scales, int64_t T, int32_t D,
+                            double* out);
+
 /* CED projection (tech-report digest "Causal Encoder-Decoder (CED)" equation C_l = H_{L/2} W_l^KV):
  * C[r][n] = fl32(sum_k H[r][k] * Wt[n][k]) with the sum in double.  H is bf16
  * [nrows][d_model]; the projection is stored output-major, Wt[n][k] = W[k][n]. */

@@ -155,6 +155,87 @@ def test_dequant_is_exact_product(orc):
             assert deq[r, c] == e2[code] * e4[r]
 
 
+# ------------------------------------------------------------------ MXFP4 variant --
+# The OCP Microscaling definition the oracle reads "MXFP4 (E2M1)" as: 32-element blocks,
+# E8M0 scale 2^(floor(log2 amax) - emax_elem) with emax_elem = 2 for E2M1 (largest
+# power of two 4), elements E2M1 round-to-nearest-even and saturating.
+
+def test_mx_scale_rule_closed_forms(orc):
+    """Scale bytes worked by hand from the definition (byte = exponent + 127)."""
+    cases = {1.0: 125, 1.5: 125, 0.75: 124, 3.0: 126, 3.999: 126, 4.0: 127, 6.0: 127,
+             7.99: 127, 8.0: 128, 100.0: 131, 2.0**-20: 105, 2.0**-125: 0, 2.0**-130: 0,
+             1.0e38: 251, 0.0: 0}
+    for amax, b in cases.items():
+        assert orc.e8m0_scale_for(amax) == b, amax
+    # library cross-check away from exact powers of two
+    rng = np.random.default_rng(7)
+    for amax in np.exp(rng.uniform(-40, 40, 200)).astype(np.float32):
+        assert orc.e8m0_scale_for(float(amax)) == int(np.floor(np.log2(np.float64(amax)))) - 2 + 127
+    assert list(orc.e8m0_decode([0, 125, 127, 130])) == [2.0**-127, 0.25, 1.0, 8.0]
+
+
+def test_mx_block_worked_by_hand(orc):
+    """amax 6.1 -> X = 2^(2-2) = 1: the elements are coded as plain E2M1 values."""
+    x = np.zeros((1, 64), np.float32)
+    x[0, :10] = [3.0, -1.5, 0.5, 2.9, 0.2, -0.3, 5.9, 6.1, -5.0, 0.25]
+    # second block: amax 0.3 -> X = 2^(-2-2) = 1/16, y = 16 x
+    x[0, 32:36] = [0.3, -0.0625, 0.01, 0.2]
+    codes, scales = orc.mx_quantize(x)
+    assert scales.tolist() == [[127, 123]]
+    nib = np.stack([codes[0] & 0xF, codes[0] >> 4], -1).ravel()
+    # 3 -> 3 (0b101), -1.5 -> -1.5, 0.5, 2.9 -> 3, 0.2 -> 0, -0.3 -> -0.5, 5.9 -> 6,
+    # 6.1 -> 6 (saturated), -5 -> -4 (tie to the even code), 0.25 -> 0 (tie to even)
+    assert nib[:10].tolist() == [0x5, 0xB, 0x1, 0x5, 0x0, 0x9, 0x7, 0x7, 0xE, 0x0]
+    # 4.8 -> 4 (0b110), -1 -> 0b1010, 0.16 -> 0, 3.2 -> 3
+    assert nib[32:36].tolist() == [0x6, 0xA, 0x0, 0x5]
+    assert not nib[10:32].any() and not nib[36:].any()
+    deq = orc.mx_dequantize(codes, scales)
+    assert deq[0, :10].tolist() == [3.0, -1.5, 0.5, 3.0, 0.0, -0.5, 6.0, 6.0, -4.0, 0.0]
+    assert deq[0, 32:36].tolist() == [0.25, -0.0625, 0.0, 0.1875]
+
+
+def test_mx_zero_and_tiny_blocks(orc):
+    x = np.zeros((2, 32), np.float32)
+    x[1, 0] = 2.0**-130  # below E8M0's range: the scale clamps to 2^-127, y = 1/8 -> 0
+    x[1, 1] = -(2.0**-127) * 0.75  # y = -0.75 -> -1 (tie to the even code 0b010)
+    codes, scales = orc.mx_quantize(x)
+    assert scales[0, 0] == 0 and not codes[0].any()
+    assert scales[1, 0] == 0
+    assert (codes[1, 0] & 0xF) == 0x0 and (codes[1, 0] >> 4) == 0xA
+
+
+def test_mx_block_properties_on_latent_rows(orc):
+    """Every nonzero block's largest element is coded 4 or 6 (y_max in [4, 8)); the error
+    is at most half an E2M1 step times X below 6 and y - 6 above it."""
+    gains = gen.latent_gains(0)
+    x = gen.latent_rows(0, 0, 0, np.arange(128), gains)
+    codes, scales = orc.mx_quantize(x)
+    deq = orc.mx_dequantize(codes, scales)
+    nib = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(128, 512)
+    mag = (nib & 7).reshape(128, 16, 32).max(axis=-1)
+    assert np.all(mag >= 6)
+    X = np.repeat(orc.e8m0_decode(scales.ravel()).reshape(128, 16), 32, axis=1)
+    y = np.abs(x.astype(np.float64)) / X
+    assert np.all(y < 8)
+    half = np.where(y <= 2, 0.25, np.where(y <= 4, 0.5, 1.0))
+    bound = np.where(y <= 6, half, y - 6)
+    err = np.abs(x - deq) / X
+    assert np.all(err <= bound * (1 + 1e-9) + 1e-12)
+
+
+def test_mx_against_e4m3_footprint_and_error(orc):
+    """Same latent rows through both formats: MX stores 272 B per 512 channels against
+    288 B, and its power-of-two, 32-wide scales cost accuracy."""
+    gains = gen.latent_gains(1)
+    x = gen.latent_rows(1, 0, 0, np.arange(256), gains).astype(np.float64)
+    c4, s4 = orc.quantize(x.astype(np.float32))
+    cm, sm = orc.mx_quantize(x.astype(np.float32))
+    assert c4.shape[1] + s4.shape[1] == 288 and cm.shape[1] + sm.shape[1] == 272
+    e4 = np.sqrt(np.mean((orc.dequantize(c4, s4) - x) ** 2)) / np.sqrt(np.mean(x ** 2))
+    em = np.sqrt(np.mean((orc.mx_dequantize(cm, sm) - x) ** 2)) / np.sqrt(np.mean(x ** 2))
+    assert 0.05 < e4 < em < 0.3, (e4, em)
+
+
 # ------------------------------------------------------------------ projection -----
 
 def _bf16(x):
