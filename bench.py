@@ -172,7 +172,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = workload_of(args.workload)
-    cache = fill_decode_cache(wl, device=dev)
+    mx = args.workload.endswith("_mx")  # the MXFP4 variant of the cache and read path
+    cache = fill_decode_cache(wl, device=dev, mx=mx)
     q_idx_h, q_h = all_queries_host(wl)
     q_idx = torch.from_numpy(q_idx_h.view(np.int16)).to(dev)
     q = torch.from_numpy(q_h.view(np.int16)).to(dev)
@@ -315,16 +316,17 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl, args.cpu_sample)
+        cpu = cpu_baseline(wl, args.cpu_sample, mx)
 
     launches_per_step = count_launches(wl, step)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp4-e2m1/e4m3 kv, bf16 keys+queries, f32 accumulate",
+        "dtype": ("fp4-e2m1/e8m0-per-32 (MXFP4) kv" if mx else "fp4-e2m1/e4m3 kv") +
+                 ", bf16 keys+queries, f32 accumulate",
         "data": "synthetic (seeded counter-based generator)",
-        "config": {"workload": wl.name, "num_seqs": int(len(wl.seq_lens)),
+        "config": {"workload": wl.name + ("_mxfp4" if mx else ""), "num_seqs": int(len(wl.seq_lens)),
                    "context_tokens": int(wl.seq_lens.max()), "query_tokens": wl.num_q,
                    "layers": L, "schedule": "".join("FRU"[m] for m in wl.schedule),
                    "pool": wl.pool_size, "topk": wl.topk,
@@ -521,6 +523,8 @@ def cpu_baseline_write(ww, sample_rows: int):
 
 def workload_of(name: str):
     import csa2_inputs as gen
+    if name.endswith("_mx"):  # the same workload over an MXFP4 cache
+        return workload_of(name[:-3])
     if name == "decode_batch16":   # the decode batch with 16 of its 64 sequences (profiling size)
         wl = gen.config_decode_batch()
         return gen.DecodeWorkload("decode_batch_16x131072", wl.seed, wl.seq_lens[:16],
@@ -570,7 +574,7 @@ def kernel_hash() -> str:
 
 # ------------------------------------------------------------------ CPU oracle ---
 
-def _oracle_query_step(wl, qi, keys, codes, scales, q_idx_h, q_h, scale):
+def _oracle_query_step(wl, qi, keys, codes, scales, q_idx_h, q_h, scale, mx=False):
     """The whole layer schedule for one query on the CPU oracle."""
     import csa2_inputs as gen
     import oracle
@@ -585,11 +589,11 @@ def _oracle_query_step(wl, qi, keys, codes, scales, q_idx_h, q_h, scale):
             idx[l], _ = oracle.index_reindex(q_idx_h[l][qi], keys, pool, wl.topk)
         else:
             idx[l] = oracle.index_reuse(idx[src[l]])
-        oracle.attention_over_cache(q_h[l][qi], codes, scales, idx[src[l]], scale)
+        oracle.attention_over_cache(q_h[l][qi], codes, scales, idx[src[l]], scale, mx=mx)
     return n
 
 
-def cpu_baseline(wl, sample_queries: int):
+def cpu_baseline(wl, sample_queries: int, mx: bool = False):
     """Time the oracle, as it stands, on a bounded sample of the workload: the full layer
     schedule for `sample_queries` queries, one host thread per query."""
     from concurrent.futures import ThreadPoolExecutor
@@ -611,7 +615,8 @@ def cpu_baseline(wl, sample_queries: int):
         b = int(wl.q_seq[qi])
         n = int(wl.seq_lens[b])
         keys = native.key_rows_host(wl.seed, 0, b, 0, n)
-        codes, scales = oracle.quantize(native.latent_rows_host(wl.seed, 0, b, 0, n, gains))
+        quant = oracle.mx_quantize if mx else oracle.quantize
+        codes, scales = quant(native.latent_rows_host(wl.seed, 0, b, 0, n, gains))
         return int(qi), keys, codes, scales
 
     with ThreadPoolExecutor(max_workers=cores) as ex:
@@ -620,8 +625,8 @@ def cpu_baseline(wl, sample_queries: int):
     threads = min(cores, len(inputs))
     t0 = time.perf_counter()
     with ThreadPoolExecutor(max_workers=threads) as ex:
-        list(ex.map(lambda a: _oracle_query_step(wl, a[0], a[1], a[2], a[3], q_idx_h, q_h, scale),
-                    inputs))
+        list(ex.map(lambda a: _oracle_query_step(wl, a[0], a[1], a[2], a[3], q_idx_h, q_h, scale,
+                                                 mx), inputs))
     dt = time.perf_counter() - t0
     return {"value": round(len(inputs) * L / dt, 3), "unit": UNIT, "cores": threads,
             "kind": "oracle",
@@ -639,11 +644,11 @@ def run_reference(args, world, rank):
     wl = workload_of(args.workload)
     per_step = max(1, args.cpu_sample // max(1, args.steps))
     for _ in range(max(0, min(args.warmup, 1))):
-        cpu_baseline(wl, 1)
+        cpu_baseline(wl, 1, args.workload.endswith("_mx"))
     vals = []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        vals.append(cpu_baseline(wl, per_step))
+        vals.append(cpu_baseline(wl, per_step, args.workload.endswith("_mx")))
     dt = time.perf_counter() - t0
     v = float(np.mean([c["value"] for c in vals]))
     cb = dict(vals[-1])
@@ -654,7 +659,8 @@ def run_reference(args, world, rank):
             "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64 (CPU oracle)",
             "data": "synthetic (seeded counter-based generator)",
-            "config": {"workload": wl.name, "num_seqs": int(len(wl.seq_lens)),
+            "config": {"workload": wl.name + ("_mxfp4" if args.workload.endswith("_mx") else ""),
+                       "num_seqs": int(len(wl.seq_lens)),
                        "context_tokens": int(wl.seq_lens.max()), "query_tokens": wl.num_q,
                        "layers": len(wl.schedule), "pool": wl.pool_size, "topk": wl.topk},
             "cpu_baseline": cb,
@@ -700,7 +706,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_batch",
                     choices=["decode_batch", "decode_batch16", "decode_short", "long_context", "ragged", "tiny",
-                             "ced_write", "decode_append"])
+                             "ced_write", "decode_append", "decode_batch_mx", "decode_short_mx"])
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-sample", type=int, default=None,
                     help="queries (decode) or token rows (write workloads) timed on the oracle; "

@@ -66,6 +66,9 @@ _index_ws = _sig("csa2_index_workspace_size", _sz, [ctypes.c_int, _i32, _i32, _i
 _attn = _sig("csa2_sparse_attn", ctypes.c_int,
              [_vp, _vp, _vp, _vp, ctypes.POINTER(Csa2Pages), _vp, _vp, _i32, _vp, _i32,
               ctypes.c_float, _vp, _sz, _vp, _vp])
+_attn_mx = _sig("csa2_sparse_attn_mx", ctypes.c_int,
+                [_vp, _vp, _vp, _vp, ctypes.POINTER(Csa2Pages), _vp, _vp, _i32, _vp, _i32,
+                 ctypes.c_float, _vp, _sz, _vp, _vp])
 _attn_ws = _sig("csa2_attn_workspace_size", _sz, [_i32, _i32])
 _attn_static = _sig("csa2_sparse_attn_static", ctypes.c_int,
                     [_vp, _vp, _vp, _vp, ctypes.POINTER(Csa2Pages), _vp, _vp, _i32, _vp, _i32,
@@ -74,6 +77,9 @@ ATTN_STATIC_SCRATCH_BYTES = 16 << 20  # CSA2_ATTN_STATIC_SCRATCH_BYTES
 ATTN_MAX_TOPK = 65536  # CSA2_ATTN_MAX_TOPK
 _quantize = _sig("csa2_quantize", ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp])
 _dequantize = _sig("csa2_dequantize", ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp])
+_quantize_mx = _sig("csa2_quantize_mx", ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp])
+_dequantize_mx = _sig("csa2_dequantize_mx", ctypes.c_int,
+                      [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp])
 _read_status = _sig("csa2_read_status", ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp])
 _status_string = _sig("csa2_status_string", ctypes.c_char_p, [ctypes.c_int])
 _version = _sig("csa2_version", _i32, [])
@@ -171,6 +177,16 @@ def csa2_sparse_attn_static(q, codes, scales, idx, pages: Csa2Pages, out, lse, n
                         ctypes.c_float(softmax_scale), _ptr(dev_status), _stream(stream))
 
 
+def csa2_sparse_attn_mx(q, codes, scales, idx, pages: Csa2Pages, out, lse, num_q, q_seq, topk,
+                        softmax_scale, workspace=None, workspace_bytes=None, dev_status=None,
+                        stream=None) -> int:
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return _attn_mx(_ptr(q), _ptr(codes), _ptr(scales), _ptr(idx), ctypes.byref(pages), _ptr(out),
+                    _ptr(lse), num_q, _ptr(q_seq), topk, ctypes.c_float(softmax_scale),
+                    _ptr(workspace), workspace_bytes, _ptr(dev_status), _stream(stream))
+
+
 def csa2_quantize(x, slot_of_token, codes, scales, T, D, num_slots, dev_status=None,
                   stream=None) -> int:
     return _quantize(_ptr(x), _ptr(slot_of_token), _ptr(codes), _ptr(scales), T, D, num_slots,
@@ -181,6 +197,18 @@ def csa2_dequantize(codes, scales, slot_of_token, x, T, D, num_slots, dev_status
                     stream=None) -> int:
     return _dequantize(_ptr(codes), _ptr(scales), _ptr(slot_of_token), _ptr(x), T, D, num_slots,
                        _ptr(dev_status), _stream(stream))
+
+
+def csa2_quantize_mx(x, slot_of_token, codes, scales, T, D, num_slots, dev_status=None,
+                     stream=None) -> int:
+    return _quantize_mx(_ptr(x), _ptr(slot_of_token), _ptr(codes), _ptr(scales), T, D, num_slots,
+                        _ptr(dev_status), _stream(stream))
+
+
+def csa2_dequantize_mx(codes, scales, slot_of_token, x, T, D, num_slots, dev_status=None,
+                       stream=None) -> int:
+    return _dequantize_mx(_ptr(codes), _ptr(scales), _ptr(slot_of_token), _ptr(x), T, D,
+                          num_slots, _ptr(dev_status), _stream(stream))
 
 
 def csa2_read_status(dev_status, stream=None):

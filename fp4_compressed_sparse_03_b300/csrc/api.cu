@@ -10,6 +10,10 @@ cudaError_t launch_quantize(const float*, const int32_t*, uint8_t*, uint8_t*, in
                             int64_t, int32_t*, cudaStream_t, int);
 cudaError_t launch_dequantize(const uint8_t*, const uint8_t*, const int32_t*, float*, int32_t,
                               int32_t, int64_t, int32_t*, cudaStream_t, int);
+cudaError_t launch_quantize_mx(const float*, const int32_t*, uint8_t*, uint8_t*, int32_t, int32_t,
+                               int64_t, int32_t*, cudaStream_t, int);
+cudaError_t launch_dequantize_mx(const uint8_t*, const uint8_t*, const int32_t*, float*, int32_t,
+                                 int32_t, int64_t, int32_t*, cudaStream_t, int);
 cudaError_t launch_score_full(const uint16_t*, const uint16_t*, const int32_t*, int32_t, int32_t,
                               const csa2_pages&, uint32_t*, int64_t, void*, uint32_t*, int32_t*,
                               cudaStream_t, int);
@@ -23,7 +27,7 @@ cudaError_t launch_select(bool, const uint32_t*, int64_t, const int32_t*, const 
 size_t wide_select_bytes(int32_t num_q, int32_t n);
 cudaError_t launch_attn(const uint16_t*, const uint8_t*, const uint8_t*, const int32_t*,
                         const csa2_pages&, float*, float*, int32_t, const int32_t*, int32_t, float,
-                        void*, int32_t*, cudaStream_t, int);
+                        void*, int32_t*, cudaStream_t, int, bool);
 size_t attn_workspace_bytes(int32_t, int32_t, int);
 cudaError_t launch_kv_write(const uint16_t*, const uint16_t*, uint8_t*, uint8_t*, uint16_t*,
                             int32_t, int32_t, int32_t, int32_t, const int32_t*, int64_t, int32_t*,
@@ -100,6 +104,30 @@ csa2_status csa2_dequantize(const uint8_t* codes, const uint8_t* scales,
   if (!al16(x) || (reinterpret_cast<uintptr_t>(codes) & 7u)) return CSA2_ERR_INVALID_ARGUMENT;
   return from_cuda(launch_dequantize(codes, scales, slot_of_token, x, T, D, num_slots, dev_status,
                                      stream, device_sms()));
+}
+
+csa2_status csa2_quantize_mx(const float* x, const int32_t* slot_of_token, uint8_t* codes,
+                             uint8_t* scales, int32_t T, int32_t D, int64_t num_slots,
+                             int32_t* dev_status, cudaStream_t stream) {
+  if (T < 0 || D <= 0 || num_slots < 0) return CSA2_ERR_INVALID_ARGUMENT;
+  if (D % 32 != 0 || D > 4096) return CSA2_ERR_UNSUPPORTED;
+  if (T == 0) return CSA2_OK;
+  if (!x || !slot_of_token || !codes || !scales) return CSA2_ERR_INVALID_ARGUMENT;
+  if (!al16(x) || !al16(codes)) return CSA2_ERR_INVALID_ARGUMENT;
+  return from_cuda(launch_quantize_mx(x, slot_of_token, codes, scales, T, D, num_slots,
+                                      dev_status, stream, device_sms()));
+}
+
+csa2_status csa2_dequantize_mx(const uint8_t* codes, const uint8_t* scales,
+                               const int32_t* slot_of_token, float* x, int32_t T, int32_t D,
+                               int64_t num_slots, int32_t* dev_status, cudaStream_t stream) {
+  if (T < 0 || D <= 0 || num_slots < 0) return CSA2_ERR_INVALID_ARGUMENT;
+  if (D % 32 != 0 || D > 4096) return CSA2_ERR_UNSUPPORTED;
+  if (T == 0) return CSA2_OK;
+  if (!x || !slot_of_token || !codes || !scales) return CSA2_ERR_INVALID_ARGUMENT;
+  if (!al16(x) || !al16(codes)) return CSA2_ERR_INVALID_ARGUMENT;
+  return from_cuda(launch_dequantize_mx(codes, scales, slot_of_token, x, T, D, num_slots,
+                                        dev_status, stream, device_sms()));
 }
 
 // Scores (one 32-bit key per candidate) followed, at a 256-byte boundary, by the FULL
@@ -187,11 +215,13 @@ size_t csa2_attn_workspace_size(int32_t num_q, int32_t topk) {
   return attn_workspace_bytes(num_q, topk, device_sms());
 }
 
-csa2_status csa2_sparse_attn(const uint16_t* q, const uint8_t* codes, const uint8_t* scales,
-                             const int32_t* idx, const csa2_pages* pages, float* out, float* lse,
-                             int32_t num_q, const int32_t* q_seq, int32_t topk, float softmax_scale,
-                             void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                             cudaStream_t stream) {
+// csa2_sparse_attn and its MXFP4 variant: the same checks, the scale format chosen by `mx`.
+static csa2_status sparse_attn_call(bool mx, const uint16_t* q, const uint8_t* codes,
+                                    const uint8_t* scales, const int32_t* idx,
+                                    const csa2_pages* pages, float* out, float* lse, int32_t num_q,
+                                    const int32_t* q_seq, int32_t topk, float softmax_scale,
+                                    void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                    cudaStream_t stream) {
   if (num_q < 1 || topk < 1 || !q || !codes || !scales || !idx || !out || !q_seq)
     return CSA2_ERR_INVALID_ARGUMENT;
   csa2_status ps = check_pages(pages);
@@ -205,7 +235,25 @@ csa2_status csa2_sparse_attn(const uint16_t* q, const uint8_t* codes, const uint
   if (need > 0 && (workspace == nullptr || workspace_bytes < need || !al16(workspace)))
     return CSA2_ERR_INVALID_ARGUMENT;
   return from_cuda(launch_attn(q, codes, scales, idx, *pages, out, lse, num_q, q_seq, topk,
-                               softmax_scale, workspace, dev_status, stream, sms));
+                               softmax_scale, workspace, dev_status, stream, sms, mx));
+}
+
+csa2_status csa2_sparse_attn(const uint16_t* q, const uint8_t* codes, const uint8_t* scales,
+                             const int32_t* idx, const csa2_pages* pages, float* out, float* lse,
+                             int32_t num_q, const int32_t* q_seq, int32_t topk, float softmax_scale,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                             cudaStream_t stream) {
+  return sparse_attn_call(false, q, codes, scales, idx, pages, out, lse, num_q, q_seq, topk,
+                          softmax_scale, workspace, workspace_bytes, dev_status, stream);
+}
+
+csa2_status csa2_sparse_attn_mx(const uint16_t* q, const uint8_t* codes, const uint8_t* scales,
+                                const int32_t* idx, const csa2_pages* pages, float* out,
+                                float* lse, int32_t num_q, const int32_t* q_seq, int32_t topk,
+                                float softmax_scale, void* workspace, size_t workspace_bytes,
+                                int32_t* dev_status, cudaStream_t stream) {
+  return sparse_attn_call(true, q, codes, scales, idx, pages, out, lse, num_q, q_seq, topk,
+                          softmax_scale, workspace, workspace_bytes, dev_status, stream);
 }
 
 csa2_status csa2_kv_write(const uint16_t* H, const uint16_t* Wt, uint8_t* codes, uint8_t* scales,

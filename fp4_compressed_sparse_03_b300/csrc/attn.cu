@@ -28,6 +28,13 @@
 // within 2^28 of the largest |q|); the scale is undone in the logit factor.  Several
 // splits per query are merged by a log-sum-exp combine kernel.
 //
+// MXFP4 variant (tech-report digest, "FP4 メイン KV Cache と SWA Bounded Replay": OCP MXFP4,
+// read as one E8M0 scale per 32 channels): E8M0 scales span 2^-127 .. 2^127, beyond f16.
+// The kernel gathers the scale bytes of the whole split up front, takes their maximum
+// `ref`, and builds the same f16 operands as code x 2^(e - ref), which is exact for
+// e >= ref - 23 (smaller contributions, 2^23 below the split's largest scale, lose
+// precision or vanish); 2^(ref - 127) is folded into the logit factor and the output.
+//
 // A 128-token tile holds only 2 M multiply-adds per product, so the kernel is bound by
 // the dequantisation arithmetic and per-tile latency, not by tensor throughput; operands
 // built in registers avoid writing a dequantised f16 tile to shared memory and reading
@@ -60,21 +67,28 @@ constexpr float kRescaleGap = 8.0f;     // log2 units
 
 static_assert(kSliceCh == 64 && kAttnThreads == 2 * kTile, "layout assumes 8 warps, 128-token tiles");
 
-struct AttnSmem {
-  unsigned char stage[kStages][kStageBytes];
+template <bool kMx>
+struct AttnSmemT {
+  // E4M3: codes + scales of each tile; MXFP4: codes only (the split's scales below)
+  unsigned char stage[kStages][kMx ? kStageCodes : kStageBytes];
   float red[kKSplit][kHq][kRedStride];     // S^T partials; reused to stage the output
   uint16_t p[kHq][kTile];                  // P (f16): 16-byte units XOR-swizzled by head
   float alpha[kHq];
   float m_fin[kHq], l_fin[kHq];
   uint32_t qmax[kAttnWarps];
+  uint32_t smax[kAttnWarps];
   int32_t slot[kMaxSplit];  // physical row of each selected entry, -1 if skipped
+  unsigned char mxs[kMx ? kMaxSplit : 1][16];  // MXFP4: E8M0 bytes of every selected entry
 };
-static_assert(offsetof(AttnSmem, red) % 16 == 0 && offsetof(AttnSmem, p) % 16 == 0,
-              "vector accesses need 16-byte alignment");
+template <bool kMx>
+constexpr bool attn_layout_ok() {
+  return offsetof(AttnSmemT<kMx>, red) % 16 == 0 && offsetof(AttnSmemT<kMx>, p) % 16 == 0 &&
+         offsetof(AttnSmemT<kMx>, mxs) % 16 == 0 &&
+         kAttnCtasPerSm * (sizeof(AttnSmemT<kMx>) + 1024) <= 233472;
+}
+static_assert(attn_layout_ok<false>() && attn_layout_ok<true>(),
+              "16-byte alignment of vector accesses; two CTAs per SM");
 static_assert(kHq * kOStride <= kKSplit * kHq * kRedStride, "output staging fits the partials");
-constexpr size_t kAttnSmem = sizeof(AttnSmem);
-static_assert(kAttnCtasPerSm * (kAttnSmem + 1024) <= 233472,
-              "sparse attention CTAs do not fit an SM's shared memory");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -133,6 +147,18 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
                : "memory");
 }
 
+// f16 bits of 2^(e - ref), e <= ref: normal down to 2^-14, subnormal to 2^-24, else 0.
+__device__ __forceinline__ uint32_t mx_factor_f16(uint32_t e, int ref) {
+  const int d = (int)e - ref;
+  if (d >= -14) return (uint32_t)(d + 15) << 10;
+  if (d >= -24) return 1u << (d + 24);
+  return 0u;
+}
+// 2^k as a float, k in [-127, 127] (2^-127 is subnormal, exact).
+__device__ __forceinline__ float pow2f_attn(int k) {
+  return k >= -126 ? __uint_as_float((uint32_t)(k + 127) << 23) : __uint_as_float(1u << 22);
+}
+
 // Position of tile row r in code slice s: rows 4..7 of every group of 8 are stored in
 // reverse order, so that both the S-phase reads (8 consecutive rows, 8 bytes each) and
 // the O-phase reads (rows 2i or 2i + 1, i = 0..3, of a group) hit distinct banks; the
@@ -152,6 +178,7 @@ struct AttnGeom {
 // Gather the tile starting at local entry `e0`.  Codes: 16 lanes per row, lane -> one
 // 16-byte piece, so each warp instruction reads two whole 256-byte rows.  Scales: two
 // lanes per row.
+template <bool kMx>
 __device__ __forceinline__ void issue_tile(unsigned char* stage, int e0, int ecount,
                                            const int32_t* slot, const uint8_t* __restrict__ codes,
                                            const uint8_t* __restrict__ scales) {
@@ -165,6 +192,7 @@ __device__ __forceinline__ void issue_tile(unsigned char* stage, int e0, int eco
     cp_async16(stage + sl_i * kSliceStride + slice_row(r, sl_i) * kSliceBytes + 16 * (piece & 1),
                codes + (ok ? (int64_t)sl * kCodeRow : 0) + 16 * piece, ok);
   }
+  if (kMx) return;  // the split's scales were gathered up front
   const int r = threadIdx.x >> 1, h = threadIdx.x & 1;
   const int e = e0 + r;
   const int32_t sl = e < ecount ? slot[e] : -1;
@@ -173,6 +201,7 @@ __device__ __forceinline__ void issue_tile(unsigned char* stage, int e0, int eco
              scales + (ok ? (int64_t)sl * kScaleRow : 0) + 16 * h, ok);
 }
 
+template <bool kMx>
 __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     sparse_attn_kernel(const uint16_t* __restrict__ q, const uint8_t* __restrict__ codes,
                        const uint8_t* __restrict__ scales, const int32_t* __restrict__ idx,
@@ -181,7 +210,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                        float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* st) {
   grid_dep_wait();
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  AttnSmem& sm = *reinterpret_cast<AttnSmem*>(smem_raw);
+  AttnSmemT<kMx>& sm = *reinterpret_cast<AttnSmemT<kMx>*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gq = lane >> 2, iq = lane & 3;  // mma fragment: row group, column pair
   const int qi = blockIdx.y, split = blockIdx.x, nsplit = gridDim.x;
@@ -236,7 +265,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
   __syncthreads();
 #pragma unroll
   for (int i = 0; i < kStages - 1; ++i) {
-    if (i < ntiles) issue_tile(sm.stage[i], i * kTile, ecount, sm.slot, codes, scales);
+    if (i < ntiles) issue_tile<kMx>(sm.stage[i], i * kTile, ecount, sm.slot, codes, scales);
     cp_async_commit();
   }
 #pragma unroll
@@ -267,7 +296,30 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
   }
   const float pre = __uint_as_float((uint32_t)(127 + sh) << 23);   // 2^sh
   const float post = __uint_as_float((uint32_t)(127 - sh) << 23);  // 2^-sh
-  const float kq = softmax_scale * 1.4426950408889634f * post;  // logits in the exp2 domain
+  float kq = softmax_scale * 1.4426950408889634f * post;  // logits in the exp2 domain
+  int mx_ref = 0;  // MXFP4: largest E8M0 byte of the split
+  if constexpr (kMx) {
+    // gather every selected entry's 16 scale bytes (the slots are published above)
+    for (int e = tid; e < kMaxSplit; e += kAttnThreads) {
+      const bool ok = e < ecount && sm.slot[e] >= 0;
+      cp_async16(&sm.mxs[e][0], scales + (ok ? (int64_t)sm.slot[e] * 16 : 0), ok);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+    uint32_t m4 = 0;
+    for (int e = tid; e < kMaxSplit; e += kAttnThreads) {
+      const uint4 v = *reinterpret_cast<const uint4*>(&sm.mxs[e][0]);
+      m4 = __vmaxu4(m4, __vmaxu4(__vmaxu4(v.x, v.y), __vmaxu4(v.z, v.w)));
+    }
+    uint32_t m = max(max(m4 & 0xFFu, (m4 >> 8) & 0xFFu), max((m4 >> 16) & 0xFFu, m4 >> 24));
+    m = __reduce_max_sync(0xffffffffu, m);
+    if (lane == 0) sm.smax[warp] = m;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) mx_ref = max(mx_ref, (int)sm.smax[w]);
+    kq *= pow2f_attn(mx_ref - 127);
+  }
   // k-step 4 j + kk covers channels 16 iq + 4 kk .. + 3 of slice j: a0/a1 the first pair
   // (heads gq / gq + 8), a2/a3 the second -- the byte order of the staged codes
   uint32_t qa[8][4];
@@ -294,7 +346,8 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     __syncthreads();               // everyone's; and every warp is done with tile t - 1
     {
       const int tn = t + kStages - 1;
-      if (tn < ntiles) issue_tile(sm.stage[tn % kStages], tn * kTile, ecount, sm.slot, codes, scales);
+      if (tn < ntiles)
+        issue_tile<kMx>(sm.stage[tn % kStages], tn * kTile, ecount, sm.slot, codes, scales);
       cp_async_commit();
     }
     const unsigned char* stg = sm.stage[t % kStages];
@@ -310,9 +363,15 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         const uint2 cw = *reinterpret_cast<const uint2*>(stg + sl_i * kSliceStride +
                                                          slice_row(tok, sl_i) * kSliceBytes + 8 * iq);
         // one scale: these 16 channels are one group
-        const uint32_t sb = stg[kStageCodes + (sl_i >> 2) * kScaleHalf + stage_row(tok) * 16 +
-                                4 * (sl_i & 3) + iq];
-        const uint32_t s2 = e4m3x2_to_f16x2(sb | (sb << 8));
+        uint32_t s2;
+        if constexpr (kMx) {
+          const uint32_t f = mx_factor_f16(sm.mxs[t * kTile + tok][2 * sl_i + (iq >> 1)], mx_ref);
+          s2 = f | (f << 16);
+        } else {
+          const uint32_t sb = stg[kStageCodes + (sl_i >> 2) * kScaleHalf + stage_row(tok) * 16 +
+                                  4 * (sl_i & 3) + iq];
+          s2 = e4m3x2_to_f16x2(sb | (sb << 8));
+        }
         uint32_t bf[8];
         e2m1x4_unpack(cw.x, bf[0], bf[1], bf[2], bf[3]);
         e2m1x4_unpack(cw.y, bf[4], bf[5], bf[6], bf[7]);
@@ -406,9 +465,19 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
       const uint32_t x1 = *reinterpret_cast<const uint32_t*>(cs + (r1 ^ xs) * kSliceBytes + 4 * gq);
       const uint32_t x8 = *reinterpret_cast<const uint32_t*>(cs + (r8 ^ xs) * kSliceBytes + 4 * gq);
       const uint32_t x9 = *reinterpret_cast<const uint32_t*>(cs + (r9 ^ xs) * kSliceBytes + 4 * gq);
-      const int sg = gq >> 1;  // scale group of this thread's channels 8 gq .. 8 gq + 7
-      const uint32_t s01 = e4m3x2_to_f16x2(ss[r0 * 16 + sg] | ((uint32_t)ss[r1 * 16 + sg] << 8));
-      const uint32_t s89 = e4m3x2_to_f16x2(ss[r8 * 16 + sg] | ((uint32_t)ss[r9 * 16 + sg] << 8));
+      uint32_t s01, s89;
+      if constexpr (kMx) {  // E8M0 group of channels 8 gq .. 8 gq + 7 of slice `warp`
+        const int gi = 2 * warp + (gq >> 2);
+        const int eb = t * kTile + t0;
+        s01 = mx_factor_f16(sm.mxs[eb][gi], mx_ref) |
+              (mx_factor_f16(sm.mxs[eb + 1][gi], mx_ref) << 16);
+        s89 = mx_factor_f16(sm.mxs[eb + 8][gi], mx_ref) |
+              (mx_factor_f16(sm.mxs[eb + 9][gi], mx_ref) << 16);
+      } else {
+        const int sg = gq >> 1;  // scale group of this thread's channels 8 gq .. 8 gq + 7
+        s01 = e4m3x2_to_f16x2(ss[r0 * 16 + sg] | ((uint32_t)ss[r1 * 16 + sg] << 8));
+        s89 = e4m3x2_to_f16x2(ss[r8 * 16 + sg] | ((uint32_t)ss[r9 * 16 + sg] << 8));
+      }
       // byte p of lo: the even channel of code byte 4 gq + p for the two tokens (first
       // token in the low nibble); hi: the odd channel
       const uint32_t lo01 = (x0 & 0x0F0F0F0Fu) | ((x1 << 4) & 0xF0F0F0F0u);
@@ -433,6 +502,13 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
   // ---- epilogue: stage the 16 x 512 output through shared memory ----
   // n-tile 2 p + hb, column c <-> channel 64 warp + 8 c + 2 p + hb
   float* ob = &sm.red[0][0][0];
+  if constexpr (kMx) {  // back to absolute scale: x 2^(ref - 127), exact
+    const float fo = pow2f_attn(mx_ref - 127);
+#pragma unroll
+    for (int n = 0; n < 8; ++n)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) oacc[n][c] *= fo;
+  }
 #pragma unroll
   for (int n = 0; n < 8; ++n) {
     const int ch = warp * kSliceCh + 16 * iq + 2 * (n >> 1) + (n & 1);
@@ -568,26 +644,26 @@ int attn_split_len(int32_t topk, int splits) {
   return per * kTile;
 }
 
-size_t attn_smem_bytes() { return kAttnSmem; }
+size_t attn_smem_bytes(bool mx) { return mx ? sizeof(AttnSmemT<true>) : sizeof(AttnSmemT<false>); }
 
 cudaError_t launch_attn(const uint16_t* q, const uint8_t* codes, const uint8_t* scales,
                         const int32_t* idx, const csa2_pages& pg, float* out, float* lse,
                         int32_t num_q, const int32_t* q_seq, int32_t topk, float softmax_scale,
-                        void* ws, int32_t* st, cudaStream_t s, int num_sms) {
+                        void* ws, int32_t* st, cudaStream_t s, int num_sms, bool mx) {
   AttnGeom g{pg.seq_lens, pg.page_table, pg.max_pages_per_seq, pg.num_pages, pg.num_seqs};
   int splits = attn_splits(num_q, topk, num_sms);
   const int split_len = attn_split_len(topk, splits);
   splits = (topk + split_len - 1) / split_len;
   if (splits < 1) splits = 1;
-  const size_t smem = attn_smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = attn_smem_bytes(mx);
+  auto kern = mx ? sparse_attn_kernel<true> : sparse_attn_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   float* part_o = reinterpret_cast<float*>(ws);
   float* part_ml = part_o + (int64_t)num_q * splits * kHq * kDkv;
   dim3 grid(splits, num_q);
-  e = launch_pdl(sparse_attn_kernel, grid, dim3(kAttnThreads), smem, s, q, codes, scales, idx, g,
-                 q_seq, topk, split_len, softmax_scale, out, lse, part_o, part_ml, st);
+  e = launch_pdl(kern, grid, dim3(kAttnThreads), smem, s, q, codes, scales, idx, g, q_seq, topk,
+                 split_len, softmax_scale, out, lse, part_o, part_ml, st);
   if (e != cudaSuccess) return e;
   if (splits > 1)
     e = launch_pdl(attn_combine_kernel, dim3(num_q, kHq), dim3(128), 0, s, (const float*)part_o,

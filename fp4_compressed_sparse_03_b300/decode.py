@@ -15,22 +15,26 @@ import torch
 
 from . import (CSA2_FULL, CSA2_REINDEX, CSA2_REUSE, D_IDX, D_KV, H_IDX, H_Q, PAGE, check,
                csa2_attn_workspace_size, csa2_index, csa2_index_workspace_size,
-               csa2_sparse_attn, make_index_args, make_pages)
+               csa2_sparse_attn, csa2_sparse_attn_mx, make_index_args, make_pages)
 
 
 class DecodeCache:
-    """Paged FP4 latent (codes + E4M3 scales) and bf16 indexer keys of `n_groups`
-    Full-layer groups, sharing one page table."""
+    """Paged FP4 latent (codes + E4M3 scales per 16 channels, or E8M0 scales per 32 for
+    the MXFP4 variant) and bf16 indexer keys of `n_groups` Full-layer groups, sharing one
+    page table."""
 
-    def __init__(self, seq_lens, page_table, num_pages: int, n_groups: int = 1, device="cuda"):
+    def __init__(self, seq_lens, page_table, num_pages: int, n_groups: int = 1, device="cuda",
+                 mx: bool = False):
         self.device = torch.device(device)
         self.seq_lens = torch.as_tensor(np.asarray(seq_lens, np.int32), device=self.device)
         self.page_table = torch.as_tensor(np.asarray(page_table, np.int32), device=self.device)
         self.num_pages = int(num_pages)
         self.n_groups = int(n_groups)
+        self.mx = bool(mx)
         slots = self.num_pages * PAGE
         self.codes = torch.zeros((n_groups, slots, D_KV // 2), dtype=torch.uint8, device=self.device)
-        self.scales = torch.zeros((n_groups, slots, D_KV // 16), dtype=torch.uint8, device=self.device)
+        self.scales = torch.zeros((n_groups, slots, D_KV // (32 if mx else 16)), dtype=torch.uint8,
+                                  device=self.device)
         self.keys = torch.zeros((n_groups, slots, D_IDX), dtype=torch.int16, device=self.device)
         self.pages = make_pages(self.seq_lens, self.page_table, self.num_pages)
 
@@ -99,9 +103,10 @@ class DecodeStep:
     def layer_attn(self, l: int, q_l, stream=None) -> None:
         g, s = self.group[l], self.src[l]
         c = self.cache
-        check(csa2_sparse_attn(q_l, c.codes[g], c.scales[g], self.idx[s], c.pages, self.out[l],
-                               self.lse[l], self.num_q, self.q_seq, self.topk, self.softmax_scale,
-                               self.workspace, None, self.dev_status, stream),
+        attn = csa2_sparse_attn_mx if c.mx else csa2_sparse_attn
+        check(attn(q_l, c.codes[g], c.scales[g], self.idx[s], c.pages, self.out[l], self.lse[l],
+                   self.num_q, self.q_seq, self.topk, self.softmax_scale, self.workspace, None,
+                   self.dev_status, stream),
               f"csa2_sparse_attn(layer {l})")
 
     def run(self, q_idx, q, stream=None) -> None:

@@ -13,19 +13,21 @@ import torch
 import csa2_inputs as gen
 from csa2_inputs import native
 
-from . import check, csa2_quantize
+from . import check, csa2_quantize, csa2_quantize_mx
 from .decode import DecodeCache
 
 _CHUNK = 1 << 18  # latent rows staged per quantise call (512 MB of fp32)
 
 
 def fill_decode_cache(wl: gen.DecodeWorkload, n_groups: int | None = None, device="cuda",
-                      stream=None) -> DecodeCache:
-    """A DecodeCache holding every Full group's quantised latent and indexer keys."""
+                      stream=None, mx: bool = False) -> DecodeCache:
+    """A DecodeCache holding every Full group's quantised latent (E4M3 / 16, or the MXFP4
+    variant with `mx`) and indexer keys."""
     if n_groups is None:
         n_groups = max(1, sum(1 for m in wl.schedule if m == gen.FULL))
     lay = wl.layout
-    cache = DecodeCache(lay.seq_lens, lay.page_table, lay.num_pages, n_groups, device)
+    cache = DecodeCache(lay.seq_lens, lay.page_table, lay.num_pages, n_groups, device, mx=mx)
+    quant = csa2_quantize_mx if mx else csa2_quantize
     B = len(lay.seq_lens)
     max_len = int(lay.seq_lens.max()) if B else 0
     stage = torch.empty((min(_CHUNK, max(max_len, 1)), gen.D_KV), dtype=torch.float32,
@@ -43,8 +45,8 @@ def fill_decode_cache(wl: gen.DecodeWorkload, n_groups: int | None = None, devic
                 native.fill_latent_dev(stage[:n], key, t0, gains, stream)
                 slots = torch.as_tensor(lay.slots(b, np.arange(t0, t0 + n)).astype(np.int32),
                                         device=cache.device)
-                check(csa2_quantize(stage[:n], slots, cache.codes[g], cache.scales[g], n, gen.D_KV,
-                                    cache.num_slots, None, stream), "csa2_quantize")
+                check(quant(stage[:n], slots, cache.codes[g], cache.scales[g], n, gen.D_KV,
+                            cache.num_slots, None, stream), "csa2_quantize")
     torch.cuda.synchronize()
     return cache
 

@@ -190,6 +190,21 @@ CSA2_API csa2_status csa2_sparse_attn(const uint16_t* q, const uint8_t* codes, c
 
 CSA2_API size_t csa2_attn_workspace_size(int32_t num_q, int32_t topk);
 
+/* csa2_sparse_attn over an MXFP4 cache (tech-report digest, "FP4 メイン KV Cache と SWA
+ * Bounded Replay": OCP MXFP4, E2M1 elements; read as one E8M0 scale per 32 channels, the
+ * layout csa2_quantize_mx writes): scales uint8 [num_pages*64][16], c_hat = e2m1(code) *
+ * 2^(byte - 127).  Same arguments, workspace and results otherwise.  The kernel rebases
+ * every split's scales on their largest byte `ref`; a value is represented exactly when
+ * its scale byte is at least ref - 23, and contributions more than 2^23 below the
+ * split's largest scale lose precision or vanish. */
+CSA2_API csa2_status csa2_sparse_attn_mx(const uint16_t* q, const uint8_t* codes,
+                                         const uint8_t* scales, const int32_t* idx,
+                                         const csa2_pages* pages, float* out, float* lse,
+                                         int32_t num_q, const int32_t* q_seq, int32_t topk,
+                                         float softmax_scale, void* workspace,
+                                         size_t workspace_bytes, int32_t* dev_status,
+                                         cudaStream_t stream);
+
 /* csa2_sparse_attn without caller workspace.  The pages have no counterpart to this
  * entry point: it exists for callers that cannot allocate device memory around the
  * call (plain C clients that hold no device allocator, or decode loops that must not
@@ -224,6 +239,25 @@ CSA2_API csa2_status csa2_quantize(const float* x, const int32_t* slot_of_token,
 CSA2_API csa2_status csa2_dequantize(const uint8_t* codes, const uint8_t* scales,
                             const int32_t* slot_of_token, float* x, int32_t T, int32_t D,
                             int64_t num_slots, int32_t* dev_status, cudaStream_t stream);
+
+/* MXFP4 variant of the codec (tech-report digest, "FP4 メイン KV Cache と SWA Bounded
+ * Replay": the main KV in the OCP-standard MXFP4 format, E2M1 elements), read as OCP MX:
+ * one E8M0 scale byte per 32 channels, X = 2^(floor(log2 amax) - 2) clamped to
+ * 2^-127 .. 2^127 (byte = exponent + 127); codes = E2M1_RNE_satfinite(x / X), sign kept;
+ * a block whose amax is 0 gets scale byte 0 and zero codes.  Dequantised values are
+ * e2m1(code) * 2^(byte - 127) in fp32 (exact within fp32's range).  272 B per 512
+ * channels against 288 B for E4M3 / 16.
+ *   x      fp32 [T][D], D % 32 == 0, D <= 4096, 16-B aligned
+ *   slot_of_token int32 [T] destination / source row in [0, num_slots)
+ *   codes  uint8 [num_slots][D/2], 16-B aligned;  scales uint8 [num_slots][D/32]
+ */
+CSA2_API csa2_status csa2_quantize_mx(const float* x, const int32_t* slot_of_token, uint8_t* codes,
+                                      uint8_t* scales, int32_t T, int32_t D, int64_t num_slots,
+                                      int32_t* dev_status, cudaStream_t stream);
+CSA2_API csa2_status csa2_dequantize_mx(const uint8_t* codes, const uint8_t* scales,
+                                        const int32_t* slot_of_token, float* x, int32_t T,
+                                        int32_t D, int64_t num_slots, int32_t* dev_status,
+                                        cudaStream_t stream);
 
 /* ------------------------------------------------------------------ status --------
  * Synchronises `stream`, copies *dev_status to *host_bits (host, nullable), resets

@@ -242,11 +242,13 @@ def sparse_attention(q: np.ndarray, chat: np.ndarray, softmax_scale: float):
 
 
 def attention_over_cache(q: np.ndarray, codes_rows: np.ndarray, scales_rows: np.ndarray,
-                         idx: np.ndarray, softmax_scale: float):
+                         idx: np.ndarray, softmax_scale: float, mx: bool = False):
     """Gather the selected rows (codes/scales given per logical token of the sequence),
-    dequantise them, attend.  -1 entries of idx are skipped."""
+    dequantise them (E4M3 / 16, or the MXFP4 variant with `mx`), attend.  -1 entries of
+    idx are skipped."""
     sel = idx[idx >= 0]
-    chat = dequantize(codes_rows[sel], scales_rows[sel]) if sel.size else np.zeros((0, 512))
+    deq = mx_dequantize if mx else dequantize
+    chat = deq(codes_rows[sel], scales_rows[sel]) if sel.size else np.zeros((0, 512))
     return sparse_attention(q, chat, softmax_scale)
 
 

@@ -35,6 +35,9 @@ def test_host_side_checks_without_device():
     assert L.csa2_index(0, None, None, None, 16, None, None, None, None) == csa2.CSA2_ERR_INVALID_ARGUMENT
     assert L.csa2_quantize(None, None, None, None, -1, 512, 0, None, None) == csa2.CSA2_ERR_INVALID_ARGUMENT
     assert L.csa2_quantize(None, None, None, None, 4, 24, 4, None, None) == csa2.CSA2_ERR_UNSUPPORTED
+    assert L.csa2_quantize_mx(None, None, None, None, 4, 48, 4, None, None) == csa2.CSA2_ERR_UNSUPPORTED
+    assert L.csa2_dequantize_mx(None, None, None, None, -1, 64, 4, None, None) == \
+        csa2.CSA2_ERR_INVALID_ARGUMENT
     assert L.csa2_kv_write(None, None, None, None, None, 4, 64, 1, 0, None, 4, None, None) == \
         csa2.CSA2_ERR_INVALID_ARGUMENT
     assert L.csa2_read_status(None, None, None) == csa2.CSA2_ERR_INVALID_ARGUMENT

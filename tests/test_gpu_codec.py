@@ -144,3 +144,32 @@ def test_host_argument_errors():
     assert csa2.csa2_quantize(None, s, c, sc, 4, 512, 4) == csa2.CSA2_ERR_INVALID_ARGUMENT
     assert csa2.csa2_quantize(x[:, 1:], s, c, sc, 4, 496, 4) == csa2.CSA2_ERR_INVALID_ARGUMENT
     assert csa2.csa2_quantize(x, s, c, sc, 0, 512, 4) == csa2.CSA2_OK
+
+
+def test_mx_codec_bit_exact_with_special_blocks():
+    """MXFP4 variant (OCP MX reading, E8M0 per 32 channels): codes and scales bit-exact
+    against the oracle on latent rows plus hand-made blocks (all zero, all negative zero,
+    below E8M0's range, amax near 1e31), and the dequantised values equal the oracle's
+    exact products."""
+    x = gen.latent_rows(3, 0, 0, np.arange(2048), gen.latent_gains(3))
+    x[0, :32] = 0.0
+    x[1, :32] = 0.0
+    x[1, 0] = 2.0**-130
+    x[1, 1] = -(2.0**-127) * 0.75
+    x[2, :32] *= 1e30
+    x[3, 32:64] = -0.0
+    x[4, :10] = [3.0, -1.5, 0.5, 2.9, 0.2, -0.3, 5.9, 6.1, -5.0, 0.25]
+    T, D = x.shape
+    slots = np.random.default_rng(5).permutation(T).astype(np.int32)
+    codes = torch.zeros((T, D // 2), dtype=torch.uint8, device="cuda")
+    scales = torch.zeros((T, D // 32), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    csa2.check(csa2.csa2_quantize_mx(dev(x), dev(slots), codes, scales, T, D, T, st), "quantize_mx")
+    oc, os_ = oracle.mx_quantize(x)
+    assert np.array_equal(host(codes)[slots], oc)
+    assert np.array_equal(host(scales)[slots], os_)
+    out = torch.full((T, D), np.nan, dtype=torch.float32, device="cuda")
+    csa2.check(csa2.csa2_dequantize_mx(codes, scales, dev(slots), out, T, D, T, st), "dequantize_mx")
+    assert np.array_equal(host(out), oracle.mx_dequantize(oc, os_).astype(np.float32))
+    status, bits = csa2.csa2_read_status(st)
+    assert status == csa2.CSA2_OK, hex(bits)

@@ -286,6 +286,66 @@ def test_attention_random_index_sets():
                 assert_attn_close(host(out[i]), o, host(lse[i]), l, f"topk {topk} q{i}")
 
 
+def test_mx_attention_random_index_sets():
+    """The MXFP4 read path (csa2_sparse_attn_mx over a cache written by csa2_quantize_mx)
+    against the oracle's attention over its own MXFP4 dequantisation: single- and
+    multi-split launches, -1 padding and an empty set."""
+    lens = np.array([3000, 100, 5000], np.int32)
+    wl = gen.DecodeWorkload("attn_mx", 23, lens, np.ones(3, np.int32), [gen.FULL], 0, 16)
+    cache = fill_decode_cache(wl, mx=True)
+    for topk, nq in [(256, 3), (2048, 3), (64, 3)]:
+        q_seq = np.array([0, 1, 2][:nq], np.int32)
+        idx = np.stack([gen.random_index_set(23, 100 * topk + i, int(lens[b]), topk,
+                                             n_invalid=(7 if i == 0 else 0))
+                        for i, b in enumerate(q_seq)])
+        if topk == 64:
+            idx[1] = -1
+        q = np.stack([gen.q_rows(23, topk, np.array([i]))[0] for i in range(nq)])
+        out = torch.zeros((nq, 16, 512), dtype=torch.float32, device="cuda")
+        lse = torch.zeros((nq, 16), dtype=torch.float32, device="cuda")
+        ws = torch.empty(max(csa2.csa2_attn_workspace_size(nq, topk), 16), dtype=torch.uint8,
+                         device="cuda")
+        csa2.check(csa2.csa2_sparse_attn_mx(dev(q), cache.codes[0], cache.scales[0], dev(idx),
+                                            cache.pages, out, lse, nq, dev(q_seq), topk,
+                                            SOFTMAX_SCALE, ws), "attn_mx")
+        for i, b in enumerate(q_seq):
+            sel = idx[i][idx[i] >= 0]
+            x = gen.latent_rows(23, 0, int(b), sel, gen.latent_gains(23))
+            c, s = oracle.mx_quantize(x)
+            o, l = oracle.sparse_attention(q[i], oracle.mx_dequantize(c, s), SOFTMAX_SCALE)
+            if sel.size == 0:
+                assert np.all(host(out[i]) == 0) and np.all(np.isneginf(host(lse[i])))
+            else:
+                assert_attn_close(host(out[i]), o, host(lse[i]), l, f"mx topk {topk} q{i}")
+
+
+def test_mx_attention_scale_spread():
+    """Rows scaled by 2^k, k in [-10, 10] per token, so the E8M0 bytes of one split span
+    more than 20 values: the kernel's rebasing on the split's largest scale keeps the
+    result within tolerance of the oracle."""
+    T = 512
+    cache = DecodeCache(np.array([T], np.int32), np.arange(T // 64, dtype=np.int32).reshape(1, -1),
+                        T // 64, mx=True)
+    k = np.random.default_rng(11).integers(-10, 11, T)
+    x = (gen.latent_rows(31, 0, 0, np.arange(T), gen.latent_gains(31)) *
+         np.exp2(k)[:, None]).astype(np.float32)
+    csa2.check(csa2.csa2_quantize_mx(dev(x), dev(np.arange(T, dtype=np.int32)), cache.codes[0],
+                                     cache.scales[0], T, 512, cache.num_slots), "quantize_mx")
+    c, s = oracle.mx_quantize(x)
+    assert np.array_equal(host(cache.codes[0]), c) and np.array_equal(host(cache.scales[0]), s)
+    assert int(s.max()) - int(s.min()) > 20
+    q = gen.q_rows(31, 0, np.array([0]))
+    idx = np.arange(T, dtype=np.int32).reshape(1, T)
+    out = torch.zeros((1, 16, 512), dtype=torch.float32, device="cuda")
+    lse = torch.zeros((1, 16), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(csa2.csa2_attn_workspace_size(1, T), 16), dtype=torch.uint8, device="cuda")
+    csa2.check(csa2.csa2_sparse_attn_mx(dev(q), cache.codes[0], cache.scales[0], dev(idx),
+                                        cache.pages, out, lse, 1, dev(np.zeros(1, np.int32)), T,
+                                        SOFTMAX_SCALE, ws), "attn_mx")
+    o, l = oracle.sparse_attention(q[0], oracle.mx_dequantize(c, s), SOFTMAX_SCALE)
+    assert_attn_close(host(out[0]), o, host(lse[0]), l, "mx scale spread")
+
+
 def test_attention_dense_equals_all_tokens():
     """K = N: the sparse path over every token equals the oracle's dense attention."""
     wl = gen.DecodeWorkload("dense", 29, np.array([512], np.int32), np.ones(1, np.int32),
