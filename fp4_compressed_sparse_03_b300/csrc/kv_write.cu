@@ -9,10 +9,11 @@
 // Kernel design (sm_103a):
 //   - persistent CTAs, one per SM, 128 x 256 output tiles (bf16 operands, fp32
 //     accumulation), K consumed in 64-wide blocks through a 4-stage TMA ring
-//     (128-byte swizzle, both operands K-major);
-//   - warp 0 lane 0 issues TMA, warp 1 lane 0 issues tcgen05.mma (M=128, N=256, K=16)
-//     into one of two TMEM accumulators (2 x 256 columns), warps 2..5 run the epilogue
-//     of the previous tile while the next one accumulates;
+//     (128-byte swizzle, both operands K-major); for T <= 128 (one M-tile: the weight
+//     stream is the whole cost) 128 x 128 tiles through a 6-stage ring;
+//   - warp 0 lane 0 issues TMA, warp 1 lane 0 issues tcgen05.mma (M=128, N=256 or 128,
+//     K=16) into one of two TMEM accumulators, warps 2..5 run the epilogue of the
+//     previous tile while the next one accumulates;
 //   - epilogue: tcgen05.ld 32 columns of one row per thread, then per 16-channel block
 //     amax -> E4M3(amax/6) -> E2M1(x/s) packed codes + scale byte (latent
 //     projections), or bf16 RNE (indexer-key projections), stored at the token's slot;
@@ -28,23 +29,33 @@ namespace csa2 {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
-constexpr int B_BYTES = BN * BK * 2;            // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
 constexpr int kThreads = 192;                   // 6 warps
 constexpr int kGroupM = 16;
-constexpr int kTmemCols = 512;
 
-struct Bars {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
-  uint64_t fin;
-  uint32_t tmem_base;
-  volatile int abort;
+// Output tile width BN and TMA ring depth.  Prefill-sized T: 256 columns, 4 stages of
+// 48 KB.  A single M-tile (T <= 128, e.g. decode-time append of one token per sequence)
+// is bound by streaming the weights: 128 columns and 6 stages of 32 KB double the CTAs
+// that stream them and the weight bytes each keeps in flight.
+template <int BN, int STAGES>
+struct KvCfg {
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int kTmemCols = 2 * BN;  // two accumulators
+  struct Bars {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t fin;
+    uint32_t tmem_base;
+    volatile int abort;
+  };
+  static constexpr size_t smem_bytes() { return (size_t)STAGES * STAGE_BYTES + sizeof(Bars) + 1024; }
 };
+static_assert(KvCfg<256, 4>::smem_bytes() <= 232448 && KvCfg<128, 6>::smem_bytes() <= 232448,
+              "write-path ring exceeds 227 KB of shared memory");
 
 __device__ __forceinline__ void fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -126,9 +137,14 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int&
 
 }  // namespace
 
+template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     kv_write_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     WriteParams p) {
+  using Cfg = KvCfg<BN, STAGES>;
+  using Bars = typename Cfg::Bars;
+  constexpr int STAGE_BYTES = Cfg::STAGE_BYTES;
+  constexpr int kTmemCols = Cfg::kTmemCols;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -274,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* crow = p.codes + ((int64_t)proj * p.num_slots + slot) * kCodeRow + c / 2;
           *reinterpret_cast<uint4*>(crow) = make_uint4(w[0], w[1], w[2], w[3]);
-          const int sidx = (c / kGroup) & 15;  // position of this pair within the 16-scale run
+          const int sidx = (c / kGroup) & (BN / kGroup - 1);  // position within the tile's scales
           sc[sidx >> 2] |= s2 << (8 * (sidx & 3));
         } else {
           const int ic = col - kv_cols;
@@ -292,8 +308,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (kv_tile && slot_ok) {
         const int proj = col0 / kDkv, c = col0 - proj * kDkv;
-        *reinterpret_cast<uint4*>(p.scales + ((int64_t)proj * p.num_slots + slot) * kScaleRow +
-                                  c / kGroup) = make_uint4(sc[0], sc[1], sc[2], sc[3]);
+        uint8_t* srow = p.scales + ((int64_t)proj * p.num_slots + slot) * kScaleRow + c / kGroup;
+        if constexpr (BN == 256)
+          *reinterpret_cast<uint4*>(srow) = make_uint4(sc[0], sc[1], sc[2], sc[3]);
+        else
+          *reinterpret_cast<uint2*>(srow) = make_uint2(sc[0], sc[1]);
       }
       fence_before();
       mbar_arrive(&bars->tempty[acc]);
@@ -313,26 +332,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-size_t kv_write_smem_bytes() { return (size_t)STAGES * STAGE_BYTES + sizeof(Bars) + 1024; }
+namespace {
+
+template <int BN, int STAGES>
+cudaError_t launch_kv_write_cfg(const uint16_t* H, const uint16_t* Wt, const WriteParams& p,
+                                cudaStream_t s, int num_sms) {
+  CUtensorMap ta, tb;
+  if (!make_bf16_map(&ta, H, p.T, p.d_model, BK, BM) ||
+      !make_bf16_map(&tb, Wt, p.n_out, p.d_model, BK, BN))
+    return cudaErrorInvalidValue;
+  const size_t smem = KvCfg<BN, STAGES>::smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(kv_write_kernel<BN, STAGES>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int tiles = ((p.T + BM - 1) / BM) * ((p.n_out + BN - 1) / BN);
+  const int grid = std::max(1, std::min(tiles, num_sms));
+  kv_write_kernel<BN, STAGES><<<grid, kThreads, smem, s>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
 
 cudaError_t launch_kv_write(const uint16_t* H, const uint16_t* Wt, uint8_t* codes, uint8_t* scales,
                             uint16_t* k_idx, int32_t T, int32_t d_model, int32_t n_kv_proj,
                             int32_t n_idx_proj, const int32_t* slot_of_token, int64_t num_slots,
                             int32_t* st, cudaStream_t s, int num_sms) {
   const int32_t n_out = n_kv_proj * kDkv + n_idx_proj * kDidx;
-  CUtensorMap ta, tb;
-  if (!make_bf16_map(&ta, H, T, d_model, BK, BM) || !make_bf16_map(&tb, Wt, n_out, d_model, BK, BN))
-    return cudaErrorInvalidValue;
   WriteParams p{codes, scales, k_idx, slot_of_token, num_slots, T, d_model, n_kv_proj, n_idx_proj,
                 n_out, st};
-  const size_t smem = kv_write_smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(kv_write_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
-  const int tiles = ((T + BM - 1) / BM) * ((n_out + BN - 1) / BN);
-  const int grid = std::max(1, std::min(tiles, num_sms));
-  kv_write_kernel<<<grid, kThreads, smem, s>>>(ta, tb, p);
-  return cudaGetLastError();
+  if (T <= BM) return launch_kv_write_cfg<128, 6>(H, Wt, p, s, num_sms);
+  return launch_kv_write_cfg<256, 4>(H, Wt, p, s, num_sms);
 }
 
 }  // namespace csa2
