@@ -501,6 +501,120 @@ def run_write(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_pages(args, world, rank, local):
+    """Persistent KV tier: export every page of the 64 x 16384-token cache (16384 pages of
+    34816 B: codes, scales, keys) per step with csa2_export_pages.  The roofline is HBM:
+    each record is read once and written once.  End to end adds the copy of the packed
+    pages into pinned host memory (the host tier)."""
+    import torch
+    import fp4_compressed_sparse_03_b300 as csa2
+    from fp4_compressed_sparse_03_b300.workload import fill_decode_cache
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = workload_of("decode_short")
+    cache = fill_decode_cache(wl, device=dev)
+    lay = wl.layout
+    ids = np.concatenate([lay.page_table[b, :-(-int(n) // 64)] for b, n in enumerate(lay.seq_lens)])
+    ids_d = torch.as_tensor(ids.astype(np.int32), device=dev)
+    n = len(ids)
+    rec = csa2.csa2_page_export_bytes(32)
+    packed = torch.empty(n * rec, dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        csa2.check(csa2.csa2_export_pages(cache.codes[0], cache.scales[0], cache.keys[0], 32,
+                                          cache.num_pages, ids_d, n, packed, st, stream))
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    clocks = ClockSampler(local)
+    barrier(world)
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(K):
+        call()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    status, bits = csa2.csa2_read_status(st)
+    if status != csa2.CSA2_OK:
+        raise RuntimeError(f"device status {bits:#x} after timed steps")
+    ms_step = reduce_max(t0.elapsed_time(t1) / K, world, dev)
+    tokens = n * 64 * world
+    value = tokens / (ms_step / 1e3)
+    hbm_peak, _, peak_src = load_peaks()
+    abytes = 2 * n * rec + n * 4
+    achieved = abytes / (t0.elapsed_time(t1) / K / 1e3) / 1e9
+    host_buf = torch.empty(n * rec, dtype=torch.uint8).pin_memory()
+    K2 = max(1, min(K, args.e2e_steps, 5))
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    w0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(K2):
+        call()
+        host_buf.copy_(packed, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_e2e = reduce_max(max(e0.elapsed_time(e1) / K2, (time.perf_counter() - w0) / K2 * 1e3),
+                        world, dev)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_pages(args.cpu_sample)
+    line = {
+        "metric": "persistent KV tier: tokens/s of cache pages exported (codes, scales, keys)",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8 (byte copy)",
+        "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": "page_export_64x16384", "pages": n, "record_bytes": rec,
+                   "l2": "no flush: %.0f MB of pages per step (> 126 MB L2)" % (n * rec / 1e6),
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "csa2_export_pages: page_copy_kernel",
+                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src + " HBM copy",
+                     "algorithmic_bytes_per_launch": int(abytes), "traffic": None},
+        "e2e": {"value": round(tokens / (ms_e2e / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": int(n * rec), "steps": K2},
+        "gpu_launches": K,
+        "clocks": clk,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def cpu_baseline_pages(sample_pages: int, repeats: int = 200):
+    """The oracle's page-record layout (numpy) on `sample_pages` pages of the first
+    sequence of the 64 x 16384 cache, packed `repeats` times."""
+    import csa2_inputs as gen
+    import oracle
+    from csa2_inputs import native
+    wl = workload_of("decode_short")
+    n = min(sample_pages, 256) * 64
+    gains = gen.latent_gains(wl.seed, 0)
+    codes, scales = oracle.quantize(native.latent_rows_host(wl.seed, 0, 0, 0, n, gains))
+    keys = native.key_rows_host(wl.seed, 0, 0, 0, n)
+    ids = np.arange(n // 64)
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        oracle.pack_pages(codes, scales, keys, ids)
+    dt = time.perf_counter() - t0
+    return {"value": round(repeats * n / dt, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n // 64} pages of page_export_64x16384 packed {repeats} times, "
+                      f"{dt:.1f} s on 1 thread"}
+
+
 def cpu_baseline_write(ww, sample_rows: int):
     """The oracle's write path (double-accumulated projection, then quantise / round) on
     `sample_rows` token rows, one host thread per row."""
@@ -641,6 +755,21 @@ def run_reference(args, world, rank):
         return
     if args.workload in ("ced_write", "decode_append"):
         return run_reference_write(args, world)
+    if args.workload == "page_export":
+        cb = cpu_baseline_pages(args.cpu_sample)
+        line = {"impl": "reference",
+                "metric": "persistent KV tier: tokens/s of cache pages exported (codes, scales, keys)",
+                "value": cb["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup,
+                # a step exports the cache's 16384 pages (1048576 tokens)
+                "ms_per_step": round(1048576 / cb["value"] * 1e3, 2), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "u8 (CPU oracle, numpy)",
+                "data": "synthetic (seeded counter-based generator)",
+                "config": {"workload": "page_export_64x16384"}, "cpu_baseline": cb,
+                "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
     wl = workload_of(args.workload)
     per_step = max(1, args.cpu_sample // max(1, args.steps))
     for _ in range(max(0, min(args.warmup, 1))):
@@ -706,7 +835,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_batch",
                     choices=["decode_batch", "decode_batch16", "decode_short", "long_context", "ragged", "tiny",
-                             "ced_write", "decode_append", "decode_batch_mx", "decode_short_mx"])
+                             "ced_write", "decode_append", "decode_batch_mx", "decode_short_mx",
+                             "page_export"])
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-sample", type=int, default=None,
                     help="queries (decode) or token rows (write workloads) timed on the oracle; "
@@ -715,13 +845,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.cpu_sample is None:
-        args.cpu_sample = {"ced_write": 256, "decode_append": 64}.get(args.workload, 32)
+        args.cpu_sample = {"ced_write": 256, "decode_append": 64,
+                           "page_export": 256}.get(args.workload, 32)
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
     elif args.workload in ("ced_write", "decode_append"):
         args.warmup = max(3, args.warmup)
         run_write(args, world, rank, local)
+    elif args.workload == "page_export":
+        args.warmup = max(3, args.warmup)
+        run_pages(args, world, rank, local)
     else:
         args.warmup = max(3, args.warmup)
         run_ours(args, world, rank, local)

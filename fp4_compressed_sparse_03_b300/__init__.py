@@ -80,6 +80,11 @@ _dequantize = _sig("csa2_dequantize", ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _
 _quantize_mx = _sig("csa2_quantize_mx", ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp])
 _dequantize_mx = _sig("csa2_dequantize_mx", ctypes.c_int,
                       [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp])
+_page_bytes = _sig("csa2_page_export_bytes", _sz, [_i32])
+_export_pages = _sig("csa2_export_pages", ctypes.c_int,
+                     [_vp, _vp, _vp, _i32, _i64, _vp, _i32, _vp, _vp, _vp])
+_import_pages = _sig("csa2_import_pages", ctypes.c_int,
+                     [_vp, _i32, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _vp])
 _read_status = _sig("csa2_read_status", ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp])
 _status_string = _sig("csa2_status_string", ctypes.c_char_p, [ctypes.c_int])
 _version = _sig("csa2_version", _i32, [])
@@ -209,6 +214,22 @@ def csa2_dequantize_mx(codes, scales, slot_of_token, x, T, D, num_slots, dev_sta
                        stream=None) -> int:
     return _dequantize_mx(_ptr(codes), _ptr(scales), _ptr(slot_of_token), _ptr(x), T, D,
                           num_slots, _ptr(dev_status), _stream(stream))
+
+
+def csa2_page_export_bytes(scale_row_bytes: int) -> int:
+    return int(_page_bytes(scale_row_bytes))
+
+
+def csa2_export_pages(codes, scales, keys, scale_row_bytes, num_pages, page_ids, n_pages, packed,
+                      dev_status=None, stream=None) -> int:
+    return _export_pages(_ptr(codes), _ptr(scales), _ptr(keys), scale_row_bytes, num_pages,
+                         _ptr(page_ids), n_pages, _ptr(packed), _ptr(dev_status), _stream(stream))
+
+
+def csa2_import_pages(packed, scale_row_bytes, page_ids, n_pages, num_pages, codes, scales, keys,
+                      dev_status=None, stream=None) -> int:
+    return _import_pages(_ptr(packed), scale_row_bytes, _ptr(page_ids), n_pages, num_pages,
+                         _ptr(codes), _ptr(scales), _ptr(keys), _ptr(dev_status), _stream(stream))
 
 
 def csa2_read_status(dev_status, stream=None):

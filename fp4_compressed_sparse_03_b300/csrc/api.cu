@@ -29,6 +29,9 @@ cudaError_t launch_attn(const uint16_t*, const uint8_t*, const uint8_t*, const i
                         const csa2_pages&, float*, float*, int32_t, const int32_t*, int32_t, float,
                         void*, int32_t*, cudaStream_t, int, bool);
 size_t attn_workspace_bytes(int32_t, int32_t, int);
+size_t page_export_bytes(int);
+cudaError_t launch_page_copy(bool, uint8_t*, uint8_t*, uint8_t*, int, int64_t, const int32_t*,
+                             int32_t, uint8_t*, int32_t*, cudaStream_t, int);
 cudaError_t launch_kv_write(const uint16_t*, const uint16_t*, uint8_t*, uint8_t*, uint16_t*,
                             int32_t, int32_t, int32_t, int32_t, const int32_t*, int64_t, int32_t*,
                             cudaStream_t, int);
@@ -272,6 +275,44 @@ csa2_status csa2_kv_write(const uint16_t* H, const uint16_t* Wt, uint8_t* codes,
   if (d_model % 64 != 0) return CSA2_ERR_UNSUPPORTED;
   return from_cuda(launch_kv_write(H, Wt, codes, scales, k_idx, T, d_model, n_kv_proj, n_idx_proj,
                                    slot_of_token, num_slots, dev_status, stream, device_sms()));
+}
+
+size_t csa2_page_export_bytes(int32_t scale_row_bytes) {
+  if (scale_row_bytes != 32 && scale_row_bytes != 16) return 0;
+  return page_export_bytes(scale_row_bytes);
+}
+
+static csa2_status page_copy_call(bool do_export, const uint8_t* codes, const uint8_t* scales,
+                                  const uint16_t* keys, int32_t scale_row_bytes, int64_t num_pages,
+                                  const int32_t* page_ids, int32_t n_pages, const uint8_t* packed,
+                                  int32_t* dev_status, cudaStream_t stream) {
+  if (n_pages < 0 || num_pages < 0) return CSA2_ERR_INVALID_ARGUMENT;
+  if (scale_row_bytes != 32 && scale_row_bytes != 16) return CSA2_ERR_UNSUPPORTED;
+  if (n_pages == 0) return CSA2_OK;
+  if (!codes || !scales || !keys || !page_ids || !packed) return CSA2_ERR_INVALID_ARGUMENT;
+  if (!al16(codes) || !al16(scales) || !al16(keys) || !al16(packed))
+    return CSA2_ERR_INVALID_ARGUMENT;
+  return from_cuda(launch_page_copy(do_export, const_cast<uint8_t*>(codes),
+                                    const_cast<uint8_t*>(scales),
+                                    reinterpret_cast<uint8_t*>(const_cast<uint16_t*>(keys)),
+                                    scale_row_bytes, num_pages, page_ids, n_pages,
+                                    const_cast<uint8_t*>(packed), dev_status, stream, device_sms()));
+}
+
+csa2_status csa2_export_pages(const uint8_t* codes, const uint8_t* scales, const uint16_t* keys,
+                              int32_t scale_row_bytes, int64_t num_pages, const int32_t* page_ids,
+                              int32_t n_pages, uint8_t* packed, int32_t* dev_status,
+                              cudaStream_t stream) {
+  return page_copy_call(true, codes, scales, keys, scale_row_bytes, num_pages, page_ids, n_pages,
+                        packed, dev_status, stream);
+}
+
+csa2_status csa2_import_pages(const uint8_t* packed, int32_t scale_row_bytes,
+                              const int32_t* page_ids, int32_t n_pages, int64_t num_pages,
+                              uint8_t* codes, uint8_t* scales, uint16_t* keys, int32_t* dev_status,
+                              cudaStream_t stream) {
+  return page_copy_call(false, codes, scales, keys, scale_row_bytes, num_pages, page_ids, n_pages,
+                        packed, dev_status, stream);
 }
 
 csa2_status csa2_read_status(int32_t* dev_status, int32_t* host_bits, cudaStream_t stream) {

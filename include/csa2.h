@@ -259,6 +259,34 @@ CSA2_API csa2_status csa2_dequantize_mx(const uint8_t* codes, const uint8_t* sca
                                         int32_t D, int64_t num_slots, int32_t* dev_status,
                                         cudaStream_t stream);
 
+/* ------------------------------------------------------------------ persistent tier -
+ * Export / import of whole cache pages for the persistent KV tier (zaikei article,
+ * opening section: the persistent KV cache that resumes sessions lives on SSD or in host
+ * memory; tech-report digest, "FP4 メイン KV Cache と SWA Bounded Replay": the
+ * sliding-window KV is left out of it, so what persists is the global cache).  A page
+ * record holds the page's 64 tokens:
+ *   codes [64][256] u8 | scales [64][S] u8 | keys [64][128] bf16
+ * with S = scale_row_bytes: 32 for E4M3 per 16 channels, 16 for the MXFP4 variant.
+ * Records are packed back to back in page_ids order; csa2_page_export_bytes(S) is the
+ * record size (34816 or 33792 B), 0 for any other S.
+ *   codes, scales, keys  the pools of one Full group ([num_pages*64][256], [..][S],
+ *          [..][128] bf16), 16-B aligned
+ *   page_ids int32 [n_pages] (device) physical pages to export from / import into
+ *   packed  n_pages records, 16-B aligned, device memory or host memory the GPU can
+ *          address (mapped pinned memory)
+ * Export copies the pages into `packed`; import copies the records into the pages.  Page
+ * ids outside [0, num_pages) set CSA2_DEV_BAD_PAGE: export writes a zero record, import
+ * skips it.  S other than 16 or 32 returns CSA2_ERR_UNSUPPORTED. */
+CSA2_API size_t csa2_page_export_bytes(int32_t scale_row_bytes);
+CSA2_API csa2_status csa2_export_pages(const uint8_t* codes, const uint8_t* scales,
+                                       const uint16_t* keys, int32_t scale_row_bytes,
+                                       int64_t num_pages, const int32_t* page_ids, int32_t n_pages,
+                                       uint8_t* packed, int32_t* dev_status, cudaStream_t stream);
+CSA2_API csa2_status csa2_import_pages(const uint8_t* packed, int32_t scale_row_bytes,
+                                       const int32_t* page_ids, int32_t n_pages, int64_t num_pages,
+                                       uint8_t* codes, uint8_t* scales, uint16_t* keys,
+                                       int32_t* dev_status, cudaStream_t stream);
+
 /* ------------------------------------------------------------------ status --------
  * Synchronises `stream`, copies *dev_status to *host_bits (host, nullable), resets
  * the device word to 0 and returns CSA2_ERR_TIMEOUT if CSA2_DEV_TIMEOUT was set,

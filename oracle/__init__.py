@@ -252,6 +252,31 @@ def attention_over_cache(q: np.ndarray, codes_rows: np.ndarray, scales_rows: np.
     return sparse_attention(q, chat, softmax_scale)
 
 
+# ------------------------------------------------------------- persistent tier ---
+# zaikei article, opening section: the persistent KV cache that resumes sessions lives on
+# SSD or in host memory; tech-report digest, "FP4 メイン KV Cache と SWA Bounded Replay":
+# the sliding-window KV is left out of it, so the persisted state is the global cache.
+# One record per page: the codes of its 64 slots, then their scales, then their keys
+# (bf16, little-endian bytes).
+
+def pack_pages(codes: np.ndarray, scales: np.ndarray, keys: np.ndarray, page_ids) -> np.ndarray:
+    """codes u8 [slots, 256], scales u8 [slots, S], keys u16 [slots, 128] -> the records of
+    `page_ids`, back to back (a page id outside the pool gives a zero record)."""
+    S = scales.shape[1]
+    rec = 64 * (256 + S + 256)
+    n_pages = codes.shape[0] // 64
+    out = []
+    for pg in np.asarray(page_ids).ravel():
+        pg = int(pg)
+        if pg < 0 or pg >= n_pages:
+            out.append(np.zeros(rec, np.uint8))
+            continue
+        rows = slice(64 * pg, 64 * pg + 64)
+        out.append(np.concatenate([codes[rows].ravel(), scales[rows].ravel(),
+                                   np.ascontiguousarray(keys[rows], dtype="<u2").view(np.uint8).ravel()]))
+    return np.concatenate(out) if out else np.zeros(0, np.uint8)
+
+
 # ------------------------------------------------------------------- footprint ---
 
 PAGES_FOOTPRINT = {

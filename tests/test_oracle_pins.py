@@ -236,6 +236,28 @@ def test_mx_against_e4m3_footprint_and_error(orc):
     assert 0.05 < e4 < em < 0.3, (e4, em)
 
 
+# ------------------------------------------------------------------ persistent tier --
+
+def test_pack_pages_worked_by_hand(orc):
+    """Two pages with recognisable bytes: each record is the page's 64 code rows, then its
+    64 scale rows, then its 64 keys as little-endian bf16; a bad id gives zeros."""
+    slots = 3 * 64
+    codes = (np.arange(slots * 256) % 251).astype(np.uint8).reshape(slots, 256)
+    scales = (np.arange(slots * 16) % 13 + 100).astype(np.uint8).reshape(slots, 16)
+    keys = (np.arange(slots * 128) * 7 + 0x1234).astype(np.uint16).reshape(slots, 128)
+    packed = orc.pack_pages(codes, scales, keys, [2, 0, 7])
+    rec = 64 * (256 + 16 + 256)
+    assert packed.shape == (3 * rec,)
+    r0 = packed[:rec]
+    assert r0[0] == codes[128, 0] and r0[64 * 256 - 1] == codes[191, 255]
+    assert r0[64 * 256] == scales[128, 0] and r0[64 * 256 + 64 * 16 - 1] == scales[191, 15]
+    k0 = 64 * 256 + 64 * 16
+    assert r0[k0] == keys[128, 0] & 0xFF and r0[k0 + 1] == keys[128, 0] >> 8
+    assert r0[rec - 1] == keys[191, 127] >> 8
+    assert np.array_equal(packed[rec:rec + 64 * 256], codes[:64].ravel())
+    assert not packed[2 * rec:].any()
+
+
 # ------------------------------------------------------------------ projection -----
 
 def _bf16(x):
