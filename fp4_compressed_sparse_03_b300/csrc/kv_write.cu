@@ -34,14 +34,16 @@ constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int kThreads = 192;                   // 6 warps
 constexpr int kGroupM = 16;
 
-// Output tile width BN and TMA ring depth.  Prefill-sized T: 256 columns, 4 stages of
-// 48 KB.  A single M-tile (T <= 128, e.g. decode-time append of one token per sequence)
-// is bound by streaming the weights: 128 columns and 6 stages of 32 KB double the CTAs
-// that stream them and the weight bytes each keeps in flight.
-template <int BN, int STAGES>
+// Output tile width BN, TMA ring depth and K-blocks of 64 per stage (KSUB).  Prefill-sized
+// T: 256 columns, 4 stages of 48 KB.  A single M-tile (T <= 128, e.g. decode-time append
+// of one token per sequence) is bound by streaming the weights: 128 columns double the
+// CTAs that stream them, and 3 stages of two adjacent K-blocks read 256 contiguous bytes
+// of each weight row at a time (6 stages of one K-block when d_model % 128 != 0).
+template <int BN, int STAGES, int KSUB>
 struct KvCfg {
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int SUB_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGE_BYTES = KSUB * SUB_BYTES;
   static constexpr int kTmemCols = 2 * BN;  // two accumulators
   struct Bars {
     uint64_t full[STAGES];
@@ -54,7 +56,8 @@ struct KvCfg {
   };
   static constexpr size_t smem_bytes() { return (size_t)STAGES * STAGE_BYTES + sizeof(Bars) + 1024; }
 };
-static_assert(KvCfg<256, 4>::smem_bytes() <= 232448 && KvCfg<128, 6>::smem_bytes() <= 232448,
+static_assert(KvCfg<256, 4, 1>::smem_bytes() <= 232448 && KvCfg<128, 6, 1>::smem_bytes() <= 232448 &&
+                  KvCfg<128, 3, 2>::smem_bytes() <= 232448,
               "write-path ring exceeds 227 KB of shared memory");
 
 __device__ __forceinline__ void fence_before() {
@@ -137,11 +140,12 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int&
 
 }  // namespace
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int KSUB>
 __global__ void __launch_bounds__(kThreads, 1)
     kv_write_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     WriteParams p) {
-  using Cfg = KvCfg<BN, STAGES>;
+  using Cfg = KvCfg<BN, STAGES, KSUB>;
+  constexpr int SUB_BYTES = Cfg::SUB_BYTES;
   using Bars = typename Cfg::Bars;
   constexpr int STAGE_BYTES = Cfg::STAGE_BYTES;
   constexpr int kTmemCols = Cfg::kTmemCols;
@@ -190,15 +194,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
       int m, n;
       tile_coords(tile, num_m, num_n, m, n);
-      for (int kb = 0; kb < kblocks; ++kb) {
+      for (int kb = 0; kb < kblocks; kb += KSUB) {  // kblocks is a multiple of KSUB
         if (!mbar_wait(&bars->abort, &bars->empty[stage], phase ^ 1u, p.st)) {
           ok = false;
           break;
         }
         unsigned char* sa = base + stage * STAGE_BYTES;
         mbar_expect_tx(&bars->full[stage], STAGE_BYTES);
-        tma_load_2d(sa, &tmA, &bars->full[stage], kb * BK, m * BM);
-        tma_load_2d(sa + A_BYTES, &tmB, &bars->full[stage], kb * BK, n * BN);
+#pragma unroll
+        for (int j = 0; j < KSUB; ++j) {
+          tma_load_2d(sa + j * SUB_BYTES, &tmA, &bars->full[stage], (kb + j) * BK, m * BM);
+          tma_load_2d(sa + j * SUB_BYTES + A_BYTES, &tmB, &bars->full[stage], (kb + j) * BK, n * BN);
+        }
         issued_mask |= 1u << stage;
         last_par = (last_par & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) {
@@ -221,18 +228,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&bars->abort, &bars->tempty[acc], acc_phase ^ 1u, p.st)) break;
       fence_after();
       const uint32_t d = tmem + (uint32_t)(acc * BN);
-      for (int kb = 0; kb < kblocks; ++kb) {
+      for (int kb = 0; kb < kblocks; kb += KSUB) {
         if (!mbar_wait(&bars->abort, &bars->full[stage], phase, p.st)) {
           ok = false;
           break;
         }
         fence_after();
-        const unsigned char* sa = base + stage * STAGE_BYTES;
-        const uint64_t adesc = sw128_desc(sa), bdesc = sw128_desc(sa + A_BYTES);
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k)
-          umma_bf16(d, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc,
-                    (kb > 0 || k > 0) ? 1u : 0u);
+        for (int j = 0; j < KSUB; ++j) {
+          const unsigned char* sa = base + stage * STAGE_BYTES + j * SUB_BYTES;
+          const uint64_t adesc = sw128_desc(sa), bdesc = sw128_desc(sa + A_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            umma_bf16(d, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc,
+                      (kb > 0 || j > 0 || k > 0) ? 1u : 0u);
+        }
         umma_commit(&bars->empty[stage]);
         if (++stage == STAGES) {
           stage = 0;
@@ -334,20 +344,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 namespace {
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int KSUB>
 cudaError_t launch_kv_write_cfg(const uint16_t* H, const uint16_t* Wt, const WriteParams& p,
                                 cudaStream_t s, int num_sms) {
   CUtensorMap ta, tb;
   if (!make_bf16_map(&ta, H, p.T, p.d_model, BK, BM) ||
       !make_bf16_map(&tb, Wt, p.n_out, p.d_model, BK, BN))
     return cudaErrorInvalidValue;
-  const size_t smem = KvCfg<BN, STAGES>::smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(kv_write_kernel<BN, STAGES>,
+  const size_t smem = KvCfg<BN, STAGES, KSUB>::smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(kv_write_kernel<BN, STAGES, KSUB>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int tiles = ((p.T + BM - 1) / BM) * ((p.n_out + BN - 1) / BN);
   const int grid = std::max(1, std::min(tiles, num_sms));
-  kv_write_kernel<BN, STAGES><<<grid, kThreads, smem, s>>>(ta, tb, p);
+  kv_write_kernel<BN, STAGES, KSUB><<<grid, kThreads, smem, s>>>(ta, tb, p);
   return cudaGetLastError();
 }
 
@@ -360,8 +370,9 @@ cudaError_t launch_kv_write(const uint16_t* H, const uint16_t* Wt, uint8_t* code
   const int32_t n_out = n_kv_proj * kDkv + n_idx_proj * kDidx;
   WriteParams p{codes, scales, k_idx, slot_of_token, num_slots, T, d_model, n_kv_proj, n_idx_proj,
                 n_out, st};
-  if (T <= BM) return launch_kv_write_cfg<128, 6>(H, Wt, p, s, num_sms);
-  return launch_kv_write_cfg<256, 4>(H, Wt, p, s, num_sms);
+  if (T <= BM && d_model % (2 * BK) == 0) return launch_kv_write_cfg<128, 3, 2>(H, Wt, p, s, num_sms);
+  if (T <= BM) return launch_kv_write_cfg<128, 6, 1>(H, Wt, p, s, num_sms);
+  return launch_kv_write_cfg<256, 4, 1>(H, Wt, p, s, num_sms);
 }
 
 }  // namespace csa2
