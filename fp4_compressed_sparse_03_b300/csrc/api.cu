@@ -142,6 +142,10 @@ static size_t scores_bytes(csa2_mode mode, int32_t num_q, int32_t max_pages_per_
   return ((size_t)num_q * n * sizeof(uint32_t) + 255) / 256 * 256;
 }
 
+// The run list's span in the workspace, rounded to 256 B so that what follows it (the
+// selection histograms, cleared with 16-byte stores) stays aligned.
+static size_t runlist_span(int32_t num_q) { return (runlist_bytes(num_q) + 255) / 256 * 256; }
+
 // FULL: per-query selection histograms (2048 bins) written by the scorer
 static size_t hist_bytes(csa2_mode mode, int32_t num_q) {
   return mode == CSA2_FULL ? ((size_t)num_q * 2048 * sizeof(uint32_t) + 255) / 256 * 256 : 0;
@@ -158,7 +162,7 @@ size_t csa2_index_workspace_size(csa2_mode mode, int32_t num_q, int32_t max_page
                                  int32_t pool_size) {
   if (num_q <= 0 || (mode != CSA2_FULL && mode != CSA2_REINDEX)) return 0;
   return scores_bytes(mode, num_q, max_pages_per_seq, pool_size) +
-         (mode == CSA2_FULL ? runlist_bytes(num_q) : 0) + hist_bytes(mode, num_q) +
+         (mode == CSA2_FULL ? runlist_span(num_q) : 0) + hist_bytes(mode, num_q) +
          wide_bytes(mode, num_q, max_pages_per_seq);
 }
 
@@ -192,7 +196,7 @@ csa2_status csa2_index(csa2_mode mode, const uint16_t* q_idx, const uint16_t* k_
     const int64_t stride = (int64_t)pages->max_pages_per_seq * kPage;
     void* rl = static_cast<char*>(args->workspace) +
                scores_bytes(mode, args->num_q, pages->max_pages_per_seq, P);
-    uint32_t* hist = reinterpret_cast<uint32_t*>(static_cast<char*>(rl) + runlist_bytes(args->num_q));
+    uint32_t* hist = reinterpret_cast<uint32_t*>(static_cast<char*>(rl) + runlist_span(args->num_q));
     void* wide = wide_bytes(mode, args->num_q, pages->max_pages_per_seq) == 0
                      ? nullptr
                      : static_cast<void*>(reinterpret_cast<char*>(hist) + hist_bytes(mode, args->num_q));

@@ -102,13 +102,22 @@ __device__ __forceinline__ int run_rows(bool reindex, const int32_t* __restrict_
   return min(max(0, __ldg(g.seq_lens + b)), g.max_pages * kPage);
 }
 
+// CTA 0 builds the run list; CTAs 1.. clear `zero_buf` (zero_vecs 16-byte vectors: the
+// Full scorer's selection histograms), which saves a separate memset in the stream.
 __global__ void __launch_bounds__(1024) group_prefix_kernel(bool batched, bool reindex,
                                                             const int32_t* __restrict__ q_seq,
                                                             int32_t num_q, ScoreGeom g,
                                                             int32_t pool_size, int32_t unit_rows,
                                                             int64_t* meta, int64_t* prefix,
-                                                            int32_t* run_q0) {
+                                                            int32_t* run_q0, uint4* zero_buf,
+                                                            int64_t zero_vecs) {
   grid_dep_wait();
+  if (blockIdx.x > 0) {
+    const int64_t stride = (int64_t)(gridDim.x - 1) * blockDim.x;
+    for (int64_t i = (int64_t)(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < zero_vecs; i += stride)
+      zero_buf[i] = make_uint4(0, 0, 0, 0);
+    return;
+  }
   __shared__ int64_t wsum[32];
   __shared__ int64_t carry_s;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -126,10 +135,12 @@ __global__ void __launch_bounds__(1024) group_prefix_kernel(bool batched, bool r
     __syncthreads();
     return x + add;
   };
-  // pass 1: run starts
-  if (tid == 0) carry_s = 0;
+  // pass 1: run starts (one query per run unless batched)
+  if (tid == 0) carry_s = batched ? 0 : num_q;
   __syncthreads();
-  for (int base = 0; base < num_q; base += 1024) {
+  if (!batched)
+    for (int i = tid; i < num_q; i += 1024) run_q0[i] = i;
+  for (int base = 0; batched && base < num_q; base += 1024) {
     const int i = base + tid;
     int start = 0;
     if (i < num_q) {
@@ -1885,9 +1896,14 @@ cudaError_t launch_score_full(const uint16_t* q_idx, const uint16_t* keys, const
   ScoreGeom g{pg.seq_lens, pg.page_table, pg.max_pages_per_seq, pg.num_pages, pg.num_seqs};
   RunList rl = make_runlist(runlist, num_q);
   const bool batched = max_q_per_seq > 1;
-  cudaError_t e = launch_pdl(group_prefix_kernel, dim3(1), dim3(1024), 0, s, batched, false, q_seq,
-                             num_q, g, 0, kPage, const_cast<int64_t*>(rl.meta),
-                             const_cast<int64_t*>(rl.prefix), const_cast<int32_t*>(rl.run_q0));
+  // the selection histograms (num_q x kHistBins words, a multiple of 4) are cleared by
+  // extra CTAs of the run-list launch, 8 vectors per thread
+  const int64_t zero_vecs = ghist != nullptr ? (int64_t)num_q * kHistBins / 4 : 0;
+  const int zero_ctas = (int)std::min<int64_t>(64, (zero_vecs + 8 * 1024 - 1) / (8 * 1024));
+  cudaError_t e = launch_pdl(group_prefix_kernel, dim3(1 + zero_ctas), dim3(1024), 0, s, batched,
+                             false, q_seq, num_q, g, 0, kPage, const_cast<int64_t*>(rl.meta),
+                             const_cast<int64_t*>(rl.prefix), const_cast<int32_t*>(rl.run_q0),
+                             reinterpret_cast<uint4*>(ghist), zero_vecs);
   if (e != cudaSuccess) return e;
   CUtensorMap keymap;
   if (!make_bf16_map(&keymap, keys, (int64_t)pg.num_pages * kPage, kDidx, 64, kPage))
@@ -1896,10 +1912,6 @@ cudaError_t launch_score_full(const uint16_t* q_idx, const uint16_t* keys, const
   e = cudaFuncSetAttribute(score_pages_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kTmaSmem);
   if (e != cudaSuccess) return e;
-  if (ghist != nullptr) {
-    e = cudaMemsetAsync(ghist, 0, (size_t)num_q * kHistBins * sizeof(uint32_t), s);
-    if (e != cudaSuccess) return e;
-  }
   return launch_pdl(score_pages_kernel, dim3(grid), dim3(kTmaThreads), kTmaSmem, s, keymap, q_idx,
                     q_seq, num_q, g, ws, ws_stride, rl, ghist, st);
 }
