@@ -346,6 +346,61 @@ def test_mx_attention_scale_spread():
     assert_attn_close(host(out[0]), o, host(lse[0]), l, "mx scale spread")
 
 
+def test_prefill_chunk_queries_against_their_own_topk():
+    """A prefill chunk: the 32 query positions 8160 .. 8191 of one 8192-token sequence, each
+    attending to its own top-512 among the tokens it may see (causal).  Each query is an
+    entry of the pages descriptor with its own length, all sharing the sequence's
+    page-table row; the read path treats them as independent queries."""
+    n, C, K = 8192, 32, 512
+    wl = gen.DecodeWorkload("chunk", 47, np.array([n], np.int32), np.ones(1, np.int32),
+                            [gen.FULL], 0, 16)
+    src = fill_decode_cache(wl)
+    pos = np.arange(n - C, n, dtype=np.int32)
+    row = host(src.page_table)[0]
+    cache = DecodeCache(pos + 1, np.tile(row, (C, 1)), src.num_pages, 1)
+    cache.codes.copy_(src.codes)
+    cache.scales.copy_(src.scales)
+    idx = np.stack([gen.random_index_set(47, i, int(p) + 1, K) for i, p in enumerate(pos)])
+    q = np.stack([gen.q_rows(47, 3, np.array([i]))[0] for i in range(C)])
+    out = torch.zeros((C, 16, 512), dtype=torch.float32, device="cuda")
+    lse = torch.zeros((C, 16), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(csa2.csa2_attn_workspace_size(C, K), 16), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    csa2.check(csa2.csa2_sparse_attn(dev(q), cache.codes[0], cache.scales[0], dev(idx), cache.pages,
+                                     out, lse, C, dev(np.arange(C, dtype=np.int32)), K,
+                                     SOFTMAX_SCALE, ws, None, st), "attn")
+    status, bits = csa2.csa2_read_status(st)
+    assert status == csa2.CSA2_OK, hex(bits)
+    gains = gen.latent_gains(47)
+    for i in range(C):
+        x = gen.latent_rows(47, 0, 0, idx[i], gains)
+        c, s = oracle.quantize(x)
+        o, l = oracle.sparse_attention(q[i], oracle.dequantize(c, s), SOFTMAX_SCALE)
+        assert_attn_close(host(out[i]), o, host(lse[i]), l, f"chunk query {i}")
+
+
+def test_mx_attention_split_with_no_valid_entry():
+    """MXFP4 read path: a query whose selection is all -1 over several splits gets zero output
+    and -inf lse; the other query is unaffected."""
+    lens = np.array([3000, 900], np.int32)
+    wl = gen.DecodeWorkload("mx_empty", 53, lens, np.ones(2, np.int32), [gen.FULL], 0, 16)
+    cache = fill_decode_cache(wl, mx=True)
+    topk = 1536
+    idx = np.stack([gen.random_index_set(53, 1, 3000, topk), np.full(topk, -1, np.int32)])
+    q = np.stack([gen.q_rows(53, 0, np.array([i]))[0] for i in range(2)])
+    out = torch.full((2, 16, 512), np.nan, dtype=torch.float32, device="cuda")
+    lse = torch.full((2, 16), np.nan, dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(csa2.csa2_attn_workspace_size(2, topk), 16), dtype=torch.uint8, device="cuda")
+    csa2.check(csa2.csa2_sparse_attn_mx(dev(q), cache.codes[0], cache.scales[0], dev(idx),
+                                        cache.pages, out, lse, 2, dev(np.array([0, 1], np.int32)),
+                                        topk, SOFTMAX_SCALE, ws), "attn_mx")
+    assert np.all(host(out[1]) == 0) and np.all(np.isneginf(host(lse[1])))
+    x = gen.latent_rows(53, 0, 0, idx[0], gen.latent_gains(53))
+    c, s = oracle.mx_quantize(x)
+    o, l = oracle.sparse_attention(q[0], oracle.mx_dequantize(c, s), SOFTMAX_SCALE)
+    assert_attn_close(host(out[0]), o, host(lse[0]), l, "mx query 0")
+
+
 def test_attention_dense_equals_all_tokens():
     """K = N: the sparse path over every token equals the oracle's dense attention."""
     wl = gen.DecodeWorkload("dense", 29, np.array([512], np.int32), np.ones(1, np.int32),

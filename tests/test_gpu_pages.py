@@ -83,3 +83,24 @@ def test_saved_sequence_resumes_in_other_pages(tmp_path):
                                          SOFTMAX_SCALE, ws), "attn")
         outs.append((host(out), host(lse)))
     assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+
+
+def test_mx_pages_round_trip_through_a_file(tmp_path):
+    """MXFP4 pools (16-byte scale rows) save and load like E4M3 ones: the resumed pages are
+    byte-identical to the saved ones."""
+    wl, cache = _cache(mx=True)
+    path = os.path.join(tmp_path, "seq_mx.csa2pages")
+    persist.save_sequence(cache, 0, 0, path)
+    n_pages = -(-1000 // 64)
+    pt = np.arange(5, 5 + n_pages, dtype=np.int32).reshape(1, -1)
+    dst = DecodeCache(np.array([1000], np.int32), pt, 5 + n_pages, 1, mx=True)
+    assert persist.load_sequence(path, dst, 0, pt[0]) == 1000
+    src_ids = host(cache.page_table)[0, :n_pages]
+    for a, b in zip(src_ids, pt[0]):
+        ra, rb = slice(64 * a, 64 * a + 64), slice(64 * b, 64 * b + 64)
+        assert torch.equal(cache.codes[0][ra], dst.codes[0][rb])
+        assert torch.equal(cache.scales[0][ra], dst.scales[0][rb])
+        assert torch.equal(cache.keys[0][ra], dst.keys[0][rb])
+    with pytest.raises(ValueError):  # an E4M3 cache refuses an MXFP4 file
+        persist.load_sequence(path, DecodeCache(np.array([1000], np.int32), pt, 5 + n_pages, 1),
+                              0, pt[0])
