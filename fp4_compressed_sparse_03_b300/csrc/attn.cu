@@ -564,6 +564,13 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restri
   __shared__ float wgt[kMaxSplits];
   __shared__ float inv;
   const float* ml = part_ml + (int64_t)qi * nsplit * 2 * kHq;
+  // 128 threads x 4 channels; the first four splits' rows are loaded before the weights
+  // are known, so their latency overlaps the weights' reductions
+  const float4* po = reinterpret_cast<const float4*>(part_o + ((int64_t)qi * nsplit * kHq + h) * kDkv);
+  float4 v0[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    if (u < nsplit) v0[u] = __ldcs(po + (int64_t)u * kHq * kDkv / 4 + threadIdx.x);
   if (threadIdx.x < 32) {
     float M = -INFINITY;
     for (int s = threadIdx.x; s < nsplit; s += 32) M = fmaxf(M, ml[s * 2 * kHq + h]);
@@ -584,10 +591,18 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restri
     }
   }
   __syncthreads();
-  // 128 threads x 4 channels
-  const float4* po = reinterpret_cast<const float4*>(part_o + ((int64_t)qi * nsplit * kHq + h) * kDkv);
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-  int s = 0;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    if (u < nsplit) {
+      const float w = wgt[u];
+      a.x += w * v0[u].x;
+      a.y += w * v0[u].y;
+      a.z += w * v0[u].z;
+      a.w += w * v0[u].w;
+    }
+  }
+  int s = min(nsplit, 4);
   for (; s + 4 <= nsplit; s += 4) {  // four independent loads in flight
     float4 v[4];
 #pragma unroll
