@@ -675,15 +675,25 @@ INDEX_SOURCES = ("index.cu", "async.cuh", "common.cuh")
 
 
 def kernel_hash() -> str:
-    """Hash of the sources the Full index call's kernels are built from; its traffic
-    counters are only reported for this exact build of them."""
+    """Hash of the code (comments and blank space removed) of the sources the Full index
+    call's kernels are built from; its traffic counters are only reported for this exact
+    code."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp4_compressed_sparse_03_b300", "csrc")
     for f in INDEX_SOURCES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
+
+
+def _code_only(src: str) -> str:
+    """C++ source without // and /* */ comments and with runs of blank space collapsed
+    (string literals holding comment markers are not expected in these kernels)."""
+    import re
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
 
 
 # ------------------------------------------------------------------ CPU oracle ---

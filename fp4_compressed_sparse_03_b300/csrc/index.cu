@@ -7,19 +7,27 @@
 //     key = (bits(score) & 0x7fffffff) + 1   for a valid candidate (score >= 0),
 //     key = 0                                for an invalid one (pool padding, bad page).
 // Keys order like the scores, every valid key is above every invalid one, and bit 31
-// of a valid key is always clear.  Selection (cluster radix select) then takes the
-// top-min(K, #valid) keys, the lower candidate position winning ties, and writes
-// their tokens in ascending order.
+// of a valid key is always clear.  Selection then takes the top-min(K, #valid) keys
+// (and the top-min(P, #valid) pool), the lower candidate position winning ties, and
+// writes their tokens in ascending order.
 //
 // Kernels:
-//   group_prefix_kernel  compact work list (runs of queries, units of rows)
+//   group_prefix_kernel  FULL: compact work list (runs of queries, units of rows); its
+//                        extra CTAs clear the selection histograms
 //   score_pages_kernel   FULL: 64-token pages streamed by TMA into a shared ring, scored
-//                        by tensor-core MMAs (1-4 draft queries of a sequence at once)
+//                        by tensor-core MMAs (1-4 draft queries of a sequence at once);
+//                        also builds each query's selection histogram
 //   score_gather_kernel  REINDEX: pool rows gathered by per-lane cp.async rings, scored
-//                        by the same MMAs
-//   select_kernel        1-8-CTA cluster per query: four 8-bit radix passes with per-warp
-//                        histograms merged through distributed shared memory, then an
-//                        ordered compaction with warp scans
+//                        by the same MMAs (an arithmetic work list: P rows per query)
+//   select_cta_kernel    one 1024-thread CTA per query up to 2^18 keys: exact histogram,
+//                        boundary bins, ordered filter, radix passes over the boundary
+//                        bin, ordered emit
+//   select_filter_kernel / select_resolve_kernel / select_emit_kernel
+//                        FULL beyond 2^18 tokens: several filter CTAs per query, one
+//                        resolving CTA, one emitting warp per candidate list
+//   select_kernel        1-8-CTA cluster per query for more than 8192 outputs: four
+//                        8-bit radix passes with per-warp histograms merged through
+//                        distributed shared memory, then an ordered compaction
 #include <cooperative_groups.h>
 #include <cstddef>
 
