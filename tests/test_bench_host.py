@@ -96,3 +96,14 @@ def test_reference_arm_under_torchrun_prints_once(world):
     lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
     assert len(lines) == 1
     assert json.loads(lines[0])["n_gpus"] == world
+
+
+def test_traffic_hash_ignores_comments_only():
+    """The traffic counters stay tied to the index kernels' code: comments and blank space
+    do not change the hash, code does."""
+    a = "int f(int x) {  // doubled\n  return 2 * x; /* note */ }\n"
+    b = "// header\nint f(int x) {\n\n  return 2 * x;\n}\n"
+    c = "int f(int x) { return 3 * x; }"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+    assert len(bench.kernel_hash()) == 16
