@@ -413,6 +413,43 @@ def test_attention_closed_forms(orc):
     np.testing.assert_allclose(o_a, o_b, rtol=1e-6, atol=1e-7)
 
 
+def test_attention_over_cache_gathers_by_hand(orc):
+    """The cache-level oracle: select rows by index (skipping -1), decode each code from the
+    E2M1 magnitude table and its scale (E4M3 / 16, or E8M0 = 2^(b - 127) / 32) by hand,
+    and attend; duplicates count once per occurrence, an all -1 selection gives zeros."""
+    mag = {int(k): v for k, v in _gold("e2m1_values.json")["code_to_magnitude"].items()}
+    rng = np.random.default_rng(31)
+    n = 40
+    codes = rng.integers(0, 256, (n, 256), dtype=np.uint8)
+    q = _bf16(rng.standard_normal((16, 512)) * 0.2)
+
+    def by_hand(row_ids, scale_of):
+        rows = np.zeros((len(row_ids), 512))
+        for i, r in enumerate(row_ids):
+            for c in range(512):
+                nib = (codes[r, c // 2] >> (4 * (c % 2))) & 0xF
+                v = mag[nib & 7] * (-1.0 if nib & 8 else 1.0)
+                rows[i, c] = v * scale_of(r, c)
+        return rows
+
+    idx = np.array([7, -1, 3, 39, 7, -1, 0], np.int32)
+    sel = [7, 3, 39, 7, 0]
+    e4 = rng.integers(0x20, 0x50, (n, 32), dtype=np.uint8)  # normal E4M3 scales
+    e4_val = lambda b: 2.0 ** ((int(b) >> 3) - 7) * (1 + (int(b) & 7) / 8)
+    out, lse = orc.attention_over_cache(q, codes, e4, idx, 0.07)
+    ref_o, ref_l = orc.sparse_attention(q, by_hand(sel, lambda r, c: e4_val(e4[r, c // 16])), 0.07)
+    assert np.array_equal(out, ref_o) and np.array_equal(lse, ref_l)
+
+    e8 = rng.integers(120, 135, (n, 16), dtype=np.uint8)
+    out, lse = orc.attention_over_cache(q, codes, e8, idx, 0.07, mx=True)
+    ref_o, ref_l = orc.sparse_attention(q, by_hand(sel, lambda r, c: 2.0 ** (int(e8[r, c // 32]) - 127)),
+                                        0.07)
+    assert np.array_equal(out, ref_o) and np.array_equal(lse, ref_l)
+
+    out, lse = orc.attention_over_cache(q, codes, e4, np.full(5, -1, np.int32), 0.07)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
 def test_attention_large_logit_stability(orc):
     """exp never overflows: a huge logit gap gives one-hot weights."""
     q = _bf16(np.full((16, 512), 4.0))
