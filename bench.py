@@ -594,6 +594,178 @@ def run_pages(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+CHUNK_METRIC = ("multi-query sparse attention: query tokens/s, 4 draft queries per sequence "
+                "with their own top-K")
+CHUNK_SHARED = 0.75  # fraction of each draft query's selection common to its chunk
+
+
+def chunk_inputs(dev=None):
+    """The draft-token chunk workload: the 64 x 16384-token cache, 4 draft queries per
+    sequence, each with top-2048 entries of which 75 % are common to the sequence's four
+    (host arrays: q bf16 bits [256, 16, 512], idx int32 [256, 2048], q_seq int32 [256])."""
+    import csa2_inputs as gen
+    wl = workload_of("decode_short")
+    B, G, K = len(wl.seq_lens), 4, wl.topk
+    idx = np.concatenate([gen.overlapping_index_sets(wl.seed, b, int(wl.seq_lens[b]), K, G,
+                                                     CHUNK_SHARED) for b in range(B)])
+    q = gen.q_rows(wl.seed, 7, np.arange(B * G))
+    q_seq = np.repeat(np.arange(B, dtype=np.int32), G)
+    return wl, q, idx, q_seq, G, K
+
+
+def run_chunk(args, world, rank, local):
+    """Multi-query sparse attention in dense-contraction form: the union of each chunk's
+    selections gathered and dequantised once for its 4 queries (csa2_sparse_attn_chunked),
+    timed per call with L2 flushed before each (the selected rows, ~66 MB, fit in L2); the
+    per-query path on the same arguments is timed the same way for comparison.  Roofline:
+    HBM, on the distinct rows the chunks select plus q, indices and outputs."""
+    import torch
+    import fp4_compressed_sparse_03_b300 as csa2
+    from fp4_compressed_sparse_03_b300.workload import fill_decode_cache
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl, q, idx, q_seq, G, K = chunk_inputs()
+    cache = fill_decode_cache(wl, device=dev)
+    nq = len(q_seq)
+    q_d = torch.as_tensor(q.view(np.int16), device=dev)
+    idx_d = torch.as_tensor(idx, device=dev)
+    qs_d = torch.as_tensor(q_seq, device=dev)
+    out = torch.empty((nq, 16, 512), dtype=torch.float32, device=dev)
+    lse = torch.empty((nq, 16), dtype=torch.float32, device=dev)
+    ws = torch.empty(csa2.csa2_chunk_attn_workspace_size(nq, G, K), dtype=torch.uint8, device=dev)
+    ws_pq = torch.empty(max(16, csa2.csa2_attn_workspace_size(nq, K)), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    scale = float(np.float32(1.0 / np.sqrt(512.0)))
+
+    def chunked(qa=q_d, ia=idx_d):
+        csa2.check(csa2.csa2_sparse_attn_chunked(qa, cache.codes[0], cache.scales[0], ia,
+                                                 cache.pages, out, lse, nq, qs_d, G, K, scale, ws,
+                                                 None, st, stream), "chunked attention")
+
+    def per_query():
+        csa2.check(csa2.csa2_sparse_attn(q_d, cache.codes[0], cache.scales[0], idx_d, cache.pages,
+                                         out, lse, nq, qs_d, K, scale, ws_pq, None, st, stream),
+                   "attention")
+
+    def timed(fn, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for k in range(n):
+            flush.fill_(k & 0xFF)
+            evs[k][0].record(stream)
+            fn()
+            evs[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return float(np.mean([a.elapsed_time(b) for a, b in evs]))
+
+    for _ in range(args.warmup):
+        chunked()
+        per_query()
+    torch.cuda.synchronize(dev)
+    Kst = args.steps
+    clocks = ClockSampler(local)
+    barrier(world)
+    clocks.start()
+    time.sleep(0.3)
+    ms_call = timed(chunked, Kst)
+    ms_pq = timed(per_query, Kst)
+    barrier(world)
+    clk = clocks.stop()
+    status, bits = csa2.csa2_read_status(st)
+    if status != csa2.CSA2_OK:
+        raise RuntimeError(f"device status {bits:#x} after timed steps")
+    ms_step = reduce_max(ms_call, world, dev)
+    value = nq * world / (ms_step / 1e3)
+    # distinct rows the chunks select (the union per sequence), and what every query moves
+    union = sum(np.unique(idx[c * G:(c + 1) * G][idx[c * G:(c + 1) * G] >= 0]).size
+                for c in range(nq // G))
+    abytes = union * 288 + nq * (16 * 512 * 2 + K * 4 + 16 * 512 * 4 + 16 * 4)
+    hbm_peak, _, peak_src = load_peaks()
+    achieved = abytes / (ms_call / 1e3) / 1e9
+
+    # end to end: q and indices from pinned host memory in, outputs and lse back out
+    q_pin = torch.empty(q_d.shape, dtype=q_d.dtype).pin_memory()
+    q_pin.copy_(q_d)
+    i_pin = torch.empty(idx_d.shape, dtype=idx_d.dtype).pin_memory()
+    i_pin.copy_(idx_d)
+    o_pin = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    l_pin = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    q_dev, i_dev = torch.empty_like(q_d), torch.empty_like(idx_d)
+    K2 = max(1, min(Kst, args.e2e_steps, 20))
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    w0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(K2):
+        flush.fill_(3)
+        q_dev.copy_(q_pin, non_blocking=True)
+        i_dev.copy_(i_pin, non_blocking=True)
+        chunked(q_dev, i_dev)
+        o_pin.copy_(out, non_blocking=True)
+        l_pin.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_e2e = reduce_max(max(e0.elapsed_time(e1) / K2, (time.perf_counter() - w0) / K2 * 1e3),
+                        world, dev)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_chunk(args.cpu_sample)
+    line = {
+        "metric": CHUNK_METRIC, "value": round(value, 1), "unit": "queries/s", "n_gpus": world,
+        "steps": Kst, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp4-e2m1/e4m3 kv, bf16 queries, f16 operands, f32 accumulate",
+        "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": "draft_chunk_64x4x16384", "num_seqs": len(wl.seq_lens),
+                   "queries_per_chunk": G, "context_tokens": int(wl.seq_lens.max()), "topk": K,
+                   "shared_fraction": CHUNK_SHARED, "union_rows": int(union),
+                   "l2": "flushed before every call (256 MB written): the selected rows fit in L2",
+                   "per_query_path_ms": round(ms_pq, 4), "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm",
+                     "kernel": "csa2_sparse_attn_chunked call: chunk_union_kernel + "
+                               "chunk_attn_kernel + attn_combine_kernel",
+                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src + " HBM copy",
+                     "algorithmic_bytes_per_launch": int(abytes), "traffic": None},
+        "e2e": {"value": round(nq * world / (ms_e2e / 1e3), 1), "unit": "queries/s",
+                "h2d_bytes_per_step": int(q_d.numel() * 2 + idx_d.numel() * 4),
+                "d2h_bytes_per_step": int(out.numel() * 4 + lse.numel() * 4), "steps": K2},
+        "gpu_launches": 3 * Kst,
+        "clocks": clk,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def cpu_baseline_chunk(sample_queries: int):
+    """The oracle (gather, dequantise, double-precision attention per query) on the first
+    `sample_queries` draft queries of the chunk workload; the cache rows of their
+    sequences are generated and quantised before the clock starts."""
+    import csa2_inputs as gen
+    import oracle
+    from csa2_inputs import native
+    wl, q, idx, q_seq, G, K = chunk_inputs()
+    n = max(1, min(sample_queries, len(q_seq)))
+    gains = gen.latent_gains(wl.seed, 0)
+    rows = {}
+    for b in sorted(set(int(x) for x in q_seq[:n])):
+        rows[b] = oracle.quantize(native.latent_rows_host(wl.seed, 0, b, 0, int(wl.seq_lens[b]), gains))
+    scale = float(np.float32(1.0 / np.sqrt(512.0)))
+    t0 = time.perf_counter()
+    for i in range(n):
+        c, s = rows[int(q_seq[i])]
+        oracle.attention_over_cache(q[i], c, s, idx[i], scale)
+    dt = time.perf_counter() - t0
+    return {"value": round(n / dt, 3), "unit": "queries/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} of {len(q_seq)} queries of draft_chunk_64x4x16384, {dt:.1f} s on 1 thread"}
+
+
 def cpu_baseline_pages(sample_pages: int, repeats: int = 200):
     """The oracle's page-record layout (numpy) on `sample_pages` pages of the first
     sequence of the 64 x 16384 cache, packed `repeats` times."""
@@ -765,6 +937,24 @@ def run_reference(args, world, rank):
         return
     if args.workload in ("ced_write", "decode_append"):
         return run_reference_write(args, world)
+    if args.workload == "draft_chunk":
+        per_step = max(1, args.cpu_sample // max(1, args.steps))
+        t0 = time.perf_counter()
+        vals = [cpu_baseline_chunk(per_step) for _ in range(args.steps)]
+        dt = time.perf_counter() - t0
+        cb = dict(vals[-1])
+        cb["value"] = round(float(np.mean([c["value"] for c in vals])), 3)
+        cb["sample"] = f"{args.steps} steps x {per_step} queries of draft_chunk_64x4x16384"
+        line = {"impl": "reference", "metric": CHUNK_METRIC, "value": cb["value"],
+                "unit": "queries/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64 (CPU oracle)",
+                "data": "synthetic (seeded counter-based generator)",
+                "config": {"workload": "draft_chunk_64x4x16384"}, "cpu_baseline": cb,
+                "e2e": {"value": cb["value"], "unit": "queries/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
     if args.workload == "page_export":
         cb = cpu_baseline_pages(args.cpu_sample)
         line = {"impl": "reference",
@@ -846,7 +1036,7 @@ def main():
     ap.add_argument("--workload", default="decode_batch",
                     choices=["decode_batch", "decode_batch16", "decode_short", "long_context", "ragged", "tiny",
                              "ced_write", "decode_append", "decode_batch_mx", "decode_short_mx",
-                             "page_export"])
+                             "page_export", "draft_chunk"])
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-sample", type=int, default=None,
                     help="queries (decode) or token rows (write workloads) timed on the oracle; "
@@ -866,6 +1056,9 @@ def main():
     elif args.workload == "page_export":
         args.warmup = max(3, args.warmup)
         run_pages(args, world, rank, local)
+    elif args.workload == "draft_chunk":
+        args.warmup = max(3, args.warmup)
+        run_chunk(args, world, rank, local)
     else:
         args.warmup = max(3, args.warmup)
         run_ours(args, world, rank, local)

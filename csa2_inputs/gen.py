@@ -50,6 +50,7 @@ TAG_PERM = 9     # physical page permutation
 TAG_LENS = 10    # ragged context lengths
 TAG_DRAFT = 11   # speculative draft-token counts
 TAG_IDX = 12     # random selected-index sets (attention-only tests)
+TAG_CHUNK = 13   # per-query parts of overlapping selections (multi-query chunks)
 
 _U64 = np.uint64
 
@@ -200,6 +201,23 @@ def random_index_set(seed: int, sub: int, n_ctx: int, k: int, n_invalid: int = 0
     pick = np.sort(np.argsort(r, kind="stable")[:m]).astype(np.int32)
     out = np.full(k, -1, dtype=np.int32)
     out[:m] = pick
+    return out
+
+
+def overlapping_index_sets(seed: int, sub: int, n_ctx: int, k: int, count: int,
+                           shared: float) -> np.ndarray:
+    """`count` sorted selections of min(k, n_ctx) tokens of [0, n_ctx), each -1 padded to
+    k: round(shared * m) tokens common to all (a random subset), the rest of each drawn
+    independently from the other tokens.  int32 [count, k]; sub < 2**35."""
+    m = min(k, n_ctx)
+    s = int(round(shared * m))
+    base = np.argsort(draws(stream_key(seed, TAG_IDX, sub), np.arange(n_ctx)), kind="stable")
+    common, rest = base[:s], base[s:]
+    out = np.full((count, k), -1, dtype=np.int32)
+    for g in range(count):
+        r = draws(stream_key(seed, TAG_CHUNK, (sub << 5) | g), np.arange(rest.size))
+        own = rest[np.argsort(r, kind="stable")[:m - s]]
+        out[g, :m] = np.sort(np.concatenate([common, own])).astype(np.int32)
     return out
 
 

@@ -75,6 +75,11 @@ _attn_static = _sig("csa2_sparse_attn_static", ctypes.c_int,
                      ctypes.c_float, _vp, _vp])
 ATTN_STATIC_SCRATCH_BYTES = 16 << 20  # CSA2_ATTN_STATIC_SCRATCH_BYTES
 ATTN_MAX_TOPK = 65536  # CSA2_ATTN_MAX_TOPK
+_attn_chunked = _sig("csa2_sparse_attn_chunked", ctypes.c_int,
+                     [_vp, _vp, _vp, _vp, ctypes.POINTER(Csa2Pages), _vp, _vp, _i32, _vp, _i32,
+                      _i32, ctypes.c_float, _vp, _sz, _vp, _vp])
+_chunk_ws = _sig("csa2_chunk_attn_workspace_size", _sz, [_i32, _i32, _i32])
+CHUNK_ATTN_MAX_UNION = 8192  # CSA2_CHUNK_ATTN_MAX_UNION
 _quantize = _sig("csa2_quantize", ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp])
 _dequantize = _sig("csa2_dequantize", ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp])
 _quantize_mx = _sig("csa2_quantize_mx", ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp])
@@ -173,6 +178,21 @@ def csa2_sparse_attn(q, codes, scales, idx, pages: Csa2Pages, out, lse, num_q, q
 
 def csa2_attn_workspace_size(num_q, topk) -> int:
     return int(_attn_ws(num_q, topk))
+
+
+def csa2_sparse_attn_chunked(q, codes, scales, idx, pages: Csa2Pages, out, lse, num_q, q_seq,
+                             chunk, topk, softmax_scale, workspace=None, workspace_bytes=None,
+                             dev_status=None, stream=None) -> int:
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return _attn_chunked(_ptr(q), _ptr(codes), _ptr(scales), _ptr(idx), ctypes.byref(pages),
+                         _ptr(out), _ptr(lse), num_q, _ptr(q_seq), chunk, topk,
+                         ctypes.c_float(softmax_scale), _ptr(workspace), workspace_bytes,
+                         _ptr(dev_status), _stream(stream))
+
+
+def csa2_chunk_attn_workspace_size(num_q, chunk, topk) -> int:
+    return int(_chunk_ws(num_q, chunk, topk))
 
 
 def csa2_sparse_attn_static(q, codes, scales, idx, pages: Csa2Pages, out, lse, num_q, q_seq, topk,

@@ -29,6 +29,12 @@ cudaError_t launch_attn(const uint16_t*, const uint8_t*, const uint8_t*, const i
                         const csa2_pages&, float*, float*, int32_t, const int32_t*, int32_t, float,
                         void*, int32_t*, cudaStream_t, int, bool);
 size_t attn_workspace_bytes(int32_t, int32_t, int);
+cudaError_t launch_chunk_attn(const uint16_t*, const uint8_t*, const uint8_t*, const int32_t*,
+                              const csa2_pages&, float*, float*, int32_t, const int32_t*, int32_t,
+                              int32_t, float, void*, int32_t*, cudaStream_t, int);
+size_t chunk_attn_workspace_bytes(int32_t, int32_t, int32_t, int);
+int chunk_attn_max_union();
+int chunk_attn_max_chunk();
 size_t page_export_bytes(int);
 cudaError_t launch_page_copy(bool, uint8_t*, uint8_t*, uint8_t*, int, int64_t, const int32_t*,
                              int32_t, uint8_t*, int32_t*, cudaStream_t, int);
@@ -261,6 +267,42 @@ csa2_status csa2_sparse_attn_mx(const uint16_t* q, const uint8_t* codes, const u
                                 int32_t* dev_status, cudaStream_t stream) {
   return sparse_attn_call(true, q, codes, scales, idx, pages, out, lse, num_q, q_seq, topk,
                           softmax_scale, workspace, workspace_bytes, dev_status, stream);
+}
+
+static bool chunk_args_ok(int32_t num_q, int32_t chunk, int32_t topk) {
+  return num_q >= 1 && chunk >= 1 && topk >= 1 && num_q % chunk == 0;
+}
+
+static bool chunk_args_supported(int32_t num_q, int32_t chunk, int32_t topk) {
+  return chunk <= chunk_attn_max_chunk() && (int64_t)chunk * topk <= chunk_attn_max_union() &&
+         num_q / chunk <= 65535;
+}
+
+size_t csa2_chunk_attn_workspace_size(int32_t num_q, int32_t chunk, int32_t topk) {
+  if (!chunk_args_ok(num_q, chunk, topk) || !chunk_args_supported(num_q, chunk, topk)) return 0;
+  return chunk_attn_workspace_bytes(num_q, chunk, topk, device_sms());
+}
+
+csa2_status csa2_sparse_attn_chunked(const uint16_t* q, const uint8_t* codes, const uint8_t* scales,
+                                     const int32_t* idx, const csa2_pages* pages, float* out,
+                                     float* lse, int32_t num_q, const int32_t* q_seq, int32_t chunk,
+                                     int32_t topk, float softmax_scale, void* workspace,
+                                     size_t workspace_bytes, int32_t* dev_status,
+                                     cudaStream_t stream) {
+  if (!chunk_args_ok(num_q, chunk, topk) || !q || !codes || !scales || !idx || !out || !q_seq)
+    return CSA2_ERR_INVALID_ARGUMENT;
+  csa2_status ps = check_pages(pages);
+  if (ps != CSA2_OK) return ps;
+  if (!al16(q) || !al16(codes) || !al16(scales) || (reinterpret_cast<uintptr_t>(out) & 7u))
+    return CSA2_ERR_INVALID_ARGUMENT;
+  if (!(softmax_scale == softmax_scale)) return CSA2_ERR_INVALID_ARGUMENT;
+  if (!chunk_args_supported(num_q, chunk, topk)) return CSA2_ERR_UNSUPPORTED;
+  const int sms = device_sms();
+  const size_t need = chunk_attn_workspace_bytes(num_q, chunk, topk, sms);
+  if (workspace == nullptr || workspace_bytes < need || !al16(workspace))
+    return CSA2_ERR_INVALID_ARGUMENT;
+  return from_cuda(launch_chunk_attn(q, codes, scales, idx, *pages, out, lse, num_q, q_seq, chunk,
+                                     topk, softmax_scale, workspace, dev_status, stream, sms));
 }
 
 csa2_status csa2_kv_write(const uint16_t* H, const uint16_t* Wt, uint8_t* codes, uint8_t* scales,

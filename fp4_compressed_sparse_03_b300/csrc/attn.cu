@@ -555,18 +555,26 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
 }
 
 // Merge the splits of each (query, head): out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+// The partials are laid out with `stride` splits per query.  With `span_count` (the
+// multi-query form), only the first ceil(span_count[query / chunk] / span_len) splits hold
+// partials; none gives zero output and -inf lse.
 __global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restrict__ part_o,
                                                            const float* __restrict__ part_ml,
-                                                           int nsplit, float* __restrict__ out,
-                                                           float* __restrict__ lse) {
+                                                           int stride, float* __restrict__ out,
+                                                           float* __restrict__ lse,
+                                                           const int32_t* __restrict__ span_count,
+                                                           int span_len, int chunk) {
   grid_dep_wait();
   const int qi = blockIdx.x, h = blockIdx.y;
+  const int nsplit = span_count == nullptr
+                         ? stride
+                         : min(stride, (__ldg(span_count + qi / chunk) + span_len - 1) / span_len);
   __shared__ float wgt[kMaxSplits];
   __shared__ float inv;
-  const float* ml = part_ml + (int64_t)qi * nsplit * 2 * kHq;
+  const float* ml = part_ml + (int64_t)qi * stride * 2 * kHq;
   // 128 threads x 4 channels; the first four splits' rows are loaded before the weights
   // are known, so their latency overlaps the weights' reductions
-  const float4* po = reinterpret_cast<const float4*>(part_o + ((int64_t)qi * nsplit * kHq + h) * kDkv);
+  const float4* po = reinterpret_cast<const float4*>(part_o + ((int64_t)qi * stride * kHq + h) * kDkv);
   float4 v0[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u)
@@ -682,8 +690,16 @@ cudaError_t launch_attn(const uint16_t* q, const uint8_t* codes, const uint8_t* 
   if (e != cudaSuccess) return e;
   if (splits > 1)
     e = launch_pdl(attn_combine_kernel, dim3(num_q, kHq), dim3(128), 0, s, (const float*)part_o,
-                   (const float*)part_ml, splits, out, lse);
+                   (const float*)part_ml, splits, out, lse, (const int32_t*)nullptr, 1, 1);
   return e;
+}
+
+cudaError_t launch_attn_combine(const float* part_o, const float* part_ml, int nsplit,
+                                int32_t num_q, float* out, float* lse, const int32_t* span_count,
+                                int32_t span_len, int32_t chunk, cudaStream_t s) {
+  if (nsplit > kMaxSplits) return cudaErrorInvalidValue;
+  return launch_pdl(attn_combine_kernel, dim3(num_q, kHq), dim3(128), 0, s, part_o, part_ml, nsplit,
+                    out, lse, span_count, (int)span_len, (int)chunk);
 }
 
 size_t attn_workspace_bytes(int32_t num_q, int32_t topk, int num_sms) {

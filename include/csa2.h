@@ -205,6 +205,35 @@ CSA2_API csa2_status csa2_sparse_attn_mx(const uint16_t* q, const uint8_t* codes
                                          size_t workspace_bytes, int32_t* dev_status,
                                          cudaStream_t stream);
 
+/* Multi-query sparse attention, dense-contraction form: the queries come in chunks of
+ * `chunk` consecutive queries (1..4) of one sequence -- the draft tokens of a decode step,
+ * or consecutive positions of a prefill chunk -- each with its own top-K selection
+ * (tech-report digest, "Reuse Mode": attention over each query's top-K entries; the
+ * digest's "Full Mode": a sequence's draft tokens each select their own entries).
+ * The union of a chunk's selections is gathered and dequantised once, and all the
+ * chunk's heads are contracted against it on the tensor cores, each query's logits
+ * masked to the entries it selected.  Results equal csa2_sparse_attn on the same
+ * arguments (same formula, rounding order aside), for selections without a repeated
+ * token: a token listed twice by one query counts once here.
+ *
+ *   chunk  1..4; num_q a multiple of chunk; every query of a chunk has the same q_seq
+ *          (otherwise CSA2_DEV_BAD_QSEQ and that chunk's queries get out = 0, lse = -inf)
+ *   topk   chunk * topk <= CSA2_CHUNK_ATTN_MAX_UNION (CSA2_ERR_UNSUPPORTED above it)
+ *   other arguments as csa2_sparse_attn (E4M3 / 16 cache); lse nullable
+ * Workspace: csa2_chunk_attn_workspace_size(num_q, chunk, topk) bytes (16-byte aligned).
+ */
+#define CSA2_CHUNK_ATTN_MAX_UNION 8192
+CSA2_API csa2_status csa2_sparse_attn_chunked(const uint16_t* q, const uint8_t* codes,
+                                              const uint8_t* scales, const int32_t* idx,
+                                              const csa2_pages* pages, float* out, float* lse,
+                                              int32_t num_q, const int32_t* q_seq, int32_t chunk,
+                                              int32_t topk, float softmax_scale, void* workspace,
+                                              size_t workspace_bytes, int32_t* dev_status,
+                                              cudaStream_t stream);
+
+/* Workspace bytes of csa2_sparse_attn_chunked; 0 for arguments it rejects. */
+CSA2_API size_t csa2_chunk_attn_workspace_size(int32_t num_q, int32_t chunk, int32_t topk);
+
 /* csa2_sparse_attn without caller workspace.  The pages have no counterpart to this
  * entry point: it exists for callers that cannot allocate device memory around the
  * call (plain C clients that hold no device allocator, or decode loops that must not

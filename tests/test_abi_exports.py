@@ -63,6 +63,37 @@ def test_host_side_checks_without_device():
     assert csa2.csa2_index_workspace_size(csa2.CSA2_REUSE, 64, 2048, 8192) == 0
 
 
+def test_chunked_attention_host_checks():
+    """Argument checks and workspace sizing of csa2_sparse_attn_chunked, before any device
+    work (fake aligned addresses are never dereferenced)."""
+    import fp4_compressed_sparse_03_b300 as csa2
+    L = csa2._lib
+    fake = 1 << 12
+    pages = csa2.Csa2Pages(1, fake, fake, 1, 1, 64)
+
+    def call(nq, chunk, k, ws=fake, wsb=1 << 30):
+        return L.csa2_sparse_attn_chunked(fake, fake, fake, fake, ctypes.byref(pages), fake, None,
+                                          nq, fake, chunk, k, ctypes.c_float(0.04), ws, wsb, None,
+                                          None)
+
+    assert call(6, 4, 16) == csa2.CSA2_ERR_INVALID_ARGUMENT      # num_q not a multiple of chunk
+    assert call(4, 0, 16) == csa2.CSA2_ERR_INVALID_ARGUMENT
+    assert call(5, 5, 16) == csa2.CSA2_ERR_UNSUPPORTED           # more than four queries
+    assert call(4, 4, 2049) == csa2.CSA2_ERR_UNSUPPORTED         # union above 8192 entries
+    assert call(4, 4, 2048, ws=None) == csa2.CSA2_ERR_INVALID_ARGUMENT
+    assert call(4, 4, 2048, wsb=1024) == csa2.CSA2_ERR_INVALID_ARGUMENT
+    assert call(4, 4, 2048, ws=fake + 8) == csa2.CSA2_ERR_INVALID_ARGUMENT
+    assert csa2.csa2_chunk_attn_workspace_size(6, 4, 16) == 0
+    assert csa2.csa2_chunk_attn_workspace_size(4, 4, 4096) == 0
+    # union slots and masks, then per query and span 16 x 512 partial outputs and 32 (m, l)
+    nq, chunk, k = 256, 4, 2048
+    ws = csa2.csa2_chunk_attn_workspace_size(nq, chunk, k)
+    per_span = nq * (16 * 512 + 32) * 4
+    union = (nq // chunk) * chunk * k * 5
+    assert union + per_span <= ws <= union + 16 * per_span + 4096
+    assert (ws - union) % per_span < 4096
+
+
 def test_generator_library_host_path():
     import numpy as np
     import csa2_inputs as gen
