@@ -104,6 +104,27 @@ def test_generator_library_host_path():
                           gen.latent_rows(3, 1, 2, np.arange(5, 25), g))
 
 
+def test_overlapping_selections_generator():
+    """The multi-query workload's selections: sorted distinct tokens of the context, -1
+    padding only at the end, the stated shared part common to every query, and every query
+    selecting the whole context when it is shorter than K."""
+    import numpy as np
+    import csa2_inputs as gen
+    sets = gen.overlapping_index_sets(5, 3, 3000, 512, 4, 0.75)
+    assert sets.shape == (4, 512) and sets.dtype == np.int32
+    for row in sets:
+        assert np.all(np.diff(row) > 0) and row.min() >= 0 and row.max() < 3000
+    common = set(sets[0]).intersection(*map(set, sets[1:]))
+    assert len(common) >= 384  # round(0.75 * 512), plus chance agreements
+    assert len(set(sets.ravel())) <= 384 + 4 * 128
+    assert np.array_equal(sets, gen.overlapping_index_sets(5, 3, 3000, 512, 4, 0.75))
+    short = gen.overlapping_index_sets(5, 4, 300, 512, 3, 0.5)
+    for row in short:
+        assert np.array_equal(row[:300], np.arange(300)) and np.all(row[300:] == -1)
+    none = gen.overlapping_index_sets(5, 6, 4096, 256, 2, 0.0)
+    assert len(set(none[0]) & set(none[1])) < 64  # independent draws: about 16 in common
+
+
 def test_graft_build_entry():
     import __graft_entry__
     __graft_entry__.build()
