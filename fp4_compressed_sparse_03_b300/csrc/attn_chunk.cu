@@ -1,6 +1,8 @@
 // Multi-query sparse attention in dense-contraction form: a chunk of up to four queries of
 // one sequence (the draft tokens of a decode step, or consecutive positions of a prefill
-// chunk), each with its own top-K selection.
+// chunk), each with its own top-K selection.  Draft tokens: tech-report digest, DSpark
+// item under "さらなるアーキテクチャ拡張技術" (speculative decoding, semi-autoregressive
+// drafts); per-query selection: the digest's "Hierarchical Sparse Indexer".
 //
 // tech-report digest (jiwasawa.github.io), "Reuse Mode": sparse attention runs over the
 // selected top-K entries; zaikei.co.jp article, "CSA2とFP4でキャッシュを圧縮": the main KV

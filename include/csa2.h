@@ -208,8 +208,11 @@ CSA2_API csa2_status csa2_sparse_attn_mx(const uint16_t* q, const uint8_t* codes
 /* Multi-query sparse attention, dense-contraction form: the queries come in chunks of
  * `chunk` consecutive queries (1..4) of one sequence -- the draft tokens of a decode step,
  * or consecutive positions of a prefill chunk -- each with its own top-K selection
- * (tech-report digest, "Reuse Mode": attention over each query's top-K entries; the
- * digest's "Full Mode": a sequence's draft tokens each select their own entries).
+ * (tech-report digest, "Reuse Mode": attention over each query's top-K entries;
+ * "Hierarchical Sparse Indexer": the search and its cost are per query; draft tokens:
+ * the digest's DSpark item under "さらなるアーキテクチャ拡張技術", speculative decoding
+ * with semi-autoregressive drafts; prefill: the zaikei article's 64K-token sparse
+ * attention training length).
  * The union of a chunk's selections is gathered and dequantised once, and all the
  * chunk's heads are contracted against it on the tensor cores, each query's logits
  * masked to the entries it selected.  Results equal csa2_sparse_attn on the same

@@ -3,7 +3,8 @@ query of a chunk against the oracle over its own selection, and against the per-
 path on the same arguments.
 
 A chunk is up to four queries of one sequence with their own top-K entries: the draft
-tokens of a decode step (tech-report digest, jiwasawa.github.io, "Full Mode") or
+tokens of a decode step (tech-report digest, jiwasawa.github.io, DSpark item under
+"さらなるアーキテクチャ拡張技術"; per-query selection: "Hierarchical Sparse Indexer") or
 consecutive positions of a prefill chunk; attention over each query's selected FP4 rows
 (digest "Reuse Mode"; zaikei.co.jp article, "CSA2とFP4でキャッシュを圧縮").  Outputs within
 2e-3 x RMS per query, lse within 1e-4."""
