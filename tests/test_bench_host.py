@@ -83,6 +83,21 @@ def test_reference_arm_line_on_decode_append():
     assert line["config"]["workload"].startswith("decode_append") and line["config"]["tokens"] == 64
 
 
+def test_reference_arm_line_on_draft_chunk():
+    """The multi-query workload's reference arm: the oracle on one of its 256 draft queries,
+    with the line's metric, unit and workload those of the GPU arm."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", "draft_chunk", "--steps", "1", "--warmup", "0",
+                          "--cpu-sample", "1"], capture_output=True, text=True, timeout=600,
+                         cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "queries/s"
+    assert line["metric"] == bench.CHUNK_METRIC
+    assert line["config"]["workload"] == "draft_chunk_64x4x16384"
+    assert line["cpu_baseline"]["kind"] == "oracle"
+
+
 @pytest.mark.parametrize("world", [2])
 def test_reference_arm_under_torchrun_prints_once(world):
     env = dict(os.environ, CSA2_BENCH_BACKEND="gloo")
