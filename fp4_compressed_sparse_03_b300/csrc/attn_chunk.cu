@@ -20,7 +20,7 @@
 //      softmax per head row, O += P C;
 //   3. the split combine of the per-query path, reading only the spans that the chunk's
 //      union reaches.
-// E2M1 x E4M3 products are exact in f16 (at most 5 significant bits, 2^-10 .. 2688), and
+// E2M1 x E4M3 products are exact in f16 (at most 6 significant bits, 2^-10 .. 2688), and
 // Q is prescaled per query by a power of two into f16 range, as in the per-query kernel.
 // A token selected twice by one query counts once here (the indexer never emits a token
 // twice).
