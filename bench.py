@@ -596,18 +596,19 @@ def run_pages(args, world, rank, local):
 
 CHUNK_METRIC = ("multi-query sparse attention: query tokens/s, 4 draft queries per sequence "
                 "with their own top-K")
-CHUNK_SHARED = 0.75  # fraction of each draft query's selection common to its chunk
+CHUNK_SHARED = 0.75  # default fraction of each draft query's selection common to its chunk
 
 
-def chunk_inputs(dev=None):
+def chunk_inputs(shared=CHUNK_SHARED):
     """The draft-token chunk workload: the 64 x 16384-token cache, 4 draft queries per
-    sequence, each with top-2048 entries of which 75 % are common to the sequence's four
-    (host arrays: q bf16 bits [256, 16, 512], idx int32 [256, 2048], q_seq int32 [256])."""
+    sequence, each with top-2048 entries of which `shared` (75 % by default) are common to
+    the sequence's four (host arrays: q bf16 bits [256, 16, 512], idx int32 [256, 2048],
+    q_seq int32 [256])."""
     import csa2_inputs as gen
     wl = workload_of("decode_short")
     B, G, K = len(wl.seq_lens), 4, wl.topk
     idx = np.concatenate([gen.overlapping_index_sets(wl.seed, b, int(wl.seq_lens[b]), K, G,
-                                                     CHUNK_SHARED) for b in range(B)])
+                                                     shared) for b in range(B)])
     q = gen.q_rows(wl.seed, 7, np.arange(B * G))
     q_seq = np.repeat(np.arange(B, dtype=np.int32), G)
     return wl, q, idx, q_seq, G, K
@@ -625,7 +626,7 @@ def run_chunk(args, world, rank, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl, q, idx, q_seq, G, K = chunk_inputs()
+    wl, q, idx, q_seq, G, K = chunk_inputs(args.shared)
     cache = fill_decode_cache(wl, device=dev)
     nq = len(q_seq)
     q_d = torch.as_tensor(q.view(np.int16), device=dev)
@@ -713,7 +714,7 @@ def run_chunk(args, world, rank, local):
                         world, dev)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline_chunk(args.cpu_sample)
+        cpu = cpu_baseline_chunk(args.cpu_sample, args.shared)
     line = {
         "metric": CHUNK_METRIC, "value": round(value, 1), "unit": "queries/s", "n_gpus": world,
         "steps": Kst, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -722,7 +723,7 @@ def run_chunk(args, world, rank, local):
         "data": "synthetic (seeded counter-based generator)",
         "config": {"workload": "draft_chunk_64x4x16384", "num_seqs": len(wl.seq_lens),
                    "queries_per_chunk": G, "context_tokens": int(wl.seq_lens.max()), "topk": K,
-                   "shared_fraction": CHUNK_SHARED, "union_rows": int(union),
+                   "shared_fraction": args.shared, "union_rows": int(union),
                    "l2": "flushed before every call (256 MB written): the selected rows fit in L2",
                    "per_query_path_ms": round(ms_pq, 4), "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm",
@@ -743,14 +744,14 @@ def run_chunk(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def cpu_baseline_chunk(sample_queries: int):
+def cpu_baseline_chunk(sample_queries: int, shared: float = CHUNK_SHARED):
     """The oracle (gather, dequantise, double-precision attention per query) on the first
     `sample_queries` draft queries of the chunk workload; the cache rows of their
     sequences are generated and quantised before the clock starts."""
     import csa2_inputs as gen
     import oracle
     from csa2_inputs import native
-    wl, q, idx, q_seq, G, K = chunk_inputs()
+    wl, q, idx, q_seq, G, K = chunk_inputs(shared)
     n = max(1, min(sample_queries, len(q_seq)))
     gains = gen.latent_gains(wl.seed, 0)
     rows = {}
@@ -940,7 +941,7 @@ def run_reference(args, world, rank):
     if args.workload == "draft_chunk":
         per_step = max(1, args.cpu_sample // max(1, args.steps))
         t0 = time.perf_counter()
-        vals = [cpu_baseline_chunk(per_step) for _ in range(args.steps)]
+        vals = [cpu_baseline_chunk(per_step, args.shared) for _ in range(args.steps)]
         dt = time.perf_counter() - t0
         cb = dict(vals[-1])
         cb["value"] = round(float(np.mean([c["value"] for c in vals])), 3)
@@ -1043,6 +1044,8 @@ def main():
                          "default 32 queries / 256 rows (all 64 for decode_append), about "
                          "10-30 s of CPU work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shared", type=float, default=CHUNK_SHARED,
+                    help="draft_chunk: fraction of each query's selection common to its chunk")
     args = ap.parse_args()
     if args.cpu_sample is None:
         args.cpu_sample = {"ced_write": 256, "decode_append": 64,
