@@ -144,6 +144,51 @@ def shard_sequences(num_seqs: int, world: int, rank: int, scaling: str = "weak")
 
 # ------------------------------------------------------------------ algorithmic bytes --
 
+def decode_config(wl, mx: bool, world: int) -> dict:
+    """The `config` of a decode-workload line; the reference arm prints the same one."""
+    return {"workload": wl.name + ("_mxfp4" if mx else ""), "num_seqs": int(len(wl.seq_lens)),
+            "context_tokens": int(wl.seq_lens.max()), "query_tokens": wl.num_q,
+            "layers": len(wl.schedule), "schedule": "".join("FRU"[m] for m in wl.schedule),
+            "pool": wl.pool_size, "topk": wl.topk,
+            "l2": "no flush: every step streams %.2f GB of indexer keys (> 126 MB L2)"
+                  % (full_index_bytes(wl) / 1e9),
+            "launch": "CUDA graph of the step's libcsa2 calls; per-mode times from "
+                      "per-call graphs",
+            "parallelism": f"replicas x{world}"}
+
+
+def write_config(ww, world: int) -> dict:
+    """The `config` of a write-path line (prefill write or decode-time append)."""
+    append = ww.T <= 128
+    l2 = ("flushed before every call (256 MB written): the %.0f MB of weights fit in L2"
+          % (ww.n_out * ww.d_model * 2 / 1e6)) if append else \
+        "no flush: H is %.0f MB (> 126 MB L2)" % (ww.T * ww.d_model * 2 / 1e6)
+    return {"workload": ww.name, "tokens": ww.T, "d_model": ww.d_model,
+            "latent_projections": ww.n_kv_proj, "key_projections": ww.n_idx_proj,
+            "l2": l2, "parallelism": f"replicas x{world}"}
+
+
+def pages_config(world: int, n: int = 16384, rec: int = 34816) -> dict:
+    """The `config` of the page-export line (every page of the 64 x 16384-token cache)."""
+    return {"workload": "page_export_64x16384", "pages": n, "record_bytes": rec,
+            "l2": "no flush: %.0f MB of pages per step (> 126 MB L2)" % (n * rec / 1e6),
+            "parallelism": f"replicas x{world}"}
+
+
+def host_cpu() -> dict:
+    """CPU model and logical core count of this host (for every CPU timing)."""
+    model = "unknown"
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.startswith("model name"):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"cpu_model": model, "nproc": os.cpu_count() or 1}
+
+
 def full_index_bytes(wl) -> int:
     """Bytes a Full-layer index step must move: every context key row (256 B) of every
     query's sequence (read once per sequence), the indexer queries, top-K and pool."""
@@ -326,15 +371,7 @@ def run_ours(args, world, rank, local):
         "dtype": ("fp4-e2m1/e8m0-per-32 (MXFP4) kv" if mx else "fp4-e2m1/e4m3 kv") +
                  ", bf16 keys+queries, f32 accumulate",
         "data": "synthetic (seeded counter-based generator)",
-        "config": {"workload": wl.name + ("_mxfp4" if mx else ""), "num_seqs": int(len(wl.seq_lens)),
-                   "context_tokens": int(wl.seq_lens.max()), "query_tokens": wl.num_q,
-                   "layers": L, "schedule": "".join("FRU"[m] for m in wl.schedule),
-                   "pool": wl.pool_size, "topk": wl.topk,
-                   "l2": "no flush: every step streams %.2f GB of indexer keys (> 126 MB L2)"
-                         % (fb / 1e9),
-                   "launch": "CUDA graph of the step's libcsa2 calls; per-mode times from "
-                             "per-call graphs",
-                   "parallelism": f"replicas x{world}"},
+        "config": decode_config(wl, mx, world),
         "per_mode_ms": {"full_index": round(full_ms, 4), "reindex": round(re_ms, 4),
                         "attention": round(attn_ms, 4)},
         "roofline": {"bound": "hbm", "kernel": "csa2_index(FULL) call: group_prefix_kernel + score_pages_kernel + select_cta_kernel",
@@ -471,13 +508,11 @@ def run_write(args, world, rank, local):
                 "achieved": round(achieved_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved_gbs / hbm_peak, 4), "peak_source": peak_src + " HBM copy",
                 "algorithmic_bytes_per_launch": int(abytes), "traffic": None}
-        l2 = "flushed before every call (256 MB written): the 105 MB of weights fit in L2"
     else:
         roof = {"bound": "tensor", "kernel": "csa2_kv_write: kv_write_kernel",
                 "achieved": round(achieved, 1), "peak": tc_peak, "unit": "TFLOP/s",
                 "frac": round(achieved / tc_peak, 4), "peak_source": peak_src + " bf16 burst",
                 "algorithmic_flops_per_launch": flops, "traffic": None}
-        l2 = "no flush: H is %.0f MB (> 126 MB L2)" % (H.numel() * 2 / 1e6)
     line = {
         "metric": ("decode-time append: new tokens/s projected and quantised into the paged cache"
                    if append else "CED write path: tokens/s projected and quantised on write"),
@@ -486,11 +521,11 @@ def run_write(args, world, rank, local):
         "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 operands, f32 accumulate, fp4-e2m1/e4m3 + bf16 out",
         "data": "synthetic (seeded counter-based generator)",
-        "config": {"workload": ww.name, "tokens": ww.T, "d_model": ww.d_model,
-                   "latent_projections": ww.n_kv_proj, "key_projections": ww.n_idx_proj,
-                   "l2": l2, "parallelism": f"replicas x{world}"},
+        "config": write_config(ww, world),
         "roofline": roof,
         "e2e": {"value": round(units / (ms_e2e / 1e3), 1), "unit": "tokens/s",
+                "l2_flush": ("each timed step includes the 256 MB L2 flush write (about 40 us)"
+                             if append else "none"),
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": K2},
         "gpu_launches": K,
         "clocks": clk,
@@ -576,9 +611,7 @@ def run_pages(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8 (byte copy)",
         "data": "synthetic (seeded counter-based generator)",
-        "config": {"workload": "page_export_64x16384", "pages": n, "record_bytes": rec,
-                   "l2": "no flush: %.0f MB of pages per step (> 126 MB L2)" % (n * rec / 1e6),
-                   "parallelism": f"replicas x{world}"},
+        "config": pages_config(world, n, rec),
         "roofline": {"bound": "hbm", "kernel": "csa2_export_pages: page_copy_kernel",
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src + " HBM copy",
@@ -733,6 +766,7 @@ def run_chunk(args, world, rank, local):
                      "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src + " HBM copy",
                      "algorithmic_bytes_per_launch": int(abytes), "traffic": None},
         "e2e": {"value": round(nq * world / (ms_e2e / 1e3), 1), "unit": "queries/s",
+                "l2_flush": "each timed step includes the 256 MB L2 flush write (about 40 us)",
                 "h2d_bytes_per_step": int(q_d.numel() * 2 + idx_d.numel() * 4),
                 "d2h_bytes_per_step": int(out.numel() * 4 + lse.numel() * 4), "steps": K2},
         "gpu_launches": 3 * Kst,
@@ -763,7 +797,7 @@ def cpu_baseline_chunk(sample_queries: int, shared: float = CHUNK_SHARED):
         c, s = rows[int(q_seq[i])]
         oracle.attention_over_cache(q[i], c, s, idx[i], scale)
     dt = time.perf_counter() - t0
-    return {"value": round(n / dt, 3), "unit": "queries/s", "cores": 1, "kind": "oracle",
+    return {"value": round(n / dt, 3), "unit": "queries/s", "cores": 1, "kind": "oracle", **host_cpu(),
             "sample": f"{n} of {len(q_seq)} queries of draft_chunk_64x4x16384, {dt:.1f} s on 1 thread"}
 
 
@@ -783,7 +817,7 @@ def cpu_baseline_pages(sample_pages: int, repeats: int = 200):
     for _ in range(repeats):
         oracle.pack_pages(codes, scales, keys, ids)
     dt = time.perf_counter() - t0
-    return {"value": round(repeats * n / dt, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+    return {"value": round(repeats * n / dt, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle", **host_cpu(),
             "sample": f"{n // 64} pages of page_export_64x16384 packed {repeats} times, "
                       f"{dt:.1f} s on 1 thread"}
 
@@ -803,7 +837,7 @@ def cpu_baseline_write(ww, sample_rows: int):
     with ThreadPoolExecutor(max_workers=threads) as ex:
         list(ex.map(lambda h: oracle.kv_write_rows(h, Wt, ww.n_kv_proj, ww.n_idx_proj), Hs))
     dt = time.perf_counter() - t0
-    return {"value": round(len(Hs) / dt, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+    return {"value": round(len(Hs) / dt, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle", **host_cpu(),
             "sample": f"{len(Hs)} of {ww.T} token rows x {ww.n_out} output columns of {ww.name}, "
                       f"{dt:.1f} s wall on {threads} threads"}
 
@@ -898,7 +932,7 @@ def cpu_baseline(wl, sample_queries: int, mx: bool = False):
     import csa2_inputs as gen
     import oracle
     from csa2_inputs import native
-    from fp4_compressed_sparse_03_b300.workload import layer_queries_host
+    from csa2_inputs.native import layer_queries_host
 
     cores = os.cpu_count() or 1
     qs = np.linspace(0, wl.num_q - 1, min(sample_queries, wl.num_q)).astype(int)
@@ -926,7 +960,7 @@ def cpu_baseline(wl, sample_queries: int, mx: bool = False):
                                                  mx), inputs))
     dt = time.perf_counter() - t0
     return {"value": round(len(inputs) * L / dt, 3), "unit": UNIT, "cores": threads,
-            "kind": "oracle",
+            "kind": "oracle", **host_cpu(),
             "sample": f"{len(inputs)} of {wl.num_q} queries x {L} layers of {wl.name}, "
                       f"{dt:.1f} s wall on {threads} threads"}
 
@@ -966,7 +1000,7 @@ def run_reference(args, world, rank):
                 "ms_per_step": round(1048576 / cb["value"] * 1e3, 2), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "u8 (CPU oracle, numpy)",
                 "data": "synthetic (seeded counter-based generator)",
-                "config": {"workload": "page_export_64x16384"}, "cpu_baseline": cb,
+                "config": pages_config(world), "cpu_baseline": cb,
                 "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
@@ -989,10 +1023,7 @@ def run_reference(args, world, rank):
             "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64 (CPU oracle)",
             "data": "synthetic (seeded counter-based generator)",
-            "config": {"workload": wl.name + ("_mxfp4" if args.workload.endswith("_mx") else ""),
-                       "num_seqs": int(len(wl.seq_lens)),
-                       "context_tokens": int(wl.seq_lens.max()), "query_tokens": wl.num_q,
-                       "layers": len(wl.schedule), "pool": wl.pool_size, "topk": wl.topk},
+            "config": decode_config(wl, args.workload.endswith("_mx"), world),
             "cpu_baseline": cb,
             "e2e": {"value": round(v, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -1020,8 +1051,7 @@ def run_reference_write(args, world):
             "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64 (CPU oracle)", "data": "synthetic (seeded counter-based generator)",
-            "config": {"workload": ww.name, "tokens": ww.T, "d_model": ww.d_model,
-                       "latent_projections": ww.n_kv_proj, "key_projections": ww.n_idx_proj},
+            "config": write_config(ww, world),
             "cpu_baseline": cb,
             "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}

@@ -109,3 +109,24 @@ def seq_keys(seed: int, tag: int, group: int, num_seqs: int) -> np.ndarray:
     """Stream keys of every sequence (uint64), for the paged device fill."""
     return np.array([gen.stream_key(seed, tag, (group << 24) | b) for b in range(num_seqs)],
                     dtype=np.uint64)
+
+
+# ------------------------------------------------------------------ queries -------
+
+def layer_queries_host(wl: "gen.DecodeWorkload", layer: int):
+    """(q_idx bf16 bits [num_q, 4, 128], q bf16 bits [num_q, 16, 512]) of one layer."""
+    nq = wl.num_q
+    q_idx = np.empty((nq, gen.H_IDX, gen.D_IDX), np.uint16)
+    q = np.empty((nq, gen.H_Q, gen.D_KV), np.uint16)
+    for i in range(nq):
+        kq = gen.stream_key(wl.seed, gen.TAG_QIDX, (layer << 24) | i)
+        q_idx[i] = normal_bf16_host(kq, 0, gen.H_IDX * gen.D_IDX).reshape(gen.H_IDX, gen.D_IDX)
+        ka = gen.stream_key(wl.seed, gen.TAG_Q, (layer << 24) | i)
+        q[i] = normal_bf16_host(ka, 0, gen.H_Q * gen.D_KV).reshape(gen.H_Q, gen.D_KV)
+    return q_idx, q
+
+
+def all_queries_host(wl: "gen.DecodeWorkload"):
+    """Stacked per-layer queries: q_idx [L, num_q, 4, 128], q [L, num_q, 16, 512] (bf16 bits)."""
+    qs = [layer_queries_host(wl, l) for l in range(len(wl.schedule))]
+    return np.stack([a for a, _ in qs]), np.stack([b for _, b in qs])

@@ -10,7 +10,13 @@
 // of each head) are written in full by the attention kernel before the combine kernel
 // reads them, so nothing in the array has to start at zero and no clearing pass runs.
 // The array is shared by every call on a device: calls that overlap in time (on two
-// streams, or from two host threads) race on it.
+// streams, or from two host threads) race on it.  Being a module global, its 16 MiB are
+// reserved on every device where the module of this file is loaded: under lazy module
+// loading (the CUDA default) at the first call of this entry point on the device (the
+// module holds no kernel, only the array), and under CUDA_MODULE_LOADING=EAGER at
+// context creation, whether or not this entry point is ever called.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "csa2.h"
@@ -21,10 +27,29 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
+// Per device: the context the address was resolved in, and the address.  A context that
+// was destroyed and recreated (cudaDeviceReset) reloads this module at a new address, so
+// the address is resolved again whenever the current context differs from the recorded one.
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of g_attn_scratch on the current device, resolved on the first call
-// made with that device current.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  if (fn == nullptr) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(f);
+  }
+  return fn;
+}
+
+// Device address of g_attn_scratch in the current device's current context, resolved on
+// the first call made in that context.
 csa2_status scratch_of_current_device(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -32,14 +57,22 @@ csa2_status scratch_of_current_device(void** out) {
     return CSA2_ERR_CUDA;
   }
   if (dev < 0 || dev >= kMaxDevices) return CSA2_ERR_UNSUPPORTED;
+  CtxGetCurrentFn get = ctx_get_current();
+  if (get == nullptr) return CSA2_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  // cudaGetSymbolAddress makes the device's primary context current if none is
+  // (a first runtime call), so the context is read after it when it is resolved
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) return CSA2_ERR_CUDA;
+  if (g_scratch_ptr[dev] == nullptr || ctx == nullptr || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || p == nullptr) {
       (void)cudaGetLastError();
       return CSA2_ERR_CUDA;
     }
+    if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr) return CSA2_ERR_CUDA;
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_ptr[dev];
   return CSA2_OK;

@@ -249,7 +249,14 @@ CSA2_API size_t csa2_chunk_attn_workspace_size(int32_t num_q, int32_t chunk, int
  * before any stream capture.  Returns CSA2_ERR_UNSUPPORTED when
  * csa2_attn_workspace_size(num_q, topk) exceeds CSA2_ATTN_STATIC_SCRATCH_BYTES, and
  * CSA2_ERR_CUDA if the address cannot be resolved.  The array is shared by all calls
- * on a device: calls that overlap in time (several streams or host threads) race. */
+ * on a device: calls that overlap in time (several streams or host threads) race; calls
+ * issued one after another on one stream do not, so a batch over the limit can be split
+ * into several calls on one stream.  The address is resolved again after the device's
+ * context is destroyed and recreated (cudaDeviceReset).  Footprint: the array occupies
+ * CSA2_ATTN_STATIC_SCRATCH_BYTES of device memory on every device where it is loaded --
+ * at the first call of this function on the device under lazy module loading (the CUDA
+ * default), or at context creation under CUDA_MODULE_LOADING=EAGER even if the function
+ * is never called -- and until the context is destroyed. */
 #define CSA2_ATTN_STATIC_SCRATCH_BYTES (16u << 20)
 CSA2_API csa2_status csa2_sparse_attn_static(const uint16_t* q, const uint8_t* codes,
                                              const uint8_t* scales, const int32_t* idx,

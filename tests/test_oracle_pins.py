@@ -294,6 +294,67 @@ def test_projection_one_hot_columns_and_library_gemm(orc):
     np.testing.assert_allclose(C, ref.astype(np.float32), rtol=1e-6, atol=1e-7)
 
 
+def _bf16_ties():
+    """fp32 patterns whose low 16 bits are exactly half a bf16 unit (0x8000), over upper
+    halves with an even and an odd last bit, both signs, normal and subnormal exponents,
+    plus the patterns one below and one above each tie."""
+    uppers = np.array([0x3F80, 0x3F81, 0x3F82, 0x3F83, 0x4000, 0x4001, 0x7F7E, 0x0000, 0x0001,
+                       0x0080, 0x0081, 0x1234, 0x1235, 0x4B7F, 0x4B80], np.uint32)
+    uppers = np.concatenate([uppers, uppers | 0x8000])
+    ties = (uppers << 16) | 0x8000
+    return np.concatenate([ties, ties - 1, ties + 1]).view(np.float32)
+
+
+def test_bf16_store_worked_by_hand(orc):
+    """The indexer-key store is fp32 -> bf16 round-to-nearest, ties to even (tech-report
+    digest "Causal Encoder-Decoder (CED) アーキテクチャ": the keys are the projection C_l,
+    held as bf16).  bf16 keeps 8 significant bits, so at 1.0 one unit is 2^-7:
+      1 + 2^-8     lies halfway between 1 (even) and 1 + 2^-7 (odd)      -> 0x3F80
+      1 + 3*2^-8   halfway between 1 + 2^-7 (odd) and 1 + 2^-6 (even)    -> 0x3F82
+      1 + 2^-8 + 2^-23  just above the first tie                          -> 0x3F81
+      -(1 + 2^-8)  the same tie, negative                                 -> 0xBF80
+      3.39e38 (0x7F7F8000): halfway to the next power, even side is 0x7F80 = inf
+      the smallest positive subnormal rounds to 0, 2^-133 (subnormal, exact in bf16) stays."""
+    x = np.array([1 + 2.0**-8, 1 + 3 * 2.0**-8, 1 + 2.0**-8 + 2.0**-23, -(1 + 2.0**-8)],
+                 np.float32)
+    assert orc.f32_to_bf16_bits(x).tolist() == [0x3F80, 0x3F82, 0x3F81, 0xBF80]
+    big = np.array([0x7F7F8000, 0x7F7E8000], np.uint32).view(np.float32)
+    assert orc.f32_to_bf16_bits(big).tolist() == [0x7F80, 0x7F7E]
+    sub = np.array([0x00000001, 0x00008000, 0x00018000, 0x00010000], np.uint32).view(np.float32)
+    assert orc.f32_to_bf16_bits(sub).tolist() == [0x0000, 0x0000, 0x0002, 0x0001]
+
+
+def test_bf16_store_matches_torch(orc):
+    """Against the library's own fp32 -> bf16 conversion (round to nearest even), bit for
+    bit, on 2^21 random finite fp32 patterns (every exponent) and on the exact ties."""
+    import torch
+    rng = np.random.default_rng(21)
+    u = rng.integers(0, 2**32, size=1 << 21, dtype=np.uint64).astype(np.uint32)
+    u = u[(u & 0x7F800000) != 0x7F800000]                    # finite only
+    x = np.concatenate([u.view(np.float32), _bf16_ties()])
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = orc.f32_to_bf16_bits(x)
+    bad = np.flatnonzero(got != want)
+    assert bad.size == 0, f"{bad.size} mismatches, first fp32 {x[bad[:4]].view(np.uint32)}"
+
+
+def test_write_path_keys_round_the_fp32_projection(orc):
+    """Keys of the write path are bf16(fl32(sum)) of sums that are not bf16 values: two
+    nonzero weights per column put C = H[:, a] + H[:, b] / 3 between bf16 neighbours, and the
+    stored key must equal torch's rounding of the oracle's fp32 C."""
+    import torch
+    rng = np.random.default_rng(22)
+    H = _bf16(rng.standard_normal((16, 256)))
+    Wt = np.zeros((128, 256), np.uint16)
+    a, b = rng.permutation(256)[:128], rng.permutation(256)[:128]
+    Wt[np.arange(128), a] = 0x3F80                      # 1.0
+    Wt[np.arange(128), b] = _bf16(np.float32(1 / 3))    # bf16(1/3), 8 significant bits
+    codes, scales, keys, C = orc.kv_write_rows(H, Wt, 0, 1)
+    want = torch.from_numpy(C.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+    assert np.array_equal(keys[0], want.view(np.uint16))
+    assert np.mean(gen.bf16_bits_to_f32(keys[0]) != C) > 0.9   # the rounding is exercised
+
+
 # ------------------------------------------------------------------ indexer --------
 
 def test_index_score_special_cases(orc):
