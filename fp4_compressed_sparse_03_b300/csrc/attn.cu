@@ -669,17 +669,28 @@ int attn_split_len(int32_t topk, int splits) {
 
 size_t attn_smem_bytes(bool mx) { return mx ? sizeof(AttnSmemT<true>) : sizeof(AttnSmemT<false>); }
 
+cudaError_t launch_attn_nvf4(const uint16_t* q, const uint8_t* codes, const uint8_t* scales,
+                             const int32_t* idx, const csa2_pages& pg, float* out, float* lse,
+                             int32_t num_q, const int32_t* q_seq, int32_t topk, float softmax_scale,
+                             void* ws, int32_t* st, cudaStream_t s, int num_sms);
+size_t attn_nvf4_workspace_bytes(int32_t num_q, int32_t topk, int num_sms);
+
+// The E4M3 / 16 cache takes the block-scaled FP4 tensor-core path (attn_nvf4.cu); the
+// MXFP4 variant runs sparse_attn_kernel<true> above.
 cudaError_t launch_attn(const uint16_t* q, const uint8_t* codes, const uint8_t* scales,
                         const int32_t* idx, const csa2_pages& pg, float* out, float* lse,
                         int32_t num_q, const int32_t* q_seq, int32_t topk, float softmax_scale,
                         void* ws, int32_t* st, cudaStream_t s, int num_sms, bool mx) {
+  if (!mx)
+    return launch_attn_nvf4(q, codes, scales, idx, pg, out, lse, num_q, q_seq, topk, softmax_scale, ws,
+                            st, s, num_sms);
   AttnGeom g{pg.seq_lens, pg.page_table, pg.max_pages_per_seq, pg.num_pages, pg.num_seqs};
   int splits = attn_splits(num_q, topk, num_sms);
   const int split_len = attn_split_len(topk, splits);
   splits = (topk + split_len - 1) / split_len;
   if (splits < 1) splits = 1;
-  const size_t smem = attn_smem_bytes(mx);
-  auto kern = mx ? sparse_attn_kernel<true> : sparse_attn_kernel<false>;
+  const size_t smem = attn_smem_bytes(true);
+  auto kern = sparse_attn_kernel<true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   float* part_o = reinterpret_cast<float*>(ws);
@@ -702,12 +713,13 @@ cudaError_t launch_attn_combine(const float* part_o, const float* part_ml, int n
                     out, lse, span_count, (int)span_len, (int)chunk);
 }
 
+// Workspace of either scale format (the larger of the two paths' needs).
 size_t attn_workspace_bytes(int32_t num_q, int32_t topk, int num_sms) {
   int splits = attn_splits(num_q, topk, num_sms);
   const int split_len = attn_split_len(topk, splits);
   splits = (topk + split_len - 1) / split_len;
-  if (splits <= 1) return 0;
-  return (size_t)num_q * splits * (kHq * kDkv + 2 * kHq) * sizeof(float);
+  const size_t mx = splits <= 1 ? 0 : (size_t)num_q * splits * (kHq * kDkv + 2 * kHq) * sizeof(float);
+  return std::max(mx, attn_nvf4_workspace_bytes(num_q, topk, num_sms));
 }
 
 }  // namespace csa2
