@@ -18,33 +18,16 @@
 //     once per query by q_terms_kernel;
 //   - one MMA per 64 channels, M = 128 tokens x N = 96 (term, head) rows, A = the gathered
 //     codes (128-byte swizzled, K-major), B = the terms, scale factors in TMEM, fp32
-//     accumulators in TMEM; the softmax warps weight the six term columns by 2^-p_k.
+//     accumulators in TMEM; the softmax weights the six term columns by 2^-p_k.
 // The weighted sum O = P . c_hat contracts over tokens, across the scale groups, so it
 // runs on mma.sync with each code dequantised once into operand registers (E2M1 x E4M3 is
 // exact in f16): 16 heads x 8 channels x 16 tokens per instruction, once with the hi part
-// of P and once with the lo part on the same operand registers.
+// of P and once with the lo part on the same operand registers.  One f16 part per weight
+// (11 significant bits) leaves output errors of the order of the 2e-3 x RMS accuracy bound
+// on a fraction of queries; hi + lo carry 22 bits.
 //
-// Work division (one wave, one CTA per SM): the num_q x ceil(topk / 128) tiles of 128
-// selected entries are cut into equal contiguous ranges, one per CTA, so a CTA may hold
-// the end of one query and the start of the next.  Each (CTA, query) segment leaves a
-// partial (O, running max, sum) unless it covers its query whole, in which case it writes
-// the normalised output itself; attn_stream_combine_kernel merges the partials of the
-// other queries by log-sum-exp.
-//
-// Warp roles in a CTA (384 threads):
-//   warps 0-3 ("gather" group, thread j <-> row j of a tile): resolve indices to rows,
-//     request the selected rows into L2 four tiles ahead (bulk prefetch), gather codes +
-//     scales with cp.async into a 4-stage ring two tiles ahead, write the
-//     tile's scale factors to TMEM, issue the MMAs (one thread), then the softmax of the
-//     tile before: fp32 in the exp2 domain with a lazily moved reference max per head
-//     (it moves, and the output is rescaled, only when a tile's logit exceeds it by more
-//     than 2^8); P is passed as two f16 parts, hi = f16(p) and lo = f16(p - hi), so the
-//     weights carry 22 significant bits (one f16 part alone, 11 bits, leaves output errors
-//     of the order of the 2e-3 x RMS accuracy bound), and the normaliser sums p in fp32;
-//   warps 4-11 ("output" group): O += P . c_hat, 64 output channels per warp.
-// Hand-offs use mbarriers: S ready (MMA commit), P ready (gather group), tile done
-// (output group; frees the stage and the P buffer).  Every wait is bounded: on expiry the
-// CTA reports CSA2_DEV_TIMEOUT, stops, drains its own copies and MMAs and frees TMEM.
+// Work division: one CTA per (query, split of its selected entries, at most 512), two CTAs
+// per SM; splits are merged by attn_combine_kernel (log-sum-exp).
 #include <algorithm>
 #include <cstddef>
 
