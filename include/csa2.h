@@ -247,7 +247,8 @@ CSA2_API size_t csa2_chunk_attn_workspace_size(int32_t num_q, int32_t chunk, int
  * call allocates nothing.  The first call on a device, made with that device current,
  * resolves the array's device address (cudaGetSymbolAddress); make that first call
  * before any stream capture.  Returns CSA2_ERR_UNSUPPORTED when
- * csa2_attn_workspace_size(num_q, topk) exceeds CSA2_ATTN_STATIC_SCRATCH_BYTES, and
+ * csa2_attn_workspace_size(num_q, topk) exceeds CSA2_ATTN_STATIC_SCRATCH_BYTES -- on a
+ * 148-SM B300 that is more than 74 queries at topk 2048 (64 queries need 9.8 MiB) -- and
  * CSA2_ERR_CUDA if the address cannot be resolved.  The array is shared by all calls
  * on a device: calls that overlap in time (several streams or host threads) race; calls
  * issued one after another on one stream do not, so a batch over the limit can be split

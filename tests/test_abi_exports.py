@@ -128,3 +128,14 @@ def test_overlapping_selections_generator():
 def test_graft_build_entry():
     import __graft_entry__
     __graft_entry__.build()
+
+
+def test_static_attention_scratch_limit():
+    """csa2_sparse_attn_static holds its scratch in a fixed array: at top-K 2048 on 148 SMs
+    the decode batch's 64 queries fit (9.8 MiB) and 74 is the most one call takes; a larger
+    batch is issued as several calls on one stream.  (Workspace sizes are host arithmetic;
+    without a device the library sizes for 148 SMs.)"""
+    import fp4_compressed_sparse_03_b300 as csa2
+    lim = csa2.ATTN_STATIC_SCRATCH_BYTES
+    assert csa2.csa2_attn_workspace_size(64, 2048) <= lim
+    assert csa2.csa2_attn_workspace_size(74, 2048) <= lim < csa2.csa2_attn_workspace_size(75, 2048)

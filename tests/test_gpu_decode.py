@@ -286,6 +286,59 @@ def test_attention_random_index_sets():
                 assert_attn_close(host(out[i]), o, host(lse[i]), l, f"topk {topk} q{i}")
 
 
+def _trend_cache(n_tok: int, slope: float, seed: int):
+    """A one-sequence cache (identity page table) whose latent rows drift along a fixed
+    direction d: x_t = base_t + slope * t * d, quantised by libcsa2's codec (bit-exact with
+    the oracle's).  Returns (cache, d, dequantised rows [n_tok, 512] from the oracle)."""
+    from fp4_compressed_sparse_03_b300.decode import DecodeCache
+    rng = np.random.default_rng(seed)
+    d = rng.standard_normal(512).astype(np.float32)
+    base = (rng.standard_normal((n_tok, 512)) * np.exp(0.5 * rng.standard_normal(512))).astype(np.float32)
+    x = (base + slope * np.arange(n_tok, dtype=np.float32)[:, None] * d).astype(np.float32)
+    pages = n_tok // 64
+    cache = DecodeCache(np.array([n_tok], np.int32), np.arange(pages, dtype=np.int32)[None, :], pages)
+    slots = torch.arange(n_tok, dtype=torch.int32, device="cuda")
+    csa2.check(csa2.csa2_quantize(dev(x), slots, cache.codes[0], cache.scales[0], n_tok, 512,
+                                  cache.num_slots), "quantize")
+    c, s = oracle.quantize(x)
+    return cache, d, oracle.dequantize(c, s)
+
+
+@pytest.mark.parametrize("direction", ["rising", "falling"])
+def test_attention_logits_far_apart_across_tiles_and_splits(direction):
+    """Logits that move by ~12 log2 units per 128-token tile (q_h = beta_h * d on rows drifting
+    along d), over 2048 selected entries: rising, the lazily moved reference max moves on
+    nearly every tile and the four 512-entry splits' maxima lie 2^40 and more apart, so
+    the split combine merges partials whose weights differ by many orders of magnitude;
+    falling, the first tile holds the maximum and no later tile rescales.  The earliest
+    entries' weights underflow to zero in both the kernel and the oracle."""
+    n_tok, topk = 4096, 2048
+    cache, d, chat = _trend_cache(n_tok, 2e-3 if direction == "rising" else -2e-3, 61)
+    beta = np.linspace(0.7, 2.2, 16, dtype=np.float32)
+    rng = np.random.default_rng(62)
+    q32 = beta[:, None] * d[None, :] + 0.05 * rng.standard_normal((16, 512)).astype(np.float32)
+    q = gen.f32_to_bf16_bits(q32)[None]
+    idx = np.arange(0, n_tok, 2, dtype=np.int32)[None, :]
+    assert idx.shape[1] == topk
+    out = torch.zeros((1, 16, 512), dtype=torch.float32, device="cuda")
+    lse = torch.zeros((1, 16), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(csa2.csa2_attn_workspace_size(1, topk), 16), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q_seq = dev(np.zeros(1, np.int32))
+    csa2.check(csa2.csa2_sparse_attn(dev(q), cache.codes[0], cache.scales[0], dev(idx), cache.pages,
+                                     out, lse, 1, q_seq, topk, SOFTMAX_SCALE, ws, dev_status=st), "attn")
+    status, bits = csa2.csa2_read_status(st)
+    assert status == csa2.CSA2_OK, hex(bits)
+    o, l = oracle.sparse_attention(q[0], chat[idx[0]], SOFTMAX_SCALE)
+    # the logits really span far more than the lazy gap and the split combine's range
+    z = (gen.bf16_bits_to_f32(q[0]).astype(np.float64) @ chat[idx[0]].T) * SOFTMAX_SCALE / np.log(2)
+    span = z.max(axis=1) - z.min(axis=1)
+    assert span.min() > 100, span.min()
+    split_max = z.reshape(16, 4, 512).max(axis=2)
+    assert np.abs(split_max[:, 3] - split_max[:, 0]).min() > 40
+    assert_attn_close(host(out[0]), o, host(lse[0]), l, f"{direction} logits")
+
+
 def test_mx_attention_random_index_sets():
     """The MXFP4 read path (csa2_sparse_attn_mx over a cache written by csa2_quantize_mx)
     against the oracle's attention over its own MXFP4 dequantisation: single- and
