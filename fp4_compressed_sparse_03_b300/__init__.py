@@ -91,6 +91,7 @@ _export_pages = _sig("csa2_export_pages", ctypes.c_int,
 _import_pages = _sig("csa2_import_pages", ctypes.c_int,
                      [_vp, _i32, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _vp])
 _read_status = _sig("csa2_read_status", ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp])
+_check_wait = _sig("csa2_check_bounded_wait", ctypes.c_int, [_i32, ctypes.c_uint32, _vp, _vp])
 _status_string = _sig("csa2_status_string", ctypes.c_char_p, [ctypes.c_int])
 _version = _sig("csa2_version", _i32, [])
 
@@ -257,6 +258,10 @@ def csa2_read_status(dev_status, stream=None):
     bits = _i32(0)
     st = _read_status(_ptr(dev_status), ctypes.byref(bits), _stream(stream))
     return int(st), int(bits.value)
+
+
+def csa2_check_bounded_wait(arrive, limit, dev_status, stream=None) -> int:
+    return _check_wait(1 if arrive else 0, limit, _ptr(dev_status), _stream(stream))
 
 
 from .decode import DecodeCache, DecodeStep  # noqa: E402,F401

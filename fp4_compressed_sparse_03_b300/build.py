@@ -8,7 +8,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libcsa2.so")
 SOURCES = ["api.cu", "codec.cu", "index.cu", "attn.cu", "kv_write.cu", "tensor_map.cu",
-           "attn_static.cu", "pages.cu", "attn_chunk.cu", "attn_nvf4.cu"]
+           "attn_static.cu", "pages.cu", "attn_chunk.cu", "attn_nvf4.cu", "diag.cu"]
 HEADERS = ["common.cuh", "async.cuh"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 

@@ -41,6 +41,7 @@ cudaError_t launch_page_copy(bool, uint8_t*, uint8_t*, uint8_t*, int, int64_t, c
 cudaError_t launch_kv_write(const uint16_t*, const uint16_t*, uint8_t*, uint8_t*, uint16_t*,
                             int32_t, int32_t, int32_t, int32_t, const int32_t*, int64_t, int32_t*,
                             cudaStream_t, int);
+cudaError_t launch_bounded_wait(int, uint32_t, int32_t*, cudaStream_t);
 }  // namespace csa2
 
 using namespace csa2;
@@ -373,6 +374,12 @@ csa2_status csa2_read_status(int32_t* dev_status, int32_t* host_bits, cudaStream
   if (bits & CSA2_DEV_TIMEOUT) return CSA2_ERR_TIMEOUT;
   if (bits) return CSA2_ERR_DEVICE_FAULT;
   return CSA2_OK;
+}
+
+csa2_status csa2_check_bounded_wait(int32_t arrive, uint32_t limit, int32_t* dev_status,
+                                    cudaStream_t stream) {
+  if (dev_status == nullptr || limit < 1 || limit > (1u << 20)) return CSA2_ERR_INVALID_ARGUMENT;
+  return from_cuda(launch_bounded_wait(arrive != 0, limit, dev_status, stream));
 }
 
 }  // extern "C"

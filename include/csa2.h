@@ -179,7 +179,12 @@ CSA2_API size_t csa2_index_workspace_size(csa2_mode mode, int32_t num_q, int32_t
  *   out    fp32 [num_q][16][512];  lse fp32 [num_q][16] (nullable)
  *   q_seq  int32 [num_q]
  * Workspace: csa2_attn_workspace_size(num_q, topk) bytes (may be 0).
- * fp32 online softmax, split over the selected set, merged by log-sum-exp.
+ * Arithmetic: the logits are taken on the block-scaled FP4 tensor cores from the codes
+ * and scales as stored, against q written as six NVFP4 terms (|q - terms| <= (3/16)^6 of
+ * each 16-channel block's maximum), with fp32 accumulation; fp32 online softmax (exp2),
+ * split over the selected set and merged by log-sum-exp; the weighted sum uses the
+ * softmax weights as f16 high + low parts against the exactly dequantised rows, with
+ * fp32 accumulation.  Outputs agree with the exact definition within 2e-3 x RMS(out).
  */
 #define CSA2_ATTN_MAX_TOPK 65536
 CSA2_API csa2_status csa2_sparse_attn(const uint16_t* q, const uint8_t* codes, const uint8_t* scales,
@@ -332,6 +337,18 @@ CSA2_API csa2_status csa2_import_pages(const uint8_t* packed, int32_t scale_row_
  * the device word to 0 and returns CSA2_ERR_TIMEOUT if CSA2_DEV_TIMEOUT was set,
  * CSA2_ERR_DEVICE_FAULT if any other bit was set, CSA2_OK otherwise. */
 CSA2_API csa2_status csa2_read_status(int32_t* dev_status, int32_t* host_bits, cudaStream_t stream);
+
+/* ------------------------------------------------------------------ diagnostic ----
+ * Exercises the failure-detection contract on the device without a fault.  One warp
+ * waits, with the bounded mbarrier wait every TMA- or tcgen05-fed kernel of this library
+ * uses, on a barrier phase that completes only if `arrive` is nonzero.  With arrive = 0
+ * the wait gives up after `limit` polls (1 <= limit <= 2^20; each poll may suspend for a
+ * hardware-chosen interval, so 2^20 polls stay well under a second), ORs CSA2_DEV_TIMEOUT
+ * into *dev_status and the kernel returns; nothing is left in flight and the context
+ * stays usable.  With arrive != 0 the wait completes and nothing is reported.
+ * Returns CSA2_ERR_INVALID_ARGUMENT for a null dev_status or a limit out of range. */
+CSA2_API csa2_status csa2_check_bounded_wait(int32_t arrive, uint32_t limit, int32_t* dev_status,
+                                             cudaStream_t stream);
 
 CSA2_API const char* csa2_status_string(csa2_status s);
 CSA2_API int32_t csa2_version(void);

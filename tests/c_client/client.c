@@ -73,6 +73,10 @@ int main(void) {
   CHECK(csa2_chunk_attn_workspace_size(6, 4, 16) == 0);
   /* status read with a null device word */
   CHECK(csa2_read_status(NULL, NULL, NULL) == CSA2_ERR_INVALID_ARGUMENT);
+  /* bounded-wait diagnostic: limit range and null status word */
+  CHECK(csa2_check_bounded_wait(0, 1024, NULL, NULL) == CSA2_ERR_INVALID_ARGUMENT);
+  CHECK(csa2_check_bounded_wait(0, (1u << 20) + 1, (int32_t*)fake, NULL) ==
+        CSA2_ERR_INVALID_ARGUMENT);
 
   if (failures) return 1;
   printf("ok\n");

@@ -41,6 +41,11 @@ def test_host_side_checks_without_device():
     assert L.csa2_kv_write(None, None, None, None, None, 4, 64, 1, 0, None, 4, None, None) == \
         csa2.CSA2_ERR_INVALID_ARGUMENT
     assert L.csa2_read_status(None, None, None) == csa2.CSA2_ERR_INVALID_ARGUMENT
+    # the bounded-wait diagnostic checks its limit and status word before launching
+    fake_st = 1 << 12
+    assert L.csa2_check_bounded_wait(0, 1024, None, None) == csa2.CSA2_ERR_INVALID_ARGUMENT
+    assert L.csa2_check_bounded_wait(0, 0, fake_st, None) == csa2.CSA2_ERR_INVALID_ARGUMENT
+    assert L.csa2_check_bounded_wait(0, (1 << 20) + 1, fake_st, None) == csa2.CSA2_ERR_INVALID_ARGUMENT
     # attention over more than CSA2_ATTN_MAX_TOPK entries per query is refused on the host
     # (fake aligned addresses: nothing is dereferenced before the check)
     fake = 1 << 12
