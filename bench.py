@@ -883,7 +883,9 @@ def count_launches(wl, step) -> int:
     """Kernels libcsa2 launches per decode step.  Full index call: the run-list kernel, the
     page scorer and one selection kernel (three, filter / resolve / emit, beyond 2^18
     tokens of context); Reindex: the gather scorer and one selection kernel; Reuse: none;
-    attention: one kernel, plus the split combine when the selected set is split."""
+    attention: over the E4M3 cache the query-term kernel and the attention kernel, over the
+    MXFP4 cache the attention kernel; either plus the split combine when the selected set
+    spans more than one 128-entry tile (it is then split)."""
     import fp4_compressed_sparse_03_b300 as csa2
     wide = step.cache.page_table.shape[1] * 64 > (1 << 18)
     n = 0
@@ -892,9 +894,8 @@ def count_launches(wl, step) -> int:
             n += 2 + (3 if wide else 1)
         elif m == csa2.CSA2_REINDEX:
             n += 2
-    ws = csa2.csa2_attn_workspace_size(step.num_q, step.topk)
-    n += len(wl.schedule) * (2 if ws > 0 else 1)
-    return n
+    per_attn = (1 if step.cache.mx else 2) + (1 if step.topk > 128 else 0)
+    return n + len(wl.schedule) * per_attn
 
 
 # Sources of the Full index call's kernels (the roofline line's kernels)

@@ -207,6 +207,7 @@ __device__ __forceinline__ bool mbar_drain(uint64_t* b, uint32_t parity) {
 __global__ void __launch_bounds__(512) q_terms_kernel(const uint16_t* __restrict__ q,
                                                       unsigned char* __restrict__ terms) {
   grid_dep_wait();
+  grid_dep_launch();  // the attention CTAs allocate TMEM and set up while the terms are made
   __shared__ uint32_t wmax[16];
   const int qi = blockIdx.x, tid = threadIdx.x, h = tid >> 5, g = tid & 31;
   unsigned char* img = terms + (size_t)qi * kTermsBytes;

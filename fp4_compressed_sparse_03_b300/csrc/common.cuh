@@ -30,6 +30,9 @@ constexpr uint32_t kSpinLimit = 1u << 26;
 // the stream is still finishing; the wait (a no-op after an ordinary launch) returns once
 // that kernel has completed and its writes are visible, so stream order is unchanged.
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel in the stream be scheduled before this one completes; that kernel
+// still waits (grid_dep_wait) for this one's completion before touching its results.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,

@@ -1180,7 +1180,58 @@ constexpr int kBigThreads = 1024;
 constexpr int kBigWarps = kBigThreads / 32;
 constexpr int kBigCap = 512;    // kept keys per warp
 constexpr int kBigBatch = 8;    // 16-byte loads in flight per lane in the histogram sweep
-constexpr int kFiltBatch = 4;   // 128-key groups in flight per warp in the filtering sweep
+constexpr int kFiltBatch = 8;   // 128-key groups in flight per warp in the wide filter's sweep
+constexpr int kCtaFiltBatch = 4;  // the same in the single-CTA selection's sweep
+
+// Ordered filter of one warp's position segment [seg_lo, seg_hi) (seg_lo a multiple of
+// 128): every valid key whose histogram bin is >= bmin is passed to keep(p, position, key)
+// with p its rank among the kept keys, so the kept keys come out in position order.  Lane
+// l reads keys 4 l .. 4 l + 3 of each 128-key group with one 16-byte load (kFiltBatch
+// groups in flight); ranks come from a warp scan of the per-lane counts.  Returns the
+// number kept.
+template <typename Keep>
+__device__ __forceinline__ uint32_t filter_segment(const uint32_t* __restrict__ src, int seg_lo,
+                                                   int seg_hi, uint32_t bmin, Keep keep) {
+  const int lane = threadIdx.x & 31;
+  uint32_t cnt = 0;
+  for (int i0 = seg_lo; i0 < seg_hi; i0 += 128 * kFiltBatch) {
+    uint4 k[kFiltBatch];
+#pragma unroll
+    for (int bb = 0; bb < kFiltBatch; ++bb) {
+      const int i = i0 + 128 * bb + 4 * lane;
+      if (i + 4 <= seg_hi) {
+        k[bb] = __ldcg(reinterpret_cast<const uint4*>(src + i));
+      } else {
+        k[bb].x = i < seg_hi ? __ldcg(src + i) : 0u;
+        k[bb].y = i + 1 < seg_hi ? __ldcg(src + i + 1) : 0u;
+        k[bb].z = i + 2 < seg_hi ? __ldcg(src + i + 2) : 0u;
+        k[bb].w = 0u;
+      }
+    }
+#pragma unroll
+    for (int bb = 0; bb < kFiltBatch; ++bb) {
+      const int i = i0 + 128 * bb + 4 * lane;
+      const uint32_t kk[4] = {k[bb].x, k[bb].y, k[bb].z, k[bb].w};
+      uint32_t m = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (kk[e] != 0 && (kk[e] >> 20) >= bmin) m |= 1u << e;
+      const uint32_t c = __popc(m);
+      uint32_t x = c;  // inclusive scan of the per-lane counts
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      uint32_t p = cnt + x - c;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (m & (1u << e)) keep(p++, (uint32_t)(i + e), kk[e]);
+      cnt += __shfl_sync(0xffffffffu, x, 31);
+    }
+  }
+  return cnt;
+}
 
 struct BigShared {
   uint32_t hist[kHistBins];
@@ -1348,22 +1399,23 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   if (want1 > 0) bmin = min(bmin, B1);
 
   // ---- 3. ordered sweep: keep keys with bin >= bmin ----
-  // A 128-key group is read slot-major (lane l holds keys l, 32 + l, 64 + l, 96 + l), so
-  // each slot compacts with one ballot: rank = popc(ballot & lanes below).
   const uint32_t lt = (1u << lane) - 1u;
   uint32_t cnt = 0;
   if (want0 > 0) {
-    for (int i0 = seg_lo; i0 < seg_hi; i0 += 128 * kFiltBatch) {
-      uint32_t k[kFiltBatch][4];
+    // slot-major groups (lane l holds keys l, 32 + l, 64 + l, 96 + l): each slot compacts
+    // with one ballot.  (The 16-byte-load form of filter_segment measured slower here, where
+    // the sweep is bound by instruction issue, not by the loads.)
+    for (int i0 = seg_lo; i0 < seg_hi; i0 += 128 * kCtaFiltBatch) {
+      uint32_t k[kCtaFiltBatch][4];
 #pragma unroll
-      for (int bb = 0; bb < kFiltBatch; ++bb)
+      for (int bb = 0; bb < kCtaFiltBatch; ++bb)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int i = i0 + 128 * bb + 32 * e + lane;
           k[bb][e] = i < seg_hi ? __ldcg(src + i) : 0u;
         }
 #pragma unroll
-      for (int bb = 0; bb < kFiltBatch; ++bb)
+      for (int bb = 0; bb < kCtaFiltBatch; ++bb)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const bool m = k[bb][e] != 0 && (k[bb][e] >> 20) >= bmin;
@@ -1656,33 +1708,12 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   const int64_t list = ((int64_t)q * wl.C + c) * kBigWarps + warp;
   uint32_t* lpos = wl.pos + list * wl.seg;
   uint32_t* lkey = wl.key + list * wl.seg;
-  const uint32_t lt = (1u << lane) - 1u;
   uint32_t cnt = 0;
-  if (want0 > 0) {
-    for (int i0 = seg_lo; i0 < seg_hi; i0 += 128 * kFiltBatch) {
-      uint32_t k[kFiltBatch][4];
-#pragma unroll
-      for (int bb = 0; bb < kFiltBatch; ++bb)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = i0 + 128 * bb + 32 * e + lane;
-          k[bb][e] = i < seg_hi ? __ldcg(src + i) : 0u;
-        }
-#pragma unroll
-      for (int bb = 0; bb < kFiltBatch; ++bb)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const bool m = k[bb][e] != 0 && (k[bb][e] >> 20) >= bmin;
-          const uint32_t bal = __ballot_sync(0xffffffffu, m);
-          const uint32_t p = cnt + __popc(bal & lt);
-          if (m) {  // p < seg: at most seg keys in the warp's segment
-            lpos[p] = (uint32_t)(i0 + 128 * bb + 32 * e + lane);
-            lkey[p] = k[bb][e];
-          }
-          cnt += __popc(bal);
-        }
-    }
-  }
+  if (want0 > 0)  // at most seg keys in the warp's segment, so p < seg
+    cnt = filter_segment(src, seg_lo, seg_hi, bmin, [&](uint32_t p, uint32_t pos, uint32_t key) {
+      lpos[p] = pos;
+      lkey[p] = key;
+    });
   if (lane == 0) wl.cnt[list] = cnt;
 }
 
@@ -1710,9 +1741,15 @@ __device__ __forceinline__ uint32_t block_excl(BigShared& sh, uint32_t v, uint32
 }
 
 // Resolve (one CTA per query): the candidate lists of the query, concatenated in
-// position order (list-major), are staged in shared memory when they fit and split into
-// contiguous per-thread chunks for three radix passes over the boundary-bin keys; the
-// exact boundary keys, the per-list output bases and tie quotas go to the query's meta.
+// position order (list-major), are staged in shared memory when they fit (a warp per
+// list; the kernel takes all the shared memory a CTA may have, about 53k keys), else
+// walked from L2 in contiguous per-thread chunks, for three radix passes over the
+// boundary-bin keys; the exact boundary keys, the per-list output bases and tie quotas
+// (two block-wide scans over the lists) go to the query's meta.
+constexpr int kResolveSmem = 232448;  // 227 KB, the per-CTA maximum on sm_103a
+constexpr size_t kResolveKeyOff = offsetof(BigShared, u) + (3 * kMaxWideLists + 32) * sizeof(uint32_t);
+static_assert(kResolveKeyOff % 4 == 0 && kResolveKeyOff < (size_t)kResolveSmem, "resolve key staging");
+static_assert(kMaxWideLists <= kBigThreads, "one thread per list in the base scans");
 __global__ void __launch_bounds__(kBigThreads, 1)
     select_resolve_kernel(int32_t pool_size, int32_t topk, const uint32_t* __restrict__ ghist,
                           WideLists wl) {
@@ -1741,32 +1778,59 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   if (tid < nlists) loff[tid] = off;
   if (tid == 0) loff[nlists] = total;
   __syncthreads();
-  auto list_of = [&](uint32_t e) {  // the last l with loff[l] <= e
-    int lo = 0, hi = nlists - 1;
-    while (lo < hi) {
-      const int m = (lo + hi + 1) >> 1;
-      if (loff[m] <= e) lo = m; else hi = m - 1;
-    }
-    return lo;
-  };
-  const uint32_t skey_cap = (uint32_t)((sizeof(sh.u) - (3 * kMaxWideLists + 32) * sizeof(uint32_t)) /
-                                       sizeof(uint32_t));
+  const uint32_t skey_cap = (uint32_t)((kResolveSmem - kResolveKeyOff) / sizeof(uint32_t));
   const bool in_smem = total <= skey_cap;
-  if (in_smem) {
-    for (uint32_t e = tid; e < total; e += kBigThreads) {
-      const int l = list_of(e);
-      skey[e] = __ldcg(wl.key + (list0 + l) * wl.seg + (e - loff[l]));
+  if (in_smem) {  // warp w copies lists w, w + 32, ...: coalesced, no per-key list search
+    for (int l = warp; l < nlists; l += kBigWarps) {
+      const uint32_t o = loff[l], c = loff[l + 1] - o;
+      const uint32_t* src = wl.key + (list0 + l) * wl.seg;
+      for (uint32_t j0 = 0; j0 < c; j0 += 4 * 32) {
+        uint32_t v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t j = j0 + 32 * u + lane;
+          v[u] = j < c ? __ldcg(src + j) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t j = j0 + 32 * u + lane;
+          if (j < c) skey[o + j] = v[u];
+        }
+      }
     }
     __syncthreads();
   }
+  // every candidate key once (order is irrelevant to the radix histograms): strided over
+  // the staged keys, else each thread walks a contiguous chunk of the lists in L2
   const uint32_t per = (total + kBigThreads - 1) / kBigThreads;
   const uint32_t e_lo = min(total, per * tid), e_hi = min(total, e_lo + per);
-  const int l_first = list_of(e_lo);
+  int l_first = 0;
+  if (!in_smem) {  // the last list with loff[l] <= e_lo
+    int hi = nlists - 1;
+    while (l_first < hi) {
+      const int m = (l_first + hi + 1) >> 1;
+      if (loff[m] <= e_lo) l_first = m; else hi = m - 1;
+    }
+  }
   auto walk = [&](auto f) {
+    if (in_smem) {
+      for (uint32_t e = tid; e < total; e += kBigThreads) f(skey[e]);
+      return;
+    }
     int l = l_first;
-    for (uint32_t e = e_lo; e < e_hi; ++e) {
-      while (loff[l + 1] <= e) ++l;
-      f(in_smem ? skey[e] : __ldcg(wl.key + (list0 + l) * wl.seg + (e - loff[l])));
+    for (uint32_t e0 = e_lo; e0 < e_hi; e0 += 8) {  // 8 keys fetched before any is used
+      uint32_t v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t e = e0 + u;
+        if (e < e_hi) {
+          while (loff[l + 1] <= e) ++l;
+          v[u] = __ldcg(wl.key + (list0 + l) * wl.seg + (e - loff[l]));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (e0 + u < e_hi) f(v[u]);
     }
   };
 
@@ -1820,15 +1884,16 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       }
     }
     __syncthreads();
-    if (tid == 0) {
-      uint32_t base = 0, ties_before = 0;
-      for (int l = 0; l < nlists; ++l) {
-        const uint32_t take = quota > ties_before ? min(quota - ties_before, leq[l]) : 0u;
-        meta[4 + t * kMaxWideLists + l] = base;
-        meta[4 + (2 + t) * kMaxWideLists + l] = take;
-        base += lgt[l] + take;
-        ties_before += leq[l];
-      }
+    // list l takes min(leq[l], the quota left after the ties of lists before it), and its
+    // base is the count of keys taken by the lists before it: two block-wide scans
+    uint32_t tot;
+    const uint32_t eq_l = tid < nlists ? leq[tid] : 0u;
+    const uint32_t ties_before = block_excl(sh, eq_l, tot);
+    const uint32_t take = quota > ties_before ? min(quota - ties_before, eq_l) : 0u;
+    const uint32_t base = block_excl(sh, tid < nlists ? lgt[tid] + take : 0u, tot);
+    if (tid < nlists) {
+      meta[4 + t * kMaxWideLists + tid] = base;
+      meta[4 + (2 + t) * kMaxWideLists + tid] = take;
     }
     __syncthreads();
   }
@@ -2005,7 +2070,7 @@ cudaError_t launch_select(bool reindex, const uint32_t* ws, int64_t ws_stride, c
     wl.key = wl.pos + lists;
     wl.cnt = wl.key + lists;
     wl.meta = wl.cnt + (size_t)num_q * C * kBigWarps;
-    const size_t fsmem = offsetof(BigShared, u), bsmem = sizeof(BigShared);
+    const size_t fsmem = offsetof(BigShared, u), bsmem = kResolveSmem;
     cudaError_t e = cudaFuncSetAttribute(select_resolve_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bsmem);
     if (e != cudaSuccess) return e;
