@@ -1603,8 +1603,8 @@ __global__ void __launch_bounds__(kBigThreads, 1)
 //   select_emit_kernel (the filter's grid, one warp per list): each list writes its
 //     selected positions at its base.
 constexpr int kWideThreshold = 1 << 18;  // Full contexts longer than this use the wide path
-constexpr int kWideMinKeys = 1 << 16;  // positions per filter CTA at least
-constexpr int kWideMaxCtas = 16;       // filter CTAs per query at most
+constexpr int kWideMinKeys = 1 << 15;  // positions per filter CTA at least
+constexpr int kWideMaxCtas = 32;       // filter CTAs per query at most (the sweep is issue-bound)
 constexpr int kMaxWideLists = kWideMaxCtas * kBigWarps;
 
 // Per-CTA position range of the wide filter: a multiple of 4096 (so each warp segment is
@@ -1741,13 +1741,13 @@ __device__ __forceinline__ uint32_t block_excl(BigShared& sh, uint32_t v, uint32
 }
 
 // Resolve (one CTA per query): the candidate lists of the query, concatenated in
-// position order (list-major), are staged in shared memory when they fit (a warp per
-// list; the kernel takes all the shared memory a CTA may have, about 53k keys), else
+// position order (list-major), are staged in shared memory when they fit (a warp per run
+// of lists; the kernel takes all the shared memory a CTA may have, about 53k keys), else
 // walked from L2 in contiguous per-thread chunks, for three radix passes over the
 // boundary-bin keys; the exact boundary keys, the per-list output bases and tie quotas
 // (two block-wide scans over the lists) go to the query's meta.
 constexpr int kResolveSmem = 232448;  // 227 KB, the per-CTA maximum on sm_103a
-constexpr size_t kResolveKeyOff = offsetof(BigShared, u) + (3 * kMaxWideLists + 32) * sizeof(uint32_t);
+constexpr size_t kResolveKeyOff = offsetof(BigShared, u) + (kMaxWideLists + 32) * sizeof(uint32_t);
 static_assert(kResolveKeyOff % 4 == 0 && kResolveKeyOff < (size_t)kResolveSmem, "resolve key staging");
 static_assert(kMaxWideLists <= kBigThreads, "one thread per list in the base scans");
 __global__ void __launch_bounds__(kBigThreads, 1)
@@ -1757,9 +1757,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   extern __shared__ __align__(128) unsigned char smem_raw[];
   BigShared& sh = *reinterpret_cast<BigShared*>(smem_raw);
   uint32_t* loff = sh.u.c.pos[0];                 // [nlists + 1] list offsets
-  uint32_t* lgt = loff + kMaxWideLists + 32;      // [nlists] keys > T_t per list
-  uint32_t* leq = lgt + kMaxWideLists;            // [nlists] keys == T_t per list
-  uint32_t* skey = leq + kMaxWideLists;           // staged keys
+  uint32_t* skey = loff + kMaxWideLists + 32;     // staged keys
   const int q = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nlists = wl.C * kBigWarps;
@@ -1780,22 +1778,27 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   __syncthreads();
   const uint32_t skey_cap = (uint32_t)((kResolveSmem - kResolveKeyOff) / sizeof(uint32_t));
   const bool in_smem = total <= skey_cap;
-  if (in_smem) {  // warp w copies lists w, w + 32, ...: coalesced, no per-key list search
-    for (int l = warp; l < nlists; l += kBigWarps) {
-      const uint32_t o = loff[l], c = loff[l + 1] - o;
-      const uint32_t* src = wl.key + (list0 + l) * wl.seg;
-      for (uint32_t j0 = 0; j0 < c; j0 += 4 * 32) {
-        uint32_t v[4];
+  if (in_smem) {
+    // warp w copies the keys of a contiguous run of lists (contiguous in skey too), lane-
+    // strided with 8 loads in flight per lane; each lane follows its list boundary forward
+    const int lpw = (nlists + kBigWarps - 1) / kBigWarps;
+    const int la = min(nlists, warp * lpw), lb = min(nlists, la + lpw);
+    const uint32_t ea = loff[la], eb = loff[lb];
+    int l = la;
+    for (uint32_t e0 = ea; e0 < eb; e0 += 8 * 32) {
+      uint32_t v[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t j = j0 + 32 * u + lane;
-          v[u] = j < c ? __ldcg(src + j) : 0u;
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t e = e0 + 32 * u + lane;
+        if (e < eb) {
+          while (loff[l + 1] <= e) ++l;
+          v[u] = __ldcg(wl.key + (list0 + l) * wl.seg + (e - loff[l]));
         }
+      }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t j = j0 + 32 * u + lane;
-          if (j < c) skey[o + j] = v[u];
-        }
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t e = e0 + 32 * u + lane;
+        if (e < eb) skey[e] = v[u];
       }
     }
     __syncthreads();
@@ -1864,38 +1867,36 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     meta[tid] = pre[tid];
     meta[2 + tid] = want[tid];
   }
-  // per-list counts, then bases and tie quotas in list (= position) order
+  // per-list counts of the keys above and equal to each boundary key (one thread per
+  // list, both targets in one pass), then bases and tie quotas in list (= position) order
+  uint32_t cgt[2] = {0u, 0u}, ceq[2] = {0u, 0u};
+  if (tid < nlists) {
+    const uint32_t a = loff[tid], b = loff[tid + 1];
+    const uint32_t* lk = wl.key + (list0 + tid) * wl.seg;
+#pragma unroll 4
+    for (uint32_t e = a; e < b; ++e) {
+      const uint32_t k = in_smem ? skey[e] : __ldcg(lk + (e - a));
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        cgt[t] += k > pre[t];
+        ceq[t] += k == pre[t];
+      }
+    }
+  }
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     if (want[t] == 0) continue;
-    const uint32_t T = pre[t], quota = want[t] - abv[t];
-    for (int l = warp; l < nlists; l += kBigWarps) {
-      uint32_t gt = 0, eq = 0;
-      for (uint32_t e = loff[l] + lane; e < loff[l + 1]; e += 32) {
-        const uint32_t k = in_smem ? skey[e] : __ldcg(wl.key + (list0 + l) * wl.seg + (e - loff[l]));
-        gt += k > T;
-        eq += k == T;
-      }
-      gt = __reduce_add_sync(0xffffffffu, gt);
-      eq = __reduce_add_sync(0xffffffffu, eq);
-      if (lane == 0) {
-        lgt[l] = gt;
-        leq[l] = eq;
-      }
-    }
-    __syncthreads();
-    // list l takes min(leq[l], the quota left after the ties of lists before it), and its
-    // base is the count of keys taken by the lists before it: two block-wide scans
+    // list l takes min(its ties, the quota left after the ties of the lists before it),
+    // and its base is the count of keys the lists before it take: two block-wide scans
+    const uint32_t quota = want[t] - abv[t];
     uint32_t tot;
-    const uint32_t eq_l = tid < nlists ? leq[tid] : 0u;
-    const uint32_t ties_before = block_excl(sh, eq_l, tot);
-    const uint32_t take = quota > ties_before ? min(quota - ties_before, eq_l) : 0u;
-    const uint32_t base = block_excl(sh, tid < nlists ? lgt[tid] + take : 0u, tot);
+    const uint32_t ties_before = block_excl(sh, ceq[t], tot);
+    const uint32_t take = quota > ties_before ? min(quota - ties_before, ceq[t]) : 0u;
+    const uint32_t base = block_excl(sh, cgt[t] + take, tot);
     if (tid < nlists) {
       meta[4 + t * kMaxWideLists + tid] = base;
       meta[4 + (2 + t) * kMaxWideLists + tid] = take;
     }
-    __syncthreads();
   }
 }
 
