@@ -117,6 +117,15 @@ def dist_setup():
     return world, rank, local
 
 
+def flush_l2(buf, k):
+    """Evict L2 before a timed call: write a 256 MB buffer (larger than the 126 MB L2), then
+    read it back, so that L2 holds only clean lines of the buffer and the timed call pays
+    no write-back of the flush's own dirty lines."""
+    import torch
+    buf.fill_(k & 0xFF)
+    buf.view(torch.int64).sum()
+
+
 def reduce_max(x: float, world: int, device) -> float:
     if world == 1:
         return x
@@ -160,7 +169,7 @@ def decode_config(wl, mx: bool, world: int) -> dict:
 def write_config(ww, world: int) -> dict:
     """The `config` of a write-path line (prefill write or decode-time append)."""
     append = ww.T <= 128
-    l2 = ("flushed before every call (256 MB written): the %.0f MB of weights fit in L2"
+    l2 = ("flushed before every call (256 MB written, then read back): the %.0f MB of weights fit in L2"
           % (ww.n_out * ww.d_model * 2 / 1e6)) if append else \
         "no flush: H is %.0f MB (> 126 MB L2)" % (ww.T * ww.d_model * 2 / 1e6)
     return {"workload": ww.name, "tokens": ww.T, "d_model": ww.d_model,
@@ -270,7 +279,7 @@ def run_ours(args, world, rank, local):
             g_call[(l, "attn")].replay()
             ev[(k, l, "a1")].record(stream)
     torch.cuda.synchronize(dev)
-    # per-layer attention with L2 flushed before each layer (a 256 MB buffer written): the
+    # per-layer attention with L2 flushed before each layer (a 256 MB buffer written and read): the
     # Reuse layers' attention otherwise re-reads rows the previous layer just gathered
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     K3 = max(1, min(K, 20))
@@ -278,7 +287,7 @@ def run_ours(args, world, rank, local):
            for k in range(K3) for l in range(L) for w in (0, 1)}
     for k in range(K3):
         for l in range(L):
-            flush.fill_((k * L + l) & 0xFF)
+            flush_l2(flush, k * L + l)
             evc[(k, l, 0)].record(stream)
             g_call[(l, "attn")].replay()
             evc[(k, l, 1)].record(stream)
@@ -393,7 +402,7 @@ def run_ours(args, world, rank, local):
                         "attention": round(attn_ms, 4), "attention_per_layer": attn_layer_ms,
                         "attention_cold_per_layer": attn_cold_ms,
                         "attention_cold_note": "each layer's attention replayed alone after a "
-                                               "256 MB L2 flush"},
+                                               "256 MB L2 flush (written, then read back)"},
         "roofline": {"bound": "hbm", "kernel": "csa2_index(FULL) call: group_prefix_kernel + score_pages_kernel + select_cta_kernel",
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
@@ -418,7 +427,7 @@ def run_write(args, world, rank, local):
     flops per call.
     decode_append: the new token of each of 64 sequences through the same projections;
     roofline HBM, the 105 MB of projection weights streamed per call.  The weights fit
-    in L2, so L2 is flushed (a 256 MB buffer written) before every timed call, and each
+    in L2, so L2 is flushed (a 256 MB buffer written, then read) before every timed call, and each
     call is timed by its own events."""
     import torch
     import csa2_inputs as gen
@@ -458,7 +467,7 @@ def run_write(args, world, rank, local):
     t0.record(stream)
     for k in range(K):
         if flush is not None:
-            flush.fill_(k & 0xFF)
+            flush_l2(flush, k)
         evs[k][0].record(stream)
         call()
         evs[k][1].record(stream)
@@ -502,7 +511,7 @@ def run_write(args, world, rank, local):
     e0.record(stream)
     for _ in range(K2):
         if flush is not None:
-            flush.fill_(7)
+            flush_l2(flush, 7)
         H_dev.copy_(H_pin, non_blocking=True)
         call(H_dev)
         if append:
@@ -544,7 +553,7 @@ def run_write(args, world, rank, local):
         "config": write_config(ww, world),
         "roofline": roof,
         "e2e": {"value": round(units / (ms_e2e / 1e3), 1), "unit": "tokens/s",
-                "l2_flush": ("each timed step includes the 256 MB L2 flush write (about 40 us)"
+                "l2_flush": ("each timed step includes the 256 MB L2 flush (written and read back, about 80 us)"
                              if append else "none"),
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": K2},
         "gpu_launches": K,
@@ -708,7 +717,7 @@ def run_chunk(args, world, rank, local):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(n)]
         for k in range(n):
-            flush.fill_(k & 0xFF)
+            flush_l2(flush, k)
             evs[k][0].record(stream)
             fn()
             evs[k][1].record(stream)
@@ -755,7 +764,7 @@ def run_chunk(args, world, rank, local):
     w0 = time.perf_counter()
     e0.record(stream)
     for _ in range(K2):
-        flush.fill_(3)
+        flush_l2(flush, 3)
         q_dev.copy_(q_pin, non_blocking=True)
         i_dev.copy_(i_pin, non_blocking=True)
         chunked(q_dev, i_dev)
@@ -777,7 +786,7 @@ def run_chunk(args, world, rank, local):
         "config": {"workload": "draft_chunk_64x4x16384", "num_seqs": len(wl.seq_lens),
                    "queries_per_chunk": G, "context_tokens": int(wl.seq_lens.max()), "topk": K,
                    "shared_fraction": args.shared, "union_rows": int(union),
-                   "l2": "flushed before every call (256 MB written): the selected rows fit in L2",
+                   "l2": "flushed before every call (256 MB written, then read back): the selected rows fit in L2",
                    "per_query_path_ms": round(ms_pq, 4), "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm",
                      "kernel": "csa2_sparse_attn_chunked call: chunk_union_kernel + "
@@ -786,7 +795,7 @@ def run_chunk(args, world, rank, local):
                      "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src + " HBM copy",
                      "algorithmic_bytes_per_launch": int(abytes), "traffic": None},
         "e2e": {"value": round(nq * world / (ms_e2e / 1e3), 1), "unit": "queries/s",
-                "l2_flush": "each timed step includes the 256 MB L2 flush write (about 40 us)",
+                "l2_flush": "each timed step includes the 256 MB L2 flush (written and read back, about 80 us)",
                 "h2d_bytes_per_step": int(q_d.numel() * 2 + idx_d.numel() * 4),
                 "d2h_bytes_per_step": int(out.numel() * 4 + lse.numel() * 4), "steps": K2},
         "gpu_launches": 3 * Kst,

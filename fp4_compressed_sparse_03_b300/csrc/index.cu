@@ -1233,30 +1233,43 @@ __device__ __forceinline__ uint32_t filter_segment(const uint32_t* __restrict__ 
   return cnt;
 }
 
-struct BigShared {
+// Shared layout of the single-CTA selection with NT threads and a kept list of CAP keys
+// per warp (positions stored as 16-bit offsets into the warp's segment, which is at most
+// 2^18 / (NT / 32) <= 16384 positions).  BigShared (1024 threads) also serves the wide
+// path's filter and resolve kernels.
+template <int NT, int CAP>
+struct BigSharedT {
+  static constexpr int NW = NT / 32;
   uint32_t hist[kHistBins];
-  uint32_t wsel[2][kBigWarps];  // per-warp keys > T_t
-  uint32_t wtie[2][kBigWarps];  // per-warp keys == T_t
-  uint32_t wcnt[kBigWarps];     // per-warp kept keys
+  uint32_t wsel[2][NW];  // per-warp keys > T_t
+  uint32_t wtie[2][NW];  // per-warp keys == T_t
+  uint32_t wcnt[NW];     // per-warp kept keys
   uint32_t rh[2][256];
-  uint32_t scan[2][kBigThreads / 32];
-  uint32_t res[2][2];           // per target: (bin, keys above it)
+  uint32_t scan[2][32];
+  uint32_t res[2][2];    // per target: (bin, keys above it)
   uint32_t nvalid;
   uint32_t overflow;
   union {
     struct {
-      uint32_t pos[kBigWarps][kBigCap];
-      uint32_t key[kBigWarps][kBigCap];
+      uint32_t key[NW][CAP];
+      uint16_t pos[NW][CAP];
     } c;
-    uint32_t whist[kBigWarps][256];
+    uint32_t raw[1];
   } u;
 };
+using BigShared = BigSharedT<kBigThreads, kBigCap>;
+constexpr int kSmallThreads = 512;  // the selection's 2-CTAs-per-SM form (many queries)
+constexpr int kSmallCap = 1024;
+using SmallShared = BigSharedT<kSmallThreads, kSmallCap>;
+static_assert(sizeof(SmallShared) <= 113 * 1024 && sizeof(BigShared) <= 113 * 1024,
+              "two selection CTAs per SM");
 
 // Block-wide: thread tid holds v = count of bin (tid % nb) for target tid / nb (two
 // targets, nb bins each, 2 nb <= 1024 threads).  For each target with want_t > 0, find
 // the bin where (abv_t + keys in strictly higher bins) < want_t <= ... + v, and return
 // it in res[t][0] (res[t][1] = keys above it, abv_t included).
-__device__ __forceinline__ void big_find(BigShared& sh, uint32_t v, int nb, uint32_t want0,
+template <class SH>
+__device__ __forceinline__ void big_find(SH& sh, uint32_t v, int nb, uint32_t want0,
                                          uint32_t want1, uint32_t abv0, uint32_t abv1) {
   const int tid = threadIdx.x, lane = tid & 31;
   const int t = tid / nb, bin = tid % nb, tw = bin >> 5;
@@ -1285,8 +1298,8 @@ __device__ __forceinline__ void big_find(BigShared& sh, uint32_t v, int nb, uint
 
 // kReindex: the query's keys are its P pool entries (n = pool_size), the output is the
 // pool entry's token, and no pool is emitted.
-template <bool kReindex>
-__global__ void __launch_bounds__(kBigThreads, 1)
+template <bool kReindex, int NT, int CAP>
+__global__ void __launch_bounds__(NT, 1024 / NT)
     select_cta_kernel(const uint32_t* __restrict__ ws, int64_t ws_stride,
                       const int32_t* __restrict__ q_seq, const int32_t* __restrict__ seq_lens,
                       int32_t num_seqs, const int32_t* __restrict__ pool_in, int32_t pool_size,
@@ -1294,7 +1307,9 @@ __global__ void __launch_bounds__(kBigThreads, 1)
                       int32_t max_ctx, const uint32_t* __restrict__ ghist) {
   grid_dep_wait();
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  BigShared& sh = *reinterpret_cast<BigShared*>(smem_raw);
+  using SH = BigSharedT<NT, CAP>;
+  constexpr int NW = SH::NW;
+  SH& sh = *reinterpret_cast<SH*>(smem_raw);
   const int q = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int n;
@@ -1311,7 +1326,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   int32_t* out1 = two ? pool_out + (int64_t)q * pool_size : nullptr;
 
   // position segment of this warp: multiples of 128, in position order across warps
-  int S = (n + kBigWarps - 1) / kBigWarps;
+  int S = (n + NW - 1) / NW;
   S = (S + 127) & ~127;
   const int seg_lo = min(n, warp * S), seg_hi = min(n, seg_lo + S);
   auto load4 = [&](int i, uint32_t (&k)[4]) {
@@ -1331,13 +1346,13 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   }
   uint32_t nv = 0;
   if (ghist != nullptr) {
-    for (int i = tid; i < kHistBins; i += kBigThreads) {
+    for (int i = tid; i < kHistBins; i += NT) {
       const uint32_t v = __ldcg(ghist + (int64_t)q * kHistBins + i);
       sh.hist[i] = v;
       nv += v;
     }
   } else {
-    for (int i = tid; i < kHistBins; i += kBigThreads) sh.hist[i] = 0;
+    for (int i = tid; i < kHistBins; i += NT) sh.hist[i] = 0;
   }
   __syncthreads();
   for (int i0 = seg_lo; ghist == nullptr && i0 < seg_hi; i0 += 128 * kBigBatch) {
@@ -1360,11 +1375,17 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   const uint32_t want0 = min((uint32_t)topk, nvalid);
   const uint32_t want1 = two ? min((uint32_t)pool_size, nvalid) : 0u;
 
-  // ---- 2. boundary bins (two bins per thread: 2 tid + 1 is the higher one) ----
+  // ---- 2. boundary bins (thread tid holds bins BPT tid .. BPT tid + BPT - 1) ----
+  constexpr int BPT = kHistBins / NT;
   uint32_t B0 = 0, B1 = 0, A0 = 0, A1 = 0;  // boundary bins and keys in higher bins
   {
-    const uint32_t hi = sh.hist[2 * tid + 1], lo = sh.hist[2 * tid];
-    uint32_t x = hi + lo;  // inclusive suffix sum of pair counts within the warp
+    uint32_t c[BPT], tot = 0;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) {
+      c[j] = sh.hist[BPT * tid + j];
+      tot += c[j];
+    }
+    uint32_t x = tot;  // inclusive suffix sum of the threads' counts within the warp
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t y = __shfl_down_sync(0xffffffffu, x, o);
@@ -1374,19 +1395,19 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     if (tid < 4) sh.res[tid >> 1][tid & 1] = 0;
     __syncthreads();
     uint32_t later = 0;
-    for (int w = warp + 1; w < kBigWarps; ++w) later += sh.scan[0][w];
-    const uint32_t above_hi = later + x - (hi + lo), above_lo = above_hi + hi;
+    for (int w = warp + 1; w < NW; ++w) later += sh.scan[0][w];
+    uint32_t above = later + x - tot;  // keys in bins above this thread's
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      const uint32_t want_t = t == 0 ? want0 : want1;
-      if (want_t == 0) continue;
-      if (above_hi < want_t && above_hi + hi >= want_t) {
-        sh.res[t][0] = 2 * tid + 1;
-        sh.res[t][1] = above_hi;
-      } else if (above_lo < want_t && above_lo + lo >= want_t) {
-        sh.res[t][0] = 2 * tid;
-        sh.res[t][1] = above_lo;
+    for (int j = BPT - 1; j >= 0; --j) {
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const uint32_t want_t = t == 0 ? want0 : want1;
+        if (want_t > 0 && above < want_t && above + c[j] >= want_t) {
+          sh.res[t][0] = BPT * tid + j;
+          sh.res[t][1] = above;
+        }
       }
+      above += c[j];
     }
     __syncthreads();
     B0 = sh.res[0][0];
@@ -1421,8 +1442,8 @@ __global__ void __launch_bounds__(kBigThreads, 1)
           const bool m = k[bb][e] != 0 && (k[bb][e] >> 20) >= bmin;
           const uint32_t bal = __ballot_sync(0xffffffffu, m);
           const uint32_t p = cnt + __popc(bal & lt);
-          if (m && p < (uint32_t)kBigCap) {
-            sh.u.c.pos[warp][p] = (uint32_t)(i0 + 128 * bb + 32 * e + lane);
+          if (m && p < (uint32_t)CAP) {
+            sh.u.c.pos[warp][p] = (uint16_t)(i0 + 128 * bb + 32 * e + lane - seg_lo);
             sh.u.c.key[warp][p] = k[bb][e];
           }
           cnt += __popc(bal);
@@ -1430,7 +1451,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     }
     if (lane == 0) {
       sh.wcnt[warp] = cnt;
-      if (cnt > (uint32_t)kBigCap) atomicOr(&sh.overflow, 1u);
+      if (cnt > (uint32_t)CAP) atomicOr(&sh.overflow, 1u);
     }
   }
   __syncthreads();
@@ -1440,10 +1461,12 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   uint32_t T0 = 0, T1 = 0, Q0 = 0, Q1 = 0;  // boundary key and ties to take
   if (want0 > 0) {
     uint32_t pre[2] = {B0, B1}, abv[2] = {A0, A1};
-    const uint32_t want[2] = {want0, want1};
+    // a target that takes every valid key needs no search (T = 1, the smallest valid key,
+    // with every tie taken)
+    const uint32_t want[2] = {want0 < nvalid ? want0 : 0u, want1 < nvalid ? want1 : 0u};
     // kept: digits of bits 19..12, 11..4, 3..0 within the boundary bin;
     // full range: digits of bits 30..23, 22..15, 14..7, 6..0
-    const int passes = kept ? 3 : 4;
+    const int passes = (want[0] == 0 && want[1] == 0) ? 0 : kept ? 3 : 4;
     for (int pass = 0; pass < passes; ++pass) {
       const int shift = kept ? (pass == 0 ? 12 : pass == 1 ? 4 : 0) : (pass == 0 ? 23 : pass == 1 ? 15 : pass == 2 ? 7 : 0);
       const int width = kept ? (pass == 2 ? 4 : 8) : (pass == 3 ? 7 : 8);
@@ -1452,7 +1475,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
         pre[0] = pre[1] = 0;
         abv[0] = abv[1] = 0;
       }
-      for (int i = tid; i < 2 * 256; i += kBigThreads) sh.rh[i >> 8][i & 255] = 0;
+      for (int i = tid; i < 2 * 256; i += NT) sh.rh[i >> 8][i & 255] = 0;
       __syncthreads();
       if (kept) {
         for (uint32_t j = lane; j < cnt; j += 32) {
@@ -1487,36 +1510,89 @@ __global__ void __launch_bounds__(kBigThreads, 1)
         }
       __syncthreads();
     }
-    T0 = pre[0];
-    Q0 = want0 - abv[0];
-    T1 = pre[1];
-    Q1 = want1 - abv[1];
+    T0 = want[0] > 0 ? pre[0] : 1u;
+    Q0 = want[0] > 0 ? want0 - abv[0] : want0;
+    T1 = want[1] > 0 ? pre[1] : 1u;
+    Q1 = want[1] > 0 ? want1 - abv[1] : want1;
   }
 
   // ---- 5. ordered emit ----
+  if (kept) {
+    // both targets in one traversal of the kept lists: per-warp counts of keys > T_t and
+    // == T_t, the warp's output base and tie quota, then ballot ranks per 32-key chunk
+    const uint32_t Tt[2] = {T0, T1}, Qt[2] = {Q0, Q1}, wt[2] = {want0, want1};
+    int32_t* const ot[2] = {out0, out1};
+    uint32_t gt[2] = {0u, 0u}, eq[2] = {0u, 0u};
+    for (uint32_t j = lane; j < cnt; j += 32) {
+      const uint32_t k = sh.u.c.key[warp][j];
 #pragma unroll
-  for (int t = 0; t < 2; ++t) {
+      for (int t = 0; t < 2; ++t) {
+        gt[t] += k > Tt[t];
+        eq[t] += k == Tt[t];
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      gt[t] = __reduce_add_sync(0xffffffffu, gt[t]);
+      eq[t] = __reduce_add_sync(0xffffffffu, eq[t]);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        sh.wsel[t][warp] = gt[t];
+        sh.wtie[t][warp] = eq[t];
+      }
+    }
+    __syncthreads();
+    uint32_t base[2], take[2], tie_run[2] = {0u, 0u}, sel_run[2] = {0u, 0u};
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      uint32_t b = 0, ties_before = 0;
+      for (int w = 0; w < warp; ++w) {
+        const uint32_t e_w = sh.wtie[t][w];
+        b += sh.wsel[t][w] + (Qt[t] > ties_before ? min(Qt[t] - ties_before, e_w) : 0u);
+        ties_before += e_w;
+      }
+      base[t] = b;
+      take[t] = Qt[t] > ties_before ? min(Qt[t] - ties_before, sh.wtie[t][warp]) : 0u;
+    }
+    for (uint32_t j0 = 0; j0 < cnt; j0 += 32) {
+      const uint32_t j = j0 + lane;
+      const uint32_t k = j < cnt ? sh.u.c.key[warp][j] : 0u;
+      const uint32_t pos = j < cnt ? (uint32_t)seg_lo + sh.u.c.pos[warp][j] : 0u;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (wt[t] == 0) continue;
+        const bool tie = j < cnt && k == Tt[t];
+        const uint32_t tb = __ballot_sync(0xffffffffu, tie);
+        const bool sel = j < cnt && (k > Tt[t] || (tie && tie_run[t] + __popc(tb & lt) < take[t]));
+        const uint32_t sb = __ballot_sync(0xffffffffu, sel);
+        const uint32_t p = base[t] + sel_run[t] + __popc(sb & lt);
+        if (sel && p < wt[t]) ot[t][p] = kReindex ? __ldg(pin + pos) : (int32_t)pos;
+        tie_run[t] += __popc(tb);
+        sel_run[t] += __popc(sb);
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  // the full-range path (a warp's kept list overflowed): each target in turn, keys read
+  // from the workspace again
+#pragma unroll
+  for (int t = 0; t < 2 && !kept; ++t) {
     const uint32_t want_t = t == 0 ? want0 : want1;
     if (want_t == 0) continue;
     const uint32_t T = t == 0 ? T0 : T1, quota = t == 0 ? Q0 : Q1;
     int32_t* outp = t == 0 ? out0 : out1;
     // per-warp counts of keys > T and == T
     uint32_t gt = 0, eq = 0;
-    if (kept) {
-      for (uint32_t j = lane; j < cnt; j += 32) {
-        const uint32_t k = sh.u.c.key[warp][j];
-        gt += k > T;
-        eq += k == T;
-      }
-    } else {
-      for (int i = seg_lo + 4 * lane; i < seg_hi; i += 128) {
-        uint32_t k[4];
-        load4(i, k);
+    for (int i = seg_lo + 4 * lane; i < seg_hi; i += 128) {
+      uint32_t k[4];
+      load4(i, k);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          gt += k[e] > T;
-          eq += k[e] == T;
-        }
+      for (int e = 0; e < 4; ++e) {
+        gt += k[e] > T;
+        eq += k[e] == T;
       }
     }
     gt = __reduce_add_sync(0xffffffffu, gt);
@@ -1534,13 +1610,18 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     }
     const uint32_t take = quota > ties_before ? min(quota - ties_before, sh.wtie[t][warp]) : 0u;
     uint32_t tie_run = 0, sel_run = 0;
-    auto emit = [&](const uint32_t* k, const uint32_t* pos, int nk) {
+    for (int i0 = seg_lo; i0 < seg_hi; i0 += 128) {
+      const int i = i0 + 4 * lane;
+      uint32_t k[4];
+      load4(i, k);
       uint32_t nt = 0;
-      for (int e = 0; e < nk; ++e) nt += k[e] == T;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) nt += k[e] == T;
       uint32_t ttot;
       uint32_t tr = tie_run + warp_excl(nt, ttot);
       uint32_t selm = 0, ns = 0;
-      for (int e = 0; e < nk; ++e) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
         const bool tie = k[e] == T;
         if (k[e] > T || (tie && tr < take)) {
           selm |= 1u << e;
@@ -1550,45 +1631,21 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       }
       uint32_t stot;
       uint32_t p = base + sel_run + warp_excl(ns, stot);
-      for (int e = 0; e < nk; ++e)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
         if (selm & (1u << e)) {
-          if (p < want_t) outp[p] = kReindex ? __ldg(pin + pos[e]) : (int32_t)pos[e];
+          if (p < want_t) outp[p] = kReindex ? __ldg(pin + i + e) : (int32_t)(i + e);
           ++p;
         }
       tie_run += ttot;
       sel_run += stot;
-    };
-    if (kept) {
-      for (uint32_t j0 = 0; j0 < cnt; j0 += 32) {  // one kept key per lane: ballot ranks
-        const uint32_t j = j0 + lane;
-        const uint32_t k = j < cnt ? sh.u.c.key[warp][j] : 0u;
-        const bool tie = j < cnt && k == T;
-        const uint32_t tb = __ballot_sync(0xffffffffu, tie);
-        const bool sel = j < cnt && (k > T || (tie && tie_run + __popc(tb & lt) < take));
-        const uint32_t sb = __ballot_sync(0xffffffffu, sel);
-        const uint32_t p = base + sel_run + __popc(sb & lt);
-        if (sel && p < want_t) {
-          const uint32_t pos = sh.u.c.pos[warp][j];
-          outp[p] = kReindex ? __ldg(pin + pos) : (int32_t)pos;
-        }
-        tie_run += __popc(tb);
-        sel_run += __popc(sb);
-      }
-    } else {
-      for (int i0 = seg_lo; i0 < seg_hi; i0 += 128) {
-        const int i = i0 + 4 * lane;
-        uint32_t k[4];
-        load4(i, k);
-        const uint32_t pos[4] = {(uint32_t)i, (uint32_t)i + 1, (uint32_t)i + 2, (uint32_t)i + 3};
-        emit(k, pos, 4);
-      }
     }
     __syncthreads();
   }
   // -1 padding after the selected entries
-  for (int i = (int)want0 + tid; i < topk; i += kBigThreads) out0[i] = -1;
+  for (int i = (int)want0 + tid; i < topk; i += NT) out0[i] = -1;
   if (two)
-    for (int i = (int)want1 + tid; i < pool_size; i += kBigThreads) out1[i] = -1;
+    for (int i = (int)want1 + tid; i < pool_size; i += NT) out1[i] = -1;
 }
 
 // ------------------------------------------------------------ wide selection (Full) --
@@ -1756,7 +1813,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   grid_dep_wait();
   extern __shared__ __align__(128) unsigned char smem_raw[];
   BigShared& sh = *reinterpret_cast<BigShared*>(smem_raw);
-  uint32_t* loff = sh.u.c.pos[0];                 // [nlists + 1] list offsets
+  uint32_t* loff = sh.u.raw;                      // [nlists + 1] list offsets
   uint32_t* skey = loff + kMaxWideLists + 32;     // staged keys
   const int q = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -2087,15 +2144,21 @@ cudaError_t launch_select(bool reindex, const uint32_t* ws, int64_t ws_stride, c
   // Up to 2^18 keys per query: one CTA per query, no cluster synchronisation (measured on
   // B300: 64 Full queries x 131072 keys took ~90 us in two waves of 8-CTA clusters, 46 us
   // this way; 64 Reindex queries x 8192 pool entries 27 us with single-CTA clusters)
-  (void)num_sms;
   if (n <= (1 << 18) && want_max <= 8192) {
-    const size_t smem = sizeof(BigShared);
-    auto kern = reindex ? select_cta_kernel<true> : select_cta_kernel<false>;
+    // one CTA per query: 1024 threads while the queries fit one per SM; beyond that the
+    // 512-thread form runs two CTAs per SM (each warp keeps up to 1024 keys of a segment
+    // twice as long)
+    const bool small = num_q > num_sms;
+    const size_t smem = small ? sizeof(SmallShared) : sizeof(BigShared);
+    auto kern = small ? (reindex ? select_cta_kernel<true, kSmallThreads, kSmallCap>
+                                 : select_cta_kernel<false, kSmallThreads, kSmallCap>)
+                      : (reindex ? select_cta_kernel<true, kBigThreads, kBigCap>
+                                 : select_cta_kernel<false, kBigThreads, kBigCap>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(num_q), dim3(kBigThreads), smem, s, ws, ws_stride, q_seq,
-                      pg.seq_lens, pg.num_seqs, pool_in,
+    return launch_pdl(kern, dim3(num_q), dim3(small ? kSmallThreads : kBigThreads), smem, s, ws,
+                      ws_stride, q_seq, pg.seq_lens, pg.num_seqs, pool_in,
                       reindex ? pool_size : (pool_out ? pool_size : 0), topk, out_idx,
                       reindex ? nullptr : pool_out, pg.max_pages_per_seq * kPage,
                       reindex ? nullptr : ghist);
