@@ -47,7 +47,9 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks / throttle reasons sampled every 20 ms while running; each sample
+    is stamped on arrival, and the summary keeps the samples between mark() and stop()
+    (the timed loops), or all of them when mark() was not called."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -58,12 +60,13 @@ class ClockSampler:
         self.proc = None
         self.lines = []
         self._t = None
+        self._mark = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
@@ -72,12 +75,17 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def mark(self):
+        """Start of the timed loops: samples before this are not summarised."""
+        self._mark = time.monotonic()
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
                     "samples": 0}
+        t_end = time.monotonic()
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -87,7 +95,10 @@ class ClockSampler:
             self._t.join(timeout=2)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        t_lo = self._mark if self._mark is not None else -1e30
+        for ts, ln in self.lines:
+            if ts < t_lo or ts > t_end:
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -259,6 +270,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     clocks.start()
     time.sleep(0.3)
+    clocks.mark()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -462,6 +474,7 @@ def run_write(args, world, rank, local):
     torch.cuda.synchronize(dev)
     clocks.start()
     time.sleep(0.3)
+    clocks.mark()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -605,6 +618,7 @@ def run_pages(args, world, rank, local):
     barrier(world)
     clocks.start()
     time.sleep(0.3)
+    clocks.mark()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -739,6 +753,7 @@ def run_chunk(args, world, rank, local):
     barrier(world)
     clocks.start()
     time.sleep(0.3)
+    clocks.mark()
     ms_call = timed(chunked, Kst)
     ms_pq = timed(per_query, Kst)
     barrier(world)
