@@ -10,7 +10,8 @@
 //   - persistent CTAs, one per SM, 128 x 256 output tiles (bf16 operands, fp32
 //     accumulation), K consumed in 64-wide blocks through a 4-stage TMA ring
 //     (128-byte swizzle, both operands K-major); for T <= 128 (one M-tile: the weight
-//     stream is the whole cost) 128 x 128 tiles through a 6-stage ring;
+//     stream is the whole cost) 128 x 128 tiles through 3 stages of two K-blocks, and
+//     for T <= 64 through 4 such stages holding only H's 64 real rows;
 //   - warp 0 lane 0 issues TMA, warp 1 lane 0 issues tcgen05.mma (M=128, N=256 or 128,
 //     K=16) into one of two TMEM accumulators, warps 2..5 run the epilogue of the
 //     previous tile while the next one accumulates;
@@ -30,20 +31,27 @@ namespace csa2 {
 namespace {
 
 constexpr int BM = 128, BK = 64;
-constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int kThreads = 192;                   // 6 warps
 constexpr int kGroupM = 16;
 
-// Output tile width BN, TMA ring depth and K-blocks of 64 per stage (KSUB).  Prefill-sized
-// T: 256 columns, 4 stages of 48 KB.  A single M-tile (T <= 128, e.g. decode-time append
-// of one token per sequence) is bound by streaming the weights: 128 columns double the
-// CTAs that stream them, and 3 stages of two adjacent K-blocks read 256 contiguous bytes
-// of each weight row at a time (6 stages of one K-block when d_model % 128 != 0).
-template <int BN, int STAGES, int KSUB>
+// Output tile width BN, TMA ring depth, K-blocks of 64 per stage (KSUB) and A rows loaded
+// per K-block (AROWS).  Prefill-sized T: 256 columns, 4 stages of 48 KB.  A single M-tile
+// (T <= 128, e.g. decode-time append of one token per sequence) is bound by streaming the
+// weights: 128 columns double the CTAs that stream them, and stages of two adjacent
+// K-blocks read 256 contiguous bytes of each weight row at a time.  With T <= 64 only 64
+// rows of H are loaded per K-block (8 KB instead of 16): the MMA still has M = 128, and its
+// A rows 64..127 read whatever follows in the stage (the next A block, or the first B
+// block); those accumulator rows are never stored.  The smem saved holds a fourth stage,
+// so a third more of the weights is in flight.  A stage is all its A blocks, then all its
+// B blocks.
+template <int BN, int STAGES, int KSUB, int AROWS = BM>
 struct KvCfg {
+  static constexpr int A_SUB = AROWS * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int SUB_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGE_BYTES = KSUB * SUB_BYTES;
+  static constexpr int A_PART = KSUB * A_SUB;  // offset of the B blocks in a stage
+  static constexpr int STAGE_BYTES = KSUB * (A_SUB + B_BYTES);
+  static_assert(AROWS == BM || A_PART + B_BYTES >= KSUB * A_SUB + (BM - AROWS) * BK * 2,
+                "the MMA's overread of the last A block stays inside the stage");
   static constexpr int kTmemCols = 2 * BN;  // two accumulators
   struct Bars {
     uint64_t full[STAGES];
@@ -57,7 +65,8 @@ struct KvCfg {
   static constexpr size_t smem_bytes() { return (size_t)STAGES * STAGE_BYTES + sizeof(Bars) + 1024; }
 };
 static_assert(KvCfg<256, 4, 1>::smem_bytes() <= 232448 && KvCfg<128, 6, 1>::smem_bytes() <= 232448 &&
-                  KvCfg<128, 3, 2>::smem_bytes() <= 232448,
+                  KvCfg<128, 3, 2>::smem_bytes() <= 232448 && KvCfg<128, 4, 2, 64>::smem_bytes() <= 232448 &&
+                  KvCfg<128, 8, 1, 64>::smem_bytes() <= 232448,
               "write-path ring exceeds 227 KB of shared memory");
 
 __device__ __forceinline__ void fence_before() {
@@ -140,12 +149,12 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int&
 
 }  // namespace
 
-template <int BN, int STAGES, int KSUB>
+template <int BN, int STAGES, int KSUB, int AROWS>
 __global__ void __launch_bounds__(kThreads, 1)
     kv_write_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     WriteParams p) {
-  using Cfg = KvCfg<BN, STAGES, KSUB>;
-  constexpr int SUB_BYTES = Cfg::SUB_BYTES;
+  using Cfg = KvCfg<BN, STAGES, KSUB, AROWS>;
+  constexpr int A_SUB = Cfg::A_SUB, A_PART = Cfg::A_PART, B_BYTES = Cfg::B_BYTES;
   using Bars = typename Cfg::Bars;
   constexpr int STAGE_BYTES = Cfg::STAGE_BYTES;
   constexpr int kTmemCols = Cfg::kTmemCols;
@@ -203,8 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(&bars->full[stage], STAGE_BYTES);
 #pragma unroll
         for (int j = 0; j < KSUB; ++j) {
-          tma_load_2d(sa + j * SUB_BYTES, &tmA, &bars->full[stage], (kb + j) * BK, m * BM);
-          tma_load_2d(sa + j * SUB_BYTES + A_BYTES, &tmB, &bars->full[stage], (kb + j) * BK, n * BN);
+          tma_load_2d(sa + j * A_SUB, &tmA, &bars->full[stage], (kb + j) * BK, m * BM);
+          tma_load_2d(sa + A_PART + j * B_BYTES, &tmB, &bars->full[stage], (kb + j) * BK, n * BN);
         }
         issued_mask |= 1u << stage;
         last_par = (last_par & ~(1u << stage)) | (phase << stage);
@@ -236,8 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_after();
 #pragma unroll
         for (int j = 0; j < KSUB; ++j) {
-          const unsigned char* sa = base + stage * STAGE_BYTES + j * SUB_BYTES;
-          const uint64_t adesc = sw128_desc(sa), bdesc = sw128_desc(sa + A_BYTES);
+          const unsigned char* st_base = base + stage * STAGE_BYTES;
+          const uint64_t adesc = sw128_desc(st_base + j * A_SUB);
+          const uint64_t bdesc = sw128_desc(st_base + A_PART + j * B_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             umma_bf16(d, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc,
@@ -344,20 +354,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 namespace {
 
-template <int BN, int STAGES, int KSUB>
+template <int BN, int STAGES, int KSUB, int AROWS = BM>
 cudaError_t launch_kv_write_cfg(const uint16_t* H, const uint16_t* Wt, const WriteParams& p,
                                 cudaStream_t s, int num_sms) {
   CUtensorMap ta, tb;
-  if (!make_bf16_map(&ta, H, p.T, p.d_model, BK, BM) ||
+  if (!make_bf16_map(&ta, H, p.T, p.d_model, BK, AROWS) ||
       !make_bf16_map(&tb, Wt, p.n_out, p.d_model, BK, BN))
     return cudaErrorInvalidValue;
-  const size_t smem = KvCfg<BN, STAGES, KSUB>::smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(kv_write_kernel<BN, STAGES, KSUB>,
+  const size_t smem = KvCfg<BN, STAGES, KSUB, AROWS>::smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(kv_write_kernel<BN, STAGES, KSUB, AROWS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int tiles = ((p.T + BM - 1) / BM) * ((p.n_out + BN - 1) / BN);
   const int grid = std::max(1, std::min(tiles, num_sms));
-  kv_write_kernel<BN, STAGES, KSUB><<<grid, kThreads, smem, s>>>(ta, tb, p);
+  kv_write_kernel<BN, STAGES, KSUB, AROWS><<<grid, kThreads, smem, s>>>(ta, tb, p);
   return cudaGetLastError();
 }
 
@@ -370,6 +380,8 @@ cudaError_t launch_kv_write(const uint16_t* H, const uint16_t* Wt, uint8_t* code
   const int32_t n_out = n_kv_proj * kDkv + n_idx_proj * kDidx;
   WriteParams p{codes, scales, k_idx, slot_of_token, num_slots, T, d_model, n_kv_proj, n_idx_proj,
                 n_out, st};
+  if (T <= BM / 2 && d_model % (2 * BK) == 0) return launch_kv_write_cfg<128, 4, 2, BM / 2>(H, Wt, p, s, num_sms);
+  if (T <= BM / 2) return launch_kv_write_cfg<128, 8, 1, BM / 2>(H, Wt, p, s, num_sms);
   if (T <= BM && d_model % (2 * BK) == 0) return launch_kv_write_cfg<128, 3, 2>(H, Wt, p, s, num_sms);
   if (T <= BM) return launch_kv_write_cfg<128, 6, 1>(H, Wt, p, s, num_sms);
   return launch_kv_write_cfg<256, 4, 1>(H, Wt, p, s, num_sms);
