@@ -88,7 +88,8 @@ def _oracle_rows(Hh, Wth, nkv, nidx):
 
 @pytest.mark.parametrize("T,d,nkv,nidx", [(256, 256, 2, 2), (384, 512, 1, 1), (128, 192, 0, 3),
                                           (256, 1024, 3, 0), (64, 256, 2, 2), (200, 512, 1, 1),
-                                          (1, 128, 1, 1), (33, 192, 1, 1), (65, 192, 1, 1)])
+                                          (1, 128, 1, 1), (33, 192, 1, 1), (65, 192, 1, 1),
+                                          (100, 256, 1, 1)])
 def test_small_projections(T, d, nkv, nidx):
     ww = gen.WriteWorkload("small", 50 + T + d, T, d, nkv, nidx)
     H, Wt, slots = fill_write_inputs(ww)
