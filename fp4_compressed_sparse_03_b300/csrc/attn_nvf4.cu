@@ -472,8 +472,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   for (int t = 0; t < ntiles; ++t) {
     cp_wait<0>();     // this thread's copies of tile t have landed
     __syncthreads();  // everyone's; and the weighted sum of tile t - 1 is done with its stage
-    if (t + 1 < ntiles) gather(t + 1);
-    cp_commit();
     // ---- logits: scale factors of tile t into TMEM, then the MMAs ----
     if (warp < 4) {
       const unsigned char* sc = sm.stage[t & 1] + kStageCodes;
@@ -502,6 +500,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       mma_commit(&sm.s_full);
       mma_issued = true;
     }
+    // the next tile's gather is issued while the MMAs run (the other stage is free: the
+    // weighted sum of tile t - 1 finished before the barrier at the top)
+    if (t + 1 < ntiles) gather(t + 1);
+    cp_commit();
     ok &= mbar_wait(&sm.abort, &sm.s_full, (uint32_t)(t & 1), st);
     tc_after();
     // ---- softmax of token tok, heads hb .. hb + 7 ----
