@@ -557,9 +557,9 @@ def test_long_context_4x1m():
 
 def test_ragged_serving_sampled():
     """256 sequences (lognormal lengths 1K..256K), 1-4 draft queries each (batched
-    tensor-core scoring), 20 layers in 5 Full groups; 12 sampled queries."""
+    tensor-core scoring), 20 layers in 5 Full groups; 16 sampled queries."""
     wl = gen.config_ragged()
     _, step, q_idx, q = run_workload(wl)
     rng = np.random.default_rng(4)
-    picks = np.sort(rng.choice(wl.num_q, 12, replace=False))
+    picks = np.sort(rng.choice(wl.num_q, 16, replace=False))
     check_sampled(wl, picks, step, q_idx, q, attn_budget=6, min_attn=30)
