@@ -164,7 +164,7 @@ def shard_sequences(num_seqs: int, world: int, rank: int, scaling: str = "weak")
 
 # ------------------------------------------------------------------ algorithmic bytes --
 
-def decode_config(wl, mx: bool, world: int) -> dict:
+def decode_config(wl, mx: bool, world: int, schedule: str = "parallel") -> dict:
     """The `config` of a decode-workload line; the reference arm prints the same one."""
     return {"workload": wl.name + ("_mxfp4" if mx else ""), "num_seqs": int(len(wl.seq_lens)),
             "context_tokens": int(wl.seq_lens.max()), "query_tokens": wl.num_q,
@@ -172,8 +172,11 @@ def decode_config(wl, mx: bool, world: int) -> dict:
             "pool": wl.pool_size, "topk": wl.topk,
             "l2": "no flush: every step streams %.2f GB of indexer keys (> 126 MB L2)"
                   % (full_index_bytes(wl) / 1e9),
-            "launch": "CUDA graph of the step's libcsa2 calls; per-mode times from "
-                      "per-call graphs",
+            "launch": ("CUDA graph of the step's libcsa2 calls, index calls in layer order "
+                       "and attention calls on 4 side branches after their source layer's "
+                       "index call" if schedule == "parallel" else
+                       "CUDA graph of the step's libcsa2 calls in layer order")
+                      + "; per-mode times from per-call graphs",
             "parallelism": f"replicas x{world}"}
 
 
@@ -255,8 +258,10 @@ def run_ours(args, world, rank, local):
         raise RuntimeError(f"device status {bits:#x} after warm-up")
 
     # The step is replayed as a CUDA graph of the same libcsa2 launches, so the device
-    # time is not paced by per-call host work (about 12 calls per step).
-    g_step = step.capture(q_idx, q)
+    # time is not paced by per-call host work (about 12 calls per step).  In the parallel
+    # schedule a layer's attention call overlaps the next layers' index calls.
+    par = args.step_schedule == "parallel"
+    g_step = step.capture(q_idx, q, parallel=par)
     g_call = step.capture_calls(q_idx, q)
     for _ in range(args.warmup):
         g_step.replay()
@@ -348,7 +353,7 @@ def run_ours(args, world, rank, local):
     q_idx_b, q_b = q_idx.clone(), q.clone()
     step_b.run(q_idx_b, q_b)
     torch.cuda.synchronize(dev)
-    sets = [(step, q_idx, q, g_step), (step_b, q_idx_b, q_b, step_b.capture(q_idx_b, q_b))]
+    sets = [(step, q_idx, q, g_step), (step_b, q_idx_b, q_b, step_b.capture(q_idx_b, q_b, parallel=par))]
     out_pin = [torch.empty(step.out.shape, dtype=torch.float32).pin_memory() for _ in sets]
     lse_pin = [torch.empty(step.lse.shape, dtype=torch.float32).pin_memory() for _ in sets]
     h2d = sum(q_idx_pin[l].numel() * 2 for l in idx_layers) + q_pin.numel() * 2
@@ -409,7 +414,7 @@ def run_ours(args, world, rank, local):
         "dtype": ("fp4-e2m1/e8m0-per-32 (MXFP4) kv" if mx else "fp4-e2m1/e4m3 kv") +
                  ", bf16 keys+queries, f32 accumulate",
         "data": "synthetic (seeded counter-based generator)",
-        "config": decode_config(wl, mx, world),
+        "config": decode_config(wl, mx, world, args.step_schedule),
         "per_mode_ms": {"full_index": round(full_ms, 4), "reindex": round(re_ms, 4),
                         "attention": round(attn_ms, 4), "attention_per_layer": attn_layer_ms,
                         "attention_cold_per_layer": attn_cold_ms,
@@ -1090,7 +1095,8 @@ def run_reference(args, world, rank):
             "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64 (CPU oracle)",
             "data": "synthetic (seeded counter-based generator)",
-            "config": decode_config(wl, args.workload.endswith("_mx"), world),
+            "config": decode_config(wl, args.workload.endswith("_mx"), world,
+                                    args.step_schedule),
             "cpu_baseline": cb,
             "e2e": {"value": round(v, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -1136,6 +1142,9 @@ def main():
                              "ced_write", "decode_append", "decode_batch_mx", "decode_short_mx",
                              "page_export", "draft_chunk"])
     ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--step-schedule", choices=["parallel", "serial"], default="parallel",
+                    help="decode step graph: attention calls on side branches, or every "
+                         "call in layer order on one stream")
     ap.add_argument("--cpu-sample", type=int, default=None,
                     help="queries (decode) or token rows (write workloads) timed on the oracle; "
                          "default 32 queries / 256 rows (all 64 for decode_append), about "

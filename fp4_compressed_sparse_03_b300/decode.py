@@ -86,6 +86,12 @@ class DecodeStep:
                  csa2_index_workspace_size(CSA2_REINDEX, self.num_q, cache.max_pages, self.pool_size),
                  csa2_attn_workspace_size(self.num_q, self.topk), 256)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+        # the parallel schedule (run_parallel) gives each attention branch its own workspace
+        self.attn_branches = min(L, self.ATTN_BRANCHES)
+        ws_a = max(csa2_attn_workspace_size(self.num_q, self.topk), 256)
+        self.attn_workspace = [torch.empty(ws_a, dtype=torch.uint8, device=dev)
+                               for _ in range(self.attn_branches)]
+        self._branches = [torch.cuda.Stream(dev) for _ in range(self.attn_branches)]
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.use_pool = self.pool_size > 0 and any(m == CSA2_REINDEX for m in self.schedule)
 
@@ -100,12 +106,13 @@ class DecodeStep:
         check(csa2_index(m, q_idx_l, c.keys[g], pool, self.topk, self.idx[l], c.pages, args,
                          stream), f"csa2_index(layer {l})")
 
-    def layer_attn(self, l: int, q_l, stream=None) -> None:
+    def layer_attn(self, l: int, q_l, stream=None, workspace=None) -> None:
         g, s = self.group[l], self.src[l]
         c = self.cache
         attn = csa2_sparse_attn_mx if c.mx else csa2_sparse_attn
+        ws = self.workspace if workspace is None else workspace
         check(attn(q_l, c.codes[g], c.scales[g], self.idx[s], c.pages, self.out[l], self.lse[l],
-                   self.num_q, self.q_seq, self.topk, self.softmax_scale, self.workspace, None,
+                   self.num_q, self.q_seq, self.topk, self.softmax_scale, ws, None,
                    self.dev_status, stream),
               f"csa2_sparse_attn(layer {l})")
 
@@ -117,6 +124,37 @@ class DecodeStep:
 
     def indices(self, l: int):
         return self.idx[self.src[l]]
+
+    # ---- parallel schedule: independent calls on separate streams ----
+    # A layer's attention needs only its source layer's indices, and no index call reads
+    # an attention's output, so the index calls run in order on the caller's stream while
+    # the attention calls run on ATTN_BRANCHES side streams (layer l on branch l % B, each
+    # branch with its own workspace), each waiting for the event recorded after its source
+    # layer's index call.  The caller's stream waits for every branch at the end.  The
+    # results are those of run(): the same calls on the same buffers.
+    ATTN_BRANCHES = 4
+
+    def run_parallel(self, q_idx, q) -> None:
+        main = torch.cuda.current_stream(self.cache.device)
+        start = torch.cuda.Event()
+        start.record(main)
+        for b in self._branches:
+            b.wait_event(start)
+        done = {}
+        for l, m in enumerate(self.schedule):
+            if m != CSA2_REUSE:
+                self.layer_index(l, q_idx[l], main)
+                ev = torch.cuda.Event()
+                ev.record(main)
+                done[l] = ev
+            br = self._branches[l % self.attn_branches]
+            br.wait_event(done[self.src[l]])
+            with torch.cuda.stream(br):
+                self.layer_attn(l, q[l], br, self.attn_workspace[l % self.attn_branches])
+        for b in self._branches:
+            ev = torch.cuda.Event()
+            ev.record(b)
+            main.wait_event(ev)
 
     # ---- CUDA graphs: the same libcsa2 launches, replayed without per-call host work ----
     # Every libcsa2 call is an ordered launch sequence on the given stream, so a captured
@@ -130,8 +168,11 @@ class DecodeStep:
             fn()
         return g
 
-    def capture(self, q_idx, q):
-        """Graph of one whole step reading the device buffers q_idx and q."""
+    def capture(self, q_idx, q, parallel: bool = False):
+        """Graph of one whole step reading the device buffers q_idx and q; with `parallel`,
+        of the parallel schedule (run_parallel)."""
+        if parallel:
+            return self._capture(lambda: self.run_parallel(q_idx, q))
         return self._capture(lambda: self.run(q_idx, q))
 
     def capture_calls(self, q_idx, q):

@@ -188,13 +188,20 @@ def test_small_ragged_all_modes(drafts):
     check_sampled(wl, range(wl.num_q), step, q_idx, q, min_attn=wl.num_q)
 
 
-def test_graph_replay_matches_eager_step():
+@pytest.mark.parametrize("parallel,schedule", [
+    (False, [gen.FULL, gen.REINDEX, gen.REUSE, gen.REUSE]),
+    (True, [gen.FULL, gen.REINDEX, gen.REUSE, gen.REUSE]),
+    (True, [gen.FULL, gen.REINDEX, gen.REUSE, gen.REUSE, gen.FULL, gen.REINDEX, gen.REUSE])])
+def test_graph_replay_matches_eager_step(parallel, schedule):
     """The CUDA-graph step (what the benchmark times) replays the same launches: its
     indices, pools, outputs and lse are bit-identical to the eager step's, and a replay
-    after new queries are copied into the captured buffers matches an eager run on them."""
+    after new queries are copied into the captured buffers matches an eager run on them.
+    With `parallel` the graph is of the parallel schedule (index calls in order, attention
+    calls on side branches after their source layer's index call), two Full groups wrap
+    the branches around."""
     lens = np.array([5000, 64, 300, 2113], np.int32)
     wl = gen.DecodeWorkload("graph", 31, lens, np.array([2, 1, 1, 3], np.int32),
-                            [gen.FULL, gen.REINDEX, gen.REUSE, gen.REUSE], pool_size=512, topk=128)
+                            schedule, pool_size=512, topk=128)
     cache, step, q_idx_h, q_h = run_workload(wl)
     q_idx, q = dev(q_idx_h), dev(q_h)
     written = sorted(set(step.src))  # layers whose index output the step writes
@@ -212,7 +219,7 @@ def test_graph_replay_matches_eager_step():
     step.run(q_idx, q)
     torch.cuda.synchronize()
     ref = outputs()
-    g = step.capture(q_idx, q)
+    g = step.capture(q_idx, q, parallel=parallel)
     clobber()
     g.replay()
     torch.cuda.synchronize()
