@@ -260,6 +260,18 @@ def test_two_groups_pool_larger_than_context():
     check_sampled(wl, range(2), step, q_idx, q)
 
 
+@pytest.mark.parametrize("pool,topk", [(999, 300), (2049, 2048), (12000, 700)])
+def test_reindex_pool_sizes(pool, topk):
+    """Reindex over pools of sizes that are not multiples of 4 or of the selection's
+    per-thread key count, one of them larger than 8192 entries; the 700-token sequence
+    has fewer valid pool entries than some of the top-K sizes."""
+    lens = np.array([20000, 700, 5000], np.int32)
+    wl = gen.DecodeWorkload("pools", 41, lens, np.array([1, 2, 1], np.int32),
+                            [gen.FULL, gen.REINDEX, gen.REUSE], pool_size=pool, topk=topk)
+    _, step, q_idx, q = run_workload(wl)
+    check_sampled(wl, range(wl.num_q), step, q_idx, q)
+
+
 def test_attention_random_index_sets():
     """Attention alone on seeded random selections (with -1 padding and an empty set),
     single- and multi-split launches (up to 36 splits of 128 entries, most of them empty
