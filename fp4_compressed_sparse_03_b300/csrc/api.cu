@@ -21,9 +21,10 @@ cudaError_t launch_score_reindex(const uint16_t*, const uint16_t*, const int32_t
                                  const csa2_pages&, const int32_t*, int32_t, uint32_t*, int32_t*,
                                  cudaStream_t, int);
 size_t runlist_bytes(int32_t num_q);
+int32_t* runlist_order(void* base, int32_t num_q);
 cudaError_t launch_select(bool, const uint32_t*, int64_t, const int32_t*, const csa2_pages&,
                           int32_t, const int32_t*, int32_t, int32_t, int32_t*, int32_t*,
-                          const uint32_t*, void*, int32_t*, cudaStream_t, int);
+                          const uint32_t*, void*, const int32_t*, int32_t*, cudaStream_t, int);
 size_t wide_select_bytes(int32_t num_q, int32_t n);
 cudaError_t launch_attn(const uint16_t*, const uint8_t*, const uint8_t*, const int32_t*,
                         const csa2_pages&, float*, float*, int32_t, const int32_t*, int32_t, float,
@@ -211,7 +212,8 @@ csa2_status csa2_index(csa2_mode mode, const uint16_t* q_idx, const uint16_t* k_
                           stride, rl, hist, args->dev_status, stream, sms);
     if (e != cudaSuccess) return from_cuda(e);
     e = launch_select(false, ws, stride, args->q_seq, *pages, args->num_q, nullptr,
-                      pool ? P : 0, topk, out_idx, pool, hist, wide, args->dev_status, stream, sms);
+                      pool ? P : 0, topk, out_idx, pool, hist, wide, runlist_order(rl, args->num_q),
+                      args->dev_status, stream, sms);
     return from_cuda(e);
   }
   // REINDEX
@@ -220,7 +222,7 @@ csa2_status csa2_index(csa2_mode mode, const uint16_t* q_idx, const uint16_t* k_
                            args->dev_status, stream, sms);
   if (e != cudaSuccess) return from_cuda(e);
   e = launch_select(true, ws, P, args->q_seq, *pages, args->num_q, pool, P, topk, out_idx, nullptr,
-                    nullptr, nullptr, args->dev_status, stream, sms);
+                    nullptr, nullptr, nullptr, args->dev_status, stream, sms);
   return from_cuda(e);
 }
 

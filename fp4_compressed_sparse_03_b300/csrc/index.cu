@@ -104,6 +104,10 @@ struct RunList {
   const int32_t* run_q0;
 };
 
+// CTA order of the Full selection: bucket 0 holds the longest contexts (2^18 rows)
+constexpr int kOrderBuckets = 65;
+__device__ __forceinline__ int order_bucket(int rows) { return 64 - min(rows >> 12, 64); }
+
 __device__ __forceinline__ int run_rows(bool reindex, const int32_t* __restrict__ q_seq, int q,
                                         const ScoreGeom& g, int32_t pool_size) {
   if (reindex) return pool_size;
@@ -113,17 +117,40 @@ __device__ __forceinline__ int run_rows(bool reindex, const int32_t* __restrict_
 }
 
 // CTA 0 builds the run list; CTAs 1.. clear `zero_buf` (zero_vecs 16-byte vectors: the
-// Full scorer's selection histograms), which saves a separate memset in the stream.
+// Full scorer's selection histograms), which saves a separate memset in the stream.  With
+// `order`, the last CTA writes the Full selection's CTA order: the queries by descending
+// context length (buckets of 4096 rows), so that the longest selections start first and
+// the short ones fill in behind them.
 __global__ void __launch_bounds__(1024) group_prefix_kernel(bool batched, bool reindex,
                                                             const int32_t* __restrict__ q_seq,
                                                             int32_t num_q, ScoreGeom g,
                                                             int32_t pool_size, int32_t unit_rows,
                                                             int64_t* meta, int64_t* prefix,
                                                             int32_t* run_q0, uint4* zero_buf,
-                                                            int64_t zero_vecs) {
+                                                            int64_t zero_vecs, int32_t* order) {
   grid_dep_wait();
+  if (order != nullptr && blockIdx.x == gridDim.x - 1) {
+    __shared__ uint32_t cb[kOrderBuckets];
+    for (int i = threadIdx.x; i < kOrderBuckets; i += blockDim.x) cb[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < num_q; i += blockDim.x)
+      atomicAdd(&cb[order_bucket(run_rows(false, q_seq, i, g, 0))], 1u);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t run = 0;
+      for (int b = 0; b < kOrderBuckets; ++b) {
+        const uint32_t c = cb[b];
+        cb[b] = run;
+        run += c;
+      }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < num_q; i += blockDim.x)
+      order[atomicAdd(&cb[order_bucket(run_rows(false, q_seq, i, g, 0))], 1u)] = i;
+    return;
+  }
   if (blockIdx.x > 0) {
-    const int64_t stride = (int64_t)(gridDim.x - 1) * blockDim.x;
+    const int64_t stride = (int64_t)(gridDim.x - 1 - (order != nullptr)) * blockDim.x;
     for (int64_t i = (int64_t)(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < zero_vecs; i += stride)
       zero_buf[i] = make_uint4(0, 0, 0, 0);
     return;
@@ -1306,13 +1333,14 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
                       const int32_t* __restrict__ q_seq, const int32_t* __restrict__ seq_lens,
                       int32_t num_seqs, const int32_t* __restrict__ pool_in, int32_t pool_size,
                       int32_t topk, int32_t* __restrict__ out_idx, int32_t* __restrict__ pool_out,
-                      int32_t max_ctx, const uint32_t* __restrict__ ghist) {
+                      int32_t max_ctx, const uint32_t* __restrict__ ghist,
+                      const int32_t* __restrict__ order) {
   grid_dep_wait();
   extern __shared__ __align__(128) unsigned char smem_raw[];
   using SH = BigSharedT<NT, CAP>;
   constexpr int NW = SH::NW;
   SH& sh = *reinterpret_cast<SH*>(smem_raw);
-  const int q = blockIdx.x;
+  const int q = order != nullptr ? __ldg(order + blockIdx.x) : (int)blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int n;
   if (kReindex) {
@@ -2212,9 +2240,15 @@ __global__ void __launch_bounds__(kPoolThreads, KPT <= 16 ? 2 : 1)
 
 size_t select_smem_bytes() { return kSelCacheOff + (size_t)kSelCacheKeys * 4; }
 
-// Bytes of the run list that follows the scores in the workspace.
+// Bytes of the run list that follows the scores in the workspace (meta, prefix, run
+// starts, then the Full selection's CTA order).
 size_t runlist_bytes(int32_t num_q) {
-  return (size_t)2 * 8 + (size_t)(num_q + 1) * 8 + (size_t)(num_q + 1) * 4;
+  return (size_t)2 * 8 + (size_t)(num_q + 1) * 8 + (size_t)(num_q + 1) * 4 + (size_t)num_q * 4;
+}
+
+int32_t* runlist_order(void* base, int32_t num_q) {
+  return reinterpret_cast<int32_t*>(static_cast<char*>(base) + 2 * 8 + (size_t)(num_q + 1) * 8 +
+                                    (size_t)(num_q + 1) * 4);
 }
 
 static RunList make_runlist(void* base, int32_t num_q) {
@@ -2235,10 +2269,11 @@ cudaError_t launch_score_full(const uint16_t* q_idx, const uint16_t* keys, const
   // extra CTAs of the run-list launch, 8 vectors per thread
   const int64_t zero_vecs = ghist != nullptr ? (int64_t)num_q * kHistBins / 4 : 0;
   const int zero_ctas = (int)std::min<int64_t>(64, (zero_vecs + 8 * 1024 - 1) / (8 * 1024));
-  cudaError_t e = launch_pdl(group_prefix_kernel, dim3(1 + zero_ctas), dim3(1024), 0, s, batched,
+  cudaError_t e = launch_pdl(group_prefix_kernel, dim3(2 + zero_ctas), dim3(1024), 0, s, batched,
                              false, q_seq, num_q, g, 0, kPage, const_cast<int64_t*>(rl.meta),
                              const_cast<int64_t*>(rl.prefix), const_cast<int32_t*>(rl.run_q0),
-                             reinterpret_cast<uint4*>(ghist), zero_vecs);
+                             reinterpret_cast<uint4*>(ghist), zero_vecs,
+                             runlist_order(runlist, num_q));
   if (e != cudaSuccess) return e;
   CUtensorMap keymap;
   if (!make_bf16_map(&keymap, keys, (int64_t)pg.num_pages * kPage, kDidx, 64, kPage))
@@ -2315,8 +2350,8 @@ size_t wide_select_bytes(int32_t num_q, int32_t n) {
 cudaError_t launch_select(bool reindex, const uint32_t* ws, int64_t ws_stride, const int32_t* q_seq,
                           const csa2_pages& pg, int32_t num_q, const int32_t* pool_in,
                           int32_t pool_size, int32_t topk, int32_t* out_idx, int32_t* pool_out,
-                          const uint32_t* ghist, void* wide_ws, int32_t* st, cudaStream_t s,
-                          int num_sms) {
+                          const uint32_t* ghist, void* wide_ws, const int32_t* order,
+                          int32_t* st, cudaStream_t s, int num_sms) {
   const int32_t n = reindex ? pool_size : pg.max_pages_per_seq * kPage;
   const int32_t want_max = std::max(topk, (!reindex && pool_out) ? pool_size : 0);
   // FULL beyond 2^18 tokens with the scorer's histograms: C filter CTAs per query, then
@@ -2378,7 +2413,7 @@ cudaError_t launch_select(bool reindex, const uint32_t* ws, int64_t ws_stride, c
                       ws_stride, q_seq, pg.seq_lens, pg.num_seqs, pool_in,
                       reindex ? pool_size : (pool_out ? pool_size : 0), topk, out_idx,
                       reindex ? nullptr : pool_out, pg.max_pages_per_seq * kPage,
-                      reindex ? nullptr : ghist);
+                      reindex ? nullptr : ghist, reindex ? nullptr : order);
   }
   const int c = select_cluster(n, want_max);
   if (reindex)
