@@ -342,22 +342,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  tc_before();
-  __syncthreads();
-  tc_after();
-  grid_dep_wait();
-  const uint32_t tmem = sm.tmem;
-
-  // ---- the query's terms (B operand, its scale-factor image, p_0) ----
-  if (tid == 0) {
-    const unsigned char* img = terms + (size_t)qi * kTermsBytes;
-    mbar_expect_tx(&sm.t_full, kQbBytes + kSfbBytes + 16);
-    bulk_g2s(saddr(sm.qb), img, kQbBytes, &sm.t_full);
-    bulk_g2s(saddr(sm.sfb), img + kQbBytes, kSfbBytes, &sm.t_full);
-    bulk_g2s(saddr(&sm.p0[0]), img + kTermsP0, 16, &sm.t_full);
-  }
-
-  // ---- resolve the selected entries to physical rows: the first tile first ----
+  // ---- resolve the selected entries to physical rows, and gather the first tile ----
+  // Done before the dependency wait, so that it overlaps the term kernel: the indices, the
+  // page table and the cache are inputs of this call, and every kernel before the term
+  // kernel in the stream has completed by now (the term kernel lets this one launch only
+  // after its own dependency wait).  Nothing global is written before the wait.
   int b = __ldg(q_seq + qi);
   int n_ctx = 0;
   if (b < 0 || b >= geo.num_seqs) {
@@ -367,27 +356,40 @@ __global__ void __launch_bounds__(kThreads, 2)
     n_ctx = min(max(0, __ldg(geo.seq_lens + b)), geo.max_pages * kPage);
   }
   const int32_t* idx_q = idx + (int64_t)qi * topk + jbeg;
-  auto resolve = [&](int e, int s) {
-    int32_t slot = -1;
-    if (s >= 0 && s < n_ctx) {
-      const int32_t pg = __ldg(geo.page_table + (int64_t)b * geo.max_pages + (s >> 6));
-      if (pg >= 0 && pg < geo.num_pages) slot = pg * kPage + (s & (kPage - 1));
-      else report(st, CSA2_DEV_BAD_PAGE);
-    } else if (s != -1) {
-      report(st, CSA2_DEV_BAD_INDEX);
-    }
-    sm.slot[e] = slot;
-  };
-  const int e_first = min(ecount, kTile);
-  if (tid < e_first) resolve(tid, __ldg(idx_q + tid));
-  constexpr int kRest = (kMaxSplit - kTile + kThreads - 1) / kThreads;
-  int rest_s[kRest];
+  constexpr int kPer = kMaxSplit / kThreads;  // entries resolved per thread
+  static_assert(kMaxSplit % kThreads == 0, "whole entries per thread");
+  {
+    int32_t s_of[kPer];
 #pragma unroll
-  for (int i = 0; i < kRest; ++i) {
-    const int e = e_first + tid + i * kThreads;
-    rest_s[i] = e < ecount ? __ldg(idx_q + e) : -1;
+    for (int i = 0; i < kPer; ++i) {
+      const int e = tid + i * kThreads;
+      s_of[i] = e < ecount ? __ldg(idx_q + e) : -1;
+    }
+    int32_t pg_of[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int32_t s = s_of[i];
+      pg_of[i] = (s >= 0 && s < n_ctx) ? __ldg(geo.page_table + (int64_t)b * geo.max_pages + (s >> 6)) : -1;
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = tid + i * kThreads;
+      if (e >= ecount) continue;
+      const int32_t s = s_of[i], pg = pg_of[i];
+      int32_t slot = -1;
+      if (s >= 0 && s < n_ctx) {
+        if (pg >= 0 && pg < geo.num_pages) slot = pg * kPage + (s & (kPage - 1));
+        else report(st, CSA2_DEV_BAD_PAGE);
+      } else if (s != -1) {
+        report(st, CSA2_DEV_BAD_INDEX);
+      }
+      sm.slot[e] = slot;
+    }
   }
-  __syncthreads();
+  tc_before();
+  __syncthreads();  // barriers, TMEM address and every slot visible
+  tc_after();
+  const uint32_t tmem = sm.tmem;
 
   // gather tile t (entries t * 128 ..): codes by half-warps (16 pieces of a 256-byte row),
   // scales two pieces per row; every slot is read before any copy
@@ -426,10 +428,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   };
   if (ntiles > 0) gather(0);
   cp_commit();
-#pragma unroll
-  for (int i = 0; i < kRest; ++i) {
-    const int e = e_first + tid + i * kThreads;
-    if (e < ecount) resolve(e, rest_s[i]);
+
+  grid_dep_wait();  // the term kernel's output is read from here on
+  // ---- the query's terms (B operand, its scale-factor image, p_0) ----
+  if (tid == 0) {
+    const unsigned char* img = terms + (size_t)qi * kTermsBytes;
+    mbar_expect_tx(&sm.t_full, kQbBytes + kSfbBytes + 16);
+    bulk_g2s(saddr(sm.qb), img, kQbBytes, &sm.t_full);
+    bulk_g2s(saddr(sm.sfb), img + kQbBytes, kSfbBytes, &sm.t_full);
+    bulk_g2s(saddr(&sm.p0[0]), img + kTermsP0, 16, &sm.t_full);
   }
   // B scale factors into TMEM once the terms have landed
   bool ok = mbar_wait(&sm.abort, &sm.t_full, 0, st);
