@@ -1334,7 +1334,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
                       int32_t num_seqs, const int32_t* __restrict__ pool_in, int32_t pool_size,
                       int32_t topk, int32_t* __restrict__ out_idx, int32_t* __restrict__ pool_out,
                       int32_t max_ctx, const uint32_t* __restrict__ ghist,
-                      const int32_t* __restrict__ order) {
+                      const int32_t* __restrict__ order, int32_t split_targets) {
   grid_dep_wait();
   extern __shared__ __align__(128) unsigned char smem_raw[];
   using SH = BigSharedT<NT, CAP>;
@@ -1350,6 +1350,10 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
     n = (b >= 0 && b < num_seqs) ? min(max(0, __ldg(seq_lens + b)), max_ctx) : 0;
   }
   const bool two = !kReindex && pool_out != nullptr && pool_size > 0;
+  // split_targets: two CTAs per query (grid.y = 2), the first emitting the top-K, the second
+  // the pool; each runs the whole search for its own target only
+  const bool h0 = !split_targets || blockIdx.y == 0;
+  const bool h1 = two && (!split_targets || blockIdx.y == 1);
   const uint32_t* src = ws + (int64_t)q * ws_stride;
   const int32_t* pin = kReindex ? pool_in + (int64_t)q * pool_size : nullptr;
   int32_t* out0 = out_idx + (int64_t)q * topk;
@@ -1402,8 +1406,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
   if (lane == 0) atomicAdd(&sh.nvalid, nv);
   __syncthreads();
   const uint32_t nvalid = sh.nvalid;
-  const uint32_t want0 = min((uint32_t)topk, nvalid);
-  const uint32_t want1 = two ? min((uint32_t)pool_size, nvalid) : 0u;
+  const uint32_t want0 = h0 ? min((uint32_t)topk, nvalid) : 0u;
+  const uint32_t want1 = h1 ? min((uint32_t)pool_size, nvalid) : 0u;
 
   // ---- 2. boundary bins (thread tid holds bins BPT tid .. BPT tid + BPT - 1) ----
   constexpr int BPT = kHistBins / NT;
@@ -1452,7 +1456,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
   // ---- 3. ordered sweep: keep keys with bin >= bmin ----
   const uint32_t lt = (1u << lane) - 1u;
   uint32_t cnt = 0;
-  if (want0 > 0) {
+  if (want0 > 0 || want1 > 0) {
     // slot-major groups (lane l holds keys l, 32 + l, 64 + l, 96 + l): each slot compacts
     // with one ballot.  (The 16-byte-load form of filter_segment measured slower here, where
     // the sweep is bound by instruction issue, not by the loads.)
@@ -1489,7 +1493,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
 
   // ---- 4. exact boundary keys T_t ----
   uint32_t T0 = 0, T1 = 0, Q0 = 0, Q1 = 0;  // boundary key and ties to take
-  if (want0 > 0) {
+  if (want0 > 0 || want1 > 0) {
     uint32_t pre[2] = {B0, B1}, abv[2] = {A0, A1};
     // a target that takes every valid key needs no search (T = 1, the smallest valid key,
     // with every tie taken)
@@ -1673,8 +1677,9 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
     __syncthreads();
   }
   // -1 padding after the selected entries
-  for (int i = (int)want0 + tid; i < topk; i += NT) out0[i] = -1;
-  if (two)
+  if (h0)
+    for (int i = (int)want0 + tid; i < topk; i += NT) out0[i] = -1;
+  if (h1)
     for (int i = (int)want1 + tid; i < pool_size; i += NT) out1[i] = -1;
 }
 
@@ -2409,11 +2414,14 @@ cudaError_t launch_select(bool reindex, const uint32_t* ws, int64_t ws_stride, c
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(num_q), dim3(small ? kSmallThreads : kBigThreads), smem, s, ws,
-                      ws_stride, q_seq, pg.seq_lens, pg.num_seqs, pool_in,
+    // Full with a pool, while two CTAs per query fit one per SM: one CTA per target
+    const int split = (!reindex && pool_out != nullptr && pool_size > 0 && !small &&
+                       2 * num_q <= num_sms) ? 1 : 0;
+    return launch_pdl(kern, dim3(num_q, 1 + split), dim3(small ? kSmallThreads : kBigThreads), smem, s,
+                      ws, ws_stride, q_seq, pg.seq_lens, pg.num_seqs, pool_in,
                       reindex ? pool_size : (pool_out ? pool_size : 0), topk, out_idx,
                       reindex ? nullptr : pool_out, pg.max_pages_per_seq * kPage,
-                      reindex ? nullptr : ghist, reindex ? nullptr : order);
+                      reindex ? nullptr : ghist, reindex ? nullptr : order, split);
   }
   const int c = select_cluster(n, want_max);
   if (reindex)
