@@ -272,6 +272,62 @@ def test_reindex_pool_sizes(pool, topk):
     check_sampled(wl, range(wl.num_q), step, q_idx, q)
 
 
+def _bf16_bits(x):
+    return (np.asarray(x, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("num_seqs,n,topk,pool", [
+    (4, 3000, 300, 1000),       # one CTA per target (few queries), pool of 1000
+    (150, 1500, 200, 700),      # more queries than SMs: the 512-thread form
+    (1, 300000, 2048, 8192),    # beyond 2^18 tokens: filter, resolve and emit kernels
+])
+def test_selection_ties_break_by_lower_position(num_seqs, n, topk, pool):
+    """Exact ties: every key row is one of 8 rows whose scores (one-hot queries, values
+    exact in bf16 and fp32) are 4 v_r for Full and 4 w_r for Reindex, so the top-K, the
+    pool and the Reindex top-K cut through groups of equal scores.  The lower position
+    must win every tie (tech-report digest, "Hierarchical Sparse Indexer": the top-K of
+    each search; the tie rule is this build's reading), and the outputs must equal the
+    oracle's selections exactly."""
+    P = 64
+    max_pages = (n + P - 1) // P
+    lens = np.full(num_seqs, n, np.int32)
+    table = np.arange(num_seqs * max_pages, dtype=np.int32).reshape(num_seqs, max_pages)
+    cache = DecodeCache(lens, table, num_seqs * max_pages, 1)
+    v = np.array([0.5, 1.0, 1.5, 2.0, 2.5, 3.0, 3.5, 4.0], np.float32)
+    w = v[::-1].copy()
+    pos = np.arange(n, dtype=np.int64)
+    keys_host = []
+    keys = torch.zeros((num_seqs * max_pages * P, gen.D_IDX), dtype=torch.int16)
+    for b in range(num_seqs):
+        r = (pos * 7 + b) % 8
+        k = np.zeros((n, gen.D_IDX), np.uint16)
+        k[:, 0] = _bf16_bits(v[r])
+        k[:, 1] = _bf16_bits(w[r])
+        keys_host.append(k)
+        slots = table[b][pos // P].astype(np.int64) * P + pos % P
+        keys[torch.from_numpy(slots)] = torch.from_numpy(k.view(np.int16))
+    cache.keys[0].copy_(keys.to(cache.keys.device))
+    schedule = [gen.FULL, gen.REINDEX, gen.REUSE]
+    q_idx = np.zeros((3, num_seqs, gen.H_IDX, gen.D_IDX), np.uint16)
+    q_idx[0, :, :, 0] = _bf16_bits(1.0)
+    q_idx[1, :, :, 1] = _bf16_bits(1.0)
+    q = np.zeros((3, num_seqs, gen.H_Q, gen.D_KV), np.uint16)
+    step = DecodeStep(cache, np.arange(num_seqs, dtype=np.int32), schedule, pool, topk, 1)
+    step.run(dev(q_idx), dev(q))
+    torch.cuda.synchronize()
+    status, bits = csa2.csa2_read_status(step.dev_status)
+    assert status == csa2.CSA2_OK, bits
+    got_k, got_p, got_r = host(step.indices(0)), host(step.pool[0]), host(step.indices(1))
+    tok = np.arange(n, dtype=np.int32)
+    for b in range(num_seqs):
+        s = oracle.index_scores(q_idx[0][b], keys_host[b])
+        want_p = oracle.select_topk(s, tok, pool)
+        assert np.array_equal(got_p[b], want_p), f"seq {b}: pool"
+        assert np.array_equal(got_k[b], oracle.select_topk(s, tok, topk)), f"seq {b}: top-K"
+        want_r, _ = oracle.index_reindex(q_idx[1][b], keys_host[b], want_p, topk)
+        assert np.array_equal(got_r[b], want_r), f"seq {b}: reindex"
+
+
 def test_attention_random_index_sets():
     """Attention alone on seeded random selections (with -1 padding and an empty set),
     single- and multi-split launches (up to 36 splits of 128 entries, most of them empty
