@@ -188,21 +188,28 @@ def test_small_ragged_all_modes(drafts):
     check_sampled(wl, range(wl.num_q), step, q_idx, q, min_attn=wl.num_q)
 
 
-@pytest.mark.parametrize("parallel,schedule", [
-    (False, [gen.FULL, gen.REINDEX, gen.REUSE, gen.REUSE]),
-    (True, [gen.FULL, gen.REINDEX, gen.REUSE, gen.REUSE]),
-    (True, [gen.FULL, gen.REINDEX, gen.REUSE, gen.REUSE, gen.FULL, gen.REINDEX, gen.REUSE])])
-def test_graph_replay_matches_eager_step(parallel, schedule):
+@pytest.mark.parametrize("parallel,schedule,mx", [
+    (False, [gen.FULL, gen.REINDEX, gen.REUSE, gen.REUSE], False),
+    (True, [gen.FULL, gen.REINDEX, gen.REUSE, gen.REUSE], False),
+    (True, [gen.FULL, gen.REINDEX, gen.REUSE, gen.REUSE, gen.FULL, gen.REINDEX, gen.REUSE], False),
+    (True, [gen.FULL, gen.REINDEX, gen.REUSE, gen.REUSE], True)])
+def test_graph_replay_matches_eager_step(parallel, schedule, mx):
     """The CUDA-graph step (what the benchmark times) replays the same launches: its
     indices, pools, outputs and lse are bit-identical to the eager step's, and a replay
     after new queries are copied into the captured buffers matches an eager run on them.
     With `parallel` the graph is of the parallel schedule (index calls in order, attention
     calls on side branches after their source layer's index call), two Full groups wrap
-    the branches around."""
+    the branches around; `mx` takes the MXFP4 cache (the other attention kernel)."""
     lens = np.array([5000, 64, 300, 2113], np.int32)
     wl = gen.DecodeWorkload("graph", 31, lens, np.array([2, 1, 1, 3], np.int32),
                             schedule, pool_size=512, topk=128)
-    cache, step, q_idx_h, q_h = run_workload(wl)
+    if mx:
+        cache = fill_decode_cache(wl, mx=True)
+        q_idx_h, q_h = all_queries_host(wl)
+        step = DecodeStep(cache, wl.q_seq, wl.schedule, wl.pool_size, wl.topk,
+                          int(wl.q_per_seq.max()))
+    else:
+        cache, step, q_idx_h, q_h = run_workload(wl)
     q_idx, q = dev(q_idx_h), dev(q_h)
     written = sorted(set(step.src))  # layers whose index output the step writes
 
