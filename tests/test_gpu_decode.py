@@ -279,6 +279,21 @@ def test_reindex_pool_sizes(pool, topk):
     check_sampled(wl, range(wl.num_q), step, q_idx, q)
 
 
+@pytest.mark.parametrize("tiles", [4, 5])
+def test_context_length_edges(tiles):
+    """Empty contexts, one token, page and selection boundaries (63/64/65, 255/256/257 =
+    top-K, 511/512/513 = pool), with 1-4 draft queries per sequence: 140 queries (one
+    selection CTA per target) and 175 (more queries than SMs: the two-per-SM form, taken
+    in order of context length)."""
+    base = np.array([0, 1, 63, 64, 65, 255, 256, 257, 511, 512, 513, 2049, 0, 5000], np.int32)
+    lens = np.tile(base, tiles)
+    qps = (np.arange(len(lens)) % 4 + 1).astype(np.int32)
+    wl = gen.DecodeWorkload("edges", 53 + tiles, lens, qps,
+                            [gen.FULL, gen.REINDEX, gen.REUSE], pool_size=512, topk=256)
+    _, step, q_idx, q = run_workload(wl)
+    check_sampled(wl, range(wl.num_q), step, q_idx, q)
+
+
 def _bf16_bits(x):
     return (np.asarray(x, np.float32).view(np.uint32) >> 16).astype(np.uint16)
 
