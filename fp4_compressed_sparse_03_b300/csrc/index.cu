@@ -2047,9 +2047,9 @@ __global__ void __launch_bounds__(kBigThreads, 1)
 // position 512 j + t).  Three radix steps find the exact boundary key T: the 11-bit
 // histogram bin (key >> 20), then bits 19..9 and 8..0 of the keys in the boundary bin.
 // The emit takes keys > T and the first Q keys == T in position order: per (j, warp)
-// counts of both from two ballots, one block-wide scan over those 16 KPT counts (which are
-// in position order), then each warp writes its selected pool tokens of slot j to
-// consecutive outputs.  The pool's tokens are copied to shared memory meanwhile.
+// counts of both from two ballots, one scan by a single warp over those 16 KPT counts
+// (which are in position order), then each warp writes its selected pool tokens of slot j
+// to consecutive outputs.  The pool's tokens are copied to shared memory meanwhile.
 constexpr int kPoolThreads = 512;
 constexpr int kPoolWarps = kPoolThreads / 32;
 constexpr int kPoolSelMax = 32 * kPoolThreads;  // 16384 pool entries, 32 per thread
@@ -2157,7 +2157,7 @@ __global__ void __launch_bounds__(kPoolThreads, KPT <= 16 ? 2 : 1)
   nv = __reduce_add_sync(0xffffffffu, nv);
   if (lane == 0) sh.wsum[warp] = nv;
   __syncthreads();
-  const uint32_t nvalid = pool_later_warps(sh, -1, lane);  // all warps
+  const uint32_t nvalid = pool_later_warps(sh, -1, lane);  // the warps after "-1": all of them
   const uint32_t want = min((uint32_t)topk, nvalid);
   __syncthreads();  // wsum is reused by the scans
 
