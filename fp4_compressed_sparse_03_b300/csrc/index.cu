@@ -2050,42 +2050,43 @@ __global__ void __launch_bounds__(kBigThreads, 1)
 // counts of both from two ballots, one scan by a single warp over those 16 KPT counts
 // (which are in position order), then each warp writes its selected pool tokens of slot j
 // to consecutive outputs.  The pool's tokens are copied to shared memory meanwhile.
-constexpr int kPoolThreads = 512;
-constexpr int kPoolWarps = kPoolThreads / 32;
-constexpr int kPoolSelMax = 32 * kPoolThreads;  // 16384 pool entries, 32 per thread
+constexpr int kPoolThreads = 512;                 // many queries: two CTAs per SM
+constexpr int kPoolThreadsWide = 1024;            // queries fit one per SM
+constexpr int kPoolSelMax = 32 * kPoolThreads;  // 16384 pool entries, at most 32 per thread
 
 struct PoolShared {
   uint32_t h[2][kHistBins];      // two histograms used in turn (pass 0, 1, 2 on h0, h1, h0)
-  uint32_t wsum[kPoolWarps];
+  uint32_t wsum[32];             // one word per warp
   uint32_t res[2];               // boundary digit, keys above it
 };
 
-// Suffix sums over the warps: returns the sum of wsum[w] for w > warp (wsum complete and
-// visible).  Lanes 0..15 read one warp total each.
+// Suffix sums over the NW warps: returns the sum of wsum[w] for w > warp (wsum complete
+// and visible; warp + 1 < NW, or warp = -1 for all of them).  Lane l reads warp l's total.
+template <int NW>
 __device__ __forceinline__ uint32_t pool_later_warps(const PoolShared& sh, int warp, int lane) {
-  uint32_t x = lane < kPoolWarps ? sh.wsum[lane] : 0u;
+  uint32_t x = lane < NW ? sh.wsum[lane] : 0u;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t y = __shfl_down_sync(0xffffffffu, x, o);
     if (lane + o < 32) x += y;
   }
-  return __shfl_sync(0xffffffffu, x, (warp + 1) & 31);  // warp + 1 <= 16 < 32
+  return __shfl_sync(0xffffffffu, x, warp + 1);
 }
 
 // Boundary digit of `want` keys among the NB digits of h (descending), `above` keys lying
 // above the histogram's range: returns the digit d with above + (keys in digits > d) <
 // want <= ... + h[d], and sets `above` to above + (keys in digits > d).  Thread tid owns
-// the NB / 512 consecutive digits from tid * NB / 512.
-template <int NB>
+// the BPT consecutive digits from BPT tid (none past NB).
+template <int NT, int NB>
 __device__ __forceinline__ uint32_t pool_find(PoolShared& sh, const uint32_t* h, uint32_t want,
                                               uint32_t& above) {
-  constexpr int BPT = NB / kPoolThreads;
-  static_assert(BPT >= 1 && NB % kPoolThreads == 0, "digits per thread");
+  constexpr int NW = NT / 32, BPT = NB >= NT ? NB / NT : 1;
+  static_assert(NB % NT == 0 || NT % NB == 0, "digits per thread");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t c[BPT], tot = 0;
 #pragma unroll
   for (int j = 0; j < BPT; ++j) {
-    c[j] = h[BPT * tid + j];
+    c[j] = BPT * tid + j < NB ? h[BPT * tid + j] : 0u;
     tot += c[j];
   }
   uint32_t x = tot;  // inclusive suffix sum over the warp's threads
@@ -2096,7 +2097,7 @@ __device__ __forceinline__ uint32_t pool_find(PoolShared& sh, const uint32_t* h,
   }
   if (lane == 0) sh.wsum[warp] = x;
   __syncthreads();
-  uint32_t a = above + x - tot + (warp + 1 < kPoolWarps ? pool_later_warps(sh, warp, lane) : 0u);
+  uint32_t a = above + x - tot + (warp + 1 < NW ? pool_later_warps<NW>(sh, warp, lane) : 0u);
 #pragma unroll
   for (int j = BPT - 1; j >= 0; --j) {
     if (a < want && a + c[j] >= want) {
@@ -2110,13 +2111,14 @@ __device__ __forceinline__ uint32_t pool_find(PoolShared& sh, const uint32_t* h,
   return sh.res[0];
 }
 
-template <int KPT>
-__global__ void __launch_bounds__(kPoolThreads, KPT <= 16 ? 2 : 1)
+template <int NT, int KPT>
+__global__ void __launch_bounds__(NT, (NT == kPoolThreads && KPT <= 16) ? 2 : 1)
     select_pool_kernel(const uint32_t* __restrict__ ws, const int32_t* __restrict__ pool_in,
                        int32_t pool_size, int32_t topk, int32_t* __restrict__ out_idx) {
   grid_dep_wait();
   __shared__ PoolShared sh;
-  __shared__ uint32_t cnt[KPT * kPoolWarps];   // per (slot j, warp): keys > T | (keys == T) << 16
+  constexpr int NW = NT / 32;
+  __shared__ uint32_t cnt[KPT * NW];   // per (slot j, warp): keys > T | (keys == T) << 16
   extern __shared__ __align__(16) int32_t spool[];  // the query's pool tokens (P entries)
   const int q = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int P = pool_size;
@@ -2127,19 +2129,19 @@ __global__ void __launch_bounds__(kPoolThreads, KPT <= 16 ? 2 : 1)
   uint32_t k[KPT];
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {
-    const int pos = kPoolThreads * j + tid;
+    const int pos = NT * j + tid;
     k[j] = pos < P ? __ldcg(src + pos) : 0u;
   }
   const uint32_t spool_s = smem_addr(spool);
   if ((P & 3) == 0 && (reinterpret_cast<uintptr_t>(pool_in) & 15) == 0) {
-    for (int i = 4 * tid; i < P; i += 4 * kPoolThreads) cp_async16(spool_s + 4 * i, pin + i);
+    for (int i = 4 * tid; i < P; i += 4 * NT) cp_async16(spool_s + 4 * i, pin + i);
   } else {
-    for (int i = tid; i < P; i += kPoolThreads)
+    for (int i = tid; i < P; i += NT)
       asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(spool_s + 4 * i), "l"(pin + i)
                    : "memory");
   }
   cp_async_commit();
-  for (int i = tid; i < 2 * kHistBins; i += kPoolThreads) (&sh.h[0][0])[i] = 0;
+  for (int i = tid; i < 2 * kHistBins; i += NT) (&sh.h[0][0])[i] = 0;
   __syncthreads();
   // a NaN score's key can reach 2^31, whose bin (key >> 20) would leave the histogram;
   // clamped, every key's bin is key >> 20 exactly
@@ -2157,7 +2159,7 @@ __global__ void __launch_bounds__(kPoolThreads, KPT <= 16 ? 2 : 1)
   nv = __reduce_add_sync(0xffffffffu, nv);
   if (lane == 0) sh.wsum[warp] = nv;
   __syncthreads();
-  const uint32_t nvalid = pool_later_warps(sh, -1, lane);  // the warps after "-1": all of them
+  const uint32_t nvalid = pool_later_warps<NW>(sh, -1, lane);  // the warps after "-1": all of them
   const uint32_t want = min((uint32_t)topk, nvalid);
   __syncthreads();  // wsum is reused by the scans
 
@@ -2165,19 +2167,19 @@ __global__ void __launch_bounds__(kPoolThreads, KPT <= 16 ? 2 : 1)
   uint32_t T = 0, Q = 0;
   if (want > 0 && want < nvalid) {
     uint32_t above = 0;
-    const uint32_t b0 = pool_find<kHistBins>(sh, sh.h[0], want, above);
-    for (int i = tid; i < 512; i += kPoolThreads) sh.h[0][i] = 0;  // pass 2's histogram
+    const uint32_t b0 = pool_find<NT, kHistBins>(sh, sh.h[0], want, above);
+    for (int i = tid; i < 512; i += NT) sh.h[0][i] = 0;  // pass 2's histogram
 #pragma unroll
     for (int j = 0; j < KPT; ++j)
       if (k[j] != 0 && (k[j] >> 20) == b0) atomicAdd(&sh.h[1][(k[j] >> 9) & 0x7FFu], 1u);
     __syncthreads();
-    const uint32_t d1 = pool_find<kHistBins>(sh, sh.h[1], want, above);
+    const uint32_t d1 = pool_find<NT, kHistBins>(sh, sh.h[1], want, above);
     const uint32_t pre = (b0 << 11) | d1;
 #pragma unroll
     for (int j = 0; j < KPT; ++j)
       if (k[j] != 0 && (k[j] >> 9) == pre) atomicAdd(&sh.h[0][k[j] & 0x1FFu], 1u);
     __syncthreads();
-    const uint32_t d2 = pool_find<512>(sh, sh.h[0], want, above);
+    const uint32_t d2 = pool_find<NT, 512>(sh, sh.h[0], want, above);
     T = (pre << 9) | d2;
     Q = want - above;
   }
@@ -2188,13 +2190,13 @@ __global__ void __launch_bounds__(kPoolThreads, KPT <= 16 ? 2 : 1)
   for (int j = 0; j < KPT; ++j) {
     const uint32_t gm = __ballot_sync(0xffffffffu, k[j] > T);
     const uint32_t em = __ballot_sync(0xffffffffu, k[j] == T);
-    if (lane == 0) cnt[j * kPoolWarps + warp] = __popc(gm) | ((uint32_t)__popc(em) << 16);
+    if (lane == 0) cnt[j * NW + warp] = __popc(gm) | ((uint32_t)__popc(em) << 16);
   }
   cp_async_wait<0>();
   __syncthreads();  // counts complete; every thread's pool tokens have landed
   // exclusive scan of the KPT x 16 packed counts (each half at most P < 2^16), in place,
   // by warp 0: lane l takes the NC / 32 consecutive entries from NC l / 32
-  constexpr int NC = KPT * kPoolWarps, CPL = NC / 32;
+  constexpr int NC = KPT * NW, CPL = NC / 32;
   static_assert(NC % 32 == 0, "whole counts per lane");
   if (warp == 0) {
     uint32_t c[CPL], tot = 0;
@@ -2225,8 +2227,8 @@ __global__ void __launch_bounds__(kPoolThreads, KPT <= 16 ? 2 : 1)
     int32_t tok[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int pos = kPoolThreads * (j0 + u) + tid;
-      cb[u] = cnt[(j0 + u) * kPoolWarps + warp];
+      const int pos = NT * (j0 + u) + tid;
+      cb[u] = cnt[(j0 + u) * NW + warp];
       tok[u] = pos < P ? spool[pos] : -1;
     }
 #pragma unroll
@@ -2240,7 +2242,7 @@ __global__ void __launch_bounds__(kPoolThreads, KPT <= 16 ? 2 : 1)
       if (sel && p < want) out[p] = tok[u];
     }
   }
-  for (int i = (int)want + tid; i < topk; i += kPoolThreads) out[i] = -1;
+  for (int i = (int)want + tid; i < topk; i += NT) out[i] = -1;
 }
 
 // ------------------------------------------------------------------ launchers -----
@@ -2387,16 +2389,21 @@ cudaError_t launch_select(bool reindex, const uint32_t* ws, int64_t ws_stride, c
     return launch_pdl(select_emit_kernel, dim3(C, num_q), dim3(kBigThreads), 0, s, P, topk, out_idx,
                       pool_out, wl);
   }
-  // Reindex pools of up to 16384 entries: one CTA per query with the keys in registers
+  // Reindex pools of up to 16384 entries: one CTA per query with the keys in registers,
+  // 1024 threads while the queries fit one per SM, else 512
   if (reindex && n <= kPoolSelMax && ws_stride == n) {
-    const int kpt = n <= 2048 ? 4 : n <= 4096 ? 8 : n <= 8192 ? 16 : 32;
-    auto kern = kpt == 4 ? select_pool_kernel<4> : kpt == 8 ? select_pool_kernel<8>
-              : kpt == 16 ? select_pool_kernel<16> : select_pool_kernel<32>;
+    const bool wide = num_q <= num_sms;
+    const int nt = wide ? kPoolThreadsWide : kPoolThreads;
+    const int kpt = n <= 4 * nt ? 4 : n <= 8 * nt ? 8 : n <= 16 * nt ? 16 : 32;
+    void (*kern)(const uint32_t*, const int32_t*, int32_t, int32_t, int32_t*) =
+        wide ? (kpt == 4 ? select_pool_kernel<kPoolThreadsWide, 4>
+                : kpt == 8 ? select_pool_kernel<kPoolThreadsWide, 8> : select_pool_kernel<kPoolThreadsWide, 16>)
+             : (kpt == 4 ? select_pool_kernel<kPoolThreads, 4> : kpt == 8 ? select_pool_kernel<kPoolThreads, 8>
+                : kpt == 16 ? select_pool_kernel<kPoolThreads, 16> : select_pool_kernel<kPoolThreads, 32>);
     const size_t smem = (size_t)n * sizeof(int32_t);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(num_q), dim3(kPoolThreads), smem, s, ws, pool_in, pool_size, topk,
-                      out_idx);
+    return launch_pdl(kern, dim3(num_q), dim3(nt), smem, s, ws, pool_in, pool_size, topk, out_idx);
   }
   // Up to 2^18 keys per query: one CTA per query, no cluster synchronisation (measured on
   // B300: 64 Full queries x 131072 keys took ~90 us in two waves of 8-CTA clusters, 46 us
