@@ -92,6 +92,12 @@ class DecodeStep:
         self.attn_workspace = [torch.empty(ws_a, dtype=torch.uint8, device=dev)
                                for _ in range(self.attn_branches)]
         self._branches = [torch.cuda.Stream(dev) for _ in range(self.attn_branches)]
+        # With several Full groups the index calls gate the later groups' attention, so they
+        # run on a stream of higher priority (ragged, 20 layers: 7.71 -> 7.59 ms per step);
+        # with one group the caller's stream serves (the decode batch measured 0.3 % slower
+        # with the extra stream)
+        groups = sum(1 for m in self.schedule if m == CSA2_FULL)
+        self._index_stream = torch.cuda.Stream(dev, priority=-1) if groups > 1 else None
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.use_pool = self.pool_size > 0 and any(m == CSA2_REINDEX for m in self.schedule)
 
@@ -127,31 +133,35 @@ class DecodeStep:
 
     # ---- parallel schedule: independent calls on separate streams ----
     # A layer's attention needs only its source layer's indices, and no index call reads
-    # an attention's output, so the index calls run in order on the caller's stream while
-    # the attention calls run on ATTN_BRANCHES side streams (layer l on branch l % B, each
-    # branch with its own workspace), each waiting for the event recorded after its source
-    # layer's index call.  The caller's stream waits for every branch at the end.  The
-    # results are those of run(): the same calls on the same buffers.
+    # an attention's output, so the index calls run in order on one stream (the caller's,
+    # or a high-priority one with several Full groups) while the attention calls run on
+    # ATTN_BRANCHES side streams (layer l on branch l % B, each branch with its own
+    # workspace), each waiting for the event recorded after its source layer's index call.
+    # The caller's stream waits for every stream at the end.  The results are those of
+    # run(): the same calls on the same buffers.
     ATTN_BRANCHES = 4
 
     def run_parallel(self, q_idx, q) -> None:
         main = torch.cuda.current_stream(self.cache.device)
+        ix = self._index_stream if self._index_stream is not None else main
         start = torch.cuda.Event()
         start.record(main)
+        if ix is not main:
+            ix.wait_event(start)
         for b in self._branches:
             b.wait_event(start)
         done = {}
         for l, m in enumerate(self.schedule):
             if m != CSA2_REUSE:
-                self.layer_index(l, q_idx[l], main)
+                self.layer_index(l, q_idx[l], ix)
                 ev = torch.cuda.Event()
-                ev.record(main)
+                ev.record(ix)
                 done[l] = ev
             br = self._branches[l % self.attn_branches]
             br.wait_event(done[self.src[l]])
             with torch.cuda.stream(br):
                 self.layer_attn(l, q[l], br, self.attn_workspace[l % self.attn_branches])
-        for b in self._branches:
+        for b in ([ix] if ix is not main else []) + self._branches:
             ev = torch.cuda.Event()
             ev.record(b)
             main.wait_event(ev)
