@@ -1514,6 +1514,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
       for (int i = tid; i < 2 * 256; i += NT) sh.rh[i >> 8][i & 255] = 0;
       __syncthreads();
       if (kept) {
+#pragma unroll 4
         for (uint32_t j = lane; j < cnt; j += 32) {
           const uint32_t k = sh.u.c.key[warp][j];
 #pragma unroll
@@ -1559,6 +1560,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
     const uint32_t Tt[2] = {T0, T1}, Qt[2] = {Q0, Q1}, wt[2] = {want0, want1};
     int32_t* const ot[2] = {out0, out1};
     uint32_t gt[2] = {0u, 0u}, eq[2] = {0u, 0u};
+#pragma unroll 4
     for (uint32_t j = lane; j < cnt; j += 32) {
       const uint32_t k = sh.u.c.key[warp][j];
 #pragma unroll
@@ -1580,33 +1582,48 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
       }
     }
     __syncthreads();
+    // the warp's output base and tie quota per target: lane w takes warp w's counts; the
+    // ties before each warp are an exclusive scan over the warps, a warp's contribution is
+    // its keys > T plus the ties it takes, and the base sums the contributions before it
     uint32_t base[2], take[2], tie_run[2] = {0u, 0u}, sel_run[2] = {0u, 0u};
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      uint32_t b = 0, ties_before = 0;
-      for (int w = 0; w < warp; ++w) {
-        const uint32_t e_w = sh.wtie[t][w];
-        b += sh.wsel[t][w] + (Qt[t] > ties_before ? min(Qt[t] - ties_before, e_w) : 0u);
-        ties_before += e_w;
-      }
-      base[t] = b;
-      take[t] = Qt[t] > ties_before ? min(Qt[t] - ties_before, sh.wtie[t][warp]) : 0u;
+      const uint32_t e_l = lane < NW ? sh.wtie[t][lane] : 0u;
+      const uint32_t s_l = lane < NW ? sh.wsel[t][lane] : 0u;
+      uint32_t e_tot;
+      const uint32_t e_before = warp_excl(e_l, e_tot);
+      const uint32_t take_l = Qt[t] > e_before ? min(Qt[t] - e_before, e_l) : 0u;
+      uint32_t c_tot;
+      const uint32_t c_before = warp_excl(s_l + take_l, c_tot);
+      base[t] = __shfl_sync(0xffffffffu, c_before, warp);
+      take[t] = __shfl_sync(0xffffffffu, take_l, warp);
     }
-    for (uint32_t j0 = 0; j0 < cnt; j0 += 32) {
-      const uint32_t j = j0 + lane;
-      const uint32_t k = j < cnt ? sh.u.c.key[warp][j] : 0u;
-      const uint32_t pos = j < cnt ? (uint32_t)seg_lo + sh.u.c.pos[warp][j] : 0u;
+    // four 32-key chunks per step: their keys and positions are read before any output
+    // store (a store through a generic pointer would order the later shared reads)
+    for (uint32_t j0 = 0; j0 < cnt; j0 += 128) {
+      uint32_t kc[4], pc[4];
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        if (wt[t] == 0) continue;
-        const bool tie = j < cnt && k == Tt[t];
-        const uint32_t tb = __ballot_sync(0xffffffffu, tie);
-        const bool sel = j < cnt && (k > Tt[t] || (tie && tie_run[t] + __popc(tb & lt) < take[t]));
-        const uint32_t sb = __ballot_sync(0xffffffffu, sel);
-        const uint32_t p = base[t] + sel_run[t] + __popc(sb & lt);
-        if (sel && p < wt[t]) ot[t][p] = kReindex ? __ldg(pin + pos) : (int32_t)pos;
-        tie_run[t] += __popc(tb);
-        sel_run[t] += __popc(sb);
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t j = j0 + 32 * u + lane;
+        kc[u] = j < cnt ? sh.u.c.key[warp][j] : 0u;
+        pc[u] = j < cnt ? (uint32_t)seg_lo + sh.u.c.pos[warp][j] : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t j = j0 + 32 * u + lane;
+        const uint32_t k = kc[u], pos = pc[u];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (wt[t] == 0) continue;
+          const bool tie = j < cnt && k == Tt[t];
+          const uint32_t tb = __ballot_sync(0xffffffffu, tie);
+          const bool sel = j < cnt && (k > Tt[t] || (tie && tie_run[t] + __popc(tb & lt) < take[t]));
+          const uint32_t sb = __ballot_sync(0xffffffffu, sel);
+          const uint32_t p = base[t] + sel_run[t] + __popc(sb & lt);
+          if (sel && p < wt[t]) ot[t][p] = kReindex ? __ldg(pin + pos) : (int32_t)pos;
+          tie_run[t] += __popc(tb);
+          sel_run[t] += __popc(sb);
+        }
       }
     }
     __syncthreads();
