@@ -579,6 +579,35 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restri
 #pragma unroll
   for (int u = 0; u < 4; ++u)
     if (u < nsplit) v0[u] = __ldcs(po + (int64_t)u * kHq * kDkv / 4 + threadIdx.x);
+  if (nsplit <= 4) {
+    // every thread takes the (at most four) weights itself: no barrier, no shared memory;
+    // the normaliser is summed in the order of the warp reduction below, (0 + 2) + (1 + 3)
+    float m[4], l[4], w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      m[u] = u < nsplit ? __ldg(ml + u * 2 * kHq + h) : -INFINITY;
+      l[u] = u < nsplit ? __ldg(ml + u * 2 * kHq + kHq + h) : 0.f;
+    }
+    const float M = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+#pragma unroll
+    for (int u = 0; u < 4; ++u) w[u] = (m[u] == -INFINITY) ? 0.f : exp2f(m[u] - M);
+    const float L = (w[0] * l[0] + w[2] * l[2]) + (w[1] * l[1] + w[3] * l[3]);
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (u < nsplit) {
+        a.x += w[u] * v0[u].x;
+        a.y += w[u] * v0[u].y;
+        a.z += w[u] * v0[u].z;
+        a.w += w[u] * v0[u].w;
+      }
+    }
+    const float iv = L > 0.f ? 1.0f / L : 0.f;
+    if (threadIdx.x == 0 && lse) lse[(int64_t)qi * kHq + h] = L > 0.f ? M * 0.6931471805599453f + logf(L) : -INFINITY;
+    reinterpret_cast<float4*>(out + ((int64_t)qi * kHq + h) * kDkv)[threadIdx.x] =
+        make_float4(a.x * iv, a.y * iv, a.z * iv, a.w * iv);
+    return;
+  }
   if (threadIdx.x < 32) {
     float M = -INFINITY;
     for (int s = threadIdx.x; s < nsplit; s += 32) M = fmaxf(M, ml[s * 2 * kHq + h]);
